@@ -1,0 +1,483 @@
+#!/usr/bin/env python3
+"""Benchmark: paged decode steps on GB300.
+
+One step = the whole hot path for one layer: the host block manager makes every sequence's
+append slot writable (allocating or copy-on-write), the changed block table is uploaded, the
+copy-on-write pairs are copied, every sequence's new K/V token is appended, and decode
+attention runs over the paged cache.  Positions advance one token per step through a window
+of WINDOW steps and then wrap (the later passes re-append the same slots), so every timed step
+is a real decode step while per-step inputs stay bounded.
+
+Prints ONE JSON line (rank 0).  ``value`` is achieved HBM GB/s of the attention's algorithmic
+bytes (KV attended + q + out + block-table entries used + context_lens) over the whole step
+time, with every input resident in HBM; ``e2e`` is the same metric with each step's q/k/v
+copied from pinned host memory and the output copied back inside the timed region;
+``roofline`` is the decode-attention call alone, timed with CUDA events on its stream.
+
+  python bench.py [--gpus N --steps K --warmup W --config 8b --partition 0]
+  python bench.py --impl reference   # the CPU oracle on a bounded sample of the same workload
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WINDOW = 64
+METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak); decode tokens/s/layer"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def seq_bytes(w, ctx_s: int) -> int:
+    """Algorithmic bytes one sequence contributes to a decode-attention call: its attended K
+    and V (sink positions counted at bf16), its q and out rows, the block-table entries it uses
+    and its context length."""
+    e = w.kv_elem_bytes()
+    ctx_s = int(ctx_s)
+    n_sink = min(ctx_s, w.num_sink)
+    kv = (ctx_s - n_sink) * w.H_kv * w.D * e * 2 + n_sink * w.H_kv * w.D * 2 * 2
+    return kv + 2 * w.H_q * w.D * 2 + (-(-ctx_s // 16)) * 4 + 4
+
+
+def attention_bytes(w, ctx: np.ndarray) -> int:
+    """Algorithmic bytes of one decode-attention call (what must cross HBM at least once)."""
+    scales = 2 * w.H_kv * 4 if w.k_dtype != "bf16" else 0
+    return sum(seq_bytes(w, c) for c in np.asarray(ctx)) + scales
+
+
+# ----------------------------------------------------------------------------------
+# distributed helpers (one process per GPU; replicas, no collective on the data path)
+# ----------------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max_sum(elapsed_s: float, units: float, backend_device=None):
+    """Max of the elapsed times and sum of the units over all ranks (identity at world 1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return elapsed_s, units
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=backend_device)
+    u = torch.tensor([units], dtype=torch.float64, device=backend_device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        busy = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------
+class DecodeBench:
+    """One layer's paged cache and the per-step inputs of a WINDOW-step cycle, on one GPU."""
+
+    def __init__(self, name, device, partition=0):
+        import torch
+        from paged_kv_cache_table_gb300 import native as N
+        from paged_kv_cache_table_gb300.workloads import make_workload
+        self.torch, self.N = torch, N
+        self.dev = device
+        self.partition = partition
+        w = make_workload(name, steps=WINDOW)
+        self.w = w
+        n_slots = w.num_blocks * 16
+        kvdt = torch.bfloat16 if w.k_dtype == "bf16" else torch.uint8
+        self.k = torch.empty((n_slots, w.H_kv, w.D), dtype=kvdt, device=device)
+        self.v = torch.empty((n_slots, w.H_kv, w.D), dtype=kvdt, device=device)
+        self.k_scales = None if w.k_scales is None else w.k_scales.to(device)
+        self.v_scales = None if w.v_scales is None else w.v_scales.to(device)
+        self.k_sink = self.v_sink = None
+        if w.num_sink:
+            self.k_sink = torch.empty((w.B, w.num_sink, w.H_kv, w.D), dtype=torch.bfloat16, device=device)
+            self.v_sink = torch.empty_like(self.k_sink)
+        self.desc = N.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks, w.k_dtype, w.v_dtype,
+                                self.k_scales, self.v_scales, self.k_sink, self.v_sink, w.num_sink)
+        self.tables = w.tables.copy()
+        self.tables_dev = torch.from_numpy(self.tables).to(device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.bm = N.BlockManager(w.num_blocks)
+        blocks, counts = np.unique(w.tables[w.tables >= 0], return_counts=True)
+        for b, c in zip(blocks, counts):
+            self.bm.claim(int(b))
+            for _ in range(int(c) - 1):
+                self.bm.incref(int(b))
+        # cached tokens, appended in bounded chunks
+        chunk = 1 << 17
+        for a in range(0, len(w.fill_seq), chunk):
+            b = min(len(w.fill_seq), a + chunk)
+            N.pa_kv_append_tokens(self.desc, self.k, self.v, w.fill_k[a:b].to(device), w.fill_v[a:b].to(device),
+                                  b - a, torch.from_numpy(w.fill_seq[a:b]).to(device),
+                                  torch.from_numpy(w.fill_pos[a:b]).to(device), self.tables_dev, self.err)
+        torch.cuda.synchronize()
+        # per-step inputs, resident
+        self.q = w.q.to(device)
+        self.k_new = w.k_new.to(device)
+        self.v_new = w.v_new.to(device)
+        self.pos = [w.positions(i) for i in range(WINDOW)]
+        self.ctx = [w.context_lens(i) for i in range(WINDOW)]
+        self.pos_dev = torch.from_numpy(np.stack(self.pos)).to(device)
+        self.ctx_dev = torch.from_numpy(np.stack(self.ctx)).to(device)
+        self.max_ctx = int(max(c.max() for c in self.ctx))
+        self.ws_bytes = N.pa_decode_workspace_size(self.desc, self.max_ctx, partition)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.out = torch.empty((w.B, w.H_q, w.D), dtype=torch.bfloat16, device=device)
+        self.step_bytes = [attention_bytes(w, c) for c in self.ctx]
+        # pinned staging for table uploads (one slot per step of a cycle) and e2e buffers
+        self.tab_ring = [torch.empty(self.tables.shape, dtype=torch.int32).pin_memory() for _ in range(WINDOW)]
+        self.pair_ring = [torch.empty((w.B, 2), dtype=torch.int32).pin_memory() for _ in range(WINDOW)]
+        self.pairs_dev = torch.empty((w.B, 2), dtype=torch.int32, device=device)
+        self.h_q = w.q.pin_memory()
+        self.h_k = w.k_new.pin_memory()
+        self.h_v = w.v_new.pin_memory()
+        self.h_out = torch.empty((WINDOW, w.B, w.H_q, w.D), dtype=torch.bfloat16).pin_memory()
+        self.d_q = torch.empty_like(self.q[0])
+        self.d_k = torch.empty_like(self.k_new[0])
+        self.d_v = torch.empty_like(self.v_new[0])
+        self.launches_per_step = 3  # append + attention + merge (plus a copy kernel on CoW steps)
+        self.cow_launches = 0
+
+    def step(self, i, stream, ev=None, e2e=False):
+        torch, N, w = self.torch, self.N, self.w
+        j = i % WINDOW
+        pairs, changed = self.bm.prepare_step(self.tables, self.pos[j])
+        if changed:
+            self.tab_ring[j].numpy()[...] = self.tables
+            self.tables_dev.copy_(self.tab_ring[j], non_blocking=True)
+        if len(pairs):
+            self.pair_ring[j].numpy()[:len(pairs)] = pairs
+            self.pairs_dev[:len(pairs)].copy_(self.pair_ring[j][:len(pairs)], non_blocking=True)
+            N.pa_block_copy(self.desc, self.k, self.v, self.pairs_dev, len(pairs), self.err, stream)
+            self.cow_launches += 1
+        if e2e:
+            self.d_q.copy_(self.h_q[j], non_blocking=True)
+            self.d_k.copy_(self.h_k[j], non_blocking=True)
+            self.d_v.copy_(self.h_v[j], non_blocking=True)
+            q, kn, vn = self.d_q, self.d_k, self.d_v
+        else:
+            q, kn, vn = self.q[j], self.k_new[j], self.v_new[j]
+        N.pa_kv_append(self.desc, self.k, self.v, kn, vn, self.tables_dev, self.pos_dev[j], self.err, stream)
+        if ev is not None:
+            ev[0].record()
+        N.pa_decode_attention(self.desc, self.out, q, self.k, self.v, self.tables_dev, self.ctx_dev[j],
+                              self.max_ctx, w.scale, self.partition, self.ws, self.ws_bytes, self.err, stream)
+        if ev is not None:
+            ev[1].record()
+        if e2e:
+            self.h_out[j].copy_(self.out, non_blocking=True)
+
+    def run(self, steps, warmup, e2e=False, per_call_events=False, sampler=None):
+        """Returns (elapsed_s, attention_ms_per_call or None, bytes over the timed steps)."""
+        torch = self.torch
+        stream = torch.cuda.current_stream()
+        sid = stream.cuda_stream
+        for i in range(warmup):
+            self.step(i, sid, e2e=e2e)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)] if per_call_events else None
+        barrier(self.dev)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        nbytes = 0
+        for k in range(steps):
+            i = warmup + k
+            self.step(i, sid, ev=None if evs is None else evs[k], e2e=e2e)
+            nbytes += self.step_bytes[i % WINDOW]
+        t1.record()
+        torch.cuda.synchronize()
+        barrier(self.dev)
+        elapsed = t0.elapsed_time(t1) / 1e3
+        att = None
+        if evs is not None:
+            att = [a.elapsed_time(b) for a, b in evs]
+        return elapsed, att, nbytes
+
+
+def cpu_baseline_sample(name, budget_s=15.0, max_seqs=None):
+    """The oracle, as it stands, on a bounded sample of the workload: whole decode steps
+    (append + attention) of the first sequences, on this host's CPU.  Run in a spawned child
+    with BLAS pinned to one thread, so that `cores` is exact."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_oracle_child, args=(name, budget_s, max_seqs, q))
+    p.start()
+    res = q.get(timeout=900)
+    p.join(timeout=60)
+    return res
+
+
+def _oracle_child(name, budget_s, max_seqs, q):
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    import torch
+    torch.set_num_threads(1)
+    import oracle as O
+    from paged_kv_cache_table_gb300.workloads import bf16_bits, make_workload
+    w = make_workload(name, steps=1)
+    nseq = w.B if max_seqs is None else min(w.B, max_seqs)
+    ks = None if w.k_scales is None else w.k_scales.numpy()
+    vs = None if w.v_scales is None else w.v_scales.numpy()
+    cache = O.PagedKVCache(w.num_blocks, w.H_kv, w.D, k_dtype=w.k_dtype, v_dtype=w.v_dtype, k_scales=ks,
+                           v_scales=vs, num_seqs=w.B, num_sink=w.num_sink)
+    pool = O.BlockPool(w.num_blocks)
+    for b in np.unique(w.tables[w.tables >= 0]):
+        pool.claim(int(b))
+    tables = w.tables.astype(np.int64).copy()
+    kb_all, vb_all = bf16_bits(w.fill_k), bf16_bits(w.fill_v)
+    sel = np.nonzero(w.fill_seq < nseq)[0]
+    for i in sel:
+        s = int(w.fill_seq[i])
+        cache.append(s, tables[s], int(w.fill_pos[i]), kb_all[i], vb_all[i])
+    qv = O.bf16_bits_to_f64(bf16_bits(w.q[0]))
+    kn, vn = bf16_bits(w.k_new[0]), bf16_bits(w.v_new[0])
+    pos, ctx = w.positions(0), w.context_lens(0)
+    done_bytes, done_seqs, t_total = 0, 0, 0.0
+    while t_total < budget_s and done_seqs < 10 * nseq:
+        s = done_seqs % nseq
+        t0 = time.perf_counter()
+        act = pool.prepare_append(tables[s], int(pos[s]))
+        if act[0] == "copy":
+            cache.block_copy(act[1], act[2])
+        cache.append(s, tables[s], int(pos[s]), kn[s], vn[s])
+        K, V = cache.gather(s, tables[s], int(ctx[s]))
+        O.decode_attention(qv[s], K, V, w.scale)
+        t_total += time.perf_counter() - t0
+        done_bytes += seq_bytes(w, int(ctx[s]))
+        done_seqs += 1
+    q.put({"seconds": t_total, "bytes": done_bytes, "seqs": done_seqs, "cores": 1,
+           "sample": f"{done_seqs} sequence-steps (append + attention) of the first {nseq} sequences, "
+                     f"fp64 numpy oracle, 1 thread"})
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    vals, secs, tot_bytes, cores, sample = [], 0.0, 0, 1, ""
+    for k in range(args.warmup + args.steps):
+        r = cpu_baseline_sample(args.config, budget_s=min(per_step, 20.0), max_seqs=8)
+        if k >= args.warmup:
+            vals.append(r["bytes"] / r["seconds"] / 1e9)
+            secs += r["seconds"]
+            tot_bytes += r["bytes"]
+        cores, sample = r["cores"], r["sample"]
+    value = tot_bytes / secs / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / max(1, args.steps), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.config, "oracle": "CPU fp64 numpy"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=device)
+    from paged_kv_cache_table_gb300.build import build
+    if rank == 0:
+        build()
+    barrier(device)
+    peak, peak_kind = _peaks()
+
+    b = DecodeBench(args.config, device, args.partition)
+    w = b.w
+    # device-resident run, with per-call events around the attention for the roofline
+    with ClockSampler(local) as cs:
+        elapsed, att_ms, nbytes = b.run(args.steps, args.warmup, per_call_events=True)
+    clocks = cs.summary()
+    el_max, bytes_all = reduce_max_sum(elapsed, nbytes, device)
+    value = bytes_all / el_max / 1e9
+    ms_per_step = 1e3 * el_max / args.steps
+    tok_s_layer = ws * w.B * args.steps / el_max
+    att_mean_ms = float(np.mean(att_ms))
+    att_bytes = float(np.mean([b.step_bytes[(args.warmup + k) % WINDOW] for k in range(args.steps)]))
+    achieved = att_bytes / (att_mean_ms / 1e3) / 1e9
+    # end-to-end through the same API with host buffers
+    el_e2e, _, nbytes_e2e = b.run(args.steps, args.warmup, e2e=True)
+    el_e2e, bytes_e2e = reduce_max_sum(el_e2e, nbytes_e2e, device)
+    h2d = (w.B * w.H_q * w.D + 2 * w.B * w.H_kv * w.D) * 2
+    d2h = w.B * w.H_q * w.D * 2
+    err = int(b.err.item())
+
+    extra = {}
+    if args.also and rank == 0:
+        for name in args.also.split(","):
+            nb = DecodeBench(name, device, args.partition)
+            e2, a2, by2 = nb.run(max(50, args.steps // 4), args.warmup, per_call_events=True)
+            a_ms = float(np.mean(a2))
+            ab = float(np.mean([nb.step_bytes[(args.warmup + k) % WINDOW] for k in range(len(a2))]))
+            extra[name] = {"value": round(by2 / e2 / 1e9, 1), "unit": "GB/s",
+                           "attention_gbs": round(ab / (a_ms / 1e3) / 1e9, 1),
+                           "attention_frac": round(ab / (a_ms / 1e3) / 1e9 / peak, 4),
+                           "ms_per_step": round(1e3 * e2 / len(a2), 4),
+                           "tokens_per_s_per_layer": round(nb.w.B * len(a2) / e2, 1),
+                           "err_flag": int(nb.err.item())}
+            del nb
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        r = cpu_baseline_sample(args.config, budget_s=args.cpu_seconds, max_seqs=8)
+        cpu = {"value": round(r["bytes"] / r["seconds"] / 1e9, 6), "unit": "GB/s", "cores": r["cores"],
+               "kind": "oracle", "sample": r["sample"]}
+
+    if rank == 0:
+        kv_bytes = int(sum(b.step_bytes) / WINDOW)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.k_dtype == "bf16" else "fp8e4m3/int8",
+            "data": "synthetic",
+            "config": {"workload": f"{args.config}: B={w.B}, H_q={w.H_q}, H_kv={w.H_kv}, d={w.D}, block 16, "
+                                   f"cached ctx U[{int(w.ctx_old.min())}..{int(w.ctx_old.max())}] + <=64 "
+                                   f"decoded, 1 layer per step",
+                       "partition_size": args.partition, "parallelism": f"replicas x{ws}",
+                       "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB attended per step vs "
+                             f"{L2_BYTES / 1e6:.0f} MB L2)"},
+            "tokens_per_s_per_layer": round(tok_s_layer, 1),
+            "tokens_per_s_model_32_layers": round(tok_s_layer / 32, 1),
+            "pct_of_hbm_peak": round(100 * value / peak, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                         "kernel": "pa_decode_attention (decode_kernel + merge_kernel)",
+                         "peak_kind": peak_kind, "ms_per_call": round(att_mean_ms, 5),
+                         "algorithmic_bytes_per_call": int(att_bytes)},
+            "e2e": {"value": round(bytes_e2e / el_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * el_e2e / args.steps, 5)},
+            "gpu_launches": args.steps * b.launches_per_step + b.cow_launches,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "err_flag": err,
+        }
+        if extra:
+            line["also"] = extra
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="8b")
+    ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--also", default="70b")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per attention call of this build (null when unknown)")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

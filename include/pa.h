@@ -1,0 +1,218 @@
+/*
+ * pa.h — paged KV-cache decode attention on NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * What the library computes, and where the pages define it:
+ *   - The KV cache is a pool of fixed-size physical blocks of 16 token slots; every
+ *     sequence owns a block table mapping logical block pos/16 to a physical block, and
+ *     a token's flat slot is table[pos/16]*16 + pos%16
+ *     ("KV Cache 的显存账本：PagedAttention 与连续批处理", §四, the locate() sketch).
+ *   - A decode step appends the new token's K and V at its slot (untitled article at
+ *     ldpk.cn/news/58971, §2.3), copying a shared block first when other sequences still
+ *     reference it (显存账本 §四; "大模型推理KV Cache显存优化：从PagedAttention到AI内存系统
+ *     演进", §3.2 reference counts and copy-on-write).
+ *   - It then computes one query per head against every cached token:
+ *     out = softmax(q·Kᵀ · scale) · V with scale = 1/sqrt(d_head) (ldpk §2.1), where query
+ *     head h reads KV head h / G, G = num_q_heads / num_kv_heads (显存账本 §二, GQA).
+ *   - Optional 8-bit caches store K as FP8 E4M3 and V as INT8 with one fp32 scale per KV
+ *     head, and keep the first num_sink positions of every sequence in bf16 (显存账本 §七).
+ *
+ * Memory layout (all row-major, all device memory unless stated otherwise):
+ *   k_cache, v_cache  [num_blocks * 16][num_kv_heads][head_dim]  element type per k/v_dtype
+ *                     (slot-major: one physical block is one contiguous chunk holding all
+ *                     KV heads of its 16 slots)
+ *   block_tables      int32 [num_seqs][max_blocks_per_seq]; entries past a sequence's last
+ *                     logical block are ignored and may be -1
+ *   context_lens      int32 [num_seqs]  tokens attended, including the new token
+ *   positions         int32 [num_seqs]  slot position of the appended token (= old length)
+ *   q, out            bf16  [num_seqs][num_q_heads][head_dim]
+ *   k_new, v_new      bf16  [rows][num_kv_heads][head_dim]
+ *   k_sink, v_sink    bf16  [num_seqs][num_sink][num_kv_heads][head_dim]
+ *   k_scales,v_scales fp32  [num_kv_heads]
+ *
+ * Conventions:
+ *   - The caller owns every buffer; the library allocates no device memory and keeps no
+ *     per-call state.  Calls are stream-ordered on the given stream (a cudaStream_t passed
+ *     as void*; NULL is the legacy default stream) and return after enqueueing.
+ *   - Errors the host can see (null pointers, unsupported shapes, small workspace) are
+ *     returned synchronously and nothing is enqueued.
+ *   - Errors in device data (a block id out of range, a context longer than the table or
+ *     than max_context_len, a sequence index out of range) set bits in the optional device
+ *     word *err_flag (atomicOr, never cleared by the library), skip the affected work and,
+ *     for attention, write zeros to the affected output rows.  No kernel traps.
+ *   - Every wait inside a kernel is bounded (about two seconds); on expiry the kernel sets
+ *     PA_EFLAG_TIMEOUT and returns instead of hanging.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_BLOCK_SIZE 16
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,          /* null pointer, negative size, inconsistent shapes */
+  PA_ERR_UNSUPPORTED = 2,          /* valid but not implemented (head_dim, block size, dtypes) */
+  PA_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < pa_decode_workspace_size(...) */
+  PA_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed (launch, attribute) */
+  PA_ERR_OUT_OF_BLOCKS = 5         /* block manager: no free physical block */
+} pa_status;
+
+typedef enum {
+  PA_BF16 = 0,
+  PA_FP8_E4M3 = 1, /* OCP FP8 E4M3, round-to-nearest-even, saturating at +-448 */
+  PA_INT8 = 2      /* symmetric int8, round-half-even, clamped to [-127, 127] */
+} pa_dtype;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define PA_EFLAG_BAD_BLOCK_ID 1 /* a table entry or copy pair outside [0, num_blocks) */
+#define PA_EFLAG_CTX_OVERFLOW 2 /* position/context beyond max_blocks_per_seq*16 or max_context_len */
+#define PA_EFLAG_BAD_SEQ 4      /* a token's sequence index outside [0, num_seqs) */
+#define PA_EFLAG_TIMEOUT 8      /* a bounded in-kernel wait expired */
+
+/* One layer's cache description.  Supported: block_size == 16; head_dim 64 or 128;
+ * num_q_heads % num_kv_heads == 0 with G = num_q_heads/num_kv_heads <= 8;
+ * (k_dtype, v_dtype) = (PA_BF16, PA_BF16) or (PA_FP8_E4M3, PA_INT8), the latter with
+ * head_dim 128.  k_scales/v_scales are required for 8-bit dtypes and ignored otherwise.
+ * num_sink > 0 keeps positions < num_sink in k_sink/v_sink (bf16) for any dtype. */
+typedef struct {
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int num_blocks;
+  int max_blocks_per_seq;
+  pa_dtype k_dtype;
+  pa_dtype v_dtype;
+  const float* k_scales; /* device fp32 [num_kv_heads], this layer */
+  const float* v_scales; /* device fp32 [num_kv_heads], this layer */
+  void* k_sink;          /* device bf16 [num_seqs][num_sink][num_kv_heads][head_dim] or NULL */
+  void* v_sink;
+  int num_sink;          /* 0 when unused */
+} pa_cache_desc;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* pa_status_string(pa_status status);
+
+/* ---------------------------------------------------------------------------------
+ * Append (decode): write the new token of every sequence into its slot.
+ * ldpk §2.3 (write the new K and V at the current length); 显存账本 §四 (locate());
+ * 显存账本 §七 (per-head scales, K in FP8 and V in INT8, sinks kept in bf16).
+ *
+ * Row s writes k_new[s], v_new[s] at position positions[s] of sequence s:
+ *   positions[s] < 0                   -> row skipped (padding), no flag;
+ *   positions[s] < num_sink            -> bf16 copy into k_sink[s][pos], v_sink[s][pos]; the
+ *                                         paged slot is not touched;
+ *   pos/16 >= max_blocks_per_seq       -> PA_EFLAG_CTX_OVERFLOW, row skipped;
+ *   table entry outside [0,num_blocks) -> PA_EFLAG_BAD_BLOCK_ID, row skipped;
+ *   otherwise the slot table[s][pos/16]*16 + pos%16 receives the bf16 bits unchanged, or
+ *   for 8-bit caches code = round(x / scale[kv_head]) with the division in IEEE fp32.
+ * The caller makes the slot writable first (pa_bm_prepare_step + pa_block_copy) and passes
+ * context_lens = positions + 1 to the following pa_decode_attention.
+ * Host errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA. */
+pa_status pa_kv_append(const pa_cache_desc* desc, void* k_cache, void* v_cache,
+                       const void* k_new, const void* v_new,
+                       const int32_t* block_tables, const int32_t* positions,
+                       int32_t* err_flag, void* stream);
+
+/* Bulk append (prefill / chunked fill): num_tokens rows, row i going to sequence
+ * token_seq[i] at position token_pos[i]; same rules as pa_kv_append, plus
+ * PA_EFLAG_BAD_SEQ for token_seq[i] outside [0, num_seqs).  Rows must target distinct
+ * slots.  k_new/v_new are bf16 [num_tokens][num_kv_heads][head_dim]. */
+pa_status pa_kv_append_tokens(const pa_cache_desc* desc, void* k_cache, void* v_cache,
+                              const void* k_new, const void* v_new, int num_tokens,
+                              const int32_t* token_seq, const int32_t* token_pos,
+                              const int32_t* block_tables, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Copy-on-write block copy: for each pair i, physical block dst = src_dst_pairs[2i+1]
+ * receives every byte of block src = src_dst_pairs[2i] in both k_cache and v_cache
+ * (显存账本 §四 copy only at the fork; AI内存系统 §3.2 copy before writing a shared block).
+ * src_dst_pairs: device int32 [n_pairs][2].  A pair with an id outside [0, num_blocks)
+ * sets PA_EFLAG_BAD_BLOCK_ID and is skipped.  Destinations must be distinct and must not
+ * be a source of the same call.  n_pairs == 0 enqueues nothing. */
+pa_status pa_block_copy(const pa_cache_desc* desc, void* k_cache, void* v_cache,
+                        const int32_t* src_dst_pairs, int n_pairs,
+                        int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Decode attention over the paged cache (ldpk §2.1 formula; ldpk §4.3: the kernel fetches
+ * K and V from non-contiguous places through the block table; 显存账本 §二 GQA).
+ *
+ * For every sequence s and query head h (KV head h/G), over positions 0..ctx-1 with
+ * ctx = context_lens[s]:  out[s][h] = sum_t softmax_t(scale * q[s][h]·K_t) V_t, with
+ * fp32 accumulation and the result rounded to bf16.  K_t/V_t are the bf16 values, or
+ * code*scale for 8-bit caches, or the sink rows for t < num_sink.  ctx == 0 gives zeros.
+ *
+ * partition_size: 0 = automatic (the cached blocks of all sequences are split evenly over
+ * the GPU's SMs; partial results are merged by a second kernel); a positive multiple of 16
+ * = fixed context partitions of that many tokens per CTA plus the merge kernel (a value
+ * >= max_context_len gives one pass per sequence).
+ * max_context_len bounds every context_lens[s] (larger ones set PA_EFLAG_CTX_OVERFLOW
+ * and give a zero row).  workspace: device memory of at least
+ * pa_decode_workspace_size(desc, max_context_len, partition_size) bytes, 256-byte
+ * aligned, used as scratch by this call only (its contents need not be initialised).
+ * k_cache and v_cache must be 16-byte aligned.
+ * Host errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE_TOO_SMALL,
+ * PA_ERR_CUDA. */
+size_t pa_decode_workspace_size(const pa_cache_desc* desc, int max_context_len, int partition_size);
+
+pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, const void* q,
+                              const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              int max_context_len, float scale, int partition_size,
+                              void* workspace, size_t workspace_bytes,
+                              int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Host block manager: the physical block pool with a free list and reference counts
+ * (显存账本 §四: equal-size blocks, any free one usable; AI内存系统 §3.2: reference counts,
+ * recycle at zero, copy-on-write; AI内存系统 §2.3: blocks return to the pool on every exit
+ * path).  Host memory only; every function is thread-safe (one internal mutex).
+ * Allocation hands out the lowest-numbered free block. */
+typedef struct pa_bm pa_bm;
+
+/* NULL if num_blocks <= 0 or block_size <= 0 or on allocation failure. */
+pa_bm* pa_bm_create(int num_blocks, int block_size);
+void pa_bm_destroy(pa_bm* bm);
+/* A free block with refcount 1, or -1 when none is free. */
+int pa_bm_alloc(pa_bm* bm);
+/* Take a specific free block (refcount 0 -> 1): 0 on success, -1 if not free/invalid. */
+int pa_bm_claim(pa_bm* bm, int blk);
+/* New refcount, or -1 if blk is not allocated. */
+int pa_bm_incref(pa_bm* bm, int blk);
+/* New refcount (0 = returned to the free list), or -1 if blk is not allocated. */
+int pa_bm_decref(pa_bm* bm, int blk);
+int pa_bm_refcount(const pa_bm* bm, int blk); /* 0 for free blocks, -1 if out of range */
+int pa_bm_num_free(const pa_bm* bm);
+/* dst_row[i] = src_row[i] with incref, for i < n_blocks (prefix sharing). */
+pa_status pa_bm_fork(pa_bm* bm, const int32_t* src_row, int32_t* dst_row, int n_blocks);
+/* decref row[i] and set it to -1 for i < n_blocks; returns the number of blocks freed
+ * (entries already -1 are skipped), or -1 on invalid arguments. */
+int pa_bm_release(pa_bm* bm, int32_t* row, int n_blocks);
+
+/* Make the slot of positions[s] writable for every sequence s (host tables, in place):
+ *   entry table[s][pos/16] < 0      -> allocate a block and store it (no copy);
+ *   refcount(entry) > 1 (shared)    -> allocate dst, decref the shared block, repoint the
+ *                                      entry, and emit the pair (src, dst) to cow_pairs;
+ *   otherwise                       -> nothing.
+ * Rows with positions[s] < 0 are skipped.  cow_pairs: host int32 [num_seqs][2] output,
+ * *n_pairs receives the count; *n_changed (may be NULL) receives the number of table
+ * entries changed.  On PA_ERR_OUT_OF_BLOCKS the rows handled before the failure keep their
+ * changes (and their pairs are reported); PA_ERR_INVALID_ARG for a position beyond the
+ * table. */
+pa_status pa_bm_prepare_step(pa_bm* bm, int32_t* block_tables, int num_seqs,
+                             int max_blocks_per_seq, const int32_t* positions,
+                             int32_t* cow_pairs, int* n_pairs, int* n_changed);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

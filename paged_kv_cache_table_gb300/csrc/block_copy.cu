@@ -1,0 +1,56 @@
+// Copy-on-write block copy.
+//
+// "KV Cache 的显存账本：PagedAttention 与连续批处理" §四: requests with a common prefix point
+// at the same physical blocks and copy only where they diverge.  "大模型推理KV Cache显存优化：
+// 从PagedAttention到AI内存系统演进" §3.2: a sequence that must write into a shared block first
+// copies it, so the other sequences never see the write.
+//
+// A physical block is one contiguous chunk (16 slots x kv_heads x head_dim) in the slot-major
+// cache.  Grid: (pair, tensor); each CTA streams one block of K or V with 16-byte vectors.
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+__global__ void __launch_bounds__(256) block_copy_kernel(const int32_t* pairs, int num_blocks,
+                                                         size_t block_vecs, uint4* k_cache,
+                                                         uint4* v_cache, int32_t* err) {
+  const int i = blockIdx.x;
+  const int src = pairs[2 * i];
+  const int dst = pairs[2 * i + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) set_error(err, PA_EFLAG_BAD_BLOCK_ID);
+    return;
+  }
+  if (src == dst) return;
+  uint4* base = blockIdx.y == 0 ? k_cache : v_cache;
+  const uint4* s = base + static_cast<size_t>(src) * block_vecs;
+  uint4* d = base + static_cast<size_t>(dst) * block_vecs;
+  for (size_t j = threadIdx.x; j < block_vecs; j += blockDim.x) d[j] = s[j];
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_block_copy(const pa_cache_desc* desc, void* k_cache, void* v_cache,
+                                   const int32_t* src_dst_pairs, int n_pairs, int32_t* err_flag,
+                                   void* stream) {
+  pa_status st = pa::validate_desc(desc);
+  if (st != PA_OK) return st;
+  if (n_pairs < 0) return PA_ERR_INVALID_ARG;
+  if (n_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
+    return PA_ERR_INVALID_ARG;
+  const size_t kbytes = static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * desc->head_dim *
+                        pa::dtype_bytes(desc->k_dtype);
+  const size_t vbytes = static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * desc->head_dim *
+                        pa::dtype_bytes(desc->v_dtype);
+  if (kbytes != vbytes) return PA_ERR_UNSUPPORTED;  // both 8-bit or both bf16
+  pa::block_copy_kernel<<<dim3(n_pairs, 2), 256, 0, pa::as_stream(stream)>>>(
+      src_dst_pairs, desc->num_blocks, kbytes / 16, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), err_flag);
+  return pa::launch_status();
+}

@@ -1,0 +1,861 @@
+// Decode attention over the paged KV cache: the hot path.
+//
+// What is computed (untitled KV-cache article at ldpk.cn/news/58971, §2.1 and §2.2): one query
+// row per head against every cached key, softmax(q·Kᵀ·scale)·V.  GQA ("KV Cache 的显存账本：
+// PagedAttention 与连续批处理" §二): every G consecutive query heads read one KV head.  The keys
+// and values are fetched from non-contiguous physical blocks through the block table
+// (ldpk §4.3; 显存账本 §四 locate()).  8-bit caches (显存账本 §七) are decoded in registers.
+//
+// Design (GB300, sm_103a):
+//  * Work unit = one 16-token physical block of one head group.  A CTA owns a contiguous range
+//    of the (sequence, logical block) list: in balanced mode the list of all sequences is cut
+//    into equal ranges, one per SM, so that any mix of context lengths keeps every SM busy; in
+//    fixed mode each CTA owns one partition of partition_size tokens of one sequence.
+//  * A producer warp resolves block-table entries and streams every block with TMA
+//    (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared-memory stages guarded by
+//    mbarriers.  The slot-major cache keeps each (slot, kv-head) row contiguous, and the TMA box
+//    is 16 slots x 128 bytes of one head, so a stage holds whole blocks for all heads of the
+//    group and no byte is fetched twice.
+//  * One consumer warp per (KV head, block of the stage).  q·Kᵀ for the G query heads of the KV
+//    head and the 16 tokens of the block is an m16n8k16 tensor-core product (tokens = M, query
+//    heads = N); the probabilities are transposed in registers (movmatrix) into the B operand
+//    of P·V (head_dim = M).  The softmax is the online (running max) form in fp32 with warp
+//    shuffles; partial (m, l, o) go to the workspace and a merge kernel combines them by
+//    log-sum-exp.  A warp that saw a whole sequence writes the bf16 output directly.
+//  * Every wait is bounded; invalid table entries and contexts set error bits and zero rows.
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kTileBytes = 2048;  // one TMA box: 16 slots x 128 bytes
+constexpr int kMaxConsumerWarps = 16;
+constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
+constexpr int kAutoMaxSeqs = 2048;
+constexpr int kMaxStages = 8;
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kFixedFallbackPartition = 512;
+constexpr float kNegInf = -INFINITY;
+
+struct DecodeParams {
+  int B, H_q, H_kv, G, num_blocks, max_blocks, num_sink, max_ctx;
+  int hg, nc, nbs, stages, warps_c;
+  int mode;  // 0 balanced, 1 fixed partitions
+  int ppb, max_parts;
+  int direct_ok;
+  int stage_bytes;
+  float scale_log2;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  const float* k_scales;
+  const float* v_scales;
+  const __nv_bfloat16* k_sink;
+  const __nv_bfloat16* v_sink;
+  float* partials;
+  int32_t* ws_meta;
+  int32_t* err;
+};
+
+// Blocks of a sequence with ctx tokens; -1 for an invalid context.
+__device__ __forceinline__ int seq_blocks(const DecodeParams& p, int ctx) {
+  if (ctx == 0) return 0;
+  if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_blocks * PA_BLOCK_SIZE) return -1;
+  return (ctx + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+}
+
+// Largest s in [0, n) with cum[s] <= u (cum non-decreasing, cum[0] <= u).
+__device__ __forceinline__ int find_seq(const int* cum, int n, int u) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct Smem {
+  uint8_t* stages;
+  uint64_t* full;
+  uint64_t* empty;
+  int4* meta;
+  int* cum;
+  int* ctxs;
+  int* scratch;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw, const DecodeParams& p) {
+  Smem s;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  s.stages = base;
+  s.full = reinterpret_cast<uint64_t*>(base + static_cast<size_t>(p.stages) * p.stage_bytes);
+  s.empty = s.full + p.stages;
+  s.meta = reinterpret_cast<int4*>(s.empty + p.stages);
+  s.cum = reinterpret_cast<int*>(s.meta + p.stages * p.nbs);
+  s.ctxs = s.cum + (p.mode == 0 ? p.B + 1 : 2);
+  s.scratch = s.ctxs + (p.mode == 0 ? p.B : 1);
+  return s;
+}
+
+// ------------------------------------------------------------------------------------
+// Consumer: one warp = one KV head x one block slot of every stage.
+// ------------------------------------------------------------------------------------
+template <int D, bool QUANT>
+struct Consumer {
+  static constexpr int KT = D / 16;  // k-steps of q·Kᵀ and m-tiles of P·V
+  const DecodeParams& p;
+  uint32_t qf[KT][2];
+  float o[KT][4];
+  float m[2], l[2], sl[2];
+  float vsc;
+  bool bad;
+  int lane, t4, tq, h_kv, j;
+
+  __device__ Consumer(const DecodeParams& p_, int lane_, int h_kv_, int j_)
+      : p(p_), vsc(1.f), lane(lane_), t4(lane_ >> 2), tq(lane_ & 3), h_kv(h_kv_), j(j_) {
+    sl[0] = sl[1] = p_.scale_log2;
+    reset();
+  }
+
+  __device__ __forceinline__ void reset() {
+    m[0] = m[1] = kNegInf;
+    l[0] = l[1] = 0.f;
+    bad = false;
+#pragma unroll
+    for (int i = 0; i < KT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  }
+
+  // B fragments of q for this KV head's G query heads (N = head, K = head_dim).
+  __device__ __forceinline__ void load_q(int s) {
+    const bool live = t4 < p.G;
+    const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(s) * p.H_q + h_kv * p.G + (live ? t4 : 0)) * D;
+    if constexpr (!QUANT) {
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        qf[kk][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * tq) : 0u;
+        qf[kk][1] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * tq) : 0u;
+      }
+      sl[0] = sl[1] = p.scale_log2;
+      vsc = 1.f;
+    } else {
+      // fp16 operands: q is scaled by a power of two so that its largest element lands just
+      // below 2^15 (every bf16 value in range then converts exactly), and the factor is
+      // removed again from the scores.  Dims are taken in the order the 8-bit K fragment
+      // delivers them: k-step kk uses d = 16kk + 4tq + {0,1} (b0) and {2,3} (b1).
+      float x[KT][4];
+      float mx = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        uint2 raw = live ? *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * tq) : make_uint2(0, 0);
+        x[kk][0] = __uint_as_float(raw.x << 16);
+        x[kk][1] = __uint_as_float(raw.x & 0xFFFF0000u);
+        x[kk][2] = __uint_as_float(raw.y << 16);
+        x[kk][3] = __uint_as_float(raw.y & 0xFFFF0000u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(x[kk][e]));
+      }
+      mx = warp_max_xor(mx, 1);
+      mx = warp_max_xor(mx, 2);
+      int e2 = 0;
+      if (mx > 0.f) {
+        frexpf(mx, &e2);
+        e2 = min(15 - e2, 100);
+      }
+      const float f = ldexpf(1.f, e2);
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        qf[kk][0] = pack_f16(x[kk][0] * f, x[kk][1] * f);
+        qf[kk][1] = pack_f16(x[kk][2] * f, x[kk][3] * f);
+      }
+      const int e_c0 = __shfl_sync(0xffffffffu, e2, 4 * (2 * tq));
+      const int e_c1 = __shfl_sync(0xffffffffu, e2, 4 * (2 * tq + 1));
+      const float base = p.scale_log2 * p.k_scales[h_kv];
+      sl[0] = base * ldexpf(1.f, -e_c0);
+      sl[1] = base * ldexpf(1.f, -e_c1);
+      vsc = p.v_scales[h_kv];
+    }
+  }
+
+  // One 16-token block: scores, online softmax update, P·V.
+  __device__ __forceinline__ void block(const uint8_t* kbase, const uint8_t* vbase, int lb, int ntok) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int tokA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    if constexpr (!QUANT) {
+      const int halfA = lane >> 4;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        const int ch16 = (kk & 3) * 2 + halfA;
+        const uint32_t addr =
+            smem_u32(kbase + (kk >> 2) * kTileBytes + tokA * 128 + ((ch16 ^ (tokA & 7)) << 4));
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(addr, a0, a1, a2, a3);
+        mma_bf16(acc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+      }
+    } else {
+#pragma unroll
+      for (int kp = 0; kp < KT / 2; ++kp) {
+        const int ch16 = 2 * kp + (lane >> 4);
+        const uint32_t addr = smem_u32(kbase + tokA * 128 + ((ch16 ^ (tokA & 7)) << 4));
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(addr, r0, r1, r2, r3);
+        mma_f16(acc, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0], qf[2 * kp][1]);
+        mma_f16(acc, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+      }
+    }
+    // rows t4 and t4+8 of the block; columns = query heads 2tq, 2tq+1
+    const int pos0 = lb * PA_BLOCK_SIZE + t4;
+    const bool v0 = t4 < ntok && pos0 >= p.num_sink;
+    const bool v1 = t4 + 8 < ntok && pos0 + 8 >= p.num_sink;
+    const float s00 = v0 ? acc[0] * sl[0] : kNegInf;
+    const float s01 = v0 ? acc[1] * sl[1] : kNegInf;
+    const float s10 = v1 ? acc[2] * sl[0] : kNegInf;
+    const float s11 = v1 ? acc[3] * sl[1] : kNegInf;
+    float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int mask = 4; mask <= 16; mask <<= 1) {
+      bm0 = warp_max_xor(bm0, mask);
+      bm1 = warp_max_xor(bm1, mask);
+    }
+    const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);
+    const float ms0 = mn0 == kNegInf ? 0.f : mn0;
+    const float ms1 = mn1 == kNegInf ? 0.f : mn1;
+    const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
+    const float p00 = ex2(s00 - ms0), p10 = ex2(s10 - ms0);
+    const float p01 = ex2(s01 - ms1), p11 = ex2(s11 - ms1);
+    l[0] = l[0] * al0 + p00 + p10;
+    l[1] = l[1] * al1 + p01 + p11;
+    m[0] = mn0;
+    m[1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      o[mt][0] *= al0;
+      o[mt][1] *= al1;
+      o[mt][2] *= al0;
+      o[mt][3] *= al1;
+    }
+    // P (tokens x heads) -> B operand (K = tokens, N = heads) of P·V
+    const uint32_t x0 = QUANT ? pack_f16(p00, p01) : pack_bf16(p00, p01);
+    const uint32_t x1 = QUANT ? pack_f16(p10, p11) : pack_bf16(p10, p11);
+    const uint32_t b0 = movmatrix_t(x0), b1 = movmatrix_t(x1);
+    if constexpr (!QUANT) {
+      // Slots outside the context (tail of the last block, sink positions) may hold any bits,
+      // NaN included, and 0 * NaN would poison the sum: zero those tokens' V elements.  This
+      // lane's A fragments hold tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3).
+      uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+      if (ntok < PA_BLOCK_SIZE || lb * PA_BLOCK_SIZE < p.num_sink) {
+        const int first = p.num_sink - lb * PA_BLOCK_SIZE;  // tokens below this are sinks
+        auto keep = [&](int r) { return r < ntok && r >= first; };
+        mlo = (keep(2 * tq) ? 0x0000FFFFu : 0u) | (keep(2 * tq + 1) ? 0xFFFF0000u : 0u);
+        mhi = (keep(2 * tq + 8) ? 0x0000FFFFu : 0u) | (keep(2 * tq + 9) ? 0xFFFF0000u : 0u);
+      }
+      const int tokB = (lane & 7) + (lane >> 4) * 8;
+      const int halfB = (lane >> 3) & 1;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        const int ch16 = (mt & 3) * 2 + halfB;
+        const uint32_t addr =
+            smem_u32(vbase + (mt >> 2) * kTileBytes + tokB * 128 + ((ch16 ^ (tokB & 7)) << 4));
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(addr, a0, a1, a2, a3);
+        mma_bf16(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
+      }
+    } else {
+      // int8 V: a transposed 8x8 load of 16-bit pairs gives each lane two d values of two
+      // tokens; output row m = t4 holds d = 16mt + 2t4 and row m = t4+8 holds d + 1.
+#pragma unroll
+      for (int mp = 0; mp < KT / 2; ++mp) {
+        const int ch16 = 2 * mp + (lane >> 4);
+        const uint32_t addr = smem_u32(vbase + tokA * 128 + ((ch16 ^ (tokA & 7)) << 4));
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(addr, r0, r1, r2, r3);
+        r0 ^= 0x80808080u;
+        r1 ^= 0x80808080u;
+        r2 ^= 0x80808080u;
+        r3 ^= 0x80808080u;
+        mma_f16(o[2 * mp], i8x2_to_f16x2(r0, 0x4240), i8x2_to_f16x2(r0, 0x4341),
+                i8x2_to_f16x2(r1, 0x4240), i8x2_to_f16x2(r1, 0x4341), b0, b1);
+        mma_f16(o[2 * mp + 1], i8x2_to_f16x2(r2, 0x4240), i8x2_to_f16x2(r2, 0x4341),
+                i8x2_to_f16x2(r3, 0x4240), i8x2_to_f16x2(r3, 0x4341), b0, b1);
+      }
+    }
+  }
+
+  // d index of accumulator element (mt, e): e = 0,1 -> row t4; e = 2,3 -> row t4 + 8.
+  __device__ __forceinline__ int dim_of(int mt, int upper) const {
+    if constexpr (QUANT) return mt * 16 + 2 * t4 + upper;
+    return mt * 16 + t4 + 8 * upper;
+  }
+
+  // Emit this warp's state for sequence s (global index).
+  __device__ void flush(int s, size_t slot, bool direct) {
+    float lt0 = l[0], lt1 = l[1];
+#pragma unroll
+    for (int mask = 4; mask <= 16; mask <<= 1) {
+      lt0 += __shfl_xor_sync(0xffffffffu, lt0, mask);
+      lt1 += __shfl_xor_sync(0xffffffffu, lt1, mask);
+    }
+    const int c0 = 2 * tq;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int c = c0 + half;
+      if (c >= p.G) continue;
+      const int hq = h_kv * p.G + c;
+      const float lt = half ? lt1 : lt0;
+      if (direct) {
+        const float inv = (bad || !(lt > 0.f)) ? 0.f : vsc / lt;
+        __nv_bfloat16* orow = p.out + (static_cast<size_t>(s) * p.H_q + hq) * D;
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          orow[dim_of(mt, 0)] = __float2bfloat16_rn(o[mt][half] * inv);
+          orow[dim_of(mt, 1)] = __float2bfloat16_rn(o[mt][2 + half] * inv);
+        }
+      } else {
+        float* row = p.partials + ((slot * p.nbs + j) * p.H_q + hq) * static_cast<size_t>(D + 4);
+        if (!bad && lt > 0.f) {
+#pragma unroll
+          for (int mt = 0; mt < KT; ++mt) {
+            row[dim_of(mt, 0)] = o[mt][half] * vsc;
+            row[dim_of(mt, 1)] = o[mt][2 + half] * vsc;
+          }
+        }
+        if (t4 == 0) {
+          row[D] = half ? m[1] : m[0];
+          row[D + 1] = bad ? -1.f : lt;
+        }
+      }
+    }
+  }
+
+  __device__ void flush_empty(size_t slot) {
+    if (t4 != 0) return;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int c = 2 * tq + half;
+      if (c >= p.G) continue;
+      float* row = p.partials + ((slot * p.nbs + j) * p.H_q + h_kv * p.G + c) * static_cast<size_t>(D + 4);
+      row[D] = kNegInf;
+      row[D + 1] = 0.f;
+    }
+  }
+};
+
+template <int D, bool QUANT>
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem sm = carve(smem_raw, p);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nthreads = blockDim.x;
+
+  // ---- this CTA's range [u0, u1) of the (sequence, logical block) list ----
+  int hgi, seq_base, nseq, u0, u1;
+  if (p.mode == 0) {
+    hgi = blockIdx.y;
+    seq_base = 0;
+    nseq = p.B;
+    const bool reporter = blockIdx.x == 0 && blockIdx.y == 0;
+    // exclusive scan of per-sequence block counts (every CTA computes it for itself)
+    const int per = (p.B + nthreads - 1) / nthreads;
+    const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
+    int local = 0;
+    for (int i = lo; i < hi; ++i) {
+      const int ctx = p.context_lens[i];
+      const int nb = seq_blocks(p, ctx);
+      if (nb < 0 && reporter) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
+      local += max(nb, 0);
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) sm.scratch[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0;
+      for (int w = 0; w < nthreads / 32; ++w) {
+        const int t = sm.scratch[w];
+        sm.scratch[w] = run;
+        run += t;
+      }
+      sm.cum[0] = 0;
+    }
+    __syncthreads();
+    int run = sm.scratch[warp] + incl - local;
+    for (int i = lo; i < hi; ++i) {
+      const int ctx = p.context_lens[i];
+      const int nb = seq_blocks(p, ctx);
+      run += max(nb, 0);
+      sm.cum[i + 1] = run;
+      sm.ctxs[i] = nb < 0 ? 0 : ctx;
+    }
+    __syncthreads();
+    const int T = sm.cum[p.B];
+    if (reporter) {
+      for (int i = tid; i <= p.B; i += nthreads) p.ws_meta[i] = sm.cum[i];
+      if (tid == 0) p.ws_meta[p.B + 1] = T;
+    }
+    if (T == 0) return;
+    const int W = (T + gridDim.x - 1) / gridDim.x;
+    u0 = blockIdx.x * W;
+    u1 = min(T, u0 + W);
+    if (u0 >= u1) return;
+  } else {
+    hgi = blockIdx.z;
+    seq_base = blockIdx.y;
+    nseq = 1;
+    const int ctx = p.context_lens[seq_base];
+    const int nb = seq_blocks(p, ctx);
+    if (nb < 0 && blockIdx.x == 0 && blockIdx.z == 0 && tid == 0) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
+    const int nbv = max(nb, 0);
+    if (tid == 0) {
+      sm.cum[0] = 0;
+      sm.cum[1] = nbv;
+      sm.ctxs[0] = nb < 0 ? 0 : ctx;
+    }
+    u0 = blockIdx.x * p.ppb;
+    u1 = min(nbv, u0 + p.ppb);
+    if (u0 >= u1) return;
+  }
+
+  if (tid == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], p.warps_c);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int S = p.stages, nbs = p.nbs;
+  if (warp == p.warps_c) {
+    // ------------------------------- producer -------------------------------
+    const int hgnc = p.hg * p.nc;
+    const int ops_per_block = 2 * hgnc;
+    const uint64_t policy = l2_evict_first_policy();
+    int k = 0;
+    bool ok = true;
+    for (int base = u0; base < u1 && ok; base += 32) {
+      const int u = base + lane;
+      int my_s = 0, my_lb = 0, my_pb = 0, my_nt = 0, my_bad = 0;
+      if (u < u1) {
+        my_s = find_seq(sm.cum, nseq, u);
+        my_lb = u - sm.cum[my_s];
+        my_nt = min(PA_BLOCK_SIZE, sm.ctxs[my_s] - my_lb * PA_BLOCK_SIZE);
+        my_pb = p.block_tables[static_cast<size_t>(seq_base + my_s) * p.max_blocks + my_lb];
+        my_bad = (my_pb < 0 || my_pb >= p.num_blocks) ? 1 : 0;
+        if (my_bad) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
+      }
+      const int n_here = min(32, u1 - base);
+      for (int i = 0; i < n_here; i += nbs, ++k) {
+        const int st = k % S;
+        const uint32_t ph = static_cast<uint32_t>(k / S) & 1u;
+        if (!mbar_wait(&sm.empty[st], ph ^ 1u)) {
+          if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
+          ok = false;
+          break;
+        }
+        uint32_t bytes = 0;
+        int pbs[8];
+        bool live[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          live[jj] = false;
+          pbs[jj] = 0;
+          if (jj < nbs) {
+            const int src = i + jj;  // < 32 because nbs divides 32
+            const int s_j = __shfl_sync(0xffffffffu, my_s, src);
+            const int lb_j = __shfl_sync(0xffffffffu, my_lb, src);
+            const int pb_j = __shfl_sync(0xffffffffu, my_pb, src);
+            const int nt_j = __shfl_sync(0xffffffffu, my_nt, src);
+            const int bad_j = __shfl_sync(0xffffffffu, my_bad, src);
+            const bool valid = src < n_here;
+            live[jj] = valid && !bad_j;
+            pbs[jj] = pb_j;
+            if (lane == 0) sm.meta[st * nbs + jj] = valid ? make_int4(s_j, lb_j, nt_j, bad_j) : make_int4(-1, 0, 0, 1);
+            if (live[jj]) bytes += ops_per_block * kTileBytes;
+          }
+        }
+        if (lane == 0) {
+          if (bytes) mbar_arrive_expect_tx(&sm.full[st], bytes);
+          else mbar_arrive(&sm.full[st]);
+        }
+        __syncwarp();
+        uint8_t* stage = sm.stages + static_cast<size_t>(st) * p.stage_bytes;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (jj < nbs && live[jj]) {
+            for (int o = lane; o < ops_per_block; o += 32) {
+              const int tensor = o / hgnc;
+              const int hc = o - tensor * hgnc;
+              tma_load_3d(stage + ((jj * 2 + tensor) * hgnc + hc) * kTileBytes, tensor ? &tmV : &tmK,
+                          &sm.full[st], 0, hgi * hgnc + hc, pbs[jj] * PA_BLOCK_SIZE, policy);
+            }
+          }
+        }
+      }
+    }
+    // do not leave while a copy into this CTA's shared memory may still be in flight
+    for (int st = 0; st < S && st < k; ++st) {
+      const int last = st + S * ((k - 1 - st) / S);
+      if (!mbar_wait(&sm.full[st], static_cast<uint32_t>(last / S) & 1u)) {
+        if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
+      }
+    }
+    return;
+  }
+  if (warp > p.warps_c) return;
+
+  // ------------------------------- consumers -------------------------------
+  const int j = warp / p.hg;
+  const int h_loc = warp - j * p.hg;
+  Consumer<D, QUANT> c(p, lane, hgi * p.hg + h_loc, j);
+  const int s_first = find_seq(sm.cum, nseq, u0);
+  const int s_last = find_seq(sm.cum, nseq, u1 - 1);
+  const int n_iters = (u1 - u0 + nbs - 1) / nbs;
+  const int cta = blockIdx.x;
+  auto slot_of = [&](int s_rel) -> size_t {
+    const int s = seq_base + s_rel;
+    return p.mode == 0 ? static_cast<size_t>(s + cta) : static_cast<size_t>(s) * p.max_parts + cta;
+  };
+  auto covers = [&](int s_rel) -> bool { return sm.cum[s_rel] >= u0 && sm.cum[s_rel + 1] <= u1; };
+  int cur = s_first;
+  bool q_loaded = false;
+  const size_t kofs = static_cast<size_t>((j * 2 + 0) * p.hg * p.nc + h_loc * p.nc) * kTileBytes;
+  const size_t vofs = static_cast<size_t>((j * 2 + 1) * p.hg * p.nc + h_loc * p.nc) * kTileBytes;
+  for (int k = 0; k < n_iters; ++k) {
+    const int st = k % S;
+    const uint32_t ph = static_cast<uint32_t>(k / S) & 1u;
+    if (!mbar_wait(&sm.full[st], ph)) {
+      if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
+      return;
+    }
+    const int u = u0 + k * nbs + j;
+    if (u < u1) {
+      const int4 mt = sm.meta[st * nbs + j];
+      if (mt.x != cur) {
+        c.flush(seq_base + cur, slot_of(cur), p.direct_ok && covers(cur));
+        for (int s = cur + 1; s < mt.x; ++s) c.flush_empty(slot_of(s));
+        cur = mt.x;
+        c.reset();
+        q_loaded = false;
+      }
+      if (!q_loaded) {
+        c.load_q(seq_base + cur);
+        q_loaded = true;
+      }
+      if (mt.w) {
+        c.bad = true;
+      } else {
+        const uint8_t* stage = sm.stages + static_cast<size_t>(st) * p.stage_bytes;
+        c.block(stage + kofs, stage + vofs, mt.y, mt.z);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[st]);
+  }
+  c.flush(seq_base + cur, slot_of(cur), p.direct_ok && covers(cur) && q_loaded);
+  for (int s = cur + 1; s <= s_last; ++s) c.flush_empty(slot_of(s));
+}
+
+// ------------------------------------------------------------------------------------
+// Merge: out = Σ_p e^{m_p - M} o_p / Σ_p e^{m_p - M} l_p (plus the bf16 sink tokens).
+// One warp per (sequence, query head).
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int grid_x) {
+  constexpr int E = D / 32;  // dims per lane
+  const int s = blockIdx.x;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (h >= p.H_q) return;
+  const int h_kv = h / p.G;
+  const int ctx = p.context_lens[s];
+  const int nb = seq_blocks(p, ctx);
+  __nv_bfloat16* orow = p.out + (static_cast<size_t>(s) * p.H_q + h) * D;
+
+  int c_first = 0, c_last = -1;
+  if (nb > 0) {
+    if (p.mode == 0) {
+      const int cs = p.ws_meta[s], ce = p.ws_meta[s + 1], T = p.ws_meta[p.B + 1];
+      const int W = (T + grid_x - 1) / grid_x;
+      c_first = cs / W;
+      c_last = (ce - 1) / W;
+    } else {
+      c_last = (nb + p.ppb - 1) / p.ppb - 1;
+    }
+    if (p.direct_ok && c_first == c_last) return;  // the main kernel wrote this row
+  }
+  const int n_sink = nb < 0 ? 0 : min(p.num_sink, ctx);
+  auto slot_of = [&](int c) -> size_t {
+    return p.mode == 0 ? static_cast<size_t>(s + c) : static_cast<size_t>(s) * p.max_parts + c;
+  };
+  const int n_parts = (c_last - c_first + 1) * p.nbs;
+
+  float M = kNegInf;
+  bool bad = false;
+  for (int i = lane; i < n_parts; i += 32) {
+    const int c = c_first + i / p.nbs, jj = i % p.nbs;
+    const float* row = p.partials + ((slot_of(c) * p.nbs + jj) * p.H_q + h) * static_cast<size_t>(D + 4);
+    const float lv = row[D + 1];
+    if (lv < 0.f) bad = true;
+    else if (lv > 0.f) M = fmaxf(M, row[D]);
+  }
+#pragma unroll
+  for (int mask = 1; mask < 32; mask <<= 1) M = warp_max_xor(M, mask);
+  bad = __any_sync(0xffffffffu, bad);
+
+  float qv[E];
+  if (n_sink > 0) {
+    const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(s) * p.H_q + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) qv[e] = __bfloat162float(qrow[e]);
+  }
+  auto sink_score = [&](int t) -> float {
+    const __nv_bfloat16* krow =
+        p.k_sink + ((static_cast<size_t>(s) * p.num_sink + t) * p.H_kv + h_kv) * D + lane * E;
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dot += qv[e] * __bfloat162float(krow[e]);
+#pragma unroll
+    for (int mask = 1; mask < 32; mask <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, mask);
+    return dot * p.scale_log2;
+  };
+  for (int t = 0; t < n_sink; ++t) M = fmaxf(M, sink_score(t));
+
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  if (!bad && nb > 0) {
+    for (int i = 0; i < n_parts; ++i) {
+      const int c = c_first + i / p.nbs, jj = i % p.nbs;
+      const float* row = p.partials + ((slot_of(c) * p.nbs + jj) * p.H_q + h) * static_cast<size_t>(D + 4);
+      const float lv = row[D + 1];
+      if (lv > 0.f) {
+        const float w = ex2(row[D] - M);
+        L += w * lv;
+        if constexpr (E == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(row + lane * 4);
+          acc[0] += w * v.x;
+          acc[1] += w * v.y;
+          acc[2] += w * v.z;
+          acc[3] += w * v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(row + lane * 2);
+          acc[0] += w * v.x;
+          acc[1] += w * v.y;
+        }
+      }
+    }
+    for (int t = 0; t < n_sink; ++t) {
+      const float w = ex2(sink_score(t) - M);
+      L += w;
+      const __nv_bfloat16* vrow =
+          p.v_sink + ((static_cast<size_t>(s) * p.num_sink + t) * p.H_kv + h_kv) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += w * __bfloat162float(vrow[e]);
+    }
+  }
+  const float inv = (bad || !(L > 0.f)) ? 0.f : 1.f / L;
+#pragma unroll
+  for (int e = 0; e < E; ++e) orow[lane * E + e] = __float2bfloat16_rn(acc[e] * inv);
+}
+
+// ------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------
+struct Plan {
+  int hg, n_hg, nc, nbs, warps_c, threads, stages;
+  int mode, ppb, max_parts, grid_x;
+  int stage_bytes;
+  size_t smem_bytes, meta_bytes, ws_bytes, n_slots;
+};
+
+int num_sms_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Plan* pl) {
+  pa_status st = validate_desc(d);
+  if (st != PA_OK) return st;
+  if (max_ctx < 0 || partition_size < 0 || partition_size % PA_BLOCK_SIZE != 0) return PA_ERR_INVALID_ARG;
+  const int e = dtype_bytes(d->k_dtype);
+  const int row_bytes = d->head_dim * e;  // 128 or 256
+  pl->nc = row_bytes / 128;
+  int hg = 1;
+  for (int c = 1; c <= d->num_kv_heads; ++c)
+    if (d->num_kv_heads % c == 0 && c * row_bytes <= 2048) hg = c;
+  pl->hg = hg;
+  pl->n_hg = d->num_kv_heads / hg;
+  pl->nbs = std::max(1, 8 / hg);
+  pl->warps_c = hg * pl->nbs;
+  if (pl->warps_c > kMaxConsumerWarps) return PA_ERR_UNSUPPORTED;
+  pl->threads = (pl->warps_c + 1) * 32;
+  pl->stage_bytes = pl->nbs * 2 * hg * pl->nc * kTileBytes;
+  const int B = d->num_seqs;
+  if (B > 65535) return PA_ERR_UNSUPPORTED;  // grid.y of the fixed-partition launch
+  if (partition_size == 0 && B <= kAutoMaxSeqs) {
+    pl->mode = 0;
+    pl->ppb = 0;
+    pl->max_parts = 0;
+    pl->grid_x = num_sms_current();
+    if (pl->grid_x <= 0) return PA_ERR_CUDA;
+    pl->n_slots = static_cast<size_t>(B) + pl->grid_x;
+    pl->meta_bytes = ((static_cast<size_t>(B) + 2) * 4 + 255) / 256 * 256;
+  } else {
+    const int part = partition_size ? partition_size : kFixedFallbackPartition;
+    pl->mode = 1;
+    pl->ppb = part / PA_BLOCK_SIZE;
+    const int max_blk = (max_ctx + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+    pl->max_parts = std::max(1, (max_blk + pl->ppb - 1) / pl->ppb);
+    pl->grid_x = pl->max_parts;
+    pl->n_slots = static_cast<size_t>(B) * pl->max_parts;
+    pl->meta_bytes = 256;
+  }
+  const size_t cum_ints = pl->mode == 0 ? (2 * static_cast<size_t>(B) + 1) : 3;
+  const size_t fixed_bytes = 1024 + (cum_ints + 32) * 4;
+  const size_t per_stage = pl->stage_bytes + 16 + static_cast<size_t>(pl->nbs) * 16;
+  if (fixed_bytes + 2 * per_stage > static_cast<size_t>(kSmemLimit)) return PA_ERR_UNSUPPORTED;
+  pl->stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - fixed_bytes) / per_stage));
+  pl->smem_bytes = fixed_bytes + pl->stages * per_stage;
+  const size_t partial_bytes =
+      pl->n_slots * pl->nbs * static_cast<size_t>(d->num_q_heads) * (d->head_dim + 4) * sizeof(float);
+  pl->ws_bytes = pl->meta_bytes + partial_bytes;
+  return PA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// The cache as a 3-D tensor: (128-byte row chunk, kv_head x chunk, slot).  One box is one
+// (head, chunk) row of 16 consecutive slots, i.e. of one physical block.
+bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int rows, long long slots) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / elem_bytes), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(slots)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(rows) * 128};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 1, PA_BLOCK_SIZE};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool QUANT>
+pa_status launch(const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p,
+                 cudaStream_t stream) {
+  auto kern = decode_kernel<D, QUANT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(pl.smem_bytes)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const dim3 grid = p.mode == 0 ? dim3(pl.grid_x, pl.n_hg, 1) : dim3(pl.max_parts, p.B, pl.n_hg);
+  kern<<<grid, pl.threads, pl.smem_bytes, stream>>>(mk, mv, p);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  merge_kernel<D><<<dim3(p.B, (p.H_q + 3) / 4), 128, 0, stream>>>(p, pl.grid_x);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" size_t pa_decode_workspace_size(const pa_cache_desc* desc, int max_context_len,
+                                           int partition_size) {
+  pa::Plan pl;
+  if (pa::make_plan(desc, max_context_len, partition_size, &pl) != PA_OK) return 0;
+  return pl.ws_bytes;
+}
+
+extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, const void* q,
+                                         const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         int max_context_len, float scale, int partition_size,
+                                         void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                         void* stream) {
+  pa::Plan pl;
+  pa_status st = pa::make_plan(desc, max_context_len, partition_size, &pl);
+  if (st != PA_OK) return st;
+  if (desc->num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+    return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+       reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u)
+    return PA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < pl.ws_bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+
+  const int e = pa::dtype_bytes(desc->k_dtype);
+  const long long slots = static_cast<long long>(desc->num_blocks) * PA_BLOCK_SIZE;
+  CUtensorMap mk, mv;
+  if (!pa::encode_cache_map(&mk, k_cache, e, desc->num_kv_heads * pl.nc, slots) ||
+      !pa::encode_cache_map(&mv, v_cache, e, desc->num_kv_heads * pl.nc, slots))
+    return PA_ERR_CUDA;
+
+  pa::DecodeParams p;
+  p.B = desc->num_seqs;
+  p.H_q = desc->num_q_heads;
+  p.H_kv = desc->num_kv_heads;
+  p.G = desc->num_q_heads / desc->num_kv_heads;
+  p.num_blocks = desc->num_blocks;
+  p.max_blocks = desc->max_blocks_per_seq;
+  p.num_sink = desc->num_sink;
+  p.max_ctx = max_context_len;
+  p.hg = pl.hg;
+  p.nc = pl.nc;
+  p.nbs = pl.nbs;
+  p.stages = pl.stages;
+  p.warps_c = pl.warps_c;
+  p.mode = pl.mode;
+  p.ppb = pl.ppb;
+  p.max_parts = pl.max_parts;
+  p.direct_ok = (pl.nbs == 1 && desc->num_sink == 0) ? 1 : 0;
+  p.stage_bytes = pl.stage_bytes;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.k_scales = desc->k_scales;
+  p.v_scales = desc->v_scales;
+  p.k_sink = static_cast<const __nv_bfloat16*>(desc->k_sink);
+  p.v_sink = static_cast<const __nv_bfloat16*>(desc->v_sink);
+  p.ws_meta = static_cast<int32_t*>(workspace);
+  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.meta_bytes);
+  p.err = err_flag;
+
+  cudaStream_t s = pa::as_stream(stream);
+  const bool quant = pa::is_quantized(desc);
+  if (desc->head_dim == 128)
+    return quant ? pa::launch<128, true>(pl, mk, mv, p, s) : pa::launch<128, false>(pl, mk, mv, p, s);
+  return pa::launch<64, false>(pl, mk, mv, p, s);
+}

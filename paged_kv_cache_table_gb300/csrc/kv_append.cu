@@ -1,0 +1,184 @@
+// Append: write each new token's K and V rows into its paged slot.
+//
+// untitled KV-cache article at ldpk.cn/news/58971 §2.3: every generated token's K and V are
+// written at the sequence's current length.  "KV Cache 的显存账本：PagedAttention 与连续批处理"
+// §四: the slot is table[pos / 16] * 16 + pos % 16 (the locate() sketch).  Same page §七:
+// 8-bit caches hold K as FP8 and V as INT8 with one scale per KV head, and sink tokens keep
+// their original precision.
+//
+// One CTA per appended row; each thread moves 8 elements (one 16-byte bf16 vector).  The
+// row's kv_heads x head_dim elements are contiguous in the slot-major cache, so the stores
+// are fully coalesced.
+
+#include <cuda_fp8.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+struct AppendParams {
+  int num_rows, num_seqs, H_kv, D, num_blocks, max_blocks, num_sink;
+  const int32_t* token_seq;  // NULL: row r belongs to sequence r
+  const int32_t* positions;
+  const int32_t* block_tables;
+  const uint4* k_new;
+  const uint4* v_new;
+  void* k_cache;
+  void* v_cache;
+  const float* k_scales;
+  const float* v_scales;
+  uint4* k_sink;
+  uint4* v_sink;
+  int32_t* err;
+};
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&x)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// x / scale in IEEE fp32, then FP8 E4M3 round-to-nearest-even with saturation.
+__device__ __forceinline__ uint2 encode_e4m3x8(const uint4& v, float scale) {
+  float x[8];
+  unpack_bf16x8(v, x);
+  uint32_t out[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 e = make_float2(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
+    const uint32_t two = __nv_cvt_float2_to_fp8x2(e, __NV_SATFINITE, __NV_E4M3);
+    out[i / 2] |= (two & 0xFFFFu) << (16 * (i % 2));
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+// x / scale in IEEE fp32, round half to even, clamp to [-127, 127].
+__device__ __forceinline__ uint2 encode_int8x8(const uint4& v, float scale) {
+  float x[8];
+  unpack_bf16x8(v, x);
+  uint32_t out[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    int q = __float2int_rn(__fdiv_rn(x[i], scale));
+    q = max(-127, min(127, q));
+    out[i / 4] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i % 4));
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+template <bool QUANT>
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  const int r = blockIdx.x;
+  const int s = p.token_seq ? p.token_seq[r] : r;
+  if (s < 0 || s >= p.num_seqs) {
+    if (threadIdx.x == 0) set_error(p.err, PA_EFLAG_BAD_SEQ);
+    return;
+  }
+  const int pos = p.positions[r];
+  if (pos < 0) return;  // padding row
+  const int vecs = p.H_kv * p.D / 8;  // 16-byte bf16 vectors per row
+  const uint4* kin = p.k_new + static_cast<size_t>(r) * vecs;
+  const uint4* vin = p.v_new + static_cast<size_t>(r) * vecs;
+
+  if (pos < p.num_sink) {  // sink rows keep bf16 in their own buffer
+    const size_t base = (static_cast<size_t>(s) * p.num_sink + pos) * vecs;
+    for (int i = threadIdx.x; i < vecs; i += blockDim.x) {
+      p.k_sink[base + i] = kin[i];
+      p.v_sink[base + i] = vin[i];
+    }
+    return;
+  }
+  const int lb = pos / PA_BLOCK_SIZE;
+  if (lb >= p.max_blocks) {
+    if (threadIdx.x == 0) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
+    return;
+  }
+  const int pb = p.block_tables[static_cast<size_t>(s) * p.max_blocks + lb];
+  if (pb < 0 || pb >= p.num_blocks) {
+    if (threadIdx.x == 0) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
+    return;
+  }
+  const size_t slot = static_cast<size_t>(pb) * PA_BLOCK_SIZE + pos % PA_BLOCK_SIZE;
+  for (int i = threadIdx.x; i < vecs; i += blockDim.x) {
+    const uint4 kv = kin[i];
+    const uint4 vv = vin[i];
+    if constexpr (QUANT) {
+      const int h = (i * 8) / p.D;
+      reinterpret_cast<uint2*>(p.k_cache)[slot * vecs + i] = encode_e4m3x8(kv, p.k_scales[h]);
+      reinterpret_cast<uint2*>(p.v_cache)[slot * vecs + i] = encode_int8x8(vv, p.v_scales[h]);
+    } else {
+      reinterpret_cast<uint4*>(p.k_cache)[slot * vecs + i] = kv;
+      reinterpret_cast<uint4*>(p.v_cache)[slot * vecs + i] = vv;
+    }
+  }
+}
+
+pa_status append_impl(const pa_cache_desc* d, void* k_cache, void* v_cache, const void* k_new,
+                      const void* v_new, int num_rows, const int32_t* token_seq,
+                      const int32_t* positions, const int32_t* block_tables, int32_t* err,
+                      void* stream) {
+  pa_status st = validate_desc(d);
+  if (st != PA_OK) return st;
+  if (num_rows < 0) return PA_ERR_INVALID_ARG;
+  if (num_rows == 0) return PA_OK;
+  if (!k_cache || !v_cache || !k_new || !v_new || !positions || !block_tables)
+    return PA_ERR_INVALID_ARG;
+  const auto aligned16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (d->num_sink > 0 && (!aligned16(d->k_sink) || !aligned16(d->v_sink))))
+    return PA_ERR_INVALID_ARG;
+  AppendParams p;
+  p.num_rows = num_rows;
+  p.num_seqs = d->num_seqs;
+  p.H_kv = d->num_kv_heads;
+  p.D = d->head_dim;
+  p.num_blocks = d->num_blocks;
+  p.max_blocks = d->max_blocks_per_seq;
+  p.num_sink = d->num_sink;
+  p.token_seq = token_seq;
+  p.positions = positions;
+  p.block_tables = block_tables;
+  p.k_new = static_cast<const uint4*>(k_new);
+  p.v_new = static_cast<const uint4*>(v_new);
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scales = d->k_scales;
+  p.v_scales = d->v_scales;
+  p.k_sink = static_cast<uint4*>(d->k_sink);
+  p.v_sink = static_cast<uint4*>(d->v_sink);
+  p.err = err;
+  const int vecs = p.H_kv * p.D / 8;
+  const int threads = min(256, ((vecs + 31) / 32) * 32);
+  if (is_quantized(d))
+    kv_append_kernel<true><<<num_rows, threads, 0, as_stream(stream)>>>(p);
+  else
+    kv_append_kernel<false><<<num_rows, threads, 0, as_stream(stream)>>>(p);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_kv_append(const pa_cache_desc* desc, void* k_cache, void* v_cache,
+                                  const void* k_new, const void* v_new,
+                                  const int32_t* block_tables, const int32_t* positions,
+                                  int32_t* err_flag, void* stream) {
+  if (!desc) return PA_ERR_INVALID_ARG;
+  return pa::append_impl(desc, k_cache, v_cache, k_new, v_new, desc->num_seqs, nullptr, positions,
+                         block_tables, err_flag, stream);
+}
+
+extern "C" pa_status pa_kv_append_tokens(const pa_cache_desc* desc, void* k_cache, void* v_cache,
+                                         const void* k_new, const void* v_new, int num_tokens,
+                                         const int32_t* token_seq, const int32_t* token_pos,
+                                         const int32_t* block_tables, int32_t* err_flag,
+                                         void* stream) {
+  if (!desc || !token_seq) return PA_ERR_INVALID_ARG;
+  return pa::append_impl(desc, k_cache, v_cache, k_new, v_new, num_tokens, token_seq, token_pos,
+                         block_tables, err_flag, stream);
+}

@@ -1,0 +1,266 @@
+"""ctypes binding of the C ABI in ``include/pa.h`` (argument marshalling only).
+
+Every function keeps the C name and argument order.  Tensors are passed as raw device
+pointers (``tensor.data_ptr()``); plain ints are accepted as pointers too.  A non-OK status
+raises :class:`PaError` (its ``status`` attribute holds the code).  There is no fallback: if
+the shared library has not been built, loading it raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB_PATH
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_WORKSPACE_TOO_SMALL = 3
+PA_ERR_CUDA = 4
+PA_ERR_OUT_OF_BLOCKS = 5
+
+PA_BF16 = 0
+PA_FP8_E4M3 = 1
+PA_INT8 = 2
+
+PA_EFLAG_BAD_BLOCK_ID = 1
+PA_EFLAG_CTX_OVERFLOW = 2
+PA_EFLAG_BAD_SEQ = 4
+PA_EFLAG_TIMEOUT = 8
+
+BLOCK_SIZE = 16
+
+_DTYPES = {"bf16": PA_BF16, "fp8_e4m3": PA_FP8_E4M3, "e4m3": PA_FP8_E4M3, "int8": PA_INT8}
+
+# Every symbol the header declares, for load checks.
+EXPORTED = [
+    "pa_status_string", "pa_kv_append", "pa_kv_append_tokens", "pa_block_copy",
+    "pa_decode_workspace_size", "pa_decode_attention",
+    "pa_bm_create", "pa_bm_destroy", "pa_bm_alloc", "pa_bm_claim", "pa_bm_incref", "pa_bm_decref",
+    "pa_bm_refcount", "pa_bm_num_free", "pa_bm_fork", "pa_bm_release", "pa_bm_prepare_step",
+]
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", ctypes.c_int),
+        ("num_q_heads", ctypes.c_int),
+        ("num_kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("block_size", ctypes.c_int),
+        ("num_blocks", ctypes.c_int),
+        ("max_blocks_per_seq", ctypes.c_int),
+        ("k_dtype", ctypes.c_int),
+        ("v_dtype", ctypes.c_int),
+        ("k_scales", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+        ("k_sink", ctypes.c_void_p),
+        ("v_sink", ctypes.c_void_p),
+        ("num_sink", ctypes.c_int),
+    ]
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (loaded once).  Raises if it was never built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with paged_kv_cache_table_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32p, c_int = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_int
+        dp = ctypes.POINTER(CacheDesc)
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_status_string.argtypes = [c_int]
+        L.pa_kv_append.restype = c_int
+        L.pa_kv_append.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.pa_kv_append_tokens.restype = c_int
+        L.pa_kv_append_tokens.argtypes = [dp, vp, vp, vp, vp, c_int, vp, vp, vp, vp, vp]
+        L.pa_block_copy.restype = c_int
+        L.pa_block_copy.argtypes = [dp, vp, vp, vp, c_int, vp, vp]
+        L.pa_decode_workspace_size.restype = ctypes.c_size_t
+        L.pa_decode_workspace_size.argtypes = [dp, c_int, c_int]
+        L.pa_decode_attention.restype = c_int
+        L.pa_decode_attention.argtypes = [dp, vp, vp, vp, vp, vp, vp, c_int, ctypes.c_float, c_int, vp,
+                                          ctypes.c_size_t, vp, vp]
+        L.pa_bm_create.restype = vp
+        L.pa_bm_create.argtypes = [c_int, c_int]
+        L.pa_bm_destroy.restype = None
+        L.pa_bm_destroy.argtypes = [vp]
+        for name in ("pa_bm_alloc", "pa_bm_num_free"):
+            getattr(L, name).restype = c_int
+        L.pa_bm_alloc.argtypes = [vp]
+        L.pa_bm_num_free.argtypes = [vp]
+        for name in ("pa_bm_claim", "pa_bm_incref", "pa_bm_decref", "pa_bm_refcount"):
+            getattr(L, name).restype = c_int
+            getattr(L, name).argtypes = [vp, c_int]
+        L.pa_bm_fork.restype = c_int
+        L.pa_bm_fork.argtypes = [vp, i32p, i32p, c_int]
+        L.pa_bm_release.restype = c_int
+        L.pa_bm_release.argtypes = [vp, i32p, c_int]
+        L.pa_bm_prepare_step.restype = c_int
+        L.pa_bm_prepare_step.argtypes = [vp, i32p, c_int, c_int, i32p, i32p, ctypes.POINTER(c_int),
+                                         ctypes.POINTER(c_int)]
+        _LIB = L
+    return _LIB
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+pa_status_string = status_string
+
+
+def _check(status: int, where: str):
+    if status != PA_OK:
+        raise PaError(status, where)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_desc(num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq,
+              k_dtype="bf16", v_dtype="bf16", k_scales=None, v_scales=None,
+              k_sink=None, v_sink=None, num_sink=0, block_size=BLOCK_SIZE) -> CacheDesc:
+    """Fill a pa_cache_desc.  Tensors passed here must outlive every call that uses it."""
+    return CacheDesc(int(num_seqs), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
+                     int(num_blocks), int(max_blocks_per_seq), _DTYPES.get(k_dtype, k_dtype),
+                     _DTYPES.get(v_dtype, v_dtype), _ptr(k_scales), _ptr(v_scales), _ptr(k_sink),
+                     _ptr(v_sink), int(num_sink))
+
+
+def pa_kv_append(desc, k_cache, v_cache, k_new, v_new, block_tables, positions, err_flag=None, stream=None):
+    _check(lib().pa_kv_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                              _ptr(block_tables), _ptr(positions), _ptr(err_flag), _stream(stream)),
+           "pa_kv_append")
+
+
+def pa_kv_append_tokens(desc, k_cache, v_cache, k_new, v_new, num_tokens, token_seq, token_pos,
+                        block_tables, err_flag=None, stream=None):
+    _check(lib().pa_kv_append_tokens(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(k_new),
+                                     _ptr(v_new), int(num_tokens), _ptr(token_seq), _ptr(token_pos),
+                                     _ptr(block_tables), _ptr(err_flag), _stream(stream)),
+           "pa_kv_append_tokens")
+
+
+def pa_block_copy(desc, k_cache, v_cache, src_dst_pairs, n_pairs, err_flag=None, stream=None):
+    _check(lib().pa_block_copy(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs),
+                               int(n_pairs), _ptr(err_flag), _stream(stream)), "pa_block_copy")
+
+
+def pa_decode_workspace_size(desc, max_context_len, partition_size=0) -> int:
+    return int(lib().pa_decode_workspace_size(ctypes.byref(desc), int(max_context_len), int(partition_size)))
+
+
+def pa_decode_attention(desc, out, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                        scale, partition_size, workspace, workspace_bytes=None, err_flag=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_attention(ctypes.byref(desc), _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(block_tables), _ptr(context_lens), int(max_context_len),
+                                     float(scale), int(partition_size), _ptr(workspace),
+                                     int(workspace_bytes), _ptr(err_flag), _stream(stream)),
+           "pa_decode_attention")
+
+
+def _i32(a) -> np.ndarray:
+    if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+        raise TypeError("expected a C-contiguous int32 numpy array (it is modified in place)")
+    return a
+
+
+def _p32(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+class BlockManager:
+    """The host block pool (pa_bm_*): free list, reference counts, copy-on-write decisions."""
+
+    def __init__(self, num_blocks: int, block_size: int = BLOCK_SIZE):
+        h = lib().pa_bm_create(int(num_blocks), int(block_size))
+        if not h:
+            raise PaError(PA_ERR_INVALID_ARG, "pa_bm_create")
+        self._h = ctypes.c_void_p(h)
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self) -> int:
+        return lib().pa_bm_alloc(self._h)
+
+    def claim(self, blk: int) -> bool:
+        return lib().pa_bm_claim(self._h, int(blk)) == 0
+
+    def incref(self, blk: int) -> int:
+        return lib().pa_bm_incref(self._h, int(blk))
+
+    def decref(self, blk: int) -> int:
+        return lib().pa_bm_decref(self._h, int(blk))
+
+    def refcount(self, blk: int) -> int:
+        return lib().pa_bm_refcount(self._h, int(blk))
+
+    def num_free(self) -> int:
+        return lib().pa_bm_num_free(self._h)
+
+    def fork(self, src_row: np.ndarray, n_blocks: int, dst_row: np.ndarray | None = None) -> np.ndarray:
+        src = _i32(np.ascontiguousarray(src_row, dtype=np.int32))
+        dst = np.full(len(src), -1, dtype=np.int32) if dst_row is None else _i32(dst_row)
+        _check(lib().pa_bm_fork(self._h, _p32(src), _p32(dst), int(n_blocks)), "pa_bm_fork")
+        return dst
+
+    def release(self, row: np.ndarray, n_blocks: int) -> int:
+        r = lib().pa_bm_release(self._h, _p32(_i32(row)), int(n_blocks))
+        if r < 0:
+            raise PaError(PA_ERR_INVALID_ARG, "pa_bm_release")
+        return r
+
+    def prepare_step(self, block_tables: np.ndarray, positions: np.ndarray):
+        """Make every sequence's append slot writable; returns (pairs [n][2], n_changed).
+        ``block_tables`` (int32 [B][max_blocks]) is updated in place."""
+        bt = _i32(block_tables)
+        pos = _i32(np.ascontiguousarray(positions, dtype=np.int32))
+        B, M = bt.shape
+        pairs = np.empty((max(B, 1), 2), dtype=np.int32)
+        n_pairs = ctypes.c_int(0)
+        n_changed = ctypes.c_int(0)
+        st = lib().pa_bm_prepare_step(self._h, _p32(bt), B, M, _p32(pos), _p32(pairs),
+                                      ctypes.byref(n_pairs), ctypes.byref(n_changed))
+        _check(st, "pa_bm_prepare_step")
+        return pairs[:n_pairs.value].copy(), n_changed.value

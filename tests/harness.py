@@ -1,0 +1,259 @@
+"""Test infrastructure: build the same decode state twice — once on the GPU through the C ABI,
+once in the CPU oracle — from one seeded workload, and compare.
+
+The GPU side calls only the library (block manager, bulk append, block copy, append, decode
+attention).  The oracle side calls only ``oracle``.  They share nothing but the workload's
+random inputs.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+import paged_kv_cache_table_gb300 as P
+from paged_kv_cache_table_gb300.workloads import Workload, bf16_bits
+
+# Fill patterns for never-written slots: NaN in bf16 pools (0x7FC0) and in e4m3 K pools
+# (0x7F); -128 in int8 V pools (outside the encoder's range).  Attention must never let them
+# reach the output.
+BF16_NAN = 0x7FC0
+E4M3_NAN = 0x7F
+INT8_OUTSIDE = 0x80
+
+ATOL_MAX = 2e-2   # attention: max |gpu - oracle|
+ATOL_MEAN = 2e-3  # attention: mean |gpu - oracle|
+
+
+def _refcounts_from_tables(w: Workload):
+    blocks, counts = np.unique(w.tables[w.tables >= 0], return_counts=True)
+    extra = 1 if w.prefix else 0  # the cached prefix itself holds one reference
+    return blocks, counts + extra
+
+
+class GpuState:
+    """One layer's paged cache on the GPU, driven only through the C ABI."""
+
+    def __init__(self, w: Workload, device="cuda", fill=True):
+        self.w = w
+        self.dev = device
+        n_slots = w.num_blocks * 16
+        shape = (n_slots, w.H_kv, w.D)
+        if w.k_dtype == "bf16":
+            self.k = torch.full(shape, BF16_NAN, dtype=torch.int16, device=device).view(torch.bfloat16)
+            self.v = torch.full(shape, BF16_NAN, dtype=torch.int16, device=device).view(torch.bfloat16)
+        else:
+            self.k = torch.full(shape, E4M3_NAN, dtype=torch.uint8, device=device)
+            self.v = torch.full(shape, INT8_OUTSIDE, dtype=torch.uint8, device=device)
+        self.k_scales = None if w.k_scales is None else w.k_scales.to(device)
+        self.v_scales = None if w.v_scales is None else w.v_scales.to(device)
+        self.k_sink = self.v_sink = None
+        if w.num_sink:
+            sshape = (w.B, w.num_sink, w.H_kv, w.D)
+            self.k_sink = torch.full(sshape, BF16_NAN, dtype=torch.int16, device=device).view(torch.bfloat16)
+            self.v_sink = torch.full(sshape, BF16_NAN, dtype=torch.int16, device=device).view(torch.bfloat16)
+        self.desc = P.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks, w.k_dtype, w.v_dtype,
+                                self.k_scales, self.v_scales, self.k_sink, self.v_sink, w.num_sink)
+        self.tables = w.tables.copy()
+        self.tables_dev = torch.from_numpy(self.tables).to(device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.bm = P.BlockManager(w.num_blocks)
+        blocks, counts = _refcounts_from_tables(w)
+        for b, c in zip(blocks, counts):
+            assert self.bm.claim(int(b))
+            for _ in range(int(c) - 1):
+                self.bm.incref(int(b))
+        if fill:
+            self.bulk_append(w.fill_k, w.fill_v, w.fill_seq, w.fill_pos)
+
+    def bulk_append(self, k, v, seq, pos):
+        n = len(seq)
+        if n == 0:
+            return
+        P.pa_kv_append_tokens(self.desc, self.k, self.v, k.to(self.dev), v.to(self.dev), n,
+                              torch.from_numpy(np.ascontiguousarray(seq, dtype=np.int32)).to(self.dev),
+                              torch.from_numpy(np.ascontiguousarray(pos, dtype=np.int32)).to(self.dev),
+                              self.tables_dev, self.err)
+
+    def prepare(self, positions):
+        pairs, _ = self.bm.prepare_step(self.tables, np.ascontiguousarray(positions, dtype=np.int32))
+        self.tables_dev.copy_(torch.from_numpy(self.tables))
+        if len(pairs):
+            P.pa_block_copy(self.desc, self.k, self.v, torch.from_numpy(pairs).to(self.dev), len(pairs), self.err)
+        return pairs
+
+    def append(self, k_new, v_new, positions):
+        P.pa_kv_append(self.desc, self.k, self.v, k_new.to(self.dev), v_new.to(self.dev), self.tables_dev,
+                       torch.from_numpy(np.ascontiguousarray(positions, dtype=np.int32)).to(self.dev), self.err)
+
+    def attend(self, q, context_lens, partition=0, max_ctx=None):
+        w = self.w
+        ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+        max_ctx = int(ctx.max()) if max_ctx is None else int(max_ctx)
+        out = torch.full((w.B, w.H_q, w.D), float("nan"), dtype=torch.bfloat16, device=self.dev)
+        nbytes = P.pa_decode_workspace_size(self.desc, max_ctx, partition)
+        assert nbytes > 0
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+        P.pa_decode_attention(self.desc, out, q.to(self.dev), self.k, self.v, self.tables_dev,
+                              torch.from_numpy(ctx).to(self.dev), max_ctx, w.scale, partition, ws, nbytes,
+                              self.err)
+        return out
+
+    def step(self, i, partition=0):
+        w = self.w
+        pos = w.positions(i)
+        pairs = self.prepare(pos)
+        self.append(w.k_new[i], w.v_new[i], pos)
+        out = self.attend(w.q[i], w.context_lens(i), partition)
+        return out, pairs
+
+    def err_bits(self) -> int:
+        torch.cuda.synchronize()
+        return int(self.err.item())
+
+    def pools(self):
+        """Host copies of the raw pools (uint16 bf16 bits or uint8 codes) and sink buffers."""
+        torch.cuda.synchronize()
+        def raw(t):
+            if t is None:
+                return None
+            if t.dtype == torch.bfloat16:
+                return t.view(torch.int16).cpu().numpy().view(np.uint16)
+            return t.cpu().numpy()
+        return raw(self.k), raw(self.v), raw(self.k_sink), raw(self.v_sink)
+
+
+class OracleState:
+    """The same layer in the oracle: pool, tables, refcounts, codes."""
+
+    def __init__(self, w: Workload, fill=True):
+        self.w = w
+        ks = None if w.k_scales is None else w.k_scales.numpy().astype(np.float32)
+        vs = None if w.v_scales is None else w.v_scales.numpy().astype(np.float32)
+        self.cache = O.PagedKVCache(w.num_blocks, w.H_kv, w.D, k_dtype=w.k_dtype, v_dtype=w.v_dtype,
+                                    k_scales=ks, v_scales=vs, num_seqs=w.B, num_sink=w.num_sink)
+        if w.k_dtype == "bf16":
+            self.cache.k[:] = BF16_NAN
+            self.cache.v[:] = BF16_NAN
+        else:
+            self.cache.k[:] = E4M3_NAN
+            self.cache.v[:] = INT8_OUTSIDE
+        self.cache.k_sink[:] = BF16_NAN
+        self.cache.v_sink[:] = BF16_NAN
+        self.pool = O.BlockPool(w.num_blocks)
+        blocks, counts = _refcounts_from_tables(w)
+        for b, c in zip(blocks, counts):
+            assert self.pool.claim(int(b))
+            for _ in range(int(c) - 1):
+                self.pool.incref(int(b))
+        self.tables = w.tables.astype(np.int64).copy()
+        if fill:
+            self.bulk_append(w.fill_k, w.fill_v, w.fill_seq, w.fill_pos)
+
+    def bulk_append(self, k, v, seq, pos):
+        kb, vb = bf16_bits(k), bf16_bits(v)
+        for i in range(len(seq)):
+            s = int(seq[i])
+            self.cache.append(s, self.tables[s], int(pos[i]), kb[i], vb[i])
+
+    def prepare(self, positions):
+        pairs = []
+        for s, p in enumerate(positions):
+            if p < 0:
+                continue
+            act = self.pool.prepare_append(self.tables[s], int(p))
+            if act[0] == "copy":
+                self.cache.block_copy(act[1], act[2])
+                pairs.append((act[1], act[2]))
+        return pairs
+
+    def append(self, k_new, v_new, positions):
+        kb, vb = bf16_bits(k_new), bf16_bits(v_new)
+        for s, p in enumerate(positions):
+            if p >= 0:
+                self.cache.append(s, self.tables[s], int(p), kb[s], vb[s])
+
+    def attend(self, q, context_lens):
+        w = self.w
+        qv = O.bf16_bits_to_f64(bf16_bits(q))
+        out = np.zeros((w.B, w.H_q, w.D))
+        for s in range(w.B):
+            K, V = self.cache.gather(s, self.tables[s], int(context_lens[s]))
+            out[s] = O.decode_attention(qv[s], K, V, w.scale)
+        return out
+
+    def step(self, i):
+        w = self.w
+        pos = w.positions(i)
+        pairs = self.prepare(pos)
+        self.append(w.k_new[i], w.v_new[i], pos)
+        return self.attend(w.q[i], w.context_lens(i)), pairs
+
+
+def to_f64(out: torch.Tensor) -> np.ndarray:
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def assert_attention_close(gpu: np.ndarray, ref: np.ndarray, what=""):
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite output"
+    err = np.abs(gpu - ref)
+    assert err.max() <= ATOL_MAX, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= ATOL_MEAN, f"{what}: mean abs err {err.mean():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def assert_pools_equal(gpu: GpuState, ora: OracleState):
+    gk, gv, gks, gvs = gpu.pools()
+    assert np.array_equal(gpu.tables, ora.tables.astype(np.int32)), "block tables differ"
+    assert np.array_equal(gk, ora.cache.k), "K pool differs"
+    assert np.array_equal(gv, ora.cache.v), "V pool differs"
+    if gks is not None:
+        assert np.array_equal(gks, ora.cache.k_sink), "K sink buffer differs"
+        assert np.array_equal(gvs, ora.cache.v_sink), "V sink buffer differs"
+
+
+# ----------------------------------------------------------------------------------
+# Full-size sampled checks: the oracle computes single (sequence, head) rows from the
+# workload's logical token stream, without building a whole pool.
+# ----------------------------------------------------------------------------------
+def logical_tokens(w: Workload, s: int, step: int):
+    """bf16 bit rows [ctx][H_kv][D] of sequence s as attended at `step` (positions 0..ctx-1)."""
+    parts_k, parts_v = [], []
+    if w.prefix:
+        parts_k.append(bf16_bits(w.fill_k))
+        parts_v.append(bf16_bits(w.fill_v))
+        off = int(w.suffix_len[:s].sum())
+        n = int(w.suffix_len[s])
+        parts_k.append(bf16_bits(w.suffix_k[off:off + n]))
+        parts_v.append(bf16_bits(w.suffix_v[off:off + n]))
+    else:
+        idx = np.nonzero(w.fill_seq == s)[0]
+        order = idx[np.argsort(w.fill_pos[idx])]
+        parts_k.append(bf16_bits(w.fill_k[torch.from_numpy(order)]))
+        parts_v.append(bf16_bits(w.fill_v[torch.from_numpy(order)]))
+    for i in range(step + 1):
+        parts_k.append(bf16_bits(w.k_new[i, s:s + 1]))
+        parts_v.append(bf16_bits(w.v_new[i, s:s + 1]))
+    return np.concatenate(parts_k), np.concatenate(parts_v)
+
+
+def reference_row(w: Workload, s: int, h: int, step: int, kb: np.ndarray, vb: np.ndarray) -> np.ndarray:
+    """Oracle output of query head h of sequence s (kb/vb: logical bf16 bit rows)."""
+    kv = h // w.G
+    ctx = kb.shape[0]
+    K = np.empty((ctx, 1, w.D))
+    V = np.empty((ctx, 1, w.D))
+    ns = min(ctx, w.num_sink)
+    K[:ns, 0] = O.bf16_bits_to_f64(kb[:ns, kv])
+    V[:ns, 0] = O.bf16_bits_to_f64(vb[:ns, kv])
+    if w.k_dtype == "bf16":
+        K[ns:, 0] = O.bf16_bits_to_f64(kb[ns:, kv])
+        V[ns:, 0] = O.bf16_bits_to_f64(vb[ns:, kv])
+    else:
+        ks = np.float32(w.k_scales[kv].item())
+        vs = np.float32(w.v_scales[kv].item())
+        K[ns:, 0] = O.e4m3_decode(O.quantize_row(kb[ns:, kv], ks, "e4m3")) * float(ks)
+        V[ns:, 0] = O.int8_decode(O.quantize_row(vb[ns:, kv], vs, "int8").view(np.int8)) * float(vs)
+    q = O.bf16_bits_to_f64(bf16_bits(w.q[step, s, h:h + 1]))
+    return O.decode_attention(q, K, V, w.scale)[0]

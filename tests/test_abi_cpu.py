@@ -1,0 +1,228 @@
+"""CPU-only checks of the C-ABI library: it builds and loads, exports every symbol the header
+declares, rejects bad arguments on the host before touching a GPU, and its host block
+manager makes the same decisions as the oracle's block pool."""
+
+import ctypes
+import os
+import re
+import threading
+
+import numpy as np
+import pytest
+
+import oracle as O
+from paged_kv_cache_table_gb300 import build as B
+from paged_kv_cache_table_gb300 import native as N
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    B.build()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    declared = _header_functions()
+    assert sorted(N.EXPORTED) == declared
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    assert N.status_string(0) == "PA_OK"
+    assert N.status_string(3) == "PA_ERR_WORKSPACE_TOO_SMALL"
+    assert N.status_string(99) == "PA_ERR_UNKNOWN"
+
+
+def _desc(**kw):
+    base = dict(num_seqs=4, num_q_heads=8, num_kv_heads=2, head_dim=64, num_blocks=64, max_blocks_per_seq=17)
+    base.update(kw)
+    return N.make_desc(**base)
+
+
+FAKE = 1 << 20  # never dereferenced: every call below returns before launching
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), N.PA_ERR_UNSUPPORTED),
+    (dict(block_size=32), N.PA_ERR_UNSUPPORTED),
+    (dict(num_q_heads=9), N.PA_ERR_INVALID_ARG),
+    (dict(num_q_heads=36, num_kv_heads=2), N.PA_ERR_UNSUPPORTED),  # G = 18 > 8
+    (dict(num_blocks=0), N.PA_ERR_INVALID_ARG),
+    (dict(k_dtype="e4m3", v_dtype="int8", head_dim=128), N.PA_ERR_INVALID_ARG),  # no scales
+    (dict(k_dtype="e4m3", v_dtype="int8", head_dim=64, k_scales=FAKE, v_scales=FAKE), N.PA_ERR_UNSUPPORTED),
+    (dict(k_dtype="bf16", v_dtype="int8"), N.PA_ERR_UNSUPPORTED),
+    (dict(k_dtype=7), N.PA_ERR_INVALID_ARG),
+    (dict(num_sink=4), N.PA_ERR_INVALID_ARG),  # sinks without buffers
+])
+def test_bad_descriptions_are_rejected_on_the_host(kw, status):
+    d = _desc(**kw)
+    with pytest.raises(N.PaError) as e:
+        N.pa_kv_append(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0)
+    assert e.value.status == status
+    with pytest.raises(N.PaError) as e:
+        N.pa_block_copy(d, FAKE, FAKE, FAKE, 1, None, 0)
+    assert e.value.status == status
+    assert N.pa_decode_workspace_size(d, 100, 32) == 0
+
+
+def test_null_and_misaligned_pointers_are_rejected():
+    d = _desc()
+    with pytest.raises(N.PaError) as e:
+        N.pa_kv_append(d, 0, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0)
+    assert e.value.status == N.PA_ERR_INVALID_ARG
+    with pytest.raises(N.PaError) as e:
+        N.pa_kv_append(d, FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0)
+    assert e.value.status == N.PA_ERR_INVALID_ARG
+    with pytest.raises(N.PaError) as e:
+        N.pa_kv_append_tokens(d, FAKE, FAKE, FAKE, FAKE, 3, 0, FAKE, FAKE, None, 0)
+    assert e.value.status == N.PA_ERR_INVALID_ARG
+    with pytest.raises(N.PaError) as e:
+        N.pa_block_copy(d, FAKE, FAKE, FAKE, -1, None, 0)
+    assert e.value.status == N.PA_ERR_INVALID_ARG
+    # zero rows / pairs: nothing to enqueue
+    N.pa_kv_append_tokens(d, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, FAKE, None, 0)
+    N.pa_block_copy(d, FAKE, FAKE, 0, 0, None, 0)
+
+
+def test_workspace_size_fixed_partitions():
+    d = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, num_seqs=64)
+    a = N.pa_decode_workspace_size(d, 4096, 512)
+    b = N.pa_decode_workspace_size(d, 4096, 256)
+    c = N.pa_decode_workspace_size(d, 8192, 512)
+    assert 0 < a < b and c == 2 * a - 256  # partials scale with the partition count; 256-byte header
+    assert N.pa_decode_workspace_size(d, 4096, 24) == 0  # not a multiple of 16
+    assert N.pa_decode_workspace_size(d, -1, 512) == 0
+
+
+# ----------------------------------------------------------------------------------
+# host block manager vs the oracle's pool
+# ----------------------------------------------------------------------------------
+def test_block_manager_matches_oracle_pool_on_random_operations():
+    rng = np.random.default_rng(0)
+    bm = N.BlockManager(48)
+    pool = O.BlockPool(48)
+    live = []
+    for _ in range(4000):
+        op = rng.integers(5)
+        if op == 0:
+            a, b = bm.alloc(), pool.alloc()
+            assert a == b
+            if a >= 0:
+                live.append(a)
+        elif op == 1 and live:
+            x = int(rng.choice(live))
+            assert bm.incref(x) == pool.incref(x)
+        elif op == 2 and live:
+            x = int(rng.choice(live))
+            r = bm.decref(x)
+            assert r == pool.decref(x)
+            if r == 0:
+                live.remove(x)
+        elif op == 3:
+            x = int(rng.integers(-2, 50))
+            assert bm.claim(x) == pool.claim(x)
+            if 0 <= x < 48 and x not in live and pool.refcount[x] == 1:
+                live.append(x)
+        else:
+            x = int(rng.integers(-2, 50))
+            assert bm.refcount(x) == (int(pool.refcount[x]) if 0 <= x < 48 else -1)
+        assert bm.num_free() == pool.num_free()
+
+
+def test_prepare_step_matches_oracle_prepare_append():
+    rng = np.random.default_rng(1)
+    B_, M = 6, 12
+    bm = N.BlockManager(80)
+    pool = O.BlockPool(80)
+    tabs = np.full((B_, M), -1, dtype=np.int32)
+    otabs = np.full((B_, M), -1, dtype=np.int64)
+    lens = np.zeros(B_, dtype=np.int64)
+    for step in range(120):
+        pos = np.where(rng.random(B_) < 0.8, lens, -1).astype(np.int32)
+        pairs, changed = bm.prepare_step(tabs, pos)
+        opairs = []
+        n_changed = 0
+        for s in range(B_):
+            if pos[s] >= 0:
+                act = pool.prepare_append(otabs[s], int(pos[s]))
+                if act[0] == "copy":
+                    opairs.append((act[1], act[2]))
+                if act[0] != "ok":
+                    n_changed += 1
+        assert [tuple(p) for p in pairs.tolist()] == opairs
+        assert changed == n_changed
+        assert np.array_equal(tabs, otabs)
+        lens += pos >= 0
+        if step % 30 == 29:  # fork sequence 0 into 1 and 2 (prefix sharing), then diverge
+            for dst in (1, 2):
+                bm.release(tabs[dst], M)
+                pool.release(otabs[dst], M)
+                n = -(-int(lens[0]) // 16)
+                tabs[dst] = bm.fork(tabs[0], n)
+                otabs[dst] = pool.fork(otabs[0], n)
+                lens[dst] = lens[0]
+        assert bm.num_free() == pool.num_free()
+
+
+def test_prepare_step_out_of_blocks_and_bad_position():
+    bm = N.BlockManager(2)
+    tabs = np.full((3, 4), -1, dtype=np.int32)
+    with pytest.raises(N.PaError) as e:
+        bm.prepare_step(tabs, np.array([0, 0, 0], dtype=np.int32))
+    assert e.value.status == N.PA_ERR_OUT_OF_BLOCKS
+    assert list(tabs[:, 0]) == [0, 1, -1]  # rows before the failure keep their blocks
+    with pytest.raises(N.PaError) as e:
+        bm.prepare_step(tabs, np.array([64, -1, -1], dtype=np.int32))
+    assert e.value.status == N.PA_ERR_INVALID_ARG
+
+
+def test_block_manager_is_thread_safe():
+    bm = N.BlockManager(4096)
+    base = [bm.alloc() for _ in range(64)]
+    errors = []
+
+    def worker(seed):
+        rng = np.random.default_rng(seed)
+        mine = []
+        try:
+            for _ in range(3000):
+                if rng.random() < 0.5 or not mine:
+                    b = int(base[rng.integers(len(base))])
+                    bm.incref(b)
+                    mine.append(b)
+                else:
+                    bm.decref(mine.pop())
+            for b in mine:
+                bm.decref(b)
+        except Exception as ex:  # pragma: no cover
+            errors.append(ex)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors
+    assert all(bm.refcount(b) == 1 for b in base)
+    assert bm.num_free() == 4096 - 64
+
+
+def test_release_frees_only_unshared_blocks_and_nothing_leaks():
+    bm = N.BlockManager(32)
+    row = np.full(8, -1, dtype=np.int32)
+    for p in range(100):
+        bm.prepare_step(row[None, :], np.array([p], dtype=np.int32))
+    assert bm.num_free() == 32 - 7
+    fork = bm.fork(row, 7)
+    assert bm.release(row, 8) == 0  # still held by the fork
+    assert bm.release(fork, 8) == 7
+    assert bm.num_free() == 32
