@@ -65,26 +65,34 @@ def _run(cmd, verbose):
     return r
 
 
-def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile and link the library; returns its path."""
+def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False,
+          defines=(), lib_path: str | None = None, build_dir: str | None = None) -> str:
+    """Compile and link the library; returns its path.
+
+    ``defines`` (e.g. ``("PA_PREFETCH_STAGES=2",)``) override compile-time tuning constants;
+    use them together with a separate ``lib_path`` and ``build_dir``.
+    """
+    lib_out = lib_path or LIB_PATH
+    bdir = build_dir or BUILD_DIR
+    dflags = [f"-D{d}" for d in defines]
     cuda = _cuda_home()
     nvcc = os.path.join(cuda, "bin", "nvcc")
     cxx = os.environ.get("CXX", "g++")
     cu, cpp = sources()
     headers = _headers()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     jobs = []
     objs = []
     for src in cu:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *dflags, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
             if ptxas_verbose:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)
     for src in cpp:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             jobs.append([cxx, *CXX_FLAGS, "-I", INCLUDE, "-I", CSRC, "-I", os.path.join(cuda, "include"),
@@ -93,11 +101,11 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             results = list(ex.map(lambda c: _run(c, verbose or ptxas_verbose), jobs))
         del results
-    if force or jobs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + ".tmp"
+    if force or jobs or _stale(lib_out, objs):
+        tmp = lib_out + ".tmp"
         _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs], verbose)
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_out)
+    return lib_out
 
 
 if __name__ == "__main__":

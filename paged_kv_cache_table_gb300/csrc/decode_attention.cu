@@ -40,9 +40,19 @@ constexpr int kTileBytes = 2048;  // one TMA box: 16 slots x 128 bytes
 constexpr int kMaxConsumerWarps = 16;
 constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 constexpr int kAutoMaxSeqs = 2048;
-constexpr int kMaxStages = 8;
-constexpr int kSmemLimit = 227 * 1024;
 constexpr int kFixedFallbackPartition = 512;
+// Tuning constants (compile-time; the defaults are the measured best on GB300).
+#ifndef PA_CTAS_PER_SM
+#define PA_CTAS_PER_SM 1  // balanced mode: resident CTAs per SM
+#endif
+#ifndef PA_GROUP_BYTES
+#define PA_GROUP_BYTES 2048  // KV heads per CTA: as many as fit this many bytes of one slot
+#endif
+#ifndef PA_MAX_STAGES
+#define PA_MAX_STAGES 8
+#endif
+constexpr int kMaxStages = PA_MAX_STAGES;
+constexpr int kSmemLimit = (PA_CTAS_PER_SM == 1 ? 227 * 1024 : (228 * 1024) / PA_CTAS_PER_SM - 1024);
 constexpr float kNegInf = -INFINITY;
 
 struct DecodeParams {
@@ -112,6 +122,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const DecodeParams& p) {
 template <int D, bool QUANT>
 struct Consumer {
   static constexpr int KT = D / 16;  // k-steps of q·Kᵀ and m-tiles of P·V
+  static constexpr int NC = QUANT ? 1 : D * 2 / 128;  // 128-byte chunks per head row
   const DecodeParams& p;
   uint32_t qf[KT][2];
   float o[KT][4];
@@ -187,18 +198,20 @@ struct Consumer {
 
   // One 16-token block: scores, online softmax update, P·V.
   __device__ __forceinline__ void block(const uint8_t* kbase, const uint8_t* vbase, int lb, int ntok) {
+    // two independent accumulation chains halve the dependent-MMA latency of q·Kᵀ
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
     const int tokA = (lane & 7) + ((lane >> 3) & 1) * 8;
     if constexpr (!QUANT) {
       const int halfA = lane >> 4;
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
         const int ch16 = (kk & 3) * 2 + halfA;
-        const uint32_t addr =
-            smem_u32(kbase + (kk >> 2) * kTileBytes + tokA * 128 + ((ch16 ^ (tokA & 7)) << 4));
+        const int row = tokA * NC + (kk >> 2);  // 128-byte row of the swizzled tile
+        const uint32_t addr = smem_u32(kbase + row * 128 + ((ch16 ^ (row & 7)) << 4));
         uint32_t a0, a1, a2, a3;
         ldsm_x4(addr, a0, a1, a2, a3);
-        mma_bf16(acc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        mma_bf16((kk & 1) ? acc2 : acc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
       }
     } else {
 #pragma unroll
@@ -209,10 +222,12 @@ struct Consumer {
         ldsm_x4(addr, r0, r1, r2, r3);
         mma_f16(acc, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
                 e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0], qf[2 * kp][1]);
-        mma_f16(acc, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+        mma_f16(acc2, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
                 e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
       }
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
     // rows t4 and t4+8 of the block; columns = query heads 2tq, 2tq+1
     const int pos0 = lb * PA_BLOCK_SIZE + t4;
     const bool v0 = t4 < ntok && pos0 >= p.num_sink;
@@ -227,23 +242,30 @@ struct Consumer {
       bm0 = warp_max_xor(bm0, mask);
       bm1 = warp_max_xor(bm1, mask);
     }
-    const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);
+    // The reference maximum only moves when a score exceeds it by more than 2^8 (exact: the
+    // final division by l uses the same reference), so most blocks skip the rescale of o.
+    const float mn0 = (m[0] == kNegInf || bm0 > m[0] + 8.f) ? fmaxf(m[0], bm0) : m[0];
+    const float mn1 = (m[1] == kNegInf || bm1 > m[1] + 8.f) ? fmaxf(m[1], bm1) : m[1];
     const float ms0 = mn0 == kNegInf ? 0.f : mn0;
     const float ms1 = mn1 == kNegInf ? 0.f : mn1;
-    const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
     const float p00 = ex2(s00 - ms0), p10 = ex2(s10 - ms0);
     const float p01 = ex2(s01 - ms1), p11 = ex2(s11 - ms1);
-    l[0] = l[0] * al0 + p00 + p10;
-    l[1] = l[1] * al1 + p01 + p11;
+    if (__any_sync(0xffffffffu, mn0 != m[0] || mn1 != m[1])) {
+      const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
+      l[0] *= al0;
+      l[1] *= al1;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
+    l[0] += p00 + p10;
+    l[1] += p01 + p11;
     m[0] = mn0;
     m[1] = mn1;
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
-    }
     // P (tokens x heads) -> B operand (K = tokens, N = heads) of P·V
     const uint32_t x0 = QUANT ? pack_f16(p00, p01) : pack_bf16(p00, p01);
     const uint32_t x1 = QUANT ? pack_f16(p10, p11) : pack_bf16(p10, p11);
@@ -264,8 +286,8 @@ struct Consumer {
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
         const int ch16 = (mt & 3) * 2 + halfB;
-        const uint32_t addr =
-            smem_u32(vbase + (mt >> 2) * kTileBytes + tokB * 128 + ((ch16 ^ (tokB & 7)) << 4));
+        const int row = tokB * NC + (mt >> 2);
+        const uint32_t addr = smem_u32(vbase + row * 128 + ((ch16 ^ (row & 7)) << 4));
         uint32_t a0, a1, a2, a3;
         ldsm_x4_t(addr, a0, a1, a2, a3);
         mma_bf16(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
@@ -350,8 +372,8 @@ struct Consumer {
   }
 };
 
-template <int D, bool QUANT>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+template <int D, bool QUANT, int MAXW>
+__global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -443,70 +465,73 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int S = p.stages, nbs = p.nbs;
   if (warp == p.warps_c) {
     // ------------------------------- producer -------------------------------
-    const int hgnc = p.hg * p.nc;
-    const int ops_per_block = 2 * hgnc;
+    // Every lane owns one block of the current 32-block chunk: its table entry is loaded one
+    // chunk ahead and its stage metadata is packed once when the chunk becomes current, so a
+    // stage costs one shuffle, one shared store and one TMA per (tensor, head) box.  Each box
+    // is a whole head row (all 128-byte chunks) of the block's 16 slots.
+    const uint32_t box_bytes = static_cast<uint32_t>(p.nc) * kTileBytes;
+    const int ops_per_block = 2 * p.hg;
+    const int n_ops = nbs * ops_per_block;  // <= 32
     const uint64_t policy = l2_evict_first_policy();
-    int k = 0;
-    bool ok = true;
-    for (int base = u0; base < u1 && ok; base += 32) {
+    // this lane's op (fixed for every stage): block jj of the stage, tensor, head
+    const int my_jj = lane / ops_per_block;
+    const int my_t = (lane - my_jj * ops_per_block) / p.hg;
+    const int my_h = lane - my_jj * ops_per_block - my_t * p.hg;
+    const CUtensorMap* my_map = my_t ? &tmV : &tmK;
+    const int my_row = (hgi * p.hg + my_h) * p.nc;
+    const size_t my_dst = static_cast<size_t>((my_jj * 2 + my_t) * p.hg + my_h) * box_bytes;
+    auto load_entry = [&](int u) -> int {
+      if (u >= u1) return -1;
+      const int s = find_seq(sm.cum, nseq, u);
+      return p.block_tables[static_cast<size_t>(seq_base + s) * p.max_blocks + (u - sm.cum[s])];
+    };
+    int base = u0;
+    int cur_pb = load_entry(base + lane);
+    int nxt_pb = load_entry(base + 32 + lane);
+    int4 my_meta;
+    unsigned live_mask;
+    auto pack = [&]() {
       const int u = base + lane;
-      int my_s = 0, my_lb = 0, my_pb = 0, my_nt = 0, my_bad = 0;
-      if (u < u1) {
-        my_s = find_seq(sm.cum, nseq, u);
-        my_lb = u - sm.cum[my_s];
-        my_nt = min(PA_BLOCK_SIZE, sm.ctxs[my_s] - my_lb * PA_BLOCK_SIZE);
-        my_pb = p.block_tables[static_cast<size_t>(seq_base + my_s) * p.max_blocks + my_lb];
-        my_bad = (my_pb < 0 || my_pb >= p.num_blocks) ? 1 : 0;
-        if (my_bad) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
+      const bool valid = u < u1;
+      const int s = valid ? find_seq(sm.cum, nseq, u) : 0;
+      const int lb = valid ? u - sm.cum[s] : 0;
+      const bool bad = valid && (cur_pb < 0 || cur_pb >= p.num_blocks);
+      if (bad) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
+      my_meta = valid ? make_int4(s, lb, min(PA_BLOCK_SIZE, sm.ctxs[s] - lb * PA_BLOCK_SIZE), bad ? 1 : 0)
+                      : make_int4(-1, 0, 0, 1);
+      live_mask = __ballot_sync(0xffffffffu, valid && !bad);
+    };
+    pack();
+    const int n_iters = (u1 - u0 + nbs - 1) / nbs;
+    const unsigned stage_bits = (1u << nbs) - 1u;
+    int k = 0;
+    for (; k < n_iters; ++k) {
+      int i = k * nbs - (base - u0);
+      if (i >= 32) {
+        base += 32;
+        i -= 32;
+        cur_pb = nxt_pb;
+        nxt_pb = load_entry(base + 32 + lane);
+        pack();
       }
-      const int n_here = min(32, u1 - base);
-      for (int i = 0; i < n_here; i += nbs, ++k) {
-        const int st = k % S;
-        const uint32_t ph = static_cast<uint32_t>(k / S) & 1u;
-        if (!mbar_wait(&sm.empty[st], ph ^ 1u)) {
-          if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
-          ok = false;
-          break;
-        }
-        uint32_t bytes = 0;
-        int pbs[8];
-        bool live[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          live[jj] = false;
-          pbs[jj] = 0;
-          if (jj < nbs) {
-            const int src = i + jj;  // < 32 because nbs divides 32
-            const int s_j = __shfl_sync(0xffffffffu, my_s, src);
-            const int lb_j = __shfl_sync(0xffffffffu, my_lb, src);
-            const int pb_j = __shfl_sync(0xffffffffu, my_pb, src);
-            const int nt_j = __shfl_sync(0xffffffffu, my_nt, src);
-            const int bad_j = __shfl_sync(0xffffffffu, my_bad, src);
-            const bool valid = src < n_here;
-            live[jj] = valid && !bad_j;
-            pbs[jj] = pb_j;
-            if (lane == 0) sm.meta[st * nbs + jj] = valid ? make_int4(s_j, lb_j, nt_j, bad_j) : make_int4(-1, 0, 0, 1);
-            if (live[jj]) bytes += ops_per_block * kTileBytes;
-          }
-        }
-        if (lane == 0) {
-          if (bytes) mbar_arrive_expect_tx(&sm.full[st], bytes);
-          else mbar_arrive(&sm.full[st]);
-        }
-        __syncwarp();
-        uint8_t* stage = sm.stages + static_cast<size_t>(st) * p.stage_bytes;
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          if (jj < nbs && live[jj]) {
-            for (int o = lane; o < ops_per_block; o += 32) {
-              const int tensor = o / hgnc;
-              const int hc = o - tensor * hgnc;
-              tma_load_3d(stage + ((jj * 2 + tensor) * hgnc + hc) * kTileBytes, tensor ? &tmV : &tmK,
-                          &sm.full[st], 0, hgi * hgnc + hc, pbs[jj] * PA_BLOCK_SIZE, policy);
-            }
-          }
-        }
+      const int st = k % S;
+      const uint32_t ph = static_cast<uint32_t>(k / S) & 1u;
+      const int pb = __shfl_sync(0xffffffffu, cur_pb, (i + my_jj) & 31);
+      const unsigned live = (live_mask >> i) & stage_bits;  // i + nbs <= 32 since nbs divides 32
+      if (!mbar_wait(&sm.empty[st], ph ^ 1u)) {
+        if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
+        break;
       }
+      if (lane >= i && lane < i + nbs) sm.meta[st * nbs + (lane - i)] = my_meta;
+      if (lane == 0) {
+        const uint32_t bytes = __popc(live) * ops_per_block * box_bytes;
+        if (bytes) mbar_arrive_expect_tx(&sm.full[st], bytes);
+        else mbar_arrive(&sm.full[st]);
+      }
+      __syncwarp();
+      if (lane < n_ops && ((live >> my_jj) & 1u))
+        tma_load_3d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], 0,
+                    my_row, pb * PA_BLOCK_SIZE, policy);
     }
     // do not leave while a copy into this CTA's shared memory may still be in flight
     for (int st = 0; st < S && st < k; ++st) {
@@ -600,77 +625,85 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
     if (p.direct_ok && c_first == c_last) return;  // the main kernel wrote this row
   }
   const int n_sink = nb < 0 ? 0 : min(p.num_sink, ctx);
-  auto slot_of = [&](int c) -> size_t {
-    return p.mode == 0 ? static_cast<size_t>(s + c) : static_cast<size_t>(s) * p.max_parts + c;
-  };
   const int n_parts = (c_last - c_first + 1) * p.nbs;
-
-  float M = kNegInf;
-  bool bad = false;
-  for (int i = lane; i < n_parts; i += 32) {
+  auto row_of = [&](int i) -> const float* {
     const int c = c_first + i / p.nbs, jj = i % p.nbs;
-    const float* row = p.partials + ((slot_of(c) * p.nbs + jj) * p.H_q + h) * static_cast<size_t>(D + 4);
-    const float lv = row[D + 1];
-    if (lv < 0.f) bad = true;
-    else if (lv > 0.f) M = fmaxf(M, row[D]);
-  }
-#pragma unroll
-  for (int mask = 1; mask < 32; mask <<= 1) M = warp_max_xor(M, mask);
-  bad = __any_sync(0xffffffffu, bad);
-
-  float qv[E];
-  if (n_sink > 0) {
-    const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(s) * p.H_q + h) * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) qv[e] = __bfloat162float(qrow[e]);
-  }
-  auto sink_score = [&](int t) -> float {
-    const __nv_bfloat16* krow =
-        p.k_sink + ((static_cast<size_t>(s) * p.num_sink + t) * p.H_kv + h_kv) * D + lane * E;
-    float dot = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) dot += qv[e] * __bfloat162float(krow[e]);
-#pragma unroll
-    for (int mask = 1; mask < 32; mask <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, mask);
-    return dot * p.scale_log2;
+    const size_t slot = p.mode == 0 ? static_cast<size_t>(s + c) : static_cast<size_t>(s) * p.max_parts + c;
+    return p.partials + ((slot * p.nbs + jj) * p.H_q + h) * static_cast<size_t>(D + 4);
   };
-  for (int t = 0; t < n_sink; ++t) M = fmaxf(M, sink_score(t));
 
+  // Partials are merged 32 at a time: lane i holds partial i's (m, l); every lane then
+  // accumulates its E dims of all partials of the chunk (independent loads, selected by
+  // weight so that the unwritten rows of empty partials are never used).
+  float M = kNegInf, L = 0.f;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  if (!bad && nb > 0) {
-    for (int i = 0; i < n_parts; ++i) {
-      const int c = c_first + i / p.nbs, jj = i % p.nbs;
-      const float* row = p.partials + ((slot_of(c) * p.nbs + jj) * p.H_q + h) * static_cast<size_t>(D + 4);
-      const float lv = row[D + 1];
-      if (lv > 0.f) {
-        const float w = ex2(row[D] - M);
-        L += w * lv;
-        if constexpr (E == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(row + lane * 4);
-          acc[0] += w * v.x;
-          acc[1] += w * v.y;
-          acc[2] += w * v.z;
-          acc[3] += w * v.w;
-        } else {
-          const float2 v = *reinterpret_cast<const float2*>(row + lane * 2);
-          acc[0] += w * v.x;
-          acc[1] += w * v.y;
-        }
-      }
+  bool bad = false;
+  for (int base = 0; base < n_parts; base += 32) {
+    const int n = min(32, n_parts - base);
+    float mi = kNegInf, li = 0.f;
+    if (lane < n) {
+      const float* r = row_of(base + lane);
+      mi = r[D];
+      li = r[D + 1];
     }
-    for (int t = 0; t < n_sink; ++t) {
-      const float w = ex2(sink_score(t) - M);
-      L += w;
-      const __nv_bfloat16* vrow =
-          p.v_sink + ((static_cast<size_t>(s) * p.num_sink + t) * p.H_kv + h_kv) * D + lane * E;
+    bad = bad || li < 0.f;
+    float mc = li > 0.f ? mi : kNegInf;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += w * __bfloat162float(vrow[e]);
+    for (int mask = 1; mask < 32; mask <<= 1) mc = warp_max_xor(mc, mask);
+    const float newM = fmaxf(M, mc);
+    if (newM == kNegInf) continue;
+    const float sc = ex2(M - newM);
+    L *= sc;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= sc;
+    M = newM;
+    const float wi = li > 0.f ? ex2(mi - M) : 0.f;
+    float wl = wi * li;
+#pragma unroll
+    for (int mask = 1; mask < 32; mask <<= 1) wl += __shfl_xor_sync(0xffffffffu, wl, mask);
+    L += wl;
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, wi, j);
+      const float* r = row_of(base + j) + lane * E;
+      float v[E];
+      if constexpr (E == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(r);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(r);
+        v[0] = t.x; v[1] = t.y;
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += wj != 0.f ? wj * v[e] : 0.f;
     }
   }
-  const float inv = (bad || !(L > 0.f)) ? 0.f : 1.f / L;
+  bad = __any_sync(0xffffffffu, bad);
+
+  if (n_sink > 0) {  // bf16 sink tokens join the merge as extra single-token partials
+    float qv[E];
+    const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(s) * p.H_q + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) qv[e] = __bfloat162float(qrow[e]);
+    for (int t = 0; t < n_sink; ++t) {
+      const size_t off = ((static_cast<size_t>(s) * p.num_sink + t) * p.H_kv + h_kv) * D + lane * E;
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) dot += qv[e] * __bfloat162float(p.k_sink[off + e]);
+#pragma unroll
+      for (int mask = 1; mask < 32; mask <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, mask);
+      const float st = dot * p.scale_log2;
+      const float newM = fmaxf(M, st);
+      const float sc = ex2(M - newM), w = ex2(st - newM);
+      L = L * sc + w;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = acc[e] * sc + w * __bfloat162float(p.v_sink[off + e]);
+      M = newM;
+    }
+  }
+  const float inv = (bad || nb <= 0 || !(L > 0.f)) ? 0.f : 1.f / L;
 #pragma unroll
   for (int e = 0; e < E; ++e) orow[lane * E + e] = __float2bfloat16_rn(acc[e] * inv);
 }
@@ -701,7 +734,7 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
   pl->nc = row_bytes / 128;
   int hg = 1;
   for (int c = 1; c <= d->num_kv_heads; ++c)
-    if (d->num_kv_heads % c == 0 && c * row_bytes <= 2048) hg = c;
+    if (d->num_kv_heads % c == 0 && c * row_bytes <= PA_GROUP_BYTES) hg = c;
   pl->hg = hg;
   pl->n_hg = d->num_kv_heads / hg;
   pl->nbs = std::max(1, 8 / hg);
@@ -715,8 +748,9 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
     pl->mode = 0;
     pl->ppb = 0;
     pl->max_parts = 0;
-    pl->grid_x = num_sms_current();
-    if (pl->grid_x <= 0) return PA_ERR_CUDA;
+    // one wave: every head group gets an equal share of the resident CTAs
+    pl->grid_x = std::max(1, num_sms_current() * PA_CTAS_PER_SM / pl->n_hg);
+    if (num_sms_current() <= 0) return PA_ERR_CUDA;
     pl->n_slots = static_cast<size_t>(B) + pl->grid_x;
     pl->meta_bytes = ((static_cast<size_t>(B) + 2) * 4 + 255) / 256 * 256;
   } else {
@@ -755,15 +789,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// The cache as a 3-D tensor: (128-byte row chunk, kv_head x chunk, slot).  One box is one
-// (head, chunk) row of 16 consecutive slots, i.e. of one physical block.
-bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int rows, long long slots) {
+// The cache as a 3-D tensor: (128-byte chunk of a head row, kv_head x chunk, slot).  One box is
+// one head row (nc chunks) of 16 consecutive slots, i.e. of one physical block, and lands in
+// shared memory as [slot][chunk][128 B] with the 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int rows, int nc, long long slots) {
   auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / elem_bytes), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(slots)};
   cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(rows) * 128};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 1, PA_BLOCK_SIZE};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(nc), PA_BLOCK_SIZE};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -774,7 +809,8 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int ro
 template <int D, bool QUANT>
 pa_status launch(const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p,
                  cudaStream_t stream) {
-  auto kern = decode_kernel<D, QUANT>;
+  // 9-warp CTAs get the register budget of a 288-thread launch; wider ones a 544-thread one
+  auto kern = pl.warps_c <= 8 ? decode_kernel<D, QUANT, 8> : decode_kernel<D, QUANT, kMaxConsumerWarps>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(pl.smem_bytes)) != cudaSuccess)
     return PA_ERR_CUDA;
@@ -817,8 +853,8 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, c
   const int e = pa::dtype_bytes(desc->k_dtype);
   const long long slots = static_cast<long long>(desc->num_blocks) * PA_BLOCK_SIZE;
   CUtensorMap mk, mv;
-  if (!pa::encode_cache_map(&mk, k_cache, e, desc->num_kv_heads * pl.nc, slots) ||
-      !pa::encode_cache_map(&mv, v_cache, e, desc->num_kv_heads * pl.nc, slots))
+  if (!pa::encode_cache_map(&mk, k_cache, e, desc->num_kv_heads * pl.nc, pl.nc, slots) ||
+      !pa::encode_cache_map(&mv, v_cache, e, desc->num_kv_heads * pl.nc, pl.nc, slots))
     return PA_ERR_CUDA;
 
   pa::DecodeParams p;

@@ -70,15 +70,25 @@ class CacheDesc(ctypes.Structure):
 
 
 _LIB = None
+_LIB_PATH = LIB_PATH
+
+
+def use_library(path: str) -> None:
+    """Bind to another build of the same library (e.g. one compiled with tuning defines).
+    Must be called before the first call into the library."""
+    global _LIB_PATH
+    if _LIB is not None:
+        raise RuntimeError("the library is already loaded")
+    _LIB_PATH = path
 
 
 def lib() -> ctypes.CDLL:
     """The loaded library (loaded once).  Raises if it was never built."""
     global _LIB
     if _LIB is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with paged_kv_cache_table_gb300.build.build()")
-        L = ctypes.CDLL(LIB_PATH)
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with paged_kv_cache_table_gb300.build.build()")
+        L = ctypes.CDLL(_LIB_PATH)
         vp, i32p, c_int = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_int
         dp = ctypes.POINTER(CacheDesc)
         L.pa_status_string.restype = ctypes.c_char_p
