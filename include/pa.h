@@ -30,7 +30,8 @@
  *   k_scales,v_scales fp32  [num_kv_heads]
  *
  * Conventions:
- *   - The caller owns every buffer; the library allocates no device memory and keeps no
+ *   - The caller owns every buffer; apart from the static scratch array behind
+ *     pa_decode_attention_noalloc, the library allocates no device memory and keeps no
  *     per-call state.  Calls are stream-ordered on the given stream (a cudaStream_t passed
  *     as void*; NULL is the legacy default stream) and return after enqueueing.
  *   - Errors the host can see (null pointers, unsupported shapes, small workspace) are
@@ -169,6 +170,29 @@ pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, const void* 
                               int max_context_len, float scale, int partition_size,
                               void* workspace, size_t workspace_bytes,
                               int32_t* err_flag, void* stream);
+
+/* Allocation-free decode attention.  The pages have no counterpart to this entry point: it is
+ * pa_decode_attention for callers that cannot allocate device memory when they call it, for
+ * example a plugin running inside a host framework that owns every byte of device memory, a
+ * latency-critical path where cudaMalloc/cudaFree could synchronise the device and stall other
+ * work, or a caller that has no way to recover from an out-of-memory failure in the middle of a
+ * decode step.  It takes the same arguments minus the workspace, and runs the same kernels with
+ * their scratch in a static 8 MiB device array that every GPU which loads this library holds
+ * until the process exits.
+ *   - The first call on a device looks the array's address up (cudaGetSymbolAddress, with that
+ *     device current); make that first call before any stream capture on the device.
+ *   - A problem whose pa_decode_workspace_size() exceeds 8 MiB (8388608 bytes) is rejected
+ *     with PA_ERR_WORKSPACE_TOO_SMALL and nothing is enqueued.
+ *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - Every call on a device shares the array and leaves its contents behind; the kernels write
+ *     every scratch byte before reading it, so nothing needs clearing, but calls that overlap on
+ *     the GPU (e.g. on two streams at once) race on it: serialise them.
+ * Host errors: as pa_decode_attention, plus PA_ERR_CUDA if the address lookup fails. */
+pa_status pa_decode_attention_noalloc(const pa_cache_desc* desc, void* out, const void* q,
+                                      const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      int max_context_len, float scale, int partition_size,
+                                      int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * Host block manager: the physical block pool with a free list and reference counts

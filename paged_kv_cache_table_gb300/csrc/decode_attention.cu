@@ -895,3 +895,53 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, c
     return quant ? pa::launch<128, true>(pl, mk, mv, p, s) : pa::launch<128, false>(pl, mk, mv, p, s);
   return pa::launch<64, false>(pl, mk, mv, p, s);
 }
+
+// ------------------------------------------------------------------------------------
+// Allocation-free variant: the same kernels with their scratch in a static device array.
+// ------------------------------------------------------------------------------------
+namespace pa {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB on every device that loads the library
+constexpr int kMaxDevices = 64;
+
+// Loaded with the module on each device and held until the process exits.  Kernels may name
+// it directly; host code must not (the host symbol is only a stand-in for the device address).
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per device.
+pa_status static_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return PA_ERR_CUDA;
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_decode_attention_noalloc(const pa_cache_desc* desc, void* out, const void* q,
+                                                 const void* k_cache, const void* v_cache,
+                                                 const int32_t* block_tables, const int32_t* context_lens,
+                                                 int max_context_len, float scale, int partition_size,
+                                                 int32_t* err_flag, void* stream) {
+  pa::Plan pl;
+  const pa_status st = pa::make_plan(desc, max_context_len, partition_size, &pl);
+  if (st != PA_OK) return st;
+  if (pl.ws_bytes > pa::kStaticScratchBytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  const pa_status ss = pa::static_scratch(&scratch);
+  if (ss != PA_OK) return ss;
+  return pa_decode_attention(desc, out, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                             scale, partition_size, scratch, pa::kStaticScratchBytes, err_flag, stream);
+}
