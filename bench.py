@@ -218,14 +218,18 @@ class DecodeBench:
         self.h_k = w.k_new.pin_memory()
         self.h_v = w.v_new.pin_memory()
         self.h_out = torch.empty((WINDOW, w.B, w.H_q, w.D), dtype=torch.bfloat16).pin_memory()
-        self.d_q = torch.empty_like(self.q[0])
-        self.d_k = torch.empty_like(self.k_new[0])
-        self.d_v = torch.empty_like(self.v_new[0])
+        # e2e: two device buffers per input/output, filled and drained by a copy stream
+        self.d_q = [torch.empty_like(self.q[0]) for _ in range(2)]
+        self.d_k = [torch.empty_like(self.k_new[0]) for _ in range(2)]
+        self.d_v = [torch.empty_like(self.v_new[0]) for _ in range(2)]
+        self.d_out = [torch.empty_like(self.out) for _ in range(2)]
         self.launches_per_step = 3  # append + attention + merge (plus a copy kernel on CoW steps)
         self.cow_launches = 0
 
-    def step(self, i, stream, ev=None, e2e=False):
-        torch, N, w = self.torch, self.N, self.w
+    def step(self, i, stream, ev=None, inputs=None, out=None):
+        """One decode step on `stream`.  `inputs` = (q, k_new, v_new) device tensors (default:
+        the resident ones of this step); `ev` = events around the attention call."""
+        N, w = self.N, self.w
         j = i % WINDOW
         pairs, changed = self.bm.prepare_step(self.tables, self.pos[j])
         if changed:
@@ -236,30 +240,22 @@ class DecodeBench:
             self.pairs_dev[:len(pairs)].copy_(self.pair_ring[j][:len(pairs)], non_blocking=True)
             N.pa_block_copy(self.desc, self.k, self.v, self.pairs_dev, len(pairs), self.err, stream)
             self.cow_launches += 1
-        if e2e:
-            self.d_q.copy_(self.h_q[j], non_blocking=True)
-            self.d_k.copy_(self.h_k[j], non_blocking=True)
-            self.d_v.copy_(self.h_v[j], non_blocking=True)
-            q, kn, vn = self.d_q, self.d_k, self.d_v
-        else:
-            q, kn, vn = self.q[j], self.k_new[j], self.v_new[j]
+        q, kn, vn = inputs if inputs is not None else (self.q[j], self.k_new[j], self.v_new[j])
+        out = self.out if out is None else out
         N.pa_kv_append(self.desc, self.k, self.v, kn, vn, self.tables_dev, self.pos_dev[j], self.err, stream)
         if ev is not None:
             ev[0].record()
-        N.pa_decode_attention(self.desc, self.out, q, self.k, self.v, self.tables_dev, self.ctx_dev[j],
+        N.pa_decode_attention(self.desc, out, q, self.k, self.v, self.tables_dev, self.ctx_dev[j],
                               self.max_ctx, w.scale, self.partition, self.ws, self.ws_bytes, self.err, stream)
         if ev is not None:
             ev[1].record()
-        if e2e:
-            self.h_out[j].copy_(self.out, non_blocking=True)
 
-    def run(self, steps, warmup, e2e=False, per_call_events=False, sampler=None):
-        """Returns (elapsed_s, attention_ms_per_call or None, bytes over the timed steps)."""
+    def run(self, steps, warmup, per_call_events=False):
+        """Device-resident steps.  Returns (elapsed_s, attention_ms_per_call or None, bytes)."""
         torch = self.torch
-        stream = torch.cuda.current_stream()
-        sid = stream.cuda_stream
+        sid = torch.cuda.current_stream().cuda_stream
         for i in range(warmup):
-            self.step(i, sid, e2e=e2e)
+            self.step(i, sid)
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)] if per_call_events else None
@@ -271,16 +267,70 @@ class DecodeBench:
         nbytes = 0
         for k in range(steps):
             i = warmup + k
-            self.step(i, sid, ev=None if evs is None else evs[k], e2e=e2e)
+            self.step(i, sid, ev=None if evs is None else evs[k])
             nbytes += self.step_bytes[i % WINDOW]
         t1.record()
         torch.cuda.synchronize()
         barrier(self.dev)
         elapsed = t0.elapsed_time(t1) / 1e3
-        att = None
-        if evs is not None:
-            att = [a.elapsed_time(b) for a, b in evs]
+        att = None if evs is None else [a.elapsed_time(b) for a, b in evs]
         return elapsed, att, nbytes
+
+    def run_e2e(self, steps, warmup):
+        """Steps fed from pinned host memory: a copy stream uploads step k's q/k/v into one of
+        two device buffers and downloads step k-2's output while the compute stream runs step
+        k-1; every copy of every timed step is inside the timed region."""
+        torch = self.torch
+        comp = torch.cuda.current_stream()
+        copy = torch.cuda.Stream()
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        pending = {}
+
+        def issue(k, i):
+            b = k % 2
+            j = i % WINDOW
+            with torch.cuda.stream(copy):
+                if k >= 2:
+                    copy.wait_event(done[b])  # step k-2 consumed buffer b and produced out[b]
+                    jp = pending.pop(b)
+                    self.h_out[jp].copy_(self.d_out[b], non_blocking=True)
+                self.d_q[b].copy_(self.h_q[j], non_blocking=True)
+                self.d_k[b].copy_(self.h_k[j], non_blocking=True)
+                self.d_v[b].copy_(self.h_v[j], non_blocking=True)
+                in_ready[b].record(copy)
+            comp.wait_event(in_ready[b])
+            self.step(i, comp.cuda_stream, inputs=(self.d_q[b], self.d_k[b], self.d_v[b]), out=self.d_out[b])
+            done[b].record(comp)
+            pending[b] = j
+
+        def drain():
+            with torch.cuda.stream(copy):
+                for b in sorted(pending):
+                    copy.wait_event(done[b])
+                    self.h_out[pending[b]].copy_(self.d_out[b], non_blocking=True)
+            pending.clear()
+
+        for k in range(warmup):
+            issue(k, k)
+        drain()
+        torch.cuda.synchronize()
+        barrier(self.dev)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(comp)
+        copy.wait_event(t0)
+        nbytes = 0
+        for k in range(steps):
+            issue(k, warmup + k)
+            nbytes += self.step_bytes[(warmup + k) % WINDOW]
+        drain()
+        comp.wait_stream(copy)
+        t1.record(comp)
+        torch.cuda.synchronize()
+        barrier(self.dev)
+        return t0.elapsed_time(t1) / 1e3, nbytes
 
 
 def cpu_baseline_sample(name, budget_s=15.0, max_seqs=None):
@@ -384,10 +434,12 @@ def run_native(args):
 
     b = DecodeBench(args.config, device, args.partition)
     w = b.w
-    # device-resident run, with per-call events around the attention for the roofline
+    # device-resident steps (value), clocks sampled meanwhile
     with ClockSampler(local) as cs:
-        elapsed, att_ms, nbytes = b.run(args.steps, args.warmup, per_call_events=True)
+        elapsed, _, nbytes = b.run(args.steps, args.warmup)
     clocks = cs.summary()
+    # the same steps with CUDA events around every attention call (roofline of the kernel)
+    _, att_ms, _ = b.run(args.steps, args.warmup, per_call_events=True)
     el_max, bytes_all = reduce_max_sum(elapsed, nbytes, device)
     value = bytes_all / el_max / 1e9
     ms_per_step = 1e3 * el_max / args.steps
@@ -396,17 +448,19 @@ def run_native(args):
     att_bytes = float(np.mean([b.step_bytes[(args.warmup + k) % WINDOW] for k in range(args.steps)]))
     achieved = att_bytes / (att_mean_ms / 1e3) / 1e9
     # end-to-end through the same API with host buffers
-    el_e2e, _, nbytes_e2e = b.run(args.steps, args.warmup, e2e=True)
+    el_e2e, nbytes_e2e = b.run_e2e(args.steps, args.warmup)
     el_e2e, bytes_e2e = reduce_max_sum(el_e2e, nbytes_e2e, device)
     h2d = (w.B * w.H_q * w.D + 2 * w.B * w.H_kv * w.D) * 2
     d2h = w.B * w.H_q * w.D * 2
     err = int(b.err.item())
 
     extra = {}
-    if args.also and rank == 0:
+    if args.also and args.also != "none" and rank == 0:
         for name in args.also.split(","):
             nb = DecodeBench(name, device, args.partition)
-            e2, a2, by2 = nb.run(max(50, args.steps // 4), args.warmup, per_call_events=True)
+            n2 = max(50, args.steps // 4)
+            e2, _, by2 = nb.run(n2, args.warmup)
+            _, a2, _ = nb.run(n2, args.warmup, per_call_events=True)
             a_ms = float(np.mean(a2))
             ab = float(np.mean([nb.step_bytes[(args.warmup + k) % WINDOW] for k in range(len(a2))]))
             extra[name] = {"value": round(by2 / e2 / 1e9, 1), "unit": "GB/s",

@@ -380,6 +380,8 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
   const Smem sm = carve(smem_raw, p);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nthreads = blockDim.x;
+  // The merge kernel may be scheduled now; it waits for this grid before reading its output.
+  grid_dep_launch_dependents();
 
   // ---- this CTA's range [u0, u1) of the (sequence, logical block) list ----
   int hgi, seq_base, nseq, u0, u1;
@@ -430,11 +432,17 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       for (int i = tid; i <= p.B; i += nthreads) p.ws_meta[i] = sm.cum[i];
       if (tid == 0) p.ws_meta[p.B + 1] = T;
     }
-    if (T == 0) return;
+    if (T == 0) {
+      grid_dep_wait();
+      return;
+    }
     const int W = (T + gridDim.x - 1) / gridDim.x;
     u0 = blockIdx.x * W;
     u1 = min(T, u0 + W);
-    if (u0 >= u1) return;
+    if (u0 >= u1) {
+      grid_dep_wait();  // completion of this grid then implies completion of its predecessor
+      return;
+    }
   } else {
     hgi = blockIdx.z;
     seq_base = blockIdx.y;
@@ -450,7 +458,10 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     }
     u0 = blockIdx.x * p.ppb;
     u1 = min(nbv, u0 + p.ppb);
-    if (u0 >= u1) return;
+    if (u0 >= u1) {
+      grid_dep_wait();
+      return;
+    }
   }
 
   if (tid == 0) {
@@ -488,6 +499,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     int base = u0;
     int cur_pb = load_entry(base + lane);
     int nxt_pb = load_entry(base + 32 + lane);
+    // The cache may have been written by the kernel just before this one (the append):
+    // wait for it before the first TMA read.
+    grid_dep_wait();
     int4 my_meta;
     unsigned live_mask;
     auto pack = [&]() {
@@ -603,6 +617,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
 template <int D>
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int grid_x) {
   constexpr int E = D / 32;  // dims per lane
+  constexpr int CH = 8;      // partials per round of loads
   const int s = blockIdx.x;
   const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -610,6 +625,14 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
   const int h_kv = h / p.G;
   const int ctx = p.context_lens[s];
   const int nb = seq_blocks(p, ctx);
+  const int n_sink = nb < 0 ? 0 : min(p.num_sink, ctx);
+  float qv[E];
+  if (n_sink > 0) {
+    const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(s) * p.H_q + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) qv[e] = __bfloat162float(qrow[e]);
+  }
+  grid_dep_wait();  // the decode kernel's partials and prefix sums are complete from here on
   __nv_bfloat16* orow = p.out + (static_cast<size_t>(s) * p.H_q + h) * D;
 
   int c_first = 0, c_last = -1;
@@ -624,7 +647,6 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
     }
     if (p.direct_ok && c_first == c_last) return;  // the main kernel wrote this row
   }
-  const int n_sink = nb < 0 ? 0 : min(p.num_sink, ctx);
   const int n_parts = (c_last - c_first + 1) * p.nbs;
   auto row_of = [&](int i) -> const float* {
     const int c = c_first + i / p.nbs, jj = i % p.nbs;
@@ -632,21 +654,35 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
     return p.partials + ((slot * p.nbs + jj) * p.H_q + h) * static_cast<size_t>(D + 4);
   };
 
-  // Partials are merged 32 at a time: lane i holds partial i's (m, l); every lane then
-  // accumulates its E dims of all partials of the chunk (independent loads, selected by
-  // weight so that the unwritten rows of empty partials are never used).
+  // Partials are merged CH at a time: lane i holds partial i's (m, l), every lane loads its E
+  // dims of all CH partials in the same round, and rows of empty partials (never written) are
+  // masked out by their zero weight through a select, never multiplied.
   float M = kNegInf, L = 0.f;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   bool bad = false;
-  for (int base = 0; base < n_parts; base += 32) {
-    const int n = min(32, n_parts - base);
+  for (int base = 0; base < n_parts; base += CH) {
+    const int n = min(CH, n_parts - base);
     float mi = kNegInf, li = 0.f;
     if (lane < n) {
       const float* r = row_of(base + lane);
       mi = r[D];
       li = r[D + 1];
+    }
+    float v[CH][E];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      if (j < n) {
+        const float* r = row_of(base + j) + lane * E;
+        if constexpr (E == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(r);
+          v[j][0] = t.x; v[j][1] = t.y; v[j][2] = t.z; v[j][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(r);
+          v[j][0] = t.x; v[j][1] = t.y;
+        }
+      }
     }
     bad = bad || li < 0.f;
     float mc = li > 0.f ? mi : kNegInf;
@@ -664,44 +700,31 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
 #pragma unroll
     for (int mask = 1; mask < 32; mask <<= 1) wl += __shfl_xor_sync(0xffffffffu, wl, mask);
     L += wl;
-#pragma unroll 4
-    for (int j = 0; j < n; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, wi, j);
-      const float* r = row_of(base + j) + lane * E;
-      float v[E];
-      if constexpr (E == 4) {
-        const float4 t = *reinterpret_cast<const float4*>(r);
-        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-      } else {
-        const float2 t = *reinterpret_cast<const float2*>(r);
-        v[0] = t.x; v[1] = t.y;
-      }
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += wj != 0.f ? wj * v[e] : 0.f;
+    for (int j = 0; j < CH; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, wi, j);
+      if (j < n) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += wj != 0.f ? wj * v[j][e] : 0.f;
+      }
     }
   }
   bad = __any_sync(0xffffffffu, bad);
 
-  if (n_sink > 0) {  // bf16 sink tokens join the merge as extra single-token partials
-    float qv[E];
-    const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(s) * p.H_q + h) * D + lane * E;
+  for (int t = 0; t < n_sink; ++t) {  // bf16 sink tokens join the merge as single-token partials
+    const size_t off = ((static_cast<size_t>(s) * p.num_sink + t) * p.H_kv + h_kv) * D + lane * E;
+    float dot = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) qv[e] = __bfloat162float(qrow[e]);
-    for (int t = 0; t < n_sink; ++t) {
-      const size_t off = ((static_cast<size_t>(s) * p.num_sink + t) * p.H_kv + h_kv) * D + lane * E;
-      float dot = 0.f;
+    for (int e = 0; e < E; ++e) dot += qv[e] * __bfloat162float(p.k_sink[off + e]);
 #pragma unroll
-      for (int e = 0; e < E; ++e) dot += qv[e] * __bfloat162float(p.k_sink[off + e]);
+    for (int mask = 1; mask < 32; mask <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, mask);
+    const float st = dot * p.scale_log2;
+    const float newM = fmaxf(M, st);
+    const float sc = ex2(M - newM), w = ex2(st - newM);
+    L = L * sc + w;
 #pragma unroll
-      for (int mask = 1; mask < 32; mask <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, mask);
-      const float st = dot * p.scale_log2;
-      const float newM = fmaxf(M, st);
-      const float sc = ex2(M - newM), w = ex2(st - newM);
-      L = L * sc + w;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = acc[e] * sc + w * __bfloat162float(p.v_sink[off + e]);
-      M = newM;
-    }
+    for (int e = 0; e < E; ++e) acc[e] = acc[e] * sc + w * __bfloat162float(p.v_sink[off + e]);
+    M = newM;
   }
   const float inv = (bad || nb <= 0 || !(L > 0.f)) ? 0.f : 1.f / L;
 #pragma unroll
@@ -815,10 +838,11 @@ pa_status launch(const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv, c
                            static_cast<int>(pl.smem_bytes)) != cudaSuccess)
     return PA_ERR_CUDA;
   const dim3 grid = p.mode == 0 ? dim3(pl.grid_x, pl.n_hg, 1) : dim3(pl.max_parts, p.B, pl.n_hg);
-  kern<<<grid, pl.threads, pl.smem_bytes, stream>>>(mk, mv, p);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  merge_kernel<D><<<dim3(p.B, (p.H_q + 3) / 4), 128, 0, stream>>>(p, pl.grid_x);
-  return launch_status();
+  // Both kernels may start while their predecessor drains (the decode prologue overlaps the
+  // append; the merge launch overlaps the decode tail); each waits before reading its inputs.
+  if (launch_overlapped(kern, grid, dim3(pl.threads), pl.smem_bytes, stream, mk, mv, p) != PA_OK)
+    return PA_ERR_CUDA;
+  return launch_overlapped(merge_kernel<D>, dim3(p.B, (p.H_q + 3) / 4), dim3(128), 0, stream, p, pl.grid_x);
 }
 
 }  // namespace

@@ -73,6 +73,9 @@ __device__ __forceinline__ uint2 encode_int8x8(const uint4& v, float scale) {
 
 template <bool QUANT>
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  // the decode kernel that usually follows may start its prologue now: it waits for this
+  // kernel's completion before it reads the cache
+  grid_dep_launch_dependents();
   const int r = blockIdx.x;
   const int s = p.token_seq ? p.token_seq[r] : r;
   if (s < 0 || s >= p.num_seqs) {

@@ -28,6 +28,15 @@ __device__ __forceinline__ void set_error(int32_t* err, int bits) {
   if (err) atomicOr(err, bits);
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic-serialization
+// attribute may start before the previous kernel in the stream has finished; grid_dep_wait()
+// blocks until that kernel has completed and its memory is visible.  launch_dependents() lets
+// the next kernel start early.  Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------
