@@ -214,22 +214,35 @@ class DecodeBench:
         self.tab_ring = [torch.empty(self.tables.shape, dtype=torch.int32).pin_memory() for _ in range(WINDOW)]
         self.pair_ring = [torch.empty((w.B, 2), dtype=torch.int32).pin_memory() for _ in range(WINDOW)]
         self.pairs_dev = torch.empty((w.B, 2), dtype=torch.int32, device=device)
-        self.h_q = w.q.pin_memory()
-        self.h_k = w.k_new.pin_memory()
-        self.h_v = w.v_new.pin_memory()
-        self.h_out = torch.empty((WINDOW, w.B, w.H_q, w.D), dtype=torch.bfloat16).pin_memory()
-        # e2e: two device buffers per input/output, filled and drained by a copy stream
-        self.d_q = [torch.empty_like(self.q[0]) for _ in range(2)]
-        self.d_k = [torch.empty_like(self.k_new[0]) for _ in range(2)]
-        self.d_v = [torch.empty_like(self.v_new[0]) for _ in range(2)]
+        # e2e: each step's q, k_new, v_new packed into one pinned row (one upload per step),
+        # two device copies of that row and of the output, drained by a copy stream
+        nq, nk = w.B * w.H_q * w.D, w.B * w.H_kv * w.D
+        self.in_elems = nq + 2 * nk
+        h_in = torch.empty((WINDOW, self.in_elems), dtype=torch.bfloat16)
+        h_in[:, :nq] = w.q.reshape(WINDOW, nq)
+        h_in[:, nq:nq + nk] = w.k_new.reshape(WINDOW, nk)
+        h_in[:, nq + nk:] = w.v_new.reshape(WINDOW, nk)
+        self.h_in = [r for r in h_in.pin_memory()]
+        self.h_out = [r for r in torch.empty((WINDOW, w.B, w.H_q, w.D), dtype=torch.bfloat16).pin_memory()]
+        self.d_in = [torch.empty(self.in_elems, dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.d_views = [(d[:nq].view(w.B, w.H_q, w.D), d[nq:nq + nk].view(w.B, w.H_kv, w.D),
+                         d[nq + nk:].view(w.B, w.H_kv, w.D)) for d in self.d_in]
         self.d_out = [torch.empty_like(self.out) for _ in range(2)]
+        self.host_s = 0.0
+        # raw device pointers for the per-step calls (the binding takes ints as pointers)
+        P = lambda t: t.data_ptr()
+        self.ptr = dict(k=P(self.k), v=P(self.v), tab=P(self.tables_dev), ws=P(self.ws), err=P(self.err),
+                        out=P(self.out))
+        self.ptr_step = [(P(self.q[j]), P(self.k_new[j]), P(self.v_new[j]), P(self.pos_dev[j]), P(self.ctx_dev[j]))
+                         for j in range(WINDOW)]
+        self.ptr_e2e = [tuple(P(t) for t in v) + (P(o),) for v, o in zip(self.d_views, self.d_out)]
         self.launches_per_step = 3  # append + attention + merge (plus a copy kernel on CoW steps)
         self.cow_launches = 0
 
-    def step(self, i, stream, ev=None, inputs=None, out=None):
-        """One decode step on `stream`.  `inputs` = (q, k_new, v_new) device tensors (default:
-        the resident ones of this step); `ev` = events around the attention call."""
-        N, w = self.N, self.w
+    def step(self, i, stream, ev=None, buf=None):
+        """One decode step on `stream`.  `buf` selects a double-buffered e2e input/output slot
+        (default: the resident inputs of this step); `ev` = events around the attention call."""
+        N, w, P = self.N, self.w, self.ptr
         j = i % WINDOW
         pairs, changed = self.bm.prepare_step(self.tables, self.pos[j])
         if changed:
@@ -240,13 +253,15 @@ class DecodeBench:
             self.pairs_dev[:len(pairs)].copy_(self.pair_ring[j][:len(pairs)], non_blocking=True)
             N.pa_block_copy(self.desc, self.k, self.v, self.pairs_dev, len(pairs), self.err, stream)
             self.cow_launches += 1
-        q, kn, vn = inputs if inputs is not None else (self.q[j], self.k_new[j], self.v_new[j])
-        out = self.out if out is None else out
-        N.pa_kv_append(self.desc, self.k, self.v, kn, vn, self.tables_dev, self.pos_dev[j], self.err, stream)
+        q, kn, vn, pos, ctx = self.ptr_step[j]
+        out = P["out"]
+        if buf is not None:
+            q, kn, vn, out = self.ptr_e2e[buf]
+        N.pa_kv_append(self.desc, P["k"], P["v"], kn, vn, P["tab"], pos, P["err"], stream)
         if ev is not None:
             ev[0].record()
-        N.pa_decode_attention(self.desc, out, q, self.k, self.v, self.tables_dev, self.ctx_dev[j],
-                              self.max_ctx, w.scale, self.partition, self.ws, self.ws_bytes, self.err, stream)
+        N.pa_decode_attention(self.desc, out, q, P["k"], P["v"], P["tab"], ctx, self.max_ctx, w.scale,
+                              self.partition, P["ws"], self.ws_bytes, P["err"], stream)
         if ev is not None:
             ev[1].record()
 
@@ -265,10 +280,12 @@ class DecodeBench:
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         nbytes = 0
+        h0 = time.perf_counter()
         for k in range(steps):
             i = warmup + k
             self.step(i, sid, ev=None if evs is None else evs[k])
             nbytes += self.step_bytes[i % WINDOW]
+        self.host_s = time.perf_counter() - h0
         t1.record()
         torch.cuda.synchronize()
         barrier(self.dev)
@@ -293,14 +310,11 @@ class DecodeBench:
             with torch.cuda.stream(copy):
                 if k >= 2:
                     copy.wait_event(done[b])  # step k-2 consumed buffer b and produced out[b]
-                    jp = pending.pop(b)
-                    self.h_out[jp].copy_(self.d_out[b], non_blocking=True)
-                self.d_q[b].copy_(self.h_q[j], non_blocking=True)
-                self.d_k[b].copy_(self.h_k[j], non_blocking=True)
-                self.d_v[b].copy_(self.h_v[j], non_blocking=True)
+                    self.h_out[pending.pop(b)].copy_(self.d_out[b], non_blocking=True)
+                self.d_in[b].copy_(self.h_in[j], non_blocking=True)
                 in_ready[b].record(copy)
             comp.wait_event(in_ready[b])
-            self.step(i, comp.cuda_stream, inputs=(self.d_q[b], self.d_k[b], self.d_v[b]), out=self.d_out[b])
+            self.step(i, comp.cuda_stream, buf=b)
             done[b].record(comp)
             pending[b] = j
 
@@ -322,10 +336,12 @@ class DecodeBench:
         t0.record(comp)
         copy.wait_event(t0)
         nbytes = 0
+        h0 = time.perf_counter()
         for k in range(steps):
             issue(k, warmup + k)
             nbytes += self.step_bytes[(warmup + k) % WINDOW]
         drain()
+        self.host_s = time.perf_counter() - h0
         comp.wait_stream(copy)
         t1.record(comp)
         torch.cuda.synchronize()
@@ -438,6 +454,7 @@ def run_native(args):
     with ClockSampler(local) as cs:
         elapsed, _, nbytes = b.run(args.steps, args.warmup)
     clocks = cs.summary()
+    host_ms = 1e3 * b.host_s / args.steps
     # the same steps with CUDA events around every attention call (roofline of the kernel)
     _, att_ms, _ = b.run(args.steps, args.warmup, per_call_events=True)
     el_max, bytes_all = reduce_max_sum(elapsed, nbytes, device)
@@ -449,6 +466,7 @@ def run_native(args):
     achieved = att_bytes / (att_mean_ms / 1e3) / 1e9
     # end-to-end through the same API with host buffers
     el_e2e, nbytes_e2e = b.run_e2e(args.steps, args.warmup)
+    host_ms_e2e = 1e3 * b.host_s / args.steps
     el_e2e, bytes_e2e = reduce_max_sum(el_e2e, nbytes_e2e, device)
     h2d = (w.B * w.H_q * w.D + 2 * w.B * w.H_kv * w.D) * 2
     d2h = w.B * w.H_q * w.D * 2
@@ -500,7 +518,9 @@ def run_native(args):
                          "peak_kind": peak_kind, "ms_per_call": round(att_mean_ms, 5),
                          "algorithmic_bytes_per_call": int(att_bytes)},
             "e2e": {"value": round(bytes_e2e / el_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * el_e2e / args.steps, 5)},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * el_e2e / args.steps, 5),
+                    "host_ms_per_step": round(host_ms_e2e, 5)},
+            "host_ms_per_step": round(host_ms, 5),
             "gpu_launches": args.steps * b.launches_per_step + b.cow_launches,
             "clocks": clocks,
             "cpu_baseline": cpu,
