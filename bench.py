@@ -185,9 +185,10 @@ class DecodeBench:
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.bm = N.BlockManager(w.num_blocks)
         blocks, counts = np.unique(w.tables[w.tables >= 0], return_counts=True)
+        owner = 1 if w.prefix else 0  # a cached prefix holds its own reference to its blocks
         for b, c in zip(blocks, counts):
             self.bm.claim(int(b))
-            for _ in range(int(c) - 1):
+            for _ in range(int(c) - 1 + owner):
                 self.bm.incref(int(b))
         # cached tokens, appended in bounded chunks
         chunk = 1 << 17
@@ -196,6 +197,8 @@ class DecodeBench:
             N.pa_kv_append_tokens(self.desc, self.k, self.v, w.fill_k[a:b].to(device), w.fill_v[a:b].to(device),
                                   b - a, torch.from_numpy(w.fill_seq[a:b]).to(device),
                                   torch.from_numpy(w.fill_pos[a:b]).to(device), self.tables_dev, self.err)
+        if w.prefix:
+            self._fork_and_fill_suffixes()
         torch.cuda.synchronize()
         # per-step inputs, resident
         self.q = w.q.to(device)
@@ -238,6 +241,37 @@ class DecodeBench:
         self.ptr_e2e = [tuple(P(t) for t in v) + (P(o),) for v, o in zip(self.d_views, self.d_out)]
         self.launches_per_step = 3  # append + attention + merge (plus a copy kernel on CoW steps)
         self.cow_launches = 0
+
+    def _fork_and_fill_suffixes(self):
+        """Prefix workload set-up: every sequence writes its private suffix after the shared
+        prefix.  The first suffix token lands in the shared, partly filled prefix block, so the
+        block manager copy-on-writes it for every sequence (the fork); the later tokens open
+        private blocks.  Afterwards the timed steps append at prefix + suffix length."""
+        torch, N, w, dev = self.torch, self.N, self.w, self.dev
+        lens = w.suffix_len.astype(np.int64)
+        self.fork_pairs = 0
+        for p in range(w.prefix, w.prefix + int(lens.max())):
+            pos = np.where(p < w.prefix + lens, p, -1).astype(np.int32)
+            pairs, changed = self.bm.prepare_step(self.tables, pos)
+            if changed:
+                self.tables_dev.copy_(torch.from_numpy(self.tables))
+            if len(pairs):
+                N.pa_block_copy(self.desc, self.k, self.v, torch.from_numpy(pairs).to(dev), len(pairs), self.err)
+                self.fork_pairs += len(pairs)
+        seq = np.repeat(np.arange(w.B, dtype=np.int32), lens)
+        pos = np.concatenate([np.arange(w.prefix, w.prefix + n, dtype=np.int32) for n in lens])
+        N.pa_kv_append_tokens(self.desc, self.k, self.v, w.suffix_k.to(dev), w.suffix_v.to(dev), len(seq),
+                              torch.from_numpy(seq).to(dev), torch.from_numpy(pos).to(dev), self.tables_dev,
+                              self.err)
+        w.ctx_old = (w.prefix + lens).astype(np.int32)
+        # bytes the attention reads once from DRAM: the shared prefix blocks count once
+        self.shared_tokens = w.prefix - (w.prefix % 16)
+
+    def unique_bytes(self, ctx):
+        """Prefix workload: algorithmic bytes with the shared full prefix blocks counted once."""
+        w = self.w
+        per_tok = w.H_kv * w.D * w.kv_elem_bytes() * 2
+        return attention_bytes(w, ctx) - (w.B - 1) * self.shared_tokens * per_tok
 
     def step(self, i, stream, ev=None, buf=None):
         """One decode step on `stream`.  `buf` selects a double-buffered e2e input/output slot
@@ -481,7 +515,14 @@ def run_native(args):
             _, a2, _ = nb.run(n2, args.warmup, per_call_events=True)
             a_ms = float(np.mean(a2))
             ab = float(np.mean([nb.step_bytes[(args.warmup + k) % WINDOW] for k in range(len(a2))]))
-            extra[name] = {"value": round(by2 / e2 / 1e9, 1), "unit": "GB/s",
+            if nb.w.prefix:
+                ub = float(np.mean([nb.unique_bytes(nb.ctx[(args.warmup + k) % WINDOW]) for k in range(len(a2))]))
+                extra_prefix = {"unique_bytes_per_call": int(ub),
+                                "attention_gbs_unique": round(ub / (a_ms / 1e3) / 1e9, 1),
+                                "fork_copy_pairs": nb.fork_pairs}
+            else:
+                extra_prefix = {}
+            extra[name] = {**extra_prefix, "value": round(by2 / e2 / 1e9, 1), "unit": "GB/s",
                            "attention_gbs": round(ab / (a_ms / 1e3) / 1e9, 1),
                            "attention_frac": round(ab / (a_ms / 1e3) / 1e9 / peak, 4),
                            "ms_per_step": round(1e3 * e2 / len(a2), 4),
