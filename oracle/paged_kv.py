@@ -56,6 +56,7 @@ __all__ = [
     "merge_partials",
     "decode_attention_split",
     "softmax_weights",
+    "prefill_attention",
 ]
 
 # 显存账本 §四: "典型 16 个 token 一块" — the typical block holds 16 tokens.
@@ -540,3 +541,26 @@ def decode_attention_split(q, K, V, scale: float, partition_tokens: int):
         return np.zeros(np.asarray(q).shape)
     bounds = list(range(0, ctx, partition_tokens)) + [ctx]
     return merge_partials(decode_attention_partials(q, K, V, scale, bounds))
+
+
+def prefill_attention(q, K, V, scale: float, first_pos: int) -> np.ndarray:
+    """Causal attention of a chunk of new query tokens over one sequence's cached K/V.
+
+    ldpk §2.2: during prefill every position's query attends to the keys of positions 1..i under
+    the causal mask, and only K and V are kept; ldpk §7 splits a long prompt into chunks.  The
+    chunk's queries sit at positions first_pos .. first_pos + n - 1 (their own K/V are already in
+    the cache), and the query at position p reads keys 0..p.  GQA grouping as in
+    decode_attention.  q: [n][H_q][d], K and V: [ctx][H_kv][d] with ctx >= first_pos + n (fp64).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n, H_q, d = q.shape
+    ctx, H_kv, _ = K.shape
+    G = H_q // H_kv
+    out = np.zeros((n, H_q, d))
+    for i in range(n):
+        p = first_pos + i
+        for h in range(H_q):
+            kv = h // G
+            scores = scale * (K[:p + 1, kv, :] @ q[i, h])
+            out[i, h] = softmax_weights(scores) @ V[:p + 1, kv, :]
+    return out

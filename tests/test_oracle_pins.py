@@ -576,3 +576,63 @@ def test_planted_e4m3_rounding_mistake_is_caught():
     x = np.float32(1.0 + 3 * 2.0 ** -5)  # between 1.0625 and 1.125, nearer the upper
     assert truncating(x) != int(O.e4m3_encode(x))
     assert int(O.e4m3_encode(x)) == O.e4m3_encode_bruteforce(float(x))
+
+
+# ----------------------------------------------------------------------------------
+# Chunked prefill (causal attention of several new tokens per sequence)
+# ----------------------------------------------------------------------------------
+def _sdpa_causal_rows(q_all, K, V, scale, rows):
+    """torch SDPA with is_causal over a whole sequence (queries = every position), fp64."""
+    n, H_q, d = q_all.shape
+    H_kv = K.shape[1]
+    G = H_q // H_kv
+    qt = torch.from_numpy(q_all).permute(1, 0, 2).unsqueeze(0)
+    kt = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0)
+    vt = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0)
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=scale)
+    return out[0].permute(1, 0, 2).numpy()[rows]
+
+
+@pytest.mark.parametrize("H_q,H_kv,ctx,first", [(4, 2, 40, 0), (8, 2, 37, 20), (6, 6, 19, 18), (8, 1, 50, 33)])
+def test_prefill_matches_causal_sdpa(H_q, H_kv, ctx, first):
+    rng = np.random.default_rng(20)
+    d = 16
+    q_all = rng.standard_normal((ctx, H_q, d))
+    K = rng.standard_normal((ctx, H_kv, d))
+    V = rng.standard_normal((ctx, H_kv, d))
+    got = O.prefill_attention(q_all[first:], K, V, 0.25, first)
+    ref = _sdpa_causal_rows(q_all, K, V, 0.25, slice(first, ctx))
+    assert np.allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_prefill_last_token_is_decode_and_chunks_compose():
+    rng = np.random.default_rng(21)
+    q_all = rng.standard_normal((30, 8, 16))
+    K = rng.standard_normal((30, 2, 16))
+    V = rng.standard_normal((30, 2, 16))
+    one = O.prefill_attention(q_all[29:], K, V, 0.3, 29)[0]
+    assert np.array_equal(one, O.decode_attention(q_all[29], K, V, 0.3))
+    whole = O.prefill_attention(q_all, K, V, 0.3, 0)
+    parts = np.concatenate([O.prefill_attention(q_all[a:b], K, V, 0.3, a) for a, b in [(0, 7), (7, 16), (16, 30)]])
+    assert np.array_equal(whole, parts)
+    # the first position sees only itself
+    assert np.array_equal(whole[0], V[0, [0, 0, 0, 0, 1, 1, 1, 1]])
+
+
+def test_planted_causal_mask_mistake_is_caught():
+    rng = np.random.default_rng(22)
+    q_all = rng.standard_normal((12, 4, 8))
+    K = rng.standard_normal((12, 2, 8))
+    V = rng.standard_normal((12, 2, 8))
+
+    def off_by_one(q, K, V, scale, first):  # lets each query see the next key as well
+        out = np.zeros(q.shape)
+        for i in range(q.shape[0]):
+            p = min(first + i + 1, K.shape[0] - 1)
+            for h in range(q.shape[1]):
+                s = scale * (K[:p + 1, h // 2] @ q[i, h])
+                out[i, h] = O.softmax_weights(s) @ V[:p + 1, h // 2]
+        return out
+    ref = _sdpa_causal_rows(q_all, K, V, 0.5, slice(3, 12))
+    assert np.allclose(O.prefill_attention(q_all[3:], K, V, 0.5, 3), ref, atol=1e-12)
+    assert not np.allclose(off_by_one(q_all[3:], K, V, 0.5, 3), ref, atol=1e-6)
