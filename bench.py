@@ -50,6 +50,14 @@ METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak); decode tokens/
 L2_BYTES = 129 * 1024 * 1024
 
 
+def _bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -404,6 +412,62 @@ class DecodeBench:
         return t0.elapsed_time(t1) / 1e3, nbytes
 
 
+class PrefillBench:
+    """Chunked-prefill row: each step appends every sequence's chunk of new K/V tokens and runs
+    causal prefill attention of the chunk's queries over the paged cache."""
+
+    def __init__(self, device):
+        import torch
+        from paged_kv_cache_table_gb300 import native as N
+        from paged_kv_cache_table_gb300.workloads import make_prefill_workload
+        self.torch, self.N = torch, N
+        w = make_prefill_workload()
+        self.w = w
+        shape = (w.num_blocks * 16, w.H_kv, w.D)
+        self.k = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        self.v = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        self.desc = N.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks)
+        self.tables = torch.from_numpy(w.tables).to(device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        N.pa_kv_append_tokens(self.desc, self.k, self.v, w.fill_k.to(device), w.fill_v.to(device), len(w.fill_seq),
+                              torch.from_numpy(w.fill_seq).to(device), torch.from_numpy(w.fill_pos).to(device),
+                              self.tables, self.err)
+        self.new_k, self.new_v = w.new_k.to(device), w.new_v.to(device)
+        self.new_seq = torch.from_numpy(w.new_seq).to(device)
+        self.new_pos = torch.from_numpy(w.new_pos).to(device)
+        self.q = w.q.to(device)
+        self.q_start = torch.from_numpy(w.q_start()).to(device)
+        self.ctx = torch.from_numpy(w.context_lens()).to(device)
+        self.out = torch.empty_like(self.q)
+        self.max_q = int(w.chunk.max())
+        ctx, n = w.context_lens().astype(np.int64), w.chunk.astype(np.int64)
+        # causal (query, key) pairs: the query at position p reads p + 1 keys
+        pairs = sum(int(((c - m + 1) + c) * m // 2) for c, m in zip(ctx, n))
+        self.flops = 4 * w.D * w.H_q * pairs
+        self.tokens = int(n.sum())
+
+    def step(self, stream):
+        N, w = self.N, self.w
+        N.pa_kv_append_tokens(self.desc, self.k, self.v, self.new_k, self.new_v, self.tokens, self.new_seq,
+                              self.new_pos, self.tables, self.err, stream)
+        N.pa_prefill_attention(self.desc, self.out, self.q, self.k, self.v, self.tables, self.q_start, self.ctx,
+                               self.max_q, w.scale, self.err, stream)
+
+    def run(self, steps, warmup):
+        torch = self.torch
+        sid = torch.cuda.current_stream().cuda_stream
+        for _ in range(warmup):
+            self.step(sid)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            self.step(sid)
+        t1.record()
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / 1e3 / steps
+
+
 def cpu_baseline_sample(name, budget_s=15.0, max_seqs=None):
     """The oracle, as it stands, on a bounded sample of the workload: whole decode steps
     (append + attention) of the first sequences, on this host's CPU.  Run in a spawned child
@@ -552,6 +616,20 @@ def run_native(args):
             del nb
             torch.cuda.empty_cache()
 
+    next_rows = {}
+    if rank == 0 and not args.no_next:
+        pb = PrefillBench(device)
+        sec = pb.run(max(20, args.steps // 50), args.warmup)
+        bf16_peak = _bf16_peak()
+        next_rows["chunked_prefill"] = {
+            "workload": f"{pb.w.B} sequences, cached U[0..3584], chunk {pb.max_q} tokens, "
+                        f"{pb.w.H_q}/{pb.w.H_kv} heads, d {pb.w.D}, bf16",
+            "ms_per_step": round(sec * 1e3, 4), "tflops": round(pb.flops / sec / 1e12, 1),
+            "frac_of_bf16_peak": round(pb.flops / sec / 1e12 / bf16_peak, 4),
+            "prefill_tokens_per_s_per_layer": round(pb.tokens / sec, 1), "err_flag": int(pb.err.item())}
+        del pb
+        torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         r = cpu_baseline_sample(args.config, budget_s=args.cpu_seconds, max_seqs=8)
@@ -593,6 +671,8 @@ def run_native(args):
         }
         if extra:
             line["also"] = extra
+        if next_rows:
+            line["next_rows"] = next_rows
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -609,6 +689,7 @@ def main(argv=None):
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--also", default="70b")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the rows beyond decode (chunked prefill)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per attention call of this build (null when unknown)")

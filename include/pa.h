@@ -171,6 +171,27 @@ pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, const void* 
                               void* workspace, size_t workspace_bytes,
                               int32_t* err_flag, void* stream);
 
+/* ---------------------------------------------------------------------------------
+ * Chunked-prefill (extend) attention over the paged cache (ldpk §2.2: under the causal mask the
+ * query of position i attends to positions up to i; ldpk §7: long prompts are prefilled in
+ * chunks).  Sequence s contributes the query rows q_start[s] .. q_start[s+1]-1 of q: they are its
+ * last n_s = q_start[s+1] - q_start[s] positions, ctx-n_s .. ctx-1 with ctx = context_lens[s],
+ * and their K/V must already be in the cache (pa_kv_append_tokens).  The query at position p
+ * attends to positions 0..p of its sequence.
+ *   q, out            bf16 [T][num_q_heads][head_dim], T >= q_start[num_seqs]
+ *   q_start           device int32 [num_seqs + 1], non-decreasing
+ *   max_query_len     bounds every n_s (it sizes the grid)
+ * Supported: bf16 caches without sinks (anything else returns PA_ERR_UNSUPPORTED).  A sequence
+ * with n_s < 0, n_s > ctx, n_s > max_query_len or ctx beyond its table sets
+ * PA_EFLAG_CTX_OVERFLOW and gets zero rows; a table entry outside [0, num_blocks) sets
+ * PA_EFLAG_BAD_BLOCK_ID and zeroes the rows of every query tile whose keys include it.
+ * Host errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA. */
+pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, const void* q,
+                               const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* q_start,
+                               const int32_t* context_lens, int max_query_len, float scale,
+                               int32_t* err_flag, void* stream);
+
 /* Allocation-free decode attention.  The pages have no counterpart to this entry point: it is
  * pa_decode_attention for callers that cannot allocate device memory when they call it, for
  * example a plugin running inside a host framework that owns every byte of device memory, a

@@ -24,8 +24,6 @@
 //    log-sum-exp.  A warp that saw a whole sequence writes the bf16 output directly.
 //  * Every wait is bounded; invalid table entries and contexts set error bits and zero rows.
 
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -382,6 +380,11 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
   const int nthreads = blockDim.x;
   // The merge kernel may be scheduled now; it waits for this grid before reading its output.
   grid_dep_launch_dependents();
+  // This kernel may have been launched while the previous kernel of the stream still runs
+  // (programmatic dependent launch); whatever that kernel is, it may have produced any input
+  // read below (q, context lengths, tables, the cache), so wait for it first.  What overlaps is
+  // the launch and the CTA set-up.
+  grid_dep_wait();
 
   // ---- this CTA's range [u0, u1) of the (sequence, logical block) list ----
   int hgi, seq_base, nseq, u0, u1;
@@ -432,17 +435,11 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       for (int i = tid; i <= p.B; i += nthreads) p.ws_meta[i] = sm.cum[i];
       if (tid == 0) p.ws_meta[p.B + 1] = T;
     }
-    if (T == 0) {
-      grid_dep_wait();
-      return;
-    }
+    if (T == 0) return;
     const int W = (T + gridDim.x - 1) / gridDim.x;
     u0 = blockIdx.x * W;
     u1 = min(T, u0 + W);
-    if (u0 >= u1) {
-      grid_dep_wait();  // completion of this grid then implies completion of its predecessor
-      return;
-    }
+    if (u0 >= u1) return;
   } else {
     hgi = blockIdx.z;
     seq_base = blockIdx.y;
@@ -458,10 +455,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     }
     u0 = blockIdx.x * p.ppb;
     u1 = min(nbv, u0 + p.ppb);
-    if (u0 >= u1) {
-      grid_dep_wait();
-      return;
-    }
+    if (u0 >= u1) return;
   }
 
   if (tid == 0) {
@@ -499,9 +493,6 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     int base = u0;
     int cur_pb = load_entry(base + lane);
     int nxt_pb = load_entry(base + 32 + lane);
-    // The cache may have been written by the kernel just before this one (the append):
-    // wait for it before the first TMA read.
-    grid_dep_wait();
     int4 my_meta;
     unsigned live_mask;
     auto pack = [&]() {
@@ -796,37 +787,6 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
       pl->n_slots * pl->nbs * static_cast<size_t>(d->num_q_heads) * (d->head_dim + 4) * sizeof(float);
   pl->ws_bytes = pl->meta_bytes + partial_bytes;
   return PA_OK;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// The cache as a 3-D tensor: (128-byte chunk of a head row, kv_head x chunk, slot).  One box is
-// one head row (nc chunks) of 16 consecutive slots, i.e. of one physical block, and lands in
-// shared memory as [slot][chunk][128 B] with the 128-byte swizzle.
-bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int rows, int nc, long long slots) {
-  auto fn = tensor_map_encoder();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / elem_bytes), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(slots)};
-  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(rows) * 128};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(nc), PA_BLOCK_SIZE};
-  cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, bool QUANT>

@@ -1,6 +1,7 @@
 // Host-side helpers shared by the translation units of the library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <utility>
@@ -15,6 +16,11 @@ inline bool is_quantized(const pa_cache_desc* d) { return d->k_dtype != PA_BF16;
 
 // Checks a cache description against what the kernels implement.
 pa_status validate_desc(const pa_cache_desc* d);
+
+// TMA descriptor of a paged cache pool viewed as (128-byte chunk, kv_head x chunk, slot) with
+// boxes of `box_rows` chunks x 16 slots (tensor_map.cpp).
+bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int rows, int box_rows,
+                      long long slots);
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 

@@ -1,0 +1,48 @@
+// TMA tensor maps over the slot-major paged cache (host side).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+}  // namespace
+
+// The cache as a 3-D tensor: (128-byte chunk of a head row, kv_head x chunk, slot).  One box is
+// `box_rows` consecutive 128-byte rows (chunks of one head row) of 16 consecutive slots, i.e. of
+// one physical block, and lands in shared memory as [slot][row][128 B] with the 128-byte
+// swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int rows, int box_rows,
+                      long long slots) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / elem_bytes), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(slots)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(rows) * 128};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(box_rows),
+                       PA_BLOCK_SIZE};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace pa

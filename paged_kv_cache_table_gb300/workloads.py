@@ -17,6 +17,9 @@ Workloads (seed = 20260 + index):
   5 "long_quant"  4 sequences of 131072 cached tokens, 32 / 8 heads, d 128, K stored FP8 E4M3
                   and V INT8 with per-KV-head scales from the absmax of the data, the first 4
                   positions kept in bf16 (sinks).
+  6 "prefill_chunk"  8 sequences with cached lengths uniform in [0, 3584] each receiving a chunk
+                  of 512 new tokens (queries + their K/V), 32 / 8 heads, d 128
+                  (make_prefill_workload).
 Every step appends one token per sequence at position = cached length, then attends over
 cached length + 1 tokens.  All tensors are produced on the CPU with a torch.Generator.
 """
@@ -197,3 +200,77 @@ def make_workload(name: str, steps: int = 1, **overrides) -> Workload:
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """The raw bit patterns of a bf16 tensor as uint16 (for the oracle's exact decoding)."""
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@dataclass
+class PrefillWorkload:
+    """A chunk of new tokens per sequence on top of an already cached prefix."""
+    name: str
+    seed: int
+    B: int
+    H_q: int
+    H_kv: int
+    D: int
+    scale: float
+    num_blocks: int
+    max_blocks: int
+    ctx_old: np.ndarray        # int32 [B] cached tokens before the chunk
+    chunk: np.ndarray          # int32 [B] new tokens per sequence
+    tables: np.ndarray         # int32 [B][max_blocks], blocks for cached + chunk positions
+    fill_k: torch.Tensor       # bf16 [N][H_kv][D] cached tokens
+    fill_v: torch.Tensor
+    fill_seq: np.ndarray
+    fill_pos: np.ndarray
+    new_k: torch.Tensor        # bf16 [T][H_kv][D] the chunk's tokens, sequence-major
+    new_v: torch.Tensor
+    new_seq: np.ndarray        # int32 [T]
+    new_pos: np.ndarray        # int32 [T]
+    q: torch.Tensor            # bf16 [T][H_q][D]
+
+    @property
+    def G(self) -> int:
+        return self.H_q // self.H_kv
+
+    def q_start(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.chunk)]).astype(np.int32)
+
+    def context_lens(self) -> np.ndarray:
+        return (self.ctx_old + self.chunk).astype(np.int32)
+
+
+def make_prefill_workload(B=8, H_q=32, H_kv=8, D=128, cached_range=(0, 3584), chunk=512,
+                          cached_list=None, chunk_list=None, seed=20266, name="prefill_chunk"):
+    g = torch.Generator().manual_seed(seed)
+    if cached_list is not None:
+        ctx = np.array(cached_list, dtype=np.int64)
+        B = len(ctx)
+    else:
+        lo, hi = cached_range
+        ctx = torch.randint(lo, hi + 1, (B,), generator=g).numpy().astype(np.int64)
+    n = np.array(chunk_list if chunk_list is not None else [chunk] * B, dtype=np.int64)
+    total = ctx + n
+    need = int(sum(_blocks(t) for t in total))
+    num_blocks = max(1, int(math.ceil(1.1 * need)))
+    max_blocks = max(1, int(max(_blocks(t) for t in total)))
+    perm = torch.randperm(num_blocks, generator=g).numpy().astype(np.int32)
+    tables = np.full((B, max_blocks), -1, dtype=np.int32)
+    k = 0
+    for s in range(B):
+        m = _blocks(total[s])
+        tables[s, :m] = perm[k:k + m]
+        k += m
+    fill_seq = np.repeat(np.arange(B, dtype=np.int32), ctx)
+    fill_pos = np.concatenate([np.arange(c, dtype=np.int32) for c in ctx]) if B else np.zeros(0, np.int32)
+    new_seq = np.repeat(np.arange(B, dtype=np.int32), n)
+    new_pos = np.concatenate([np.arange(c, c + m, dtype=np.int32) for c, m in zip(ctx, n)])
+    fill_k = _randn_bf16(g, (len(fill_seq), H_kv, D))
+    fill_v = _randn_bf16(g, (len(fill_seq), H_kv, D))
+    T = int(n.sum())
+    new_k = _randn_bf16(g, (T, H_kv, D))
+    new_v = _randn_bf16(g, (T, H_kv, D))
+    q = _randn_bf16(g, (T, H_q, D))
+    return PrefillWorkload(name=name, seed=seed, B=B, H_q=H_q, H_kv=H_kv, D=D, scale=1.0 / math.sqrt(D),
+                           num_blocks=num_blocks, max_blocks=max_blocks, ctx_old=ctx.astype(np.int32),
+                           chunk=n.astype(np.int32), tables=tables, fill_k=fill_k, fill_v=fill_v,
+                           fill_seq=fill_seq, fill_pos=fill_pos, new_k=new_k, new_v=new_v,
+                           new_seq=new_seq, new_pos=new_pos, q=q)
