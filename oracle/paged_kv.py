@@ -19,7 +19,11 @@ Readings taken where the pages are silent (each repeated where it is used):
   * the quantiser divides in IEEE fp32 (x_fp32 / scale_fp32) before rounding;
   * sink positions (pos < num_sink) live in a separate bf16 buffer and the paged slot
     is left untouched;
-  * the block pool hands out the lowest-numbered free block.
+  * the block pool hands out the lowest-numbered free block;
+  * sliding window W (ldpk §5.3): the query at position p attends positions
+    max(0, p - W + 1) .. p, i.e. the most recent W tokens with itself included, and W = 0
+    means no window; a block is freed once all its positions lie before the window of the
+    sequence's latest query (the block is the pool's unit, 显存账本 §四).
 
 Everything is numpy; floating point is fp64 except the fp32 quantiser division.
 """
@@ -38,6 +42,7 @@ __all__ = [
     "locate",
     "slots_of_sequence",
     "blocks_needed",
+    "window_start",
     "bf16_bits_to_f64",
     "f32_to_bf16_bits",
     "E4M3_MAX",
@@ -305,6 +310,26 @@ class BlockPool:
                 row[i] = -1
         return freed
 
+    def slide_window(self, row, ctx: int, window: int) -> int:
+        """Release the blocks of one sequence that no later query can reach.
+
+        ldpk §5.3: under a sliding window of W tokens only the K and V of the most recent W
+        positions are kept and older ones are dropped, so the cache stays O(W).  The pool's unit
+        is the block (显存账本 §四), so a block goes only when every one of its positions lies
+        before ctx - W, the window start of the sequence's latest query.  Its table entry
+        becomes -1 and it loses one reference (a shared block stays with its other holders).
+        Returns the number of blocks that went back to the free list.
+        """
+        if window <= 0 or ctx <= window:
+            return 0
+        freed = 0
+        for lb in range((ctx - window) // self.block_size):
+            if row[lb] >= 0:
+                if self.decref(int(row[lb])) == 0:
+                    freed += 1
+                row[lb] = -1
+        return freed
+
     def prepare_append(self, row, pos: int):
         """Make the slot of ``pos`` writable for this sequence.
 
@@ -419,23 +444,27 @@ class PagedKVCache:
         sc = np.asarray(self.v_scales, dtype=np.float32).astype(np.float64)
         return vals * (sc if heads is None else sc[heads])[..., :, None]
 
-    def gather(self, seq: int, table_row, ctx: int):
-        """K and V of positions 0..ctx-1 as contiguous fp64 arrays [ctx][kv_heads][dim].
+    def gather(self, seq: int, table_row, ctx: int, start: int = 0):
+        """K and V of positions start..ctx-1 as contiguous fp64 arrays [ctx - start][kv_heads][dim].
 
         ldpk §4.3: the attention path fetches K and V from non-contiguous places through
         the block table.  Codes are decoded exactly and multiplied by their per-head
-        scale in fp64; sink positions come from the sink buffer.
+        scale in fp64; sink positions come from the sink buffer.  Positions before
+        ``start`` (outside a sliding window) are never looked up, so their table entries may
+        already be released (-1).
         """
-        K = np.zeros((ctx, self.num_kv_heads, self.head_dim))
-        V = np.zeros((ctx, self.num_kv_heads, self.head_dim))
-        n_sink = min(ctx, self.num_sink)
-        if n_sink:
-            K[:n_sink] = bf16_bits_to_f64(self.k_sink[seq, :n_sink])
-            V[:n_sink] = bf16_bits_to_f64(self.v_sink[seq, :n_sink])
-        if ctx > n_sink:
-            slots = np.array([locate(table_row, p, self.block_size) for p in range(n_sink, ctx)])
-            K[n_sink:] = self._decode_k(self.k[slots])
-            V[n_sink:] = self._decode_v(self.v[slots])
+        n = max(0, ctx - start)
+        K = np.zeros((n, self.num_kv_heads, self.head_dim))
+        V = np.zeros((n, self.num_kv_heads, self.head_dim))
+        for i, p in enumerate(range(start, ctx)):
+            if p < self.num_sink:
+                K[i] = bf16_bits_to_f64(self.k_sink[seq, p])
+                V[i] = bf16_bits_to_f64(self.v_sink[seq, p])
+        paged = [p for p in range(start, ctx) if p >= self.num_sink]
+        if paged:
+            slots = np.array([locate(table_row, p, self.block_size) for p in paged])
+            K[n - len(paged):] = self._decode_k(self.k[slots])
+            V[n - len(paged):] = self._decode_v(self.v[slots])
         return K, V
 
 
@@ -462,6 +491,12 @@ class ContiguousKVCache:
 # ----------------------------------------------------------------------------------
 # Attention
 # ----------------------------------------------------------------------------------
+def window_start(ctx: int, window: int) -> int:
+    """First position a decode query of a ctx-token sequence attends (ldpk §5.3: only the most
+    recent W tokens, the query's own included); window <= 0 means the whole context."""
+    return max(0, ctx - window) if window > 0 else 0
+
+
 def softmax_weights(scores) -> np.ndarray:
     """softmax with the maximum subtracted before exp (fp64)."""
     s = np.asarray(scores, dtype=np.float64)
@@ -469,12 +504,14 @@ def softmax_weights(scores) -> np.ndarray:
     return w / w.sum()
 
 
-def decode_attention(q, K, V, scale: float) -> np.ndarray:
-    """One decode query per head against all cached tokens of one sequence.
+def decode_attention(q, K, V, scale: float, window: int = 0) -> np.ndarray:
+    """One decode query per head against the cached tokens of one sequence.
 
     ldpk §2.1: Attention(Q, K, V) = softmax(Q K^T / sqrt(d_head)) V; in decode there is
     one query row per head (ldpk §2.2).  显存账本 §二: under GQA every g query heads share
     one KV head; the grouping is contiguous (query head h reads KV head h // g).
+    ldpk §5.3: with a sliding window of W tokens the query (at position ctx - 1) attends only
+    positions ctx - W .. ctx - 1.
 
     q: [H_q][d], K and V: [ctx][H_kv][d], all fp64.  ctx == 0 gives zeros.
     """
@@ -485,11 +522,12 @@ def decode_attention(q, K, V, scale: float) -> np.ndarray:
     if ctx == 0:
         return out
     G = H_q // H_kv
+    a = window_start(ctx, window)
     for h in range(H_q):
         kv = h // G
-        scores = scale * (K[:, kv, :] @ q[h])
+        scores = scale * (K[a:, kv, :] @ q[h])
         w = softmax_weights(scores)
-        out[h] = w @ V[:, kv, :]
+        out[h] = w @ V[a:, kv, :]
     return out
 
 
@@ -543,14 +581,16 @@ def decode_attention_split(q, K, V, scale: float, partition_tokens: int):
     return merge_partials(decode_attention_partials(q, K, V, scale, bounds))
 
 
-def prefill_attention(q, K, V, scale: float, first_pos: int) -> np.ndarray:
+def prefill_attention(q, K, V, scale: float, first_pos: int, window: int = 0) -> np.ndarray:
     """Causal attention of a chunk of new query tokens over one sequence's cached K/V.
 
     ldpk §2.2: during prefill every position's query attends to the keys of positions 1..i under
     the causal mask, and only K and V are kept; ldpk §7 splits a long prompt into chunks.  The
     chunk's queries sit at positions first_pos .. first_pos + n - 1 (their own K/V are already in
     the cache), and the query at position p reads keys 0..p.  GQA grouping as in
-    decode_attention.  q: [n][H_q][d], K and V: [ctx][H_kv][d] with ctx >= first_pos + n (fp64).
+    decode_attention.  With a sliding window of W tokens (ldpk §5.3) the query at position p
+    reads keys max(0, p - W + 1) .. p instead.
+    q: [n][H_q][d], K and V: [ctx][H_kv][d] with ctx >= first_pos + n (fp64).
     """
     q = np.asarray(q, dtype=np.float64)
     n, H_q, d = q.shape
@@ -559,8 +599,9 @@ def prefill_attention(q, K, V, scale: float, first_pos: int) -> np.ndarray:
     out = np.zeros((n, H_q, d))
     for i in range(n):
         p = first_pos + i
+        a = window_start(p + 1, window)
         for h in range(H_q):
             kv = h // G
-            scores = scale * (K[:p + 1, kv, :] @ q[i, h])
-            out[i, h] = softmax_weights(scores) @ V[:p + 1, kv, :]
+            scores = scale * (K[a:p + 1, kv, :] @ q[i, h])
+            out[i, h] = softmax_weights(scores) @ V[a:p + 1, kv, :]
     return out
