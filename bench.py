@@ -80,13 +80,14 @@ def ncu_traffic(workload: str):
 
 def seq_bytes(w, ctx_s: int) -> int:
     """Algorithmic bytes one sequence contributes to a decode-attention call: its attended K
-    and V (sink positions counted at bf16), its q and out rows, the block-table entries it uses
-    and its context length."""
+    and V (sink positions counted at bf16; under a sliding window only the window's positions),
+    its q and out rows, the block-table entries it uses and its context length."""
     e = w.kv_elem_bytes()
     ctx_s = int(ctx_s)
-    n_sink = min(ctx_s, w.num_sink)
-    kv = (ctx_s - n_sink) * w.H_kv * w.D * e * 2 + n_sink * w.H_kv * w.D * 2 * 2
-    return kv + 2 * w.H_q * w.D * 2 + (-(-ctx_s // 16)) * 4 + 4
+    lo = max(0, ctx_s - w.window) if w.window else 0
+    n_sink = max(0, min(ctx_s, w.num_sink) - lo)
+    kv = (ctx_s - lo - n_sink) * w.H_kv * w.D * e * 2 + n_sink * w.H_kv * w.D * 2 * 2
+    return kv + 2 * w.H_q * w.D * 2 + (-(-ctx_s // 16) - lo // 16) * 4 + 4
 
 
 def attention_bytes(w, ctx: np.ndarray) -> int:
@@ -188,14 +189,14 @@ class ClockSampler:
 class DecodeBench:
     """One layer's paged cache and the per-step inputs of a WINDOW-step cycle, on one GPU."""
 
-    def __init__(self, name, device, partition=0):
+    def __init__(self, name, device, partition=0, horizon=None):
         import torch
         from paged_kv_cache_table_gb300 import native as N
         from paged_kv_cache_table_gb300.workloads import make_workload
         self.torch, self.N = torch, N
         self.dev = device
         self.partition = partition
-        w = make_workload(name, steps=WINDOW)
+        w = make_workload(name, steps=WINDOW, **({"horizon": horizon} if horizon else {}))
         self.w = w
         n_slots = w.num_blocks * 16
         kvdt = torch.bfloat16 if w.k_dtype == "bf16" else torch.uint8
@@ -208,7 +209,8 @@ class DecodeBench:
             self.k_sink = torch.empty((w.B, w.num_sink, w.H_kv, w.D), dtype=torch.bfloat16, device=device)
             self.v_sink = torch.empty_like(self.k_sink)
         self.desc = N.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks, w.k_dtype, w.v_dtype,
-                                self.k_scales, self.v_scales, self.k_sink, self.v_sink, w.num_sink)
+                                self.k_scales, self.v_scales, self.k_sink, self.v_sink, w.num_sink,
+                                sliding_window=w.window)
         self.tables = w.tables.copy()
         self.tables_dev = torch.from_numpy(self.tables).to(device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -410,6 +412,86 @@ class DecodeBench:
         torch.cuda.synchronize()
         barrier(self.dev)
         return t0.elapsed_time(t1) / 1e3, nbytes
+
+
+class SlidingBench(DecodeBench):
+    """Sliding-window decode: positions keep advancing (no wrap-around), every step makes the
+    append slot writable, appends, attends over the window and then releases the blocks behind
+    it (pa_bm_slide_window), so the pool holds O(window) blocks per sequence however long the
+    sequences grow.  The table goes up whenever a step changed it (an allocation or a release);
+    q/k/v reuse a WINDOW-step ring of inputs."""
+
+    def __init__(self, name, device, horizon):
+        super().__init__(name, device, 0, horizon=horizon)
+        torch, w = self.torch, self.w
+        self.horizon = horizon
+        self.t = 0
+        self.dirty = False
+        self.pos_all = [(w.ctx_old + t).astype(np.int32) for t in range(horizon)]
+        self.ctx_all = [(w.ctx_old + t + 1).astype(np.int32) for t in range(horizon)]
+        self.pos_all_dev = torch.from_numpy(np.stack(self.pos_all)).to(device)
+        self.ctx_all_dev = torch.from_numpy(np.stack(self.ctx_all)).to(device)
+        self.max_ctx = int(self.ctx_all[-1].max())
+        self.ws_bytes = self.N.pa_decode_workspace_size(self.desc, self.max_ctx, 0)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.ptr["ws"] = self.ws.data_ptr()
+        self.tab_ev = [None] * WINDOW
+        self.uploads = 0
+        self.held_blocks_max = 0
+
+    def bytes_at(self, t):
+        return attention_bytes(self.w, self.ctx_all[t])
+
+    def step(self, i, stream, ev=None, buf=None):
+        torch, N, w, P = self.torch, self.N, self.w, self.ptr
+        t = self.t
+        if t >= self.horizon:
+            raise RuntimeError("sliding bench ran past its horizon")
+        self.t += 1
+        j = t % WINDOW
+        pairs, changed = self.bm.prepare_step(self.tables, self.pos_all[t])
+        if len(pairs):
+            raise RuntimeError("unexpected copy-on-write in the sliding-window workload")
+        if changed or self.dirty:
+            if self.tab_ev[j] is not None:
+                self.tab_ev[j].synchronize()  # the copy that last read this pinned slot is done
+            self.tab_ring[j].numpy()[...] = self.tables
+            self.tables_dev.copy_(self.tab_ring[j], non_blocking=True)
+            self.tab_ev[j] = torch.cuda.Event()
+            self.tab_ev[j].record()
+            self.uploads += 1
+        q, kn, vn = self.ptr_step[j][:3]
+        pos = self.pos_all_dev[t].data_ptr()
+        ctx = self.ctx_all_dev[t].data_ptr()
+        N.pa_kv_append(self.desc, P["k"], P["v"], kn, vn, P["tab"], pos, P["err"], stream)
+        if ev is not None:
+            ev[0].record()
+        N.pa_decode_attention(self.desc, P["out"], q, P["k"], P["v"], P["tab"], ctx, self.max_ctx, w.scale,
+                              0, P["ws"], self.ws_bytes, P["err"], stream)
+        if ev is not None:
+            ev[1].record()
+        released, _ = self.bm.slide_window(self.tables, self.ctx_all[t], w.window)
+        self.dirty = released > 0
+        self.held_blocks_max = max(self.held_blocks_max, w.num_blocks - self.bm.num_free())
+
+    def run(self, steps, warmup, per_call_events=False):
+        torch = self.torch
+        sid = torch.cuda.current_stream().cuda_stream
+        for i in range(warmup):
+            self.step(i, sid)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)] if per_call_events else None
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        first = self.t
+        t0.record()
+        for k in range(steps):
+            self.step(k, sid, ev=None if evs is None else evs[k])
+        t1.record()
+        torch.cuda.synchronize()
+        nbytes = sum(self.bytes_at(t) for t in range(first, first + steps))
+        att = None if evs is None else [a.elapsed_time(b) for a, b in evs]
+        return t0.elapsed_time(t1) / 1e3, att, nbytes
 
 
 class PrefillBench:
@@ -628,6 +710,29 @@ def run_native(args):
             "frac_of_bf16_peak": round(pb.flops / sec / 1e12 / bf16_peak, 4),
             "prefill_tokens_per_s_per_layer": round(pb.tokens / sec, 1), "err_flag": int(pb.err.item())}
         del pb
+        torch.cuda.empty_cache()
+        n_sw = max(100, args.steps // 4)
+        sb = SlidingBench("swa", device, horizon=2 * (n_sw + args.warmup))
+        e_sw, _, by_sw = sb.run(n_sw, args.warmup)
+        _, a_sw, _ = sb.run(n_sw, args.warmup, per_call_events=True)
+        first = sb.t - n_sw
+        ab_sw = float(np.mean([sb.bytes_at(t) for t in range(first, sb.t)]))
+        a_ms = float(np.mean(a_sw))
+        sw = sb.w
+        next_rows["sliding_window_decode"] = {
+            "workload": f"swa: B={sw.B}, H_q={sw.H_q}, H_kv={sw.H_kv}, d={sw.D}, window {sw.window}, cached ctx "
+                        f"U[{int(sw.ctx_old.min())}..{int(sw.ctx_old.max())}], positions advancing, blocks "
+                        f"released behind the window every step",
+            "value": round(by_sw / e_sw / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(1e3 * e_sw / n_sw, 4),
+            "tokens_per_s_per_layer": round(sw.B * n_sw / e_sw, 1),
+            "attention_gbs": round(ab_sw / (a_ms / 1e3) / 1e9, 1),
+            "attention_frac": round(ab_sw / (a_ms / 1e3) / 1e9 / peak, 4),
+            "attention_ms_per_call": round(a_ms, 5),
+            "table_uploads": sb.uploads, "table_bytes": int(sb.tables.nbytes),
+            "held_blocks_max": sb.held_blocks_max, "pool_blocks": sw.num_blocks,
+            "err_flag": int(sb.err.item())}
+        del sb
         torch.cuda.empty_cache()
 
     cpu = None

@@ -15,6 +15,9 @@
  *     head h reads KV head h / G, G = num_q_heads / num_kv_heads (显存账本 §二, GQA).
  *   - Optional 8-bit caches store K as FP8 E4M3 and V as INT8 with one fp32 scale per KV
  *     head, and keep the first num_sink positions of every sequence in bf16 (显存账本 §七).
+ *   - Optional sliding window of W tokens (ldpk §5.3): each query attends only the most
+ *     recent W positions, its own included, and blocks that fall wholly before the window
+ *     go back to the pool (pa_bm_slide_window), so a sequence holds O(W) cache.
  *
  * Memory layout (all row-major, all device memory unless stated otherwise):
  *   k_cache, v_cache  [num_blocks * 16][num_kv_heads][head_dim]  element type per k/v_dtype
@@ -80,7 +83,12 @@ typedef enum {
  * num_q_heads % num_kv_heads == 0 with G = num_q_heads/num_kv_heads <= 8;
  * (k_dtype, v_dtype) = (PA_BF16, PA_BF16) or (PA_FP8_E4M3, PA_INT8), the latter with
  * head_dim 128.  k_scales/v_scales are required for 8-bit dtypes and ignored otherwise.
- * num_sink > 0 keeps positions < num_sink in k_sink/v_sink (bf16) for any dtype. */
+ * num_sink > 0 keeps positions < num_sink in k_sink/v_sink (bf16) for any dtype.
+ * sliding_window = W > 0 restricts every query to the W most recent positions (ldpk §5.3):
+ * a decode query of a ctx-token sequence reads positions max(0, ctx-W) .. ctx-1, a prefill
+ * query at position p reads max(0, p-W+1) .. p.  Table entries of logical blocks that lie
+ * wholly before those positions are never read (they may be -1 after pa_bm_slide_window);
+ * sink positions take part only when they fall inside the window.  0 = whole context. */
 typedef struct {
   int num_seqs;
   int num_q_heads;
@@ -96,6 +104,7 @@ typedef struct {
   void* k_sink;          /* device bf16 [num_seqs][num_sink][num_kv_heads][head_dim] or NULL */
   void* v_sink;
   int num_sink;          /* 0 when unused */
+  int sliding_window;    /* W > 0: attend the last W positions only; 0 = whole context */
 } pa_cache_desc;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -150,6 +159,8 @@ pa_status pa_block_copy(const pa_cache_desc* desc, void* k_cache, void* v_cache,
  * ctx = context_lens[s]:  out[s][h] = sum_t softmax_t(scale * q[s][h]·K_t) V_t, with
  * fp32 accumulation and the result rounded to bf16.  K_t/V_t are the bf16 values, or
  * code*scale for 8-bit caches, or the sink rows for t < num_sink.  ctx == 0 gives zeros.
+ * With desc->sliding_window = W > 0 the positions are max(0, ctx-W) .. ctx-1 instead, and
+ * only the table entries of the logical blocks holding them are read.
  *
  * partition_size: 0 = automatic (the cached blocks of all sequences are split evenly over
  * the GPU's SMs; partial results are merged by a second kernel); a positive multiple of 16
@@ -177,7 +188,8 @@ pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, const void* 
  * chunks).  Sequence s contributes the query rows q_start[s] .. q_start[s+1]-1 of q: they are its
  * last n_s = q_start[s+1] - q_start[s] positions, ctx-n_s .. ctx-1 with ctx = context_lens[s],
  * and their K/V must already be in the cache (pa_kv_append_tokens).  The query at position p
- * attends to positions 0..p of its sequence.
+ * attends to positions 0..p of its sequence, or max(0, p-W+1) .. p under a sliding window W
+ * (desc->sliding_window, ldpk §5.3).
  *   q, out            bf16 [T][num_q_heads][head_dim], T >= q_start[num_seqs]
  *   q_start           device int32 [num_seqs + 1], non-decreasing
  *   max_query_len     bounds every n_s (it sizes the grid)
@@ -255,6 +267,19 @@ int pa_bm_release(pa_bm* bm, int32_t* row, int n_blocks);
 pa_status pa_bm_prepare_step(pa_bm* bm, int32_t* block_tables, int num_seqs,
                              int max_blocks_per_seq, const int32_t* positions,
                              int32_t* cow_pairs, int* n_pairs, int* n_changed);
+
+/* Sliding-window release (ldpk §5.3: only the most recent W positions are kept, so the cache
+ * stays O(W)).  For every sequence s with c = context_lens[s] > window > 0, each logical block
+ * lying wholly before position c - window (blocks 0 .. (c-window)/16 - 1) that still holds a
+ * physical block is decref-ed (freed at zero; a shared block stays with its other holders)
+ * and its host table entry set to -1.  Call it after the attention that used context_lens;
+ * later queries of those sequences never reach the released positions.  Entries already -1
+ * and sequences with c <= window are left alone.  Returns the number of table entries
+ * released, and *n_freed (may be NULL) the number of blocks that went back to the free list;
+ * -1 on invalid arguments (nothing changed) or on a table entry the pool does not hold (the
+ * sequences before it keep their changes). */
+int pa_bm_slide_window(pa_bm* bm, int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                       const int32_t* context_lens, int window, int* n_freed);
 
 #ifdef __cplusplus
 }

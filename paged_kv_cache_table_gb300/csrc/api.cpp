@@ -8,7 +8,8 @@ namespace pa {
 pa_status validate_desc(const pa_cache_desc* d) {
   if (!d) return PA_ERR_INVALID_ARG;
   if (d->num_seqs < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 ||
-      d->block_size <= 0 || d->num_blocks <= 0 || d->max_blocks_per_seq <= 0 || d->num_sink < 0)
+      d->block_size <= 0 || d->num_blocks <= 0 || d->max_blocks_per_seq <= 0 || d->num_sink < 0 ||
+      d->sliding_window < 0)
     return PA_ERR_INVALID_ARG;
   if (d->num_q_heads % d->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
   if (d->block_size != PA_BLOCK_SIZE) return PA_ERR_UNSUPPORTED;

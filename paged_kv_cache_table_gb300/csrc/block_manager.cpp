@@ -8,6 +8,10 @@
 // a block is recycled only when its count reaches zero, and a sequence that writes into a
 // shared block copies it first; §2.3: blocks go back to the pool on every exit path.
 //
+// Untitled KV-cache article at ldpk.cn/news/58971 §5.3: under a sliding window only the most
+// recent W positions' K and V are kept; pa_bm_slide_window hands back, block by block, what
+// falls behind the window.
+//
 // One mutex guards the pool, so concurrent callers never corrupt a count.  The free list
 // is a min-heap: allocation returns the lowest-numbered free block (a deterministic policy
 // that makes table contents reproducible).
@@ -197,6 +201,38 @@ pa_status pa_bm_prepare_step(pa_bm* bm, int32_t* block_tables, int num_seqs,
   *n_pairs = pairs;
   if (n_changed) *n_changed = changed;
   return st;
+}
+
+int pa_bm_slide_window(pa_bm* bm, int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                       const int32_t* context_lens, int window, int* n_freed) {
+  if (n_freed) *n_freed = 0;
+  if (!bm || !block_tables || !context_lens || num_seqs < 0 || max_blocks_per_seq <= 0 || window < 0)
+    return -1;
+  if (window == 0) return 0;
+  std::lock_guard<std::mutex> g(bm->mu);
+  int released = 0, freed = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int c = context_lens[s];
+    if (c <= window) continue;
+    const int n = std::min((c - window) / bm->block_size, max_blocks_per_seq);
+    int32_t* row = block_tables + (size_t)s * max_blocks_per_seq;
+    for (int lb = 0; lb < n; ++lb) {
+      const int b = row[lb];
+      if (b < 0) continue;
+      if (!bm->valid_allocated(b)) {
+        if (n_freed) *n_freed = freed;
+        return -1;
+      }
+      if (--bm->refcount[b] == 0) {
+        bm->release_locked(b);
+        ++freed;
+      }
+      row[lb] = -1;
+      ++released;
+    }
+  }
+  if (n_freed) *n_freed = freed;
+  return released;
 }
 
 }  // extern "C"

@@ -5,6 +5,8 @@
 // PagedAttention 与连续批处理" §二): every G consecutive query heads read one KV head.  The keys
 // and values are fetched from non-contiguous physical blocks through the block table
 // (ldpk §4.3; 显存账本 §四 locate()).  8-bit caches (显存账本 §七) are decoded in registers.
+// Under a sliding window (ldpk §5.3) only the blocks holding the last W positions are listed,
+// so the work, the bytes and the table entries read scale with W, not with the context.
 //
 // Design (GB300, sm_103a):
 //  * Work unit = one 16-token physical block of one head group.  A CTA owns a contiguous range
@@ -55,6 +57,7 @@ constexpr float kNegInf = -INFINITY;
 
 struct DecodeParams {
   int B, H_q, H_kv, G, num_blocks, max_blocks, num_sink, max_ctx;
+  int window;  // sliding window in tokens, 0 = whole context
   int hg, nc, nbs, stages, warps_c;
   int mode;  // 0 balanced, 1 fixed partitions
   int ppb, max_parts;
@@ -79,6 +82,18 @@ __device__ __forceinline__ int seq_blocks(const DecodeParams& p, int ctx) {
   if (ctx == 0) return 0;
   if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_blocks * PA_BLOCK_SIZE) return -1;
   return (ctx + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+}
+
+// First position the query attends: the last `window` positions (ldpk §5.3), else 0.
+__device__ __forceinline__ int window_lo(const DecodeParams& p, int ctx) {
+  return (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
+}
+
+// Logical blocks a sequence's query visits (those holding positions window_lo .. ctx-1);
+// -1 for an invalid context.
+__device__ __forceinline__ int seq_span(const DecodeParams& p, int ctx) {
+  const int nb = seq_blocks(p, ctx);
+  return nb <= 0 ? nb : nb - window_lo(p, ctx) / PA_BLOCK_SIZE;
 }
 
 // Largest s in [0, n) with cum[s] <= u (cum non-decreasing, cum[0] <= u).
@@ -195,7 +210,9 @@ struct Consumer {
   }
 
   // One 16-token block: scores, online softmax update, P·V.
-  __device__ __forceinline__ void block(const uint8_t* kbase, const uint8_t* vbase, int lb, int ntok) {
+  // Tokens first .. ntok-1 of the block are attended; those below `first` are sink positions
+  // (read from the bf16 sink buffer by the merge) or lie before the sliding window.
+  __device__ __forceinline__ void block(const uint8_t* kbase, const uint8_t* vbase, int first, int ntok) {
     // two independent accumulation chains halve the dependent-MMA latency of q·Kᵀ
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float acc2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -227,9 +244,8 @@ struct Consumer {
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
     // rows t4 and t4+8 of the block; columns = query heads 2tq, 2tq+1
-    const int pos0 = lb * PA_BLOCK_SIZE + t4;
-    const bool v0 = t4 < ntok && pos0 >= p.num_sink;
-    const bool v1 = t4 + 8 < ntok && pos0 + 8 >= p.num_sink;
+    const bool v0 = t4 < ntok && t4 >= first;
+    const bool v1 = t4 + 8 < ntok && t4 + 8 >= first;
     const float s00 = v0 ? acc[0] * sl[0] : kNegInf;
     const float s01 = v0 ? acc[1] * sl[1] : kNegInf;
     const float s10 = v1 ? acc[2] * sl[0] : kNegInf;
@@ -269,12 +285,12 @@ struct Consumer {
     const uint32_t x1 = QUANT ? pack_f16(p10, p11) : pack_bf16(p10, p11);
     const uint32_t b0 = movmatrix_t(x0), b1 = movmatrix_t(x1);
     if constexpr (!QUANT) {
-      // Slots outside the context (tail of the last block, sink positions) may hold any bits,
-      // NaN included, and 0 * NaN would poison the sum: zero those tokens' V elements.  This
-      // lane's A fragments hold tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3).
+      // Slots outside the attended range (tail of the last block, sink positions, positions
+      // before the window) may hold any bits, NaN included, and 0 * NaN would poison the sum:
+      // zero those tokens' V elements.  This lane's A fragments hold tokens 2tq, 2tq+1 (a0, a1)
+      // and 2tq+8, 2tq+9 (a2, a3).
       uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
-      if (ntok < PA_BLOCK_SIZE || lb * PA_BLOCK_SIZE < p.num_sink) {
-        const int first = p.num_sink - lb * PA_BLOCK_SIZE;  // tokens below this are sinks
+      if (ntok < PA_BLOCK_SIZE || first > 0) {
         auto keep = [&](int r) { return r < ntok && r >= first; };
         mlo = (keep(2 * tq) ? 0x0000FFFFu : 0u) | (keep(2 * tq + 1) ? 0xFFFF0000u : 0u);
         mhi = (keep(2 * tq + 8) ? 0x0000FFFFu : 0u) | (keep(2 * tq + 9) ? 0xFFFF0000u : 0u);
@@ -399,7 +415,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     int local = 0;
     for (int i = lo; i < hi; ++i) {
       const int ctx = p.context_lens[i];
-      const int nb = seq_blocks(p, ctx);
+      const int nb = seq_span(p, ctx);
       if (nb < 0 && reporter) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
       local += max(nb, 0);
     }
@@ -424,7 +440,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     int run = sm.scratch[warp] + incl - local;
     for (int i = lo; i < hi; ++i) {
       const int ctx = p.context_lens[i];
-      const int nb = seq_blocks(p, ctx);
+      const int nb = seq_span(p, ctx);
       run += max(nb, 0);
       sm.cum[i + 1] = run;
       sm.ctxs[i] = nb < 0 ? 0 : ctx;
@@ -445,7 +461,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     seq_base = blockIdx.y;
     nseq = 1;
     const int ctx = p.context_lens[seq_base];
-    const int nb = seq_blocks(p, ctx);
+    const int nb = seq_span(p, ctx);
     if (nb < 0 && blockIdx.x == 0 && blockIdx.z == 0 && tid == 0) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
     const int nbv = max(nb, 0);
     if (tid == 0) {
@@ -485,10 +501,12 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     const CUtensorMap* my_map = my_t ? &tmV : &tmK;
     const int my_row = (hgi * p.hg + my_h) * p.nc;
     const size_t my_dst = static_cast<size_t>((my_jj * 2 + my_t) * p.hg + my_h) * box_bytes;
+    // logical block of list entry u of sequence s (the visited blocks start at the window)
+    auto logical = [&](int s, int u) { return window_lo(p, sm.ctxs[s]) / PA_BLOCK_SIZE + (u - sm.cum[s]); };
     auto load_entry = [&](int u) -> int {
       if (u >= u1) return -1;
       const int s = find_seq(sm.cum, nseq, u);
-      return p.block_tables[static_cast<size_t>(seq_base + s) * p.max_blocks + (u - sm.cum[s])];
+      return p.block_tables[static_cast<size_t>(seq_base + s) * p.max_blocks + logical(s, u)];
     };
     int base = u0;
     int cur_pb = load_entry(base + lane);
@@ -499,10 +517,14 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       const int u = base + lane;
       const bool valid = u < u1;
       const int s = valid ? find_seq(sm.cum, nseq, u) : 0;
-      const int lb = valid ? u - sm.cum[s] : 0;
+      const int lb = valid ? logical(s, u) : 0;
       const bool bad = valid && (cur_pb < 0 || cur_pb >= p.num_blocks);
       if (bad) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
-      my_meta = valid ? make_int4(s, lb, min(PA_BLOCK_SIZE, sm.ctxs[s] - lb * PA_BLOCK_SIZE), bad ? 1 : 0)
+      // first attended token of the block: sinks and positions before the window are skipped
+      const int first = valid ? min(PA_BLOCK_SIZE, max(0, max(p.num_sink, window_lo(p, sm.ctxs[s])) -
+                                                            lb * PA_BLOCK_SIZE))
+                              : 0;
+      my_meta = valid ? make_int4(s, first, min(PA_BLOCK_SIZE, sm.ctxs[s] - lb * PA_BLOCK_SIZE), bad ? 1 : 0)
                       : make_int4(-1, 0, 0, 1);
       live_mask = __ballot_sync(0xffffffffu, valid && !bad);
     };
@@ -615,10 +637,12 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
   if (h >= p.H_q) return;
   const int h_kv = h / p.G;
   const int ctx = p.context_lens[s];
-  const int nb = seq_blocks(p, ctx);
+  const int nb = seq_span(p, ctx);
+  // sink positions inside the attended range [window_lo, ctx)
+  const int sink_lo = window_lo(p, ctx);
   const int n_sink = nb < 0 ? 0 : min(p.num_sink, ctx);
   float qv[E];
-  if (n_sink > 0) {
+  if (n_sink > sink_lo) {
     const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(s) * p.H_q + h) * D + lane * E;
 #pragma unroll
     for (int e = 0; e < E; ++e) qv[e] = __bfloat162float(qrow[e]);
@@ -702,7 +726,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
   }
   bad = __any_sync(0xffffffffu, bad);
 
-  for (int t = 0; t < n_sink; ++t) {  // bf16 sink tokens join the merge as single-token partials
+  for (int t = sink_lo; t < n_sink; ++t) {  // bf16 sink tokens join the merge as single-token partials
     const size_t off = ((static_cast<size_t>(s) * p.num_sink + t) * p.H_kv + h_kv) * D + lane * E;
     float dot = 0.f;
 #pragma unroll
@@ -771,7 +795,9 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
     const int part = partition_size ? partition_size : kFixedFallbackPartition;
     pl->mode = 1;
     pl->ppb = part / PA_BLOCK_SIZE;
-    const int max_blk = (max_ctx + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+    int max_blk = (max_ctx + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+    // a window of W positions spans at most ceil((W-1)/16) + 1 blocks
+    if (d->sliding_window > 0) max_blk = std::min(max_blk, (d->sliding_window + 14) / PA_BLOCK_SIZE + 1);
     pl->max_parts = std::max(1, (max_blk + pl->ppb - 1) / pl->ppb);
     pl->grid_x = pl->max_parts;
     pl->n_slots = static_cast<size_t>(B) * pl->max_parts;
@@ -849,6 +875,7 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, c
   p.num_blocks = desc->num_blocks;
   p.max_blocks = desc->max_blocks_per_seq;
   p.num_sink = desc->num_sink;
+  p.window = desc->sliding_window;
   p.max_ctx = max_context_len;
   p.hg = pl.hg;
   p.nc = pl.nc;

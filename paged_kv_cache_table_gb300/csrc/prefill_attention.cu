@@ -5,7 +5,8 @@
 // kept for later steps; §7 splits a long prompt into chunks to cap the activation peak.  Here a
 // chunk of n new tokens per sequence (their K/V already appended to the cache) attends over the
 // whole cached context through the block table ("KV Cache 的显存账本：PagedAttention 与连续批处理"
-// §四), with GQA grouping (same page §二).
+// §四), with GQA grouping (same page §二).  Under a sliding window of W tokens (ldpk §5.3) the
+// query at position p reads keys p-W+1 .. p only, and blocks before a tile's window are not read.
 //
 // Design: one CTA per (sequence, KV head, tile of query tokens).  Four consumer warps own 16
 // (query token, query head) rows each, so every K/V element a warp loads serves up to 16 query
@@ -32,6 +33,7 @@ constexpr float kNegInfP = -INFINITY;
 
 struct PrefillParams {
   int B, H_q, H_kv, G, num_blocks, max_blocks, max_q;
+  int window;  // sliding window in tokens, 0 = whole context
   int tpw;     // query tokens per warp (16 / G)
   int q_tile;  // query tokens per CTA
   int nc;      // 128-byte chunks per head row
@@ -78,8 +80,10 @@ __global__ void __launch_bounds__(kPfThreads)
   if (t0 >= n) return;
   const int first_pos = ctx - n;
   const int t_end = min(n, t0 + p.q_tile);
-  const int kv_end = first_pos + t_end;  // keys [0, kv_end) are visible to this tile
-  const int n_blocks = (kv_end + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+  const int kv_end = first_pos + t_end;  // keys [kv_lo, kv_end) are visible to this tile
+  const int kv_lo = p.window > 0 ? max(0, first_pos + t0 - p.window + 1) : 0;
+  const int kb0 = kv_lo / PA_BLOCK_SIZE;  // first logical block read
+  const int n_blocks = (kv_end + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE - kb0;
 
   if (tid == 0) {
     for (int i = 0; i < kPfStages; ++i) {
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kPfThreads)
   if (warp == kPfWarps) {
     // ------------------------------ producer ------------------------------
     const uint64_t policy = l2_evict_first_policy();
-    const int32_t* row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+    const int32_t* row = p.block_tables + static_cast<size_t>(s) * p.max_blocks + kb0;
     int cur = lane < n_blocks ? row[lane] : -1;
     int nxt = 32 + lane < n_blocks ? row[32 + lane] : -1;
     int k = 0;
@@ -139,6 +143,8 @@ __global__ void __launch_bounds__(kPfThreads)
   const int wt0 = t0 + warp * p.tpw;                  // this warp's first query token (chunk index)
   const int w_tokens = max(0, min(p.tpw, t_end - wt0));
   const int w_last_pos = first_pos + wt0 + w_tokens - 1;  // last query position of this warp
+  // lowest key any row of this warp reads (its first token's window start)
+  const int w_lo = p.window > 0 ? max(0, first_pos + wt0 - p.window + 1) : 0;
   // rows of the 16-row tile: row r = (token r / G, head r % G); rows past the tokens are padding
   const int rows_used = w_tokens * p.G;
   int row_pos[2];
@@ -176,10 +182,10 @@ __global__ void __launch_bounds__(kPfThreads)
       if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
       return;
     }
-    const int kbase_pos = k * PA_BLOCK_SIZE;
+    const int kbase_pos = (kb0 + k) * PA_BLOCK_SIZE;
     if (bad_stage[st]) {
       bad = true;
-    } else if (w_tokens > 0 && kbase_pos <= w_last_pos) {
+    } else if (w_tokens > 0 && kbase_pos <= w_last_pos && kbase_pos + PA_BLOCK_SIZE > w_lo) {
       const uint8_t* kt = stages[st];
       const uint8_t* vt = stages[st] + NC * kChunkTile;
       // S = Q Kᵀ for the 16 keys (two n-tiles of 8)
@@ -208,7 +214,7 @@ __global__ void __launch_bounds__(kPfThreads)
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj) {
             const int kp = kbase_pos + nt * 8 + 2 * tq + jj;
-            const bool ok = row_ok[half] && kp <= row_pos[half];
+            const bool ok = row_ok[half] && kp <= row_pos[half] && (p.window <= 0 || kp > row_pos[half] - p.window);
             const float v = ok ? sacc[nt][2 * half + jj] * p.scale_log2 : kNegInfP;
             sv[half][nt][jj] = v;
             bm[half] = fmaxf(bm[half], v);
@@ -253,14 +259,16 @@ __global__ void __launch_bounds__(kPfThreads)
       const uint32_t pa1 = pack_bf16(pv[1][0][0], pv[1][0][1]);
       const uint32_t pa2 = pack_bf16(pv[0][1][0], pv[0][1][1]);
       const uint32_t pa3 = pack_bf16(pv[1][1][0], pv[1][1][1]);
-      // Slots at or beyond kv_end in the last block may never have been written (NaN included)
-      // and 0 * NaN would poison the sum: zero those keys' V elements.  This lane's B fragments
-      // hold keys 2tq, 2tq+1 (b0, b2) and 8+2tq, 9+2tq (b1, b3).
+      // Slots at or beyond kv_end in the last block may never have been written, and slots
+      // before the warp's window may hold anything (NaN included); 0 * NaN would poison the
+      // sum, so zero those keys' V elements.  This lane's B fragments hold keys 2tq, 2tq+1
+      // (b0, b2) and 8+2tq, 9+2tq (b1, b3).
       uint32_t vlo = 0xFFFFFFFFu, vhi = 0xFFFFFFFFu;
-      if (kbase_pos + PA_BLOCK_SIZE > kv_end) {
-        const int lim = kv_end - kbase_pos;
-        vlo = (2 * tq < lim ? 0x0000FFFFu : 0u) | (2 * tq + 1 < lim ? 0xFFFF0000u : 0u);
-        vhi = (2 * tq + 8 < lim ? 0x0000FFFFu : 0u) | (2 * tq + 9 < lim ? 0xFFFF0000u : 0u);
+      if (kbase_pos + PA_BLOCK_SIZE > kv_end || kbase_pos < w_lo) {
+        const int hi = kv_end - kbase_pos, lo = w_lo - kbase_pos;
+        auto keep = [&](int r) { return r < hi && r >= lo; };
+        vlo = (keep(2 * tq) ? 0x0000FFFFu : 0u) | (keep(2 * tq + 1) ? 0xFFFF0000u : 0u);
+        vhi = (keep(2 * tq + 8) ? 0x0000FFFFu : 0u) | (keep(2 * tq + 9) ? 0xFFFF0000u : 0u);
       }
       {
         const int key = (lane & 7) + ((lane >> 3) & 1) * 8;  // matrices: [k0-7,d0],[k8-15,d0],[k0-7,d8],[k8-15,d8]
@@ -334,6 +342,7 @@ extern "C" pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, 
   p.num_blocks = desc->num_blocks;
   p.max_blocks = desc->max_blocks_per_seq;
   p.max_q = max_query_len;
+  p.window = desc->sliding_window;
   p.tpw = 16 / p.G;
   p.q_tile = pa::kPfWarps * p.tpw;
   p.nc = nc;

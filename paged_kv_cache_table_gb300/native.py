@@ -41,6 +41,7 @@ EXPORTED = [
     "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_noalloc", "pa_prefill_attention",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_alloc", "pa_bm_claim", "pa_bm_incref", "pa_bm_decref",
     "pa_bm_refcount", "pa_bm_num_free", "pa_bm_fork", "pa_bm_release", "pa_bm_prepare_step",
+    "pa_bm_slide_window",
 ]
 
 
@@ -66,6 +67,7 @@ class CacheDesc(ctypes.Structure):
         ("k_sink", ctypes.c_void_p),
         ("v_sink", ctypes.c_void_p),
         ("num_sink", ctypes.c_int),
+        ("sliding_window", ctypes.c_int),
     ]
 
 
@@ -126,6 +128,8 @@ def lib() -> ctypes.CDLL:
         L.pa_bm_prepare_step.restype = c_int
         L.pa_bm_prepare_step.argtypes = [vp, i32p, c_int, c_int, i32p, i32p, ctypes.POINTER(c_int),
                                          ctypes.POINTER(c_int)]
+        L.pa_bm_slide_window.restype = c_int
+        L.pa_bm_slide_window.argtypes = [vp, i32p, c_int, c_int, i32p, c_int, ctypes.POINTER(c_int)]
         _LIB = L
     return _LIB
 
@@ -161,12 +165,12 @@ def _stream(stream):
 
 def make_desc(num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq,
               k_dtype="bf16", v_dtype="bf16", k_scales=None, v_scales=None,
-              k_sink=None, v_sink=None, num_sink=0, block_size=BLOCK_SIZE) -> CacheDesc:
+              k_sink=None, v_sink=None, num_sink=0, block_size=BLOCK_SIZE, sliding_window=0) -> CacheDesc:
     """Fill a pa_cache_desc.  Tensors passed here must outlive every call that uses it."""
     return CacheDesc(int(num_seqs), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
                      int(num_blocks), int(max_blocks_per_seq), _DTYPES.get(k_dtype, k_dtype),
                      _DTYPES.get(v_dtype, v_dtype), _ptr(k_scales), _ptr(v_scales), _ptr(k_sink),
-                     _ptr(v_sink), int(num_sink))
+                     _ptr(v_sink), int(num_sink), int(sliding_window))
 
 
 def pa_kv_append(desc, k_cache, v_cache, k_new, v_new, block_tables, positions, err_flag=None, stream=None):
@@ -296,3 +300,15 @@ class BlockManager:
                                       ctypes.byref(n_pairs), ctypes.byref(n_changed))
         _check(st, "pa_bm_prepare_step")
         return pairs[:n_pairs.value].copy(), n_changed.value
+
+    def slide_window(self, block_tables: np.ndarray, context_lens: np.ndarray, window: int):
+        """Release every block wholly before each sequence's window; returns (entries released,
+        blocks freed).  ``block_tables`` (int32 [B][max_blocks]) is updated in place."""
+        bt = _i32(block_tables)
+        ctx = _i32(np.ascontiguousarray(context_lens, dtype=np.int32))
+        B, M = bt.shape
+        n_freed = ctypes.c_int(0)
+        r = lib().pa_bm_slide_window(self._h, _p32(bt), B, M, _p32(ctx), int(window), ctypes.byref(n_freed))
+        if r < 0:
+            raise PaError(PA_ERR_INVALID_ARG, "pa_bm_slide_window")
+        return r, n_freed.value

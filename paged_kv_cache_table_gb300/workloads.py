@@ -20,6 +20,10 @@ Workloads (seed = 20260 + index):
   6 "prefill_chunk"  8 sequences with cached lengths uniform in [0, 3584] each receiving a chunk
                   of 512 new tokens (queries + their K/V), 32 / 8 heads, d 128
                   (make_prefill_workload).
+  7 "swa"         64 sequences, cached lengths uniform in [4096, 16384], 32 / 8 heads, d 128,
+                  sliding window of 4096 tokens: only the blocks holding the first step's window
+                  are in the pool (earlier table entries are -1, already released), and only the
+                  window's positions are written.
 Every step appends one token per sequence at position = cached length, then attends over
 cached length + 1 tokens.  All tensors are produced on the CPU with a torch.Generator.
 """
@@ -40,6 +44,7 @@ CONFIGS = {
     "70b": dict(index=3, B=32, H_q=64, H_kv=8, D=128, ctx_fixed=4096),
     "prefix_cow": dict(index=4, B=64, H_q=32, H_kv=8, D=128, prefix=1208, suffix_range=(200, 2000)),
     "long_quant": dict(index=5, B=4, H_q=32, H_kv=8, D=128, ctx_fixed=131072, quant=True, num_sink=4),
+    "swa": dict(index=7, B=64, H_q=32, H_kv=8, D=128, ctx_range=(4096, 16384), window=4096),
 }
 
 # Calibration code ranges of the 8-bit formats (largest finite E4M3 value; symmetric int8).
@@ -77,6 +82,7 @@ class Workload:
     suffix_len: np.ndarray | None = None  # int32 [B] private tokens after the prefix
     suffix_k: torch.Tensor | None = None  # bf16 [sum(suffix_len)][H_kv][D], sequence-major
     suffix_v: torch.Tensor | None = None
+    window: int = 0                # sliding window in tokens (0 = whole context)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -96,6 +102,8 @@ class Workload:
 def _randn_bf16(g, shape, chunk_rows=1 << 16):
     """N(0,1) drawn in fp32 and rounded to bf16 (round to nearest even), in row chunks."""
     out = torch.empty(shape, dtype=torch.bfloat16)
+    if out.numel() == 0:
+        return out
     flat = out.view(shape[0], -1)
     for a in range(0, shape[0], chunk_rows):
         b = min(shape[0], a + chunk_rows)
@@ -108,7 +116,9 @@ def _blocks(n):
 
 
 def make_workload(name: str, steps: int = 1, **overrides) -> Workload:
-    """Draw the named workload.  ``overrides`` shrink it for tests (e.g. B=8, ctx_range=(16, 300))."""
+    """Draw the named workload.  ``overrides`` shrink it for tests (e.g. B=8, ctx_range=(16, 300)).
+    ``horizon`` (default: steps) sizes the tables and the pool for that many steps of appends while
+    only ``steps`` steps of inputs are drawn; ``window`` > 0 makes it a sliding-window workload."""
     cfg = dict(CONFIGS[name])
     cfg.update(overrides)
     seed = cfg.get("seed", 20260 + cfg["index"])
@@ -117,6 +127,9 @@ def make_workload(name: str, steps: int = 1, **overrides) -> Workload:
     quant = cfg.get("quant", False)
     num_sink = cfg.get("num_sink", 0)
     prefix = cfg.get("prefix", 0)
+    window = int(cfg.get("window", 0))
+    horizon = int(cfg.get("horizon", steps))
+    assert not (window and prefix), "sliding-window workloads have no shared prefix"
 
     if "ctx_list" in cfg:
         ctx = np.array(cfg["ctx_list"], dtype=np.int64)
@@ -137,8 +150,10 @@ def make_workload(name: str, steps: int = 1, **overrides) -> Workload:
         need = _blocks(prefix) + sum(_blocks(f) - (_blocks(prefix) - 1) for f in final)
         max_blocks = int(max(_blocks(f) for f in final))
     else:
-        final = ctx + steps
-        need = int(sum(_blocks(f) for f in final))
+        final = ctx + horizon
+        # first position kept: under a window only the first step's window is cached
+        keep_from = np.maximum(0, ctx + 1 - window) if window else np.zeros(B, dtype=np.int64)
+        need = int(sum(_blocks(f) - k // BLOCK for f, k in zip(final, keep_from)))
         max_blocks = int(max(_blocks(f) for f in final))
     num_blocks = int(cfg.get("pool_blocks") or math.ceil(1.1 * need))
     max_blocks = int(cfg.get("max_blocks", max_blocks))
@@ -153,11 +168,12 @@ def make_workload(name: str, steps: int = 1, **overrides) -> Workload:
     else:
         k = 0
         for s in range(B):
-            n = _blocks(ctx[s])
-            tables[s, :n] = perm[k:k + n]
-            k += n
-        fill_seq = np.repeat(np.arange(B, dtype=np.int32), ctx)
-        fill_pos = np.concatenate([np.arange(c, dtype=np.int32) for c in ctx]) if B else np.zeros(0, np.int32)
+            b0, n = int(keep_from[s]) // BLOCK, _blocks(ctx[s])
+            tables[s, b0:n] = perm[k:k + n - b0]
+            k += n - b0
+        fill_seq = np.repeat(np.arange(B, dtype=np.int32), ctx - keep_from)
+        fill_pos = (np.concatenate([np.arange(a, c, dtype=np.int32) for a, c in zip(keep_from, ctx)])
+                    if B else np.zeros(0, np.int32))
 
     N = len(fill_seq)
     fill_k = _randn_bf16(g, (N, H_kv, D))
@@ -193,7 +209,7 @@ def make_workload(name: str, steps: int = 1, **overrides) -> Workload:
         fill_seq=fill_seq, fill_pos=fill_pos, q=q, k_new=k_new, v_new=v_new,
         k_scales=k_scales, v_scales=v_scales, prefix=prefix,
         suffix_len=None if suffix_len is None else suffix_len.astype(np.int32),
-        suffix_k=suffix_k, suffix_v=suffix_v,
+        suffix_k=suffix_k, suffix_v=suffix_v, window=window,
     )
 
 

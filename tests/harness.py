@@ -54,7 +54,8 @@ class GpuState:
             self.k_sink = torch.full(sshape, BF16_NAN, dtype=torch.int16, device=device).view(torch.bfloat16)
             self.v_sink = torch.full(sshape, BF16_NAN, dtype=torch.int16, device=device).view(torch.bfloat16)
         self.desc = P.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks, w.k_dtype, w.v_dtype,
-                                self.k_scales, self.v_scales, self.k_sink, self.v_sink, w.num_sink)
+                                self.k_scales, self.v_scales, self.k_sink, self.v_sink, w.num_sink,
+                                sliding_window=w.window)
         self.tables = w.tables.copy()
         self.tables_dev = torch.from_numpy(self.tables).to(device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -100,12 +101,22 @@ class GpuState:
                               self.err)
         return out
 
+    def slide(self, context_lens):
+        """Sliding window: release the blocks behind every sequence's window (host tables, then
+        the device copy)."""
+        released, freed = self.bm.slide_window(self.tables, context_lens, self.w.window)
+        if released:
+            self.tables_dev.copy_(torch.from_numpy(self.tables))
+        return freed
+
     def step(self, i, partition=0):
         w = self.w
         pos = w.positions(i)
         pairs = self.prepare(pos)
         self.append(w.k_new[i], w.v_new[i], pos)
         out = self.attend(w.q[i], w.context_lens(i), partition)
+        if w.window:
+            self.slide(w.context_lens(i))
         return out, pairs
 
     def err_bits(self) -> int:
@@ -179,16 +190,25 @@ class OracleState:
         qv = O.bf16_bits_to_f64(bf16_bits(q))
         out = np.zeros((w.B, w.H_q, w.D))
         for s in range(w.B):
-            K, V = self.cache.gather(s, self.tables[s], int(context_lens[s]))
+            c = int(context_lens[s])
+            # positions before the window are never gathered (their blocks may be released)
+            K, V = self.cache.gather(s, self.tables[s], c, O.window_start(c, w.window))
             out[s] = O.decode_attention(qv[s], K, V, w.scale)
         return out
+
+    def slide(self, context_lens):
+        return sum(self.pool.slide_window(self.tables[s], int(context_lens[s]), self.w.window)
+                   for s in range(self.w.B))
 
     def step(self, i):
         w = self.w
         pos = w.positions(i)
         pairs = self.prepare(pos)
         self.append(w.k_new[i], w.v_new[i], pos)
-        return self.attend(w.q[i], w.context_lens(i)), pairs
+        out = self.attend(w.q[i], w.context_lens(i))
+        if w.window:
+            self.slide(w.context_lens(i))
+        return out, pairs
 
 
 def to_f64(out: torch.Tensor) -> np.ndarray:

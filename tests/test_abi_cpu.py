@@ -173,6 +173,59 @@ def test_prepare_step_matches_oracle_prepare_append():
         assert bm.num_free() == pool.num_free()
 
 
+@pytest.mark.parametrize("window", [1, 16, 37, 100])
+def test_slide_window_matches_oracle_pool(window):
+    """Sequences that decode, fork (shared prefixes) and slide their window: the library's
+    release decisions, tables, refcounts and free list follow the oracle's slide_window."""
+    rng = np.random.default_rng(window)
+    B_, M = 5, 40
+    bm = N.BlockManager(200)
+    pool = O.BlockPool(200)
+    tabs = np.full((B_, M), -1, dtype=np.int32)
+    otabs = np.full((B_, M), -1, dtype=np.int64)
+    lens = np.zeros(B_, dtype=np.int64)
+    for step in range(500):
+        pos = np.where(rng.random(B_) < 0.9, lens, -1).astype(np.int32)
+        bm.prepare_step(tabs, pos)
+        for s in range(B_):
+            if pos[s] >= 0:
+                pool.prepare_append(otabs[s], int(pos[s]))
+        lens += pos >= 0
+        released, freed = bm.slide_window(tabs, lens.astype(np.int32), window)
+        o_before = int((otabs >= 0).sum())
+        o_freed = sum(pool.slide_window(otabs[s], int(lens[s]), window) for s in range(B_))
+        assert released == o_before - int((otabs >= 0).sum())
+        assert freed == o_freed
+        assert np.array_equal(tabs, otabs)
+        assert bm.num_free() == pool.num_free()
+        if step == 250:  # sequences 1 and 2 fork sequence 0's live blocks (shared, refcount 3)
+            for dst in (1, 2):
+                bm.release(tabs[dst], M)
+                pool.release(otabs[dst], M)
+                n = -(-int(lens[0]) // 16)
+                live = np.nonzero(otabs[0][:n] >= 0)[0]
+                for lb in live:
+                    tabs[dst][lb] = tabs[0][lb]
+                    bm.incref(int(tabs[0][lb]))
+                    otabs[dst][lb] = otabs[0][lb]
+                    pool.incref(int(otabs[0][lb]))
+                lens[dst] = lens[0]
+            assert np.array_equal(tabs, otabs)
+    for b in range(200):
+        assert bm.refcount(b) == pool.refcount[b]
+    assert bm.slide_window(tabs, lens.astype(np.int32), 0) == (0, 0)
+
+
+def test_slide_window_rejects_bad_arguments_and_foreign_blocks():
+    bm = N.BlockManager(8)
+    tabs = np.full((1, 4), -1, dtype=np.int32)
+    with pytest.raises(N.PaError):
+        bm.slide_window(tabs, np.array([40], dtype=np.int32), -1)
+    tabs[0, 0] = 3  # the pool never handed out block 3
+    with pytest.raises(N.PaError):
+        bm.slide_window(tabs, np.array([40], dtype=np.int32), 8)
+
+
 def test_prepare_step_out_of_blocks_and_bad_position():
     bm = N.BlockManager(2)
     tabs = np.full((3, 4), -1, dtype=np.int32)
