@@ -14,3 +14,4 @@ float8 cast, numpy's round-half-even) and brute force on tiny inputs.
 """
 
 from .paged_kv import *  # noqa: F401,F403
+from .prefix_cache import *  # noqa: F401,F403
