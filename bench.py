@@ -550,6 +550,85 @@ class PrefillBench:
         return t0.elapsed_time(t1) / 1e3 / steps
 
 
+def prefix_cache_row(device, warmup):
+    """Prefix-cache row: host cost of a lookup (hash chain + match + release through the binding)
+    against a cache of 64 distinct 2048-token prompts (8192 entries), and the prefill-attention
+    time of 8 requests that hit (128 new tokens over a 2048-token cached prefix) against the same
+    requests missing (all 2176 tokens prefilled)."""
+    import torch
+    from paged_kv_cache_table_gb300 import native as N
+    from paged_kv_cache_table_gb300.workloads import make_prefill_workload
+    rng = np.random.default_rng(20268)
+    n_prompts, plen, qlen = 64, 2048, 128
+    bm = N.BlockManager(n_prompts * plen // 16 + 1024)
+    pc = N.PrefixCache(bm)
+    prompts = [rng.integers(0, 128000, plen).astype(np.int32) for _ in range(n_prompts)]
+    width = (plen + qlen) // 16 + 1
+    for pr in prompts:
+        d = N.block_hashes(pr)
+        row = np.full(width, -1, dtype=np.int32)
+        for i in range(len(d)):
+            row[i] = bm.alloc()
+        pc.insert(d, row, len(d))
+        bm.release(row, width)
+    reqs = [np.concatenate([prompts[i % n_prompts], rng.integers(0, 128000, qlen).astype(np.int32)])
+            for i in range(512)]
+    hits = 0
+    t0 = time.perf_counter()
+    for r in reqs:
+        d = N.block_hashes(r)
+        row = np.full(width, -1, dtype=np.int32)
+        hits += pc.match(d, (len(r) - 1) // 16, row)
+        bm.release(row, width)
+    host_us = (time.perf_counter() - t0) / len(reqs) * 1e6
+    t0 = time.perf_counter()
+    for r in reqs[:128]:
+        N.block_hashes(r)
+    hash_us = (time.perf_counter() - t0) / 128 * 1e6
+    entries = len(pc)
+    pc.close()
+    del bm
+
+    def prefill_ms(cached, chunk):
+        w = make_prefill_workload(B=8, cached_list=[cached] * 8, chunk_list=[chunk] * 8, seed=20269)
+        shape = (w.num_blocks * 16, w.H_kv, w.D)
+        k = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        v = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        desc = N.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks)
+        tab = torch.from_numpy(w.tables).to(device)
+        err = torch.zeros(1, dtype=torch.int32, device=device)
+        allk = torch.cat([w.fill_k, w.new_k]) if len(w.fill_seq) else w.new_k
+        allv = torch.cat([w.fill_v, w.new_v]) if len(w.fill_seq) else w.new_v
+        seq = np.concatenate([w.fill_seq, w.new_seq]).astype(np.int32)
+        pos = np.concatenate([w.fill_pos, w.new_pos]).astype(np.int32)
+        N.pa_kv_append_tokens(desc, k, v, allk.to(device), allv.to(device), len(seq),
+                              torch.from_numpy(seq).to(device), torch.from_numpy(pos).to(device), tab, err)
+        q = w.q.to(device)
+        out = torch.empty_like(q)
+        qs = torch.from_numpy(w.q_start()).to(device)
+        ctx = torch.from_numpy(w.context_lens()).to(device)
+        for _ in range(max(3, warmup)):
+            N.pa_prefill_attention(desc, out, q, k, v, tab, qs, ctx, chunk, w.scale, err)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        e0.record()
+        for _ in range(reps):
+            N.pa_prefill_attention(desc, out, q, k, v, tab, qs, ctx, chunk, w.scale, err)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps, int(err.item())
+
+    hit_ms, e_hit = prefill_ms(plen, qlen)
+    miss_ms, e_miss = prefill_ms(0, plen + qlen)
+    return {"workload": f"cache of {n_prompts} x {plen}-token prompts ({entries} entries); requests = a cached "
+                        f"prompt + {qlen} new tokens; prefill of 8 such requests, 32/8 heads, d 128",
+            "host_us_per_lookup": round(host_us, 2), "host_us_per_hash_chain": round(hash_us, 2),
+            "blocks_hit_per_request": round(hits / len(reqs), 2),
+            "prefill_attention_ms_hit": round(hit_ms, 4), "prefill_attention_ms_miss": round(miss_ms, 4),
+            "prefill_attention_speedup": round(miss_ms / hit_ms, 2), "err_flag": e_hit | e_miss}
+
+
 def cpu_baseline_sample(name, budget_s=15.0, max_seqs=None):
     """The oracle, as it stands, on a bounded sample of the workload: whole decode steps
     (append + attention) of the first sequences, on this host's CPU.  Run in a spawned child
@@ -733,6 +812,8 @@ def run_native(args):
             "held_blocks_max": sb.held_blocks_max, "pool_blocks": sw.num_blocks,
             "err_flag": int(sb.err.item())}
         del sb
+        torch.cuda.empty_cache()
+        next_rows["prefix_cache"] = prefix_cache_row(device, args.warmup)
         torch.cuda.empty_cache()
 
     cpu = None

@@ -281,6 +281,53 @@ pa_status pa_bm_prepare_step(pa_bm* bm, int32_t* block_tables, int num_seqs,
 int pa_bm_slide_window(pa_bm* bm, int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
                        const int32_t* context_lens, int window, int* n_freed);
 
+/* ---------------------------------------------------------------------------------
+ * Prefix cache ("大模型推理KV Cache显存优化：从PagedAttention到AI内存系统演进", prefix-cache
+ * section, and §7.2): which physical blocks of a pool already hold the K/V of a token prefix, so a
+ * new request reuses them and computes only what follows.  Host memory only; thread-safe (its
+ * own mutex, then the pool's).
+ *
+ * Block identity: only full 16-token blocks are cached.  Block i of a request is identified by
+ *   h_i = SHA-256(h_{i-1} || tokens[16i .. 16i+15] as little-endian int32 || extra_key as
+ *                 little-endian uint64),   h_{-1} = SHA-256(salt as little-endian uint64)
+ * (FIPS 180-4), so it covers the whole prefix, the request's extra inputs (e.g. an adapter or a
+ * multimodal input id in extra_key) and the tenant's cache salt: different salts never share.
+ *
+ * The cache holds one reference of its own on every registered block (so a cached block survives
+ * its request) and orders entries by last use; eviction returns to the pool the least recently
+ * used blocks that no sequence holds (refcount 1), deeper blocks first among equally recent ones.
+ * A matched block is full and shared, so the pool's copy-on-write keeps it unmodified. */
+#define PA_PC_DIGEST_BYTES 32
+typedef struct pa_pc pa_pc;
+
+/* Digests of the n_tokens/16 full blocks of a token sequence (a partial tail block gets none)
+ * into digests [n_tokens/16][32].  Returns n_tokens/16, or -1 on invalid arguments. */
+int pa_pc_block_hashes(const int32_t* tokens, int n_tokens, uint64_t salt, uint64_t extra_key,
+                       uint8_t* digests);
+/* A cache over pool bm (which must outlive it); capacity = maximum entries, 0 = bounded by the
+ * pool only.  NULL on invalid arguments or allocation failure. */
+pa_pc* pa_pc_create(pa_bm* bm, int capacity);
+/* Drops the cache's references (pa_pc_clear) and frees the cache. */
+void pa_pc_destroy(pa_pc* pc);
+/* Longest cached leading run of digests[0 .. n_blocks-1]: its physical blocks go to
+ * table_row[0 .. n-1], each gains one reference for the request, the entries count as used now.
+ * Returns n (0 = no hit), or -1 on invalid arguments.  An engine passes at most
+ * (prompt_tokens - 1) / 16 digests so that at least one prompt token is still computed. */
+int pa_pc_match(pa_pc* pc, const uint8_t* digests, int n_blocks, int32_t* table_row);
+/* Register blocks table_row[0 .. n_blocks-1] (their K/V written) under digests[0 .. n_blocks-1].
+ * A new entry takes the cache's own reference; a digest already cached keeps its block and is
+ * only marked used.  At capacity, the LRU evictable entry makes room; registration stops when
+ * none can.  Returns the number of new entries, or -1 on invalid arguments or on a block the pool
+ * does not hold (the entries registered before it stay). */
+int pa_pc_insert(pa_pc* pc, const uint8_t* digests, const int32_t* table_row, int n_blocks);
+/* Return up to n least recently used entries whose block no sequence holds to the pool; returns
+ * how many went, or -1 on invalid arguments. */
+int pa_pc_evict(pa_pc* pc, int n);
+/* Number of cached entries (-1 for NULL). */
+int pa_pc_size(const pa_pc* pc);
+/* Drop every entry and the cache's reference on its block; returns the number dropped. */
+int pa_pc_clear(pa_pc* pc);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,7 +14,7 @@ _BINDING_NAMES = {
     "pa_kv_append", "pa_kv_append_tokens", "pa_block_copy", "pa_decode_workspace_size",
     "pa_decode_attention", "pa_decode_attention_noalloc", "pa_prefill_attention",
     "pa_status_string", "make_desc", "BlockManager", "PaError", "CacheDesc",
-    "lib", "status_string",
+    "lib", "status_string", "PrefixCache", "block_hashes",
 }
 
 

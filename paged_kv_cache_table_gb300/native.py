@@ -42,7 +42,11 @@ EXPORTED = [
     "pa_bm_create", "pa_bm_destroy", "pa_bm_alloc", "pa_bm_claim", "pa_bm_incref", "pa_bm_decref",
     "pa_bm_refcount", "pa_bm_num_free", "pa_bm_fork", "pa_bm_release", "pa_bm_prepare_step",
     "pa_bm_slide_window",
+    "pa_pc_block_hashes", "pa_pc_create", "pa_pc_destroy", "pa_pc_match", "pa_pc_insert", "pa_pc_evict",
+    "pa_pc_size", "pa_pc_clear",
 ]
+
+DIGEST_BYTES = 32
 
 
 class PaError(RuntimeError):
@@ -130,6 +134,22 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(c_int)]
         L.pa_bm_slide_window.restype = c_int
         L.pa_bm_slide_window.argtypes = [vp, i32p, c_int, c_int, i32p, c_int, ctypes.POINTER(c_int)]
+        u64, u8p = ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint8)
+        L.pa_pc_block_hashes.restype = c_int
+        L.pa_pc_block_hashes.argtypes = [i32p, c_int, u64, u64, u8p]
+        L.pa_pc_create.restype = vp
+        L.pa_pc_create.argtypes = [vp, c_int]
+        L.pa_pc_destroy.restype = None
+        L.pa_pc_destroy.argtypes = [vp]
+        L.pa_pc_match.restype = c_int
+        L.pa_pc_match.argtypes = [vp, u8p, c_int, i32p]
+        L.pa_pc_insert.restype = c_int
+        L.pa_pc_insert.argtypes = [vp, u8p, i32p, c_int]
+        L.pa_pc_evict.restype = c_int
+        L.pa_pc_evict.argtypes = [vp, c_int]
+        for name in ("pa_pc_size", "pa_pc_clear"):
+            getattr(L, name).restype = c_int
+            getattr(L, name).argtypes = [vp]
         _LIB = L
     return _LIB
 
@@ -312,3 +332,66 @@ class BlockManager:
         if r < 0:
             raise PaError(PA_ERR_INVALID_ARG, "pa_bm_slide_window")
         return r, n_freed.value
+
+
+def _p8(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+
+
+def block_hashes(tokens, salt: int = 0, extra_key: int = 0) -> np.ndarray:
+    """Digests uint8 [n_tokens // 16][32] of a token sequence's full blocks (pa_pc_block_hashes)."""
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    out = np.zeros((len(t) // BLOCK_SIZE, DIGEST_BYTES), dtype=np.uint8)
+    n = lib().pa_pc_block_hashes(_p32(t), len(t), int(salt) & (2 ** 64 - 1), int(extra_key) & (2 ** 64 - 1),
+                                 _p8(out))
+    if n < 0:
+        raise PaError(PA_ERR_INVALID_ARG, "pa_pc_block_hashes")
+    return out
+
+
+class PrefixCache:
+    """The host prefix cache over a BlockManager's pool (pa_pc_*)."""
+
+    def __init__(self, bm: "BlockManager", capacity: int = 0):
+        h = lib().pa_pc_create(bm._h, int(capacity))
+        if not h:
+            raise PaError(PA_ERR_INVALID_ARG, "pa_pc_create")
+        self._h = ctypes.c_void_p(h)
+        self.bm = bm  # the pool must outlive the cache
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().pa_pc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __len__(self):
+        return lib().pa_pc_size(self._h)
+
+    def match(self, digests: np.ndarray, n_blocks: int, table_row: np.ndarray) -> int:
+        """Longest cached leading run of digests[:n_blocks] into table_row (int32, in place)."""
+        d = np.ascontiguousarray(digests, dtype=np.uint8)
+        n = min(int(n_blocks), len(d))
+        r = lib().pa_pc_match(self._h, _p8(d), max(0, n), _p32(_i32(table_row)))
+        if r < 0:
+            raise PaError(PA_ERR_INVALID_ARG, "pa_pc_match")
+        return r
+
+    def insert(self, digests: np.ndarray, table_row: np.ndarray, n_blocks: int) -> int:
+        d = np.ascontiguousarray(digests, dtype=np.uint8)
+        r = lib().pa_pc_insert(self._h, _p8(d), _p32(_i32(np.ascontiguousarray(table_row, dtype=np.int32))),
+                               min(int(n_blocks), len(d)))
+        if r < 0:
+            raise PaError(PA_ERR_INVALID_ARG, "pa_pc_insert")
+        return r
+
+    def evict(self, n: int) -> int:
+        return lib().pa_pc_evict(self._h, int(n))
+
+    def clear(self) -> int:
+        return lib().pa_pc_clear(self._h)
