@@ -20,6 +20,13 @@ Readings taken where the pages are silent (each repeated where it is used):
   * sink positions (pos < num_sink) live in a separate bf16 buffer and the paged slot
     is left untouched;
   * the block pool hands out the lowest-numbered free block;
+  * int4 (ldpk §5.2: int4 stores a scale and a zero point besides the codes, about 0.55-0.65
+    bytes per element; K develops outlier channels, so per-tensor scales fail and finer
+    granularity is needed): asymmetric 4-bit codes per group of 32 consecutive dims of one
+    (token, KV head) row; the group's range [min(0, min x), max(0, max x)] gives
+    s = bf16((hi - lo) / 15) (1 if that is 0), z = clamp(rint(-lo / s), 0, 15) and
+    q = clamp(rint(x / s) + z, 0, 15), divisions in IEEE fp32; a code decodes to s * (q - z);
+    with a bf16 scale and the zero point in one 32-bit word that is 0.625 bytes per element;
   * sliding window W (ldpk §5.3): the query at position p attends positions
     max(0, p - W + 1) .. p, i.e. the most recent W tokens with itself included, and W = 0
     means no window; a block is freed once all its positions lie before the window of the
@@ -53,6 +60,10 @@ __all__ = [
     "int8_encode",
     "int8_decode",
     "quantize_row",
+    "INT4_GROUP",
+    "int4_encode_group",
+    "int4_encode_row",
+    "int4_decode_row",
     "BlockPool",
     "PagedKVCache",
     "ContiguousKVCache",
@@ -237,6 +248,57 @@ def quantize_row(x_bf16_bits, scale: np.float32, kind: str) -> np.ndarray:
     raise ValueError(kind)
 
 
+INT4_GROUP = 32   # dims per scale / zero-point group
+INT4_LEVELS = 15  # codes 0 .. 15
+
+
+def int4_encode_group(x_bf16_bits):
+    """One group of 32 bf16 values -> (codes uint8[32] in 0..15, bf16 scale bits, zero point).
+
+    ldpk §5.2: int4 keeps a scale and a zero point per quantisation group; the group here is
+    32 consecutive dims of one token's head row (per-token granularity, so an outlier channel
+    of another token cannot squeeze this one).  The range always contains 0, so 0 encodes
+    exactly (q = z).  Every arithmetic step is IEEE fp32 and the scale is rounded to bf16
+    before it is used, so that encoding and decoding use the same stored scale.
+    """
+    x = bf16_bits_to_f64(np.asarray(x_bf16_bits, dtype=np.uint16)).astype(np.float32)
+    lo = np.minimum(np.float32(0), x.min())
+    hi = np.maximum(np.float32(0), x.max())
+    s = np.float32(np.float32(hi - lo) / np.float32(INT4_LEVELS))
+    sb = int(f32_to_bf16_bits(np.array([s], dtype=np.float32))[0])
+    if sb & 0x7FFF == 0:
+        sb = 0x3F80  # an all-zero group: any scale works, take 1
+    sf = np.float32(bf16_bits_to_f64(np.array([sb], dtype=np.uint16))[0])
+    z = int(np.clip(np.rint(np.float32(-lo) / sf), 0, INT4_LEVELS))
+    q = np.clip(np.rint((x / sf).astype(np.float32)) + z, 0, INT4_LEVELS).astype(np.uint8)
+    return q, sb, z
+
+
+def int4_encode_row(x_bf16_bits):
+    """A head row of d values -> (codes uint8[d], params uint32[d / 32]) with each params word
+    holding the group's bf16 scale in bits 0-15 and its zero point in bits 16-23."""
+    x = np.asarray(x_bf16_bits, dtype=np.uint16)
+    d = len(x)
+    codes = np.empty(d, dtype=np.uint8)
+    params = np.empty(d // INT4_GROUP, dtype=np.uint32)
+    for g in range(d // INT4_GROUP):
+        q, sb, z = int4_encode_group(x[g * INT4_GROUP:(g + 1) * INT4_GROUP])
+        codes[g * INT4_GROUP:(g + 1) * INT4_GROUP] = q
+        params[g] = np.uint32(sb | (z << 16))
+    return codes, params
+
+
+def int4_decode_row(codes, params):
+    """Codes [..., d] and params [..., d / 32] -> fp64 values s * (q - z)."""
+    codes = np.asarray(codes).astype(np.float64)
+    params = np.asarray(params, dtype=np.uint32)
+    scale = bf16_bits_to_f64((params & 0xFFFF).astype(np.uint16))
+    zero = ((params >> 16) & 0xFF).astype(np.float64)
+    scale = np.repeat(scale, INT4_GROUP, axis=-1)
+    zero = np.repeat(zero, INT4_GROUP, axis=-1)
+    return scale * (codes - zero)
+
+
 # ----------------------------------------------------------------------------------
 # Host block pool: free list, reference counts, copy-on-write decision
 # ----------------------------------------------------------------------------------
@@ -368,7 +430,9 @@ class PagedKVCache:
 
     Layout (a reading: the pages give only the flat slot of locate()):
     ``k[slot][kv_head][dim]`` with slot = physical_block * block_size + offset.
-    bf16 pools hold uint16 bit patterns; e4m3 / int8 pools hold uint8 codes.
+    bf16 pools hold uint16 bit patterns; e4m3 / int8 pools hold uint8 codes; int4 pools hold
+    one uint8 code (0..15) per element in natural order plus ``k_params`` / ``v_params``
+    [slot][kv_head][dim / 32] uint32 (bf16 scale | zero point << 16).
     ``k_sink`` / ``v_sink`` hold the bf16 rows of positions < num_sink per sequence
     (显存账本 §七: attention-sink tokens keep their original precision).
     """
@@ -377,8 +441,8 @@ class PagedKVCache:
     num_kv_heads: int
     head_dim: int
     block_size: int = BLOCK_SIZE
-    k_dtype: str = "bf16"  # "bf16" | "e4m3"
-    v_dtype: str = "bf16"  # "bf16" | "int8"
+    k_dtype: str = "bf16"  # "bf16" | "e4m3" | "int4"
+    v_dtype: str = "bf16"  # "bf16" | "int8" | "int4"
     k_scales: np.ndarray | None = None  # fp32 [num_kv_heads]
     v_scales: np.ndarray | None = None
     num_seqs: int = 0
@@ -394,17 +458,26 @@ class PagedKVCache:
         vt = np.uint16 if self.v_dtype == "bf16" else np.uint8
         self.k = np.zeros((n_slots, self.num_kv_heads, self.head_dim), dtype=kt)
         self.v = np.zeros((n_slots, self.num_kv_heads, self.head_dim), dtype=vt)
+        pshape = (n_slots, self.num_kv_heads, self.head_dim // INT4_GROUP)
+        self.k_params = np.zeros(pshape, dtype=np.uint32) if self.k_dtype == "int4" else None
+        self.v_params = np.zeros(pshape, dtype=np.uint32) if self.v_dtype == "int4" else None
         shape = (self.num_seqs, self.num_sink, self.num_kv_heads, self.head_dim)
         self.k_sink = np.zeros(shape, dtype=np.uint16)
         self.v_sink = np.zeros(shape, dtype=np.uint16)
 
     def _encode(self, bits, kind, scales):
+        """Codes of one token's rows [kv_heads][dim], and its int4 params (else None)."""
         if kind == "bf16":
-            return np.asarray(bits, dtype=np.uint16)
+            return np.asarray(bits, dtype=np.uint16), None
         out = np.empty(bits.shape, dtype=np.uint8)
+        if kind == "int4":
+            params = np.empty((self.num_kv_heads, self.head_dim // INT4_GROUP), dtype=np.uint32)
+            for h in range(self.num_kv_heads):
+                out[h], params[h] = int4_encode_row(bits[h])
+            return out, params
         for h in range(self.num_kv_heads):
             out[h] = quantize_row(bits[h], np.float32(scales[h]), kind)
-        return out
+        return out, None
 
     def append(self, seq: int, table_row, pos: int, k_bits, v_bits):
         """Write one token's K and V rows (bf16 bits [kv_heads][dim]) at ``pos``.
@@ -421,25 +494,36 @@ class PagedKVCache:
             self.v_sink[seq, pos] = v_bits
             return
         slot = locate(table_row, pos, self.block_size)
-        self.k[slot] = self._encode(k_bits, self.k_dtype, self.k_scales)
-        self.v[slot] = self._encode(v_bits, self.v_dtype, self.v_scales)
+        self.k[slot], kp = self._encode(k_bits, self.k_dtype, self.k_scales)
+        self.v[slot], vp = self._encode(v_bits, self.v_dtype, self.v_scales)
+        if kp is not None:
+            self.k_params[slot] = kp
+        if vp is not None:
+            self.v_params[slot] = vp
 
     def block_copy(self, src: int, dst: int):
         """Copy-on-write: the destination block receives the source block's bytes."""
         bs = self.block_size
         self.k[dst * bs:(dst + 1) * bs] = self.k[src * bs:(src + 1) * bs]
         self.v[dst * bs:(dst + 1) * bs] = self.v[src * bs:(src + 1) * bs]
+        for prm in (self.k_params, self.v_params):
+            if prm is not None:
+                prm[dst * bs:(dst + 1) * bs] = prm[src * bs:(src + 1) * bs]
 
-    def _decode_k(self, codes, heads=None):
+    def _decode_k(self, codes, heads=None, slots=None):
         if self.k_dtype == "bf16":
             return bf16_bits_to_f64(codes)
+        if self.k_dtype == "int4":
+            return int4_decode_row(codes, self.k_params[slots])
         vals = e4m3_decode(codes)
         sc = np.asarray(self.k_scales, dtype=np.float32).astype(np.float64)
         return vals * (sc if heads is None else sc[heads])[..., :, None]
 
-    def _decode_v(self, codes, heads=None):
+    def _decode_v(self, codes, heads=None, slots=None):
         if self.v_dtype == "bf16":
             return bf16_bits_to_f64(codes)
+        if self.v_dtype == "int4":
+            return int4_decode_row(codes, self.v_params[slots])
         vals = int8_decode(codes)
         sc = np.asarray(self.v_scales, dtype=np.float32).astype(np.float64)
         return vals * (sc if heads is None else sc[heads])[..., :, None]
@@ -463,8 +547,8 @@ class PagedKVCache:
         paged = [p for p in range(start, ctx) if p >= self.num_sink]
         if paged:
             slots = np.array([locate(table_row, p, self.block_size) for p in paged])
-            K[n - len(paged):] = self._decode_k(self.k[slots])
-            V[n - len(paged):] = self._decode_v(self.v[slots])
+            K[n - len(paged):] = self._decode_k(self.k[slots], slots=slots)
+            V[n - len(paged):] = self._decode_v(self.v[slots], slots=slots)
         return K, V
 
 
