@@ -82,11 +82,10 @@ def seq_bytes(w, ctx_s: int) -> int:
     """Algorithmic bytes one sequence contributes to a decode-attention call: its attended K
     and V (sink positions counted at bf16; under a sliding window only the window's positions),
     its q and out rows, the block-table entries it uses and its context length."""
-    e = w.kv_elem_bytes()
     ctx_s = int(ctx_s)
     lo = max(0, ctx_s - w.window) if w.window else 0
     n_sink = max(0, min(ctx_s, w.num_sink) - lo)
-    kv = (ctx_s - lo - n_sink) * w.H_kv * w.D * e * 2 + n_sink * w.H_kv * w.D * 2 * 2
+    kv = (ctx_s - lo - n_sink) * w.H_kv * w.kv_row_bytes() * 2 + n_sink * w.H_kv * w.D * 2 * 2
     return kv + 2 * w.H_q * w.D * 2 + (-(-ctx_s // 16) - lo // 16) * 4 + 4
 
 
@@ -199,9 +198,12 @@ class DecodeBench:
         w = make_workload(name, steps=WINDOW, **({"horizon": horizon} if horizon else {}))
         self.w = w
         n_slots = w.num_blocks * 16
-        kvdt = torch.bfloat16 if w.k_dtype == "bf16" else torch.uint8
-        self.k = torch.empty((n_slots, w.H_kv, w.D), dtype=kvdt, device=device)
-        self.v = torch.empty((n_slots, w.H_kv, w.D), dtype=kvdt, device=device)
+        if w.k_dtype == "bf16":
+            shape, kvdt = (n_slots, w.H_kv, w.D), torch.bfloat16
+        else:  # 8-bit codes, or int4 codes followed by the group parameters
+            shape, kvdt = (n_slots, w.H_kv, w.kv_row_bytes()), torch.uint8
+        self.k = torch.empty(shape, dtype=kvdt, device=device)
+        self.v = torch.empty(shape, dtype=kvdt, device=device)
         self.k_scales = None if w.k_scales is None else w.k_scales.to(device)
         self.v_scales = None if w.v_scales is None else w.v_scales.to(device)
         self.k_sink = self.v_sink = None
@@ -752,30 +754,35 @@ def run_native(args):
     d2h = w.B * w.H_q * w.D * 2
     err = int(b.err.item())
 
+    def measure_decode(name):
+        nb = DecodeBench(name, device, args.partition)
+        n2 = max(50, args.steps // 4)
+        e2, _, by2 = nb.run(n2, args.warmup)
+        _, a2, _ = nb.run(n2, args.warmup, per_call_events=True)
+        a_ms = float(np.mean(a2))
+        ab = float(np.mean([nb.step_bytes[(args.warmup + k) % WINDOW] for k in range(len(a2))]))
+        if nb.w.prefix:
+            ub = float(np.mean([nb.unique_bytes(nb.ctx[(args.warmup + k) % WINDOW]) for k in range(len(a2))]))
+            extra_prefix = {"unique_bytes_per_call": int(ub),
+                            "attention_gbs_unique": round(ub / (a_ms / 1e3) / 1e9, 1),
+                            "fork_copy_pairs": nb.fork_pairs}
+        else:
+            extra_prefix = {}
+        r = {**extra_prefix, "value": round(by2 / e2 / 1e9, 1), "unit": "GB/s",
+             "attention_gbs": round(ab / (a_ms / 1e3) / 1e9, 1),
+             "attention_frac": round(ab / (a_ms / 1e3) / 1e9 / peak, 4),
+             "attention_ms_per_call": round(a_ms, 5),
+             "ms_per_step": round(1e3 * e2 / len(a2), 4),
+             "tokens_per_s_per_layer": round(nb.w.B * len(a2) / e2, 1),
+             "err_flag": int(nb.err.item())}
+        del nb
+        torch.cuda.empty_cache()
+        return r
+
     extra = {}
     if args.also and args.also != "none" and rank == 0:
         for name in args.also.split(","):
-            nb = DecodeBench(name, device, args.partition)
-            n2 = max(50, args.steps // 4)
-            e2, _, by2 = nb.run(n2, args.warmup)
-            _, a2, _ = nb.run(n2, args.warmup, per_call_events=True)
-            a_ms = float(np.mean(a2))
-            ab = float(np.mean([nb.step_bytes[(args.warmup + k) % WINDOW] for k in range(len(a2))]))
-            if nb.w.prefix:
-                ub = float(np.mean([nb.unique_bytes(nb.ctx[(args.warmup + k) % WINDOW]) for k in range(len(a2))]))
-                extra_prefix = {"unique_bytes_per_call": int(ub),
-                                "attention_gbs_unique": round(ub / (a_ms / 1e3) / 1e9, 1),
-                                "fork_copy_pairs": nb.fork_pairs}
-            else:
-                extra_prefix = {}
-            extra[name] = {**extra_prefix, "value": round(by2 / e2 / 1e9, 1), "unit": "GB/s",
-                           "attention_gbs": round(ab / (a_ms / 1e3) / 1e9, 1),
-                           "attention_frac": round(ab / (a_ms / 1e3) / 1e9 / peak, 4),
-                           "ms_per_step": round(1e3 * e2 / len(a2), 4),
-                           "tokens_per_s_per_layer": round(nb.w.B * len(a2) / e2, 1),
-                           "err_flag": int(nb.err.item())}
-            del nb
-            torch.cuda.empty_cache()
+            extra[name] = measure_decode(name)
 
     next_rows = {}
     if rank == 0 and not args.no_next:
@@ -815,6 +822,9 @@ def run_native(args):
         torch.cuda.empty_cache()
         next_rows["prefix_cache"] = prefix_cache_row(device, args.warmup)
         torch.cuda.empty_cache()
+        next_rows["int4_kv_decode"] = {
+            "workload": "int4_8b: the 8b shape with K and V as INT4 codes + bf16 scale + zero point per "
+                        "32 dims (80 bytes per token-head row)", **measure_decode("int4_8b")}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:

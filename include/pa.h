@@ -15,6 +15,10 @@
  *     head h reads KV head h / G, G = num_q_heads / num_kv_heads (显存账本 §二, GQA).
  *   - Optional 8-bit caches store K as FP8 E4M3 and V as INT8 with one fp32 scale per KV
  *     head, and keep the first num_sink positions of every sequence in bf16 (显存账本 §七).
+ *   - Optional 4-bit caches store K and V as INT4 codes with a scale and a zero point per
+ *     group of 32 dims of every token's head row (ldpk §5.2: int4 keeps a scale and a zero
+ *     point, about 0.55-0.65 bytes per element; per-token granularity against K's outlier
+ *     channels).
  *   - Optional sliding window of W tokens (ldpk §5.3): each query attends only the most
  *     recent W positions, its own included, and blocks that fall wholly before the window
  *     go back to the pool (pa_bm_slide_window), so a sequence holds O(W) cache.
@@ -31,6 +35,9 @@
  *   k_new, v_new      bf16  [rows][num_kv_heads][head_dim]
  *   k_sink, v_sink    bf16  [num_seqs][num_sink][num_kv_heads][head_dim]
  *   k_scales,v_scales fp32  [num_kv_heads]
+ *   INT4 pools        [num_blocks * 16][num_kv_heads][64] code bytes, then (at byte offset
+ *                     num_blocks*16*num_kv_heads*64 of the same allocation)
+ *                     [num_blocks * 16][num_kv_heads][4] uint32 group parameters; see PA_INT4.
  *
  * Conventions:
  *   - The caller owns every buffer; apart from the static scratch array behind
@@ -70,7 +77,21 @@ typedef enum {
 typedef enum {
   PA_BF16 = 0,
   PA_FP8_E4M3 = 1, /* OCP FP8 E4M3, round-to-nearest-even, saturating at +-448 */
-  PA_INT8 = 2      /* symmetric int8, round-half-even, clamped to [-127, 127] */
+  PA_INT8 = 2,     /* symmetric int8, round-half-even, clamped to [-127, 127] */
+  PA_INT4 = 3      /* asymmetric 4-bit codes with a bf16 scale and a zero point per 32 dims:
+                    * for each group x[0..31] of a token's head row (head_dim 128: 4 groups)
+                    *   lo = min(0, min x), hi = max(0, max x)           (fp32)
+                    *   s  = bf16(rn((hi - lo) / 15)), 1.0 if that is +-0
+                    *   z  = clamp(rint(-lo / s), 0, 15)
+                    *   q  = clamp(rint(x / s) + z, 0, 15)               (IEEE fp32 divisions)
+                    * and a code decodes to s * (q - z).  Parameter word of a group: bits 0-15
+                    * the bf16 scale, bits 16-23 z, bits 24-31 zero.  Code bytes of one
+                    * (slot, head) row, little-endian:
+                    *   K: uint32 word 4c + g (c, g in 0..3) holds dim 32g + 8c + i in bits
+                    *      4i .. 4i+3 (i in 0..7);
+                    *   V: byte 8r + m (r, m in 0..7) holds dim 16m + r in bits 0-3 and dim
+                    *      16m + r + 8 in bits 4-7.
+                    * 64 code bytes + 16 parameter bytes per row: 0.625 bytes per element. */
 } pa_dtype;
 
 /* Bits OR-ed into *err_flag by the kernels. */
@@ -81,8 +102,8 @@ typedef enum {
 
 /* One layer's cache description.  Supported: block_size == 16; head_dim 64 or 128;
  * num_q_heads % num_kv_heads == 0 with G = num_q_heads/num_kv_heads <= 8;
- * (k_dtype, v_dtype) = (PA_BF16, PA_BF16) or (PA_FP8_E4M3, PA_INT8), the latter with
- * head_dim 128.  k_scales/v_scales are required for 8-bit dtypes and ignored otherwise.
+ * (k_dtype, v_dtype) = (PA_BF16, PA_BF16), (PA_FP8_E4M3, PA_INT8) or (PA_INT4, PA_INT4), the
+ * 8-bit and 4-bit ones with head_dim 128, the 4-bit one with an even num_kv_heads.  k_scales/v_scales are required for 8-bit dtypes and ignored otherwise.
  * num_sink > 0 keeps positions < num_sink in k_sink/v_sink (bf16) for any dtype.
  * sliding_window = W > 0 restricts every query to the W most recent positions (ldpk §5.3):
  * a decode query of a ctx-token sequence reads positions max(0, ctx-W) .. ctx-1, a prefill
@@ -122,7 +143,8 @@ const char* pa_status_string(pa_status status);
  *   pos/16 >= max_blocks_per_seq       -> PA_EFLAG_CTX_OVERFLOW, row skipped;
  *   table entry outside [0,num_blocks) -> PA_EFLAG_BAD_BLOCK_ID, row skipped;
  *   otherwise the slot table[s][pos/16]*16 + pos%16 receives the bf16 bits unchanged, or
- *   for 8-bit caches code = round(x / scale[kv_head]) with the division in IEEE fp32.
+ *   for 8-bit caches code = round(x / scale[kv_head]) with the division in IEEE fp32, or for
+ *   4-bit caches the PA_INT4 codes and group parameters of the row.
  * The caller makes the slot writable first (pa_bm_prepare_step + pa_block_copy) and passes
  * context_lens = positions + 1 to the following pa_decode_attention.
  * Host errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA. */

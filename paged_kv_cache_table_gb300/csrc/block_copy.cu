@@ -14,8 +14,11 @@
 namespace pa {
 namespace {
 
+// grid.y = tensor (K, V) x region: region 0 is the block's codes (block_vecs vectors per block),
+// region 1 (int4 pools only) its group parameters (param_vecs per block at param_base).
 __global__ void __launch_bounds__(256) block_copy_kernel(const int32_t* pairs, int num_blocks,
-                                                         size_t block_vecs, uint4* k_cache,
+                                                         size_t block_vecs, size_t param_base,
+                                                         size_t param_vecs, uint4* k_cache,
                                                          uint4* v_cache, int32_t* err) {
   const int i = blockIdx.x;
   const int src = pairs[2 * i];
@@ -25,10 +28,15 @@ __global__ void __launch_bounds__(256) block_copy_kernel(const int32_t* pairs, i
     return;
   }
   if (src == dst) return;
-  uint4* base = blockIdx.y == 0 ? k_cache : v_cache;
-  const uint4* s = base + static_cast<size_t>(src) * block_vecs;
-  uint4* d = base + static_cast<size_t>(dst) * block_vecs;
-  for (size_t j = threadIdx.x; j < block_vecs; j += blockDim.x) d[j] = s[j];
+  uint4* base = (blockIdx.y & 1) == 0 ? k_cache : v_cache;
+  size_t n = block_vecs;
+  if (blockIdx.y >= 2) {
+    base += param_base;
+    n = param_vecs;
+  }
+  const uint4* s = base + static_cast<size_t>(src) * n;
+  uint4* d = base + static_cast<size_t>(dst) * n;
+  for (size_t j = threadIdx.x; j < n; j += blockDim.x) d[j] = s[j];
 }
 
 }  // namespace
@@ -44,13 +52,14 @@ extern "C" pa_status pa_block_copy(const pa_cache_desc* desc, void* k_cache, voi
   if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
     return PA_ERR_INVALID_ARG;
-  const size_t kbytes = static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * desc->head_dim *
-                        pa::dtype_bytes(desc->k_dtype);
-  const size_t vbytes = static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * desc->head_dim *
-                        pa::dtype_bytes(desc->v_dtype);
-  if (kbytes != vbytes) return PA_ERR_UNSUPPORTED;  // both 8-bit or both bf16
-  pa::block_copy_kernel<<<dim3(n_pairs, 2), 256, 0, pa::as_stream(stream)>>>(
-      src_dst_pairs, desc->num_blocks, kbytes / 16, static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), err_flag);
+  const bool int4 = pa::is_int4(desc);
+  const size_t row = int4 ? pa::int4_code_row_bytes(desc)
+                          : static_cast<size_t>(desc->head_dim) * pa::dtype_bytes(desc->k_dtype);
+  const size_t kbytes = static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * row;
+  const size_t pbytes = int4 ? static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * pa::int4_param_row_bytes(desc)
+                             : 0;
+  pa::block_copy_kernel<<<dim3(n_pairs, int4 ? 4 : 2), 256, 0, pa::as_stream(stream)>>>(
+      src_dst_pairs, desc->num_blocks, kbytes / 16, int4 ? pa::int4_params_offset(desc) / 16 : 0, pbytes / 16,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), err_flag);
   return pa::launch_status();
 }

@@ -59,6 +59,7 @@ struct DecodeParams {
   int B, H_q, H_kv, G, num_blocks, max_blocks, num_sink, max_ctx;
   int window;  // sliding window in tokens, 0 = whole context
   int hg, nc, nbs, stages, warps_c;
+  int block_bytes;  // shared-memory bytes of one block in a stage
   int mode;  // 0 balanced, 1 fixed partitions
   int ppb, max_parts;
   int direct_ok;
@@ -132,21 +133,38 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const DecodeParams& p) {
 // ------------------------------------------------------------------------------------
 // Consumer: one warp = one KV head x one block slot of every stage.
 // ------------------------------------------------------------------------------------
-template <int D, bool QUANT>
+// KIND 0: bf16 K and V; 1: FP8 E4M3 K and INT8 V with per-head scales; 2: INT4 K and V with a
+// scale and zero point per 32 dims of every token's head row.
+template <int D, int KIND>
 struct Consumer {
+  static constexpr bool QUANT = KIND == 1;
+  static constexpr bool I4 = KIND == 2;
   static constexpr int KT = D / 16;  // k-steps of q·Kᵀ and m-tiles of P·V
-  static constexpr int NC = QUANT ? 1 : D * 2 / 128;  // 128-byte chunks per head row
+  static constexpr int NC = KIND != 0 ? 1 : D * 2 / 128;  // 128-byte chunks per head row
   const DecodeParams& p;
   uint32_t qf[KT][2];
   float o[KT][4];
   float m[2], l[2], sl[2];
   float vsc;
   bool bad;
-  int lane, t4, tq, h_kv, j;
+  int lane, t4, tq, h_kv, j, h_loc;
+  uint32_t kofs, vofs, kpofs, vpofs;  // this warp's tiles inside a stage
 
-  __device__ Consumer(const DecodeParams& p_, int lane_, int h_kv_, int j_)
-      : p(p_), vsc(1.f), lane(lane_), t4(lane_ >> 2), tq(lane_ & 3), h_kv(h_kv_), j(j_) {
+  __device__ Consumer(const DecodeParams& p_, int lane_, int h_kv_, int j_, int h_loc_)
+      : p(p_), vsc(1.f), lane(lane_), t4(lane_ >> 2), tq(lane_ & 3), h_kv(h_kv_), j(j_), h_loc(h_loc_) {
     sl[0] = sl[1] = p_.scale_log2;
+    if constexpr (I4) {
+      // block j of a stage: [K codes][V codes] (16 slots x hg/2 rows x 128 B, swizzled), then
+      // [K params][V params] (16 slots x hg heads x 16 B)
+      kofs = j * p_.block_bytes;
+      vofs = kofs + p_.hg * 1024;
+      kpofs = kofs + 2 * p_.hg * 1024;
+      vpofs = kpofs + p_.hg * 256;
+    } else {
+      kofs = ((j * 2 + 0) * p_.hg * p_.nc + h_loc_ * p_.nc) * kTileBytes;
+      vofs = ((j * 2 + 1) * p_.hg * p_.nc + h_loc_ * p_.nc) * kTileBytes;
+      kpofs = vpofs = 0;
+    }
     reset();
   }
 
@@ -162,7 +180,20 @@ struct Consumer {
   __device__ __forceinline__ void load_q(int s) {
     const bool live = t4 < p.G;
     const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(s) * p.H_q + h_kv * p.G + (live ? t4 : 0)) * D;
-    if constexpr (!QUANT) {
+    if constexpr (I4) {
+      // k-steps 2g and 2g+1 take the dims of 32-dim group g that lane tq's K words hold:
+      // 32g + 8tq + {0,4 | 1,5} and {2,6 | 3,7} (the pairs one mask pulls out of a code word)
+#pragma unroll
+      for (int g = 0; g < D / 32; ++g) {
+        const uint4 x = live ? *reinterpret_cast<const uint4*>(qrow + g * 32 + tq * 8) : make_uint4(0, 0, 0, 0);
+        qf[2 * g][0] = prmt(x.x, x.z, 0x5410);
+        qf[2 * g][1] = prmt(x.x, x.z, 0x7632);
+        qf[2 * g + 1][0] = prmt(x.y, x.w, 0x5410);
+        qf[2 * g + 1][1] = prmt(x.y, x.w, 0x7632);
+      }
+      sl[0] = sl[1] = p.scale_log2;
+      vsc = 1.f;
+    } else if constexpr (!QUANT) {
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
         qf[kk][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * tq) : 0u;
@@ -209,10 +240,143 @@ struct Consumer {
     }
   }
 
+  // Online-softmax update for the block's scores acc (rows = tokens t4, t4+8; columns = query
+  // heads 2tq, 2tq+1, not yet scaled); returns this lane's unnormalised probabilities.
+  __device__ __forceinline__ void softmax(const float (&acc)[4], int first, int ntok, float& p00, float& p01,
+                                          float& p10, float& p11) {
+    // rows t4 and t4+8 of the block; columns = query heads 2tq, 2tq+1
+    const bool v0 = t4 < ntok && t4 >= first;
+    const bool v1 = t4 + 8 < ntok && t4 + 8 >= first;
+    const float s00 = v0 ? acc[0] * sl[0] : kNegInf;
+    const float s01 = v0 ? acc[1] * sl[1] : kNegInf;
+    const float s10 = v1 ? acc[2] * sl[0] : kNegInf;
+    const float s11 = v1 ? acc[3] * sl[1] : kNegInf;
+    float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int mask = 4; mask <= 16; mask <<= 1) {
+      bm0 = warp_max_xor(bm0, mask);
+      bm1 = warp_max_xor(bm1, mask);
+    }
+    // The reference maximum only moves when a score exceeds it by more than 2^8 (exact: the
+    // final division by l uses the same reference), so most blocks skip the rescale of o.
+    const float mn0 = (m[0] == kNegInf || bm0 > m[0] + 8.f) ? fmaxf(m[0], bm0) : m[0];
+    const float mn1 = (m[1] == kNegInf || bm1 > m[1] + 8.f) ? fmaxf(m[1], bm1) : m[1];
+    const float ms0 = mn0 == kNegInf ? 0.f : mn0;
+    const float ms1 = mn1 == kNegInf ? 0.f : mn1;
+    p00 = ex2(s00 - ms0);
+    p10 = ex2(s10 - ms0);
+    p01 = ex2(s01 - ms1);
+    p11 = ex2(s11 - ms1);
+    if (__any_sync(0xffffffffu, mn0 != m[0] || mn1 != m[1])) {
+      const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
+      l[0] *= al0;
+      l[1] *= al1;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
+    l[0] += p00 + p10;
+    l[1] += p01 + p11;
+    m[0] = mn0;
+    m[1] = mn1;
+  }
+
+  // INT4: byte x (0..63) of this warp's head row in slot `slot` of a codes tile, whose 128-byte
+  // rows hold two heads each and carry the 128-byte swizzle of the TMA box.
+  __device__ __forceinline__ const uint8_t* i4_code(const uint8_t* tile, int slot, int x) const {
+    const int R = slot * (p.hg >> 1) + (h_loc >> 1);
+    const int xb = ((h_loc & 1) << 6) + x;
+    return tile + R * 128 + ((((xb >> 4) ^ (R & 7)) << 4) | (xb & 15));
+  }
+  // INT4: the four group parameter words of this warp's head in slot `slot`.
+  __device__ __forceinline__ uint4 i4_param(const uint8_t* tile, int slot) const {
+    return *reinterpret_cast<const uint4*>(tile + (slot * p.hg + h_loc) * 16);
+  }
+
+  // INT4 block.  Codes become exact bf16 integers (128 + n) - (128 + z) = n - z.  Scores: lane
+  // tq's K words hold whole 32-dim groups, so the two k-steps of group g accumulate apart and
+  // the group's scale multiplies the fp32 sum.  P·V: the MMA sums over tokens, so each token's
+  // group scale goes into P before the transpose; the output rows are dims 16mt + t4 (+8).
+  __device__ __forceinline__ void block_i4(const uint8_t* stage, int first, int ntok) {
+    constexpr uint32_t kOne = 0x3F803F80u;  // bf16 pair (1, 1)
+    const uint8_t* kc = stage + kofs;
+    const uint8_t* vc = stage + vofs;
+    const uint8_t* kp = stage + kpofs;
+    const uint8_t* vp = stage + vpofs;
+    const uint4 kw0 = *reinterpret_cast<const uint4*>(i4_code(kc, t4, tq * 16));
+    const uint4 kw1 = *reinterpret_cast<const uint4*>(i4_code(kc, t4 + 8, tq * 16));
+    const uint4 kq0 = i4_param(kp, t4), kq1 = i4_param(kp, t4 + 8);
+    const uint32_t w0[4] = {kw0.x, kw0.y, kw0.z, kw0.w}, w1[4] = {kw1.x, kw1.y, kw1.z, kw1.w};
+    const uint32_t q0[4] = {kq0.x, kq0.y, kq0.z, kq0.w}, q1[4] = {kq1.x, kq1.y, kq1.z, kq1.w};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t z0 = (((q0[g] >> 16) & 0xFFu) * 0x00010001u) | 0xC300C300u;  // -(128 + z), twice
+      const uint32_t z1 = (((q1[g] >> 16) & 0xFFu) * 0x00010001u) | 0xC300C300u;
+      float ag[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_bf16(ag, fma_bf16x2(nib_pair(w0[g], 0), kOne, z0), fma_bf16x2(nib_pair(w1[g], 0), kOne, z1),
+               fma_bf16x2(nib_pair(w0[g], 1), kOne, z0), fma_bf16x2(nib_pair(w1[g], 1), kOne, z1),
+               qf[2 * g][0], qf[2 * g][1]);
+      mma_bf16(ag, fma_bf16x2(nib_pair(w0[g], 2), kOne, z0), fma_bf16x2(nib_pair(w1[g], 2), kOne, z1),
+               fma_bf16x2(nib_pair(w0[g], 3), kOne, z0), fma_bf16x2(nib_pair(w1[g], 3), kOne, z1),
+               qf[2 * g + 1][0], qf[2 * g + 1][1]);
+      const float s0 = __uint_as_float(q0[g] << 16), s1 = __uint_as_float(q1[g] << 16);
+      acc[0] = fmaf(s0, ag[0], acc[0]);
+      acc[1] = fmaf(s0, ag[1], acc[1]);
+      acc[2] = fmaf(s1, ag[2], acc[2]);
+      acc[3] = fmaf(s1, ag[3], acc[3]);
+    }
+    float p00, p01, p10, p11;
+    softmax(acc, first, ntok, p00, p01, p10, p11);
+    // scales of the P rows (tokens t4, t4 + 8); a masked token's slot may hold any bits, so its
+    // scale is replaced by 0 rather than multiplied in
+    const bool v0 = t4 < ntok && t4 >= first;
+    const bool v1 = t4 + 8 < ntok && t4 + 8 >= first;
+    const uint4 vs0 = i4_param(vp, t4), vs1 = i4_param(vp, t4 + 8);
+    const uint32_t sv0w[4] = {vs0.x, vs0.y, vs0.z, vs0.w}, sv1w[4] = {vs1.x, vs1.y, vs1.z, vs1.w};
+    // zero points and codes of the A columns: tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
+    const uint4 zA = i4_param(vp, 2 * tq), zB = i4_param(vp, 2 * tq + 1);
+    const uint4 zC = i4_param(vp, 2 * tq + 8), zD = i4_param(vp, 2 * tq + 9);
+    const uint32_t zAw[4] = {zA.x, zA.y, zA.z, zA.w}, zBw[4] = {zB.x, zB.y, zB.z, zB.w};
+    const uint32_t zCw[4] = {zC.x, zC.y, zC.z, zC.w}, zDw[4] = {zD.x, zD.y, zD.z, zD.w};
+    const uint2 cA = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq, t4 * 8));
+    const uint2 cB = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq + 1, t4 * 8));
+    const uint2 cC = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq + 8, t4 * 8));
+    const uint2 cD = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq + 9, t4 * 8));
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float sv0 = v0 ? __uint_as_float(sv0w[g] << 16) : 0.f;
+      const float sv1 = v1 ? __uint_as_float(sv1w[g] << 16) : 0.f;
+      const uint32_t b0 = movmatrix_t(pack_bf16(p00 * sv0, p01 * sv0));
+      const uint32_t b1 = movmatrix_t(pack_bf16(p10 * sv1, p11 * sv1));
+      const uint32_t zAB = (prmt(zAw[g], zBw[g], 0x0602) & 0x00FF00FFu) | 0xC300C300u;
+      const uint32_t zCD = (prmt(zCw[g], zDw[g], 0x0602) & 0x00FF00FFu) | 0xC300C300u;
+#pragma unroll
+      for (int mm = 0; mm < 2; ++mm) {
+        const int mt = 2 * g + mm, k = mt & 3;
+        const uint32_t sel = static_cast<uint32_t>(k | ((k + 4) << 8));  // byte k of each token
+        const uint32_t tAB = prmt(mt < 4 ? cA.x : cA.y, mt < 4 ? cB.x : cB.y, sel);
+        const uint32_t tCD = prmt(mt < 4 ? cC.x : cC.y, mt < 4 ? cD.x : cD.y, sel);
+        mma_bf16(o[mt], fma_bf16x2(nib_pair(tAB, 0), kOne, zAB), fma_bf16x2(nib_pair(tAB, 1), kOne, zAB),
+                 fma_bf16x2(nib_pair(tCD, 0), kOne, zCD), fma_bf16x2(nib_pair(tCD, 1), kOne, zCD), b0, b1);
+      }
+    }
+  }
+
   // One 16-token block: scores, online softmax update, P·V.
   // Tokens first .. ntok-1 of the block are attended; those below `first` are sink positions
   // (read from the bf16 sink buffer by the merge) or lie before the sliding window.
-  __device__ __forceinline__ void block(const uint8_t* kbase, const uint8_t* vbase, int first, int ntok) {
+  __device__ __forceinline__ void block(const uint8_t* stage, int first, int ntok) {
+    if constexpr (I4) {
+      block_i4(stage, first, ntok);
+      return;
+    }
+    const uint8_t* kbase = stage + kofs;
+    const uint8_t* vbase = stage + vofs;
     // two independent accumulation chains halve the dependent-MMA latency of q·Kᵀ
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float acc2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -243,43 +407,8 @@ struct Consumer {
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
-    // rows t4 and t4+8 of the block; columns = query heads 2tq, 2tq+1
-    const bool v0 = t4 < ntok && t4 >= first;
-    const bool v1 = t4 + 8 < ntok && t4 + 8 >= first;
-    const float s00 = v0 ? acc[0] * sl[0] : kNegInf;
-    const float s01 = v0 ? acc[1] * sl[1] : kNegInf;
-    const float s10 = v1 ? acc[2] * sl[0] : kNegInf;
-    const float s11 = v1 ? acc[3] * sl[1] : kNegInf;
-    float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
-#pragma unroll
-    for (int mask = 4; mask <= 16; mask <<= 1) {
-      bm0 = warp_max_xor(bm0, mask);
-      bm1 = warp_max_xor(bm1, mask);
-    }
-    // The reference maximum only moves when a score exceeds it by more than 2^8 (exact: the
-    // final division by l uses the same reference), so most blocks skip the rescale of o.
-    const float mn0 = (m[0] == kNegInf || bm0 > m[0] + 8.f) ? fmaxf(m[0], bm0) : m[0];
-    const float mn1 = (m[1] == kNegInf || bm1 > m[1] + 8.f) ? fmaxf(m[1], bm1) : m[1];
-    const float ms0 = mn0 == kNegInf ? 0.f : mn0;
-    const float ms1 = mn1 == kNegInf ? 0.f : mn1;
-    const float p00 = ex2(s00 - ms0), p10 = ex2(s10 - ms0);
-    const float p01 = ex2(s01 - ms1), p11 = ex2(s11 - ms1);
-    if (__any_sync(0xffffffffu, mn0 != m[0] || mn1 != m[1])) {
-      const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
-      l[0] *= al0;
-      l[1] *= al1;
-#pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
-      }
-    }
-    l[0] += p00 + p10;
-    l[1] += p01 + p11;
-    m[0] = mn0;
-    m[1] = mn1;
+    float p00, p01, p10, p11;
+    softmax(acc, first, ntok, p00, p01, p10, p11);
     // P (tokens x heads) -> B operand (K = tokens, N = heads) of P·V
     const uint32_t x0 = QUANT ? pack_f16(p00, p01) : pack_bf16(p00, p01);
     const uint32_t x1 = QUANT ? pack_f16(p10, p11) : pack_bf16(p10, p11);
@@ -386,9 +515,10 @@ struct Consumer {
   }
 };
 
-template <int D, bool QUANT, int MAXW>
+template <int D, int KIND, int MAXW>
 __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmKp, const __grid_constant__ CUtensorMap tmVp,
                   const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve(smem_raw, p);
@@ -490,17 +620,30 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     // chunk ahead and its stage metadata is packed once when the chunk becomes current, so a
     // stage costs one shuffle, one shared store and one TMA per (tensor, head) box.  Each box
     // is a whole head row (all 128-byte chunks) of the block's 16 slots.
-    const uint32_t box_bytes = static_cast<uint32_t>(p.nc) * kTileBytes;
-    const int ops_per_block = 2 * p.hg;
+    // INT4 stages take four boxes per block: K and V codes of all the group's heads (128-byte
+    // rows of two heads), then K and V group parameters.
+    const int ops_per_block = KIND == 2 ? 4 : 2 * p.hg;
     const int n_ops = nbs * ops_per_block;  // <= 32
     const uint64_t policy = l2_evict_first_policy();
     // this lane's op (fixed for every stage): block jj of the stage, tensor, head
     const int my_jj = lane / ops_per_block;
-    const int my_t = (lane - my_jj * ops_per_block) / p.hg;
-    const int my_h = lane - my_jj * ops_per_block - my_t * p.hg;
-    const CUtensorMap* my_map = my_t ? &tmV : &tmK;
-    const int my_row = (hgi * p.hg + my_h) * p.nc;
-    const size_t my_dst = static_cast<size_t>((my_jj * 2 + my_t) * p.hg + my_h) * box_bytes;
+    const int my_op = lane - my_jj * ops_per_block;
+    const CUtensorMap* my_map;
+    int my_row;
+    size_t my_dst;
+    if constexpr (KIND == 2) {
+      const int t = my_op & 1, prm = my_op >> 1;
+      my_map = prm ? (t ? &tmVp : &tmKp) : (t ? &tmV : &tmK);
+      my_row = prm ? hgi * p.hg : hgi * (p.hg >> 1);
+      my_dst = static_cast<size_t>(my_jj) * p.block_bytes +
+               (prm ? 2 * p.hg * 1024 + t * p.hg * 256 : t * p.hg * 1024);
+    } else {
+      const int my_t = my_op / p.hg;
+      const int my_h = my_op - my_t * p.hg;
+      my_map = my_t ? &tmV : &tmK;
+      my_row = (hgi * p.hg + my_h) * p.nc;
+      my_dst = static_cast<size_t>((my_jj * 2 + my_t) * p.hg + my_h) * p.nc * kTileBytes;
+    }
     // logical block of list entry u of sequence s (the visited blocks start at the window)
     auto logical = [&](int s, int u) { return window_lo(p, sm.ctxs[s]) / PA_BLOCK_SIZE + (u - sm.cum[s]); };
     auto load_entry = [&](int u) -> int {
@@ -551,7 +694,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       }
       if (lane >= i && lane < i + nbs) sm.meta[st * nbs + (lane - i)] = my_meta;
       if (lane == 0) {
-        const uint32_t bytes = __popc(live) * ops_per_block * box_bytes;
+        const uint32_t bytes = __popc(live) * static_cast<uint32_t>(p.block_bytes);
         if (bytes) mbar_arrive_expect_tx(&sm.full[st], bytes);
         else mbar_arrive(&sm.full[st]);
       }
@@ -574,7 +717,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
   // ------------------------------- consumers -------------------------------
   const int j = warp / p.hg;
   const int h_loc = warp - j * p.hg;
-  Consumer<D, QUANT> c(p, lane, hgi * p.hg + h_loc, j);
+  Consumer<D, KIND> c(p, lane, hgi * p.hg + h_loc, j, h_loc);
   const int s_first = find_seq(sm.cum, nseq, u0);
   const int s_last = find_seq(sm.cum, nseq, u1 - 1);
   const int n_iters = (u1 - u0 + nbs - 1) / nbs;
@@ -586,8 +729,6 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
   auto covers = [&](int s_rel) -> bool { return sm.cum[s_rel] >= u0 && sm.cum[s_rel + 1] <= u1; };
   int cur = s_first;
   bool q_loaded = false;
-  const size_t kofs = static_cast<size_t>((j * 2 + 0) * p.hg * p.nc + h_loc * p.nc) * kTileBytes;
-  const size_t vofs = static_cast<size_t>((j * 2 + 1) * p.hg * p.nc + h_loc * p.nc) * kTileBytes;
   for (int k = 0; k < n_iters; ++k) {
     const int st = k % S;
     const uint32_t ph = static_cast<uint32_t>(k / S) & 1u;
@@ -613,7 +754,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
         c.bad = true;
       } else {
         const uint8_t* stage = sm.stages + static_cast<size_t>(st) * p.stage_bytes;
-        c.block(stage + kofs, stage + vofs, mt.y, mt.z);
+        c.block(stage, mt.y, mt.z);
       }
     }
     __syncwarp();
@@ -752,7 +893,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
 struct Plan {
   int hg, n_hg, nc, nbs, warps_c, threads, stages;
   int mode, ppb, max_parts, grid_x;
-  int stage_bytes;
+  int stage_bytes, block_bytes;
   size_t smem_bytes, meta_bytes, ws_bytes, n_slots;
 };
 
@@ -767,19 +908,22 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
   pa_status st = validate_desc(d);
   if (st != PA_OK) return st;
   if (max_ctx < 0 || partition_size < 0 || partition_size % PA_BLOCK_SIZE != 0) return PA_ERR_INVALID_ARG;
+  const bool int4 = is_int4(d);
   const int e = dtype_bytes(d->k_dtype);
-  const int row_bytes = d->head_dim * e;  // 128 or 256
-  pl->nc = row_bytes / 128;
+  const int row_bytes = int4 ? d->head_dim / 2 : d->head_dim * e;  // 64, 128 or 256
+  pl->nc = int4 ? 1 : row_bytes / 128;
   int hg = 1;
   for (int c = 1; c <= d->num_kv_heads; ++c)
-    if (d->num_kv_heads % c == 0 && c * row_bytes <= PA_GROUP_BYTES) hg = c;
+    if (d->num_kv_heads % c == 0 && c * row_bytes <= PA_GROUP_BYTES && (!int4 || c % 2 == 0)) hg = c;
   pl->hg = hg;
   pl->n_hg = d->num_kv_heads / hg;
   pl->nbs = std::max(1, 8 / hg);
   pl->warps_c = hg * pl->nbs;
   if (pl->warps_c > kMaxConsumerWarps) return PA_ERR_UNSUPPORTED;
   pl->threads = (pl->warps_c + 1) * 32;
-  pl->stage_bytes = pl->nbs * 2 * hg * pl->nc * kTileBytes;
+  // int4 block: K and V codes (hg x 1 KiB each) and group parameters (hg x 256 B each)
+  pl->block_bytes = int4 ? 2560 * hg : 2 * hg * pl->nc * kTileBytes;
+  pl->stage_bytes = pl->nbs * pl->block_bytes;
   const int B = d->num_seqs;
   if (B > 65535) return PA_ERR_UNSUPPORTED;  // grid.y of the fixed-partition launch
   if (partition_size == 0 && B <= kAutoMaxSeqs) {
@@ -815,18 +959,18 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
   return PA_OK;
 }
 
-template <int D, bool QUANT>
-pa_status launch(const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p,
-                 cudaStream_t stream) {
+template <int D, int KIND>
+pa_status launch(const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mkp,
+                 const CUtensorMap& mvp, const DecodeParams& p, cudaStream_t stream) {
   // 9-warp CTAs get the register budget of a 288-thread launch; wider ones a 544-thread one
-  auto kern = pl.warps_c <= 8 ? decode_kernel<D, QUANT, 8> : decode_kernel<D, QUANT, kMaxConsumerWarps>;
+  auto kern = pl.warps_c <= 8 ? decode_kernel<D, KIND, 8> : decode_kernel<D, KIND, kMaxConsumerWarps>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(pl.smem_bytes)) != cudaSuccess)
     return PA_ERR_CUDA;
   const dim3 grid = p.mode == 0 ? dim3(pl.grid_x, pl.n_hg, 1) : dim3(pl.max_parts, p.B, pl.n_hg);
   // Both kernels may start while their predecessor drains (the decode prologue overlaps the
   // append; the merge launch overlaps the decode tail); each waits before reading its inputs.
-  if (launch_overlapped(kern, grid, dim3(pl.threads), pl.smem_bytes, stream, mk, mv, p) != PA_OK)
+  if (launch_overlapped(kern, grid, dim3(pl.threads), pl.smem_bytes, stream, mk, mv, mkp, mvp, p) != PA_OK)
     return PA_ERR_CUDA;
   return launch_overlapped(merge_kernel<D>, dim3(p.B, (p.H_q + 3) / 4), dim3(128), 0, stream, p, pl.grid_x);
 }
@@ -862,10 +1006,23 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, c
 
   const int e = pa::dtype_bytes(desc->k_dtype);
   const long long slots = static_cast<long long>(desc->num_blocks) * PA_BLOCK_SIZE;
-  CUtensorMap mk, mv;
-  if (!pa::encode_cache_map(&mk, k_cache, e, desc->num_kv_heads * pl.nc, pl.nc, slots) ||
-      !pa::encode_cache_map(&mv, v_cache, e, desc->num_kv_heads * pl.nc, pl.nc, slots))
-    return PA_ERR_CUDA;
+  const bool int4 = pa::is_int4(desc);
+  CUtensorMap mk, mv, mkp, mvp;
+  if (int4) {
+    // codes: 128-byte rows of two heads; parameters: 16-byte rows of one head
+    const size_t po = pa::int4_params_offset(desc);
+    if (!pa::encode_cache_map(&mk, k_cache, 1, desc->num_kv_heads / 2, pl.hg / 2, slots) ||
+        !pa::encode_cache_map(&mv, v_cache, 1, desc->num_kv_heads / 2, pl.hg / 2, slots) ||
+        !pa::encode_param_map(&mkp, static_cast<const uint8_t*>(k_cache) + po, desc->num_kv_heads, pl.hg, slots) ||
+        !pa::encode_param_map(&mvp, static_cast<const uint8_t*>(v_cache) + po, desc->num_kv_heads, pl.hg, slots))
+      return PA_ERR_CUDA;
+  } else {
+    if (!pa::encode_cache_map(&mk, k_cache, e, desc->num_kv_heads * pl.nc, pl.nc, slots) ||
+        !pa::encode_cache_map(&mv, v_cache, e, desc->num_kv_heads * pl.nc, pl.nc, slots))
+      return PA_ERR_CUDA;
+    mkp = mk;  // unused by the bf16 and 8-bit kernels
+    mvp = mv;
+  }
 
   pa::DecodeParams p;
   p.B = desc->num_seqs;
@@ -887,6 +1044,7 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, c
   p.max_parts = pl.max_parts;
   p.direct_ok = (pl.nbs == 1 && desc->num_sink == 0) ? 1 : 0;
   p.stage_bytes = pl.stage_bytes;
+  p.block_bytes = pl.block_bytes;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.block_tables = block_tables;
   p.context_lens = context_lens;
@@ -903,8 +1061,10 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, c
   cudaStream_t s = pa::as_stream(stream);
   const bool quant = pa::is_quantized(desc);
   if (desc->head_dim == 128)
-    return quant ? pa::launch<128, true>(pl, mk, mv, p, s) : pa::launch<128, false>(pl, mk, mv, p, s);
-  return pa::launch<64, false>(pl, mk, mv, p, s);
+    return int4    ? pa::launch<128, 2>(pl, mk, mv, mkp, mvp, p, s)
+           : quant ? pa::launch<128, 1>(pl, mk, mv, mkp, mvp, p, s)
+                   : pa::launch<128, 0>(pl, mk, mv, mkp, mvp, p, s);
+  return pa::launch<64, 0>(pl, mk, mv, mkp, mvp, p, s);
 }
 
 // ------------------------------------------------------------------------------------

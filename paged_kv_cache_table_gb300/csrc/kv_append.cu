@@ -4,7 +4,9 @@
 // written at the sequence's current length.  "KV Cache 的显存账本：PagedAttention 与连续批处理"
 // §四: the slot is table[pos / 16] * 16 + pos % 16 (the locate() sketch).  Same page §七:
 // 8-bit caches hold K as FP8 and V as INT8 with one scale per KV head, and sink tokens keep
-// their original precision.
+// their original precision.  Untitled KV-cache article at ldpk.cn/news/58971 §5.2: 4-bit caches
+// keep a scale and a zero point besides the codes; here one of each per 32 dims of a token's
+// head row (the PA_INT4 rule in pa.h).
 //
 // One CTA per appended row; each thread moves 8 elements (one 16-byte bf16 vector).  The
 // row's kv_heads x head_dim elements are contiguous in the slot-major cache, so the stores
@@ -31,6 +33,7 @@ struct AppendParams {
   const float* v_scales;
   uint4* k_sink;
   uint4* v_sink;
+  size_t params_offset;  // int4: byte offset of the group parameters in each pool
   int32_t* err;
 };
 
@@ -71,7 +74,55 @@ __device__ __forceinline__ uint2 encode_int8x8(const uint4& v, float scale) {
   return make_uint2(out[0], out[1]);
 }
 
-template <bool QUANT>
+// One thread per (tensor, kv head, 32-dim group) of the row: range, bf16 scale, zero point and
+// codes in IEEE fp32, then the codes in the K or V byte order of PA_INT4 and the group's
+// parameter word after the code bytes of every slot.
+__device__ __forceinline__ void encode_int4_group(const uint4* src, int h, int g, int tensor, int H_kv,
+                                                  size_t slot, uint8_t* cache, size_t params_offset) {
+  float x[32];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    float t[8];
+    unpack_bf16x8(src[v], t);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[8 * v + e] = t[e];
+  }
+  float lo = 0.f, hi = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    lo = fminf(lo, x[i]);
+    hi = fmaxf(hi, x[i]);
+  }
+  const float s = __fdiv_rn(__fsub_rn(hi, lo), 15.f);
+  uint32_t sb = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+  if ((sb & 0x7FFFu) == 0) sb = 0x3F80u;  // an all-zero group
+  const float sf = __uint_as_float(sb << 16);
+  const float z = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.f), 15.f);
+  uint32_t q[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    q[i] = static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(x[i], sf)) + z, 0.f), 15.f));
+  uint8_t* row = cache + (slot * H_kv + h) * 64;
+  if (tensor == 0) {  // K: word 4c + g holds dims 32g + 8c + i at bits 4i
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w |= q[8 * c + i] << (4 * i);
+      reinterpret_cast<uint32_t*>(row)[4 * c + g] = w;
+    }
+  } else {  // V: byte 8r + m holds dim 16m + r (low) and 16m + r + 8 (high); m = 2g, 2g + 1
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const uint32_t b0 = q[r] | (q[r + 8] << 4), b1 = q[16 + r] | (q[24 + r] << 4);
+      reinterpret_cast<uint16_t*>(row + 8 * r + 2 * g)[0] = static_cast<uint16_t>(b0 | (b1 << 8));
+    }
+  }
+  reinterpret_cast<uint32_t*>(cache + params_offset)[(slot * H_kv + h) * 4 + g] =
+      sb | (static_cast<uint32_t>(z) << 16);
+}
+
+template <int KIND>  // 0 bf16, 1 fp8 K / int8 V, 2 int4
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   // the decode kernel that usually follows may start its prologue now: it waits for this
   // kernel's completion before it reads the cache
@@ -107,10 +158,19 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
     return;
   }
   const size_t slot = static_cast<size_t>(pb) * PA_BLOCK_SIZE + pos % PA_BLOCK_SIZE;
+  if constexpr (KIND == 2) {
+    const int groups = p.H_kv * 4;  // head_dim 128
+    for (int i = threadIdx.x; i < 2 * groups; i += blockDim.x) {
+      const int tensor = i / groups, h = (i % groups) / 4, g = i % 4;
+      encode_int4_group((tensor ? vin : kin) + h * 16 + g * 4, h, g, tensor, p.H_kv, slot,
+                        static_cast<uint8_t*>(tensor ? p.v_cache : p.k_cache), p.params_offset);
+    }
+    return;
+  }
   for (int i = threadIdx.x; i < vecs; i += blockDim.x) {
     const uint4 kv = kin[i];
     const uint4 vv = vin[i];
-    if constexpr (QUANT) {
+    if constexpr (KIND == 1) {
       const int h = (i * 8) / p.D;
       reinterpret_cast<uint2*>(p.k_cache)[slot * vecs + i] = encode_e4m3x8(kv, p.k_scales[h]);
       reinterpret_cast<uint2*>(p.v_cache)[slot * vecs + i] = encode_int8x8(vv, p.v_scales[h]);
@@ -155,12 +215,15 @@ pa_status append_impl(const pa_cache_desc* d, void* k_cache, void* v_cache, cons
   p.k_sink = static_cast<uint4*>(d->k_sink);
   p.v_sink = static_cast<uint4*>(d->v_sink);
   p.err = err;
+  p.params_offset = is_int4(d) ? int4_params_offset(d) : 0;
   const int vecs = p.H_kv * p.D / 8;
   const int threads = min(256, ((vecs + 31) / 32) * 32);
-  if (is_quantized(d))
-    kv_append_kernel<true><<<num_rows, threads, 0, as_stream(stream)>>>(p);
+  if (is_int4(d))
+    kv_append_kernel<2><<<num_rows, threads, 0, as_stream(stream)>>>(p);
+  else if (is_quantized(d))
+    kv_append_kernel<1><<<num_rows, threads, 0, as_stream(stream)>>>(p);
   else
-    kv_append_kernel<false><<<num_rows, threads, 0, as_stream(stream)>>>(p);
+    kv_append_kernel<0><<<num_rows, threads, 0, as_stream(stream)>>>(p);
   return launch_status();
 }
 

@@ -198,6 +198,19 @@ __device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t biased_codes, uint32_
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// d = a * b + c on bf16 pairs, rounded to nearest.
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Nibbles i and i + 4 of w (bits 4i.. and 16 + 4i..) as the bf16 pair (128 + n_i, 128 + n_{i+4}):
+// 0x4300 is 128.0 and the seven mantissa bits below it count units.
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int i) {
+  return ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+}
+
 __device__ __forceinline__ float warp_max_xor(float v, int mask) {
   return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, mask));
 }

@@ -14,6 +14,18 @@ inline int dtype_bytes(pa_dtype t) { return t == PA_BF16 ? 2 : 1; }
 
 inline bool is_quantized(const pa_cache_desc* d) { return d->k_dtype != PA_BF16; }
 
+inline bool is_int4(const pa_cache_desc* d) { return d->k_dtype == PA_INT4; }
+
+// INT4 pools: code bytes of every slot first, then the group parameter words.
+constexpr int kInt4Group = 32;
+inline size_t int4_code_row_bytes(const pa_cache_desc* d) { return static_cast<size_t>(d->head_dim) / 2; }
+inline size_t int4_param_row_bytes(const pa_cache_desc* d) {
+  return static_cast<size_t>(d->head_dim) / kInt4Group * 4;
+}
+inline size_t int4_params_offset(const pa_cache_desc* d) {
+  return static_cast<size_t>(d->num_blocks) * PA_BLOCK_SIZE * d->num_kv_heads * int4_code_row_bytes(d);
+}
+
 // Checks a cache description against what the kernels implement.
 pa_status validate_desc(const pa_cache_desc* d);
 
@@ -21,6 +33,10 @@ pa_status validate_desc(const pa_cache_desc* d);
 // boxes of `box_rows` chunks x 16 slots (tensor_map.cpp).
 bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int rows, int box_rows,
                       long long slots);
+
+// TMA descriptor of the INT4 group parameters viewed as (16-byte head row, kv_head, slot) with
+// boxes of `box_heads` heads x 16 slots, no swizzle (tensor_map.cpp).
+bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots);
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 

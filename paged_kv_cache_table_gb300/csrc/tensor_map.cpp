@@ -45,4 +45,16 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int ro
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {4, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(slots)};
+  cuuint64_t strides[2] = {16, static_cast<cuuint64_t>(heads) * 16};
+  cuuint32_t box[3] = {4, static_cast<cuuint32_t>(box_heads), PA_BLOCK_SIZE};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace pa

@@ -24,6 +24,8 @@ Workloads (seed = 20260 + index):
                   sliding window of 4096 tokens: only the blocks holding the first step's window
                   are in the pool (earlier table entries are -1, already released), and only the
                   window's positions are written.
+  8 "int4_8b"     the 8b shape (64 sequences, cached U[512, 4096], 32 / 8 heads, d 128) with K and V
+                  stored as INT4 codes with a scale and zero point per 32 dims of every row.
 Every step appends one token per sequence at position = cached length, then attends over
 cached length + 1 tokens.  All tensors are produced on the CPU with a torch.Generator.
 """
@@ -45,6 +47,7 @@ CONFIGS = {
     "prefix_cow": dict(index=4, B=64, H_q=32, H_kv=8, D=128, prefix=1208, suffix_range=(200, 2000)),
     "long_quant": dict(index=5, B=4, H_q=32, H_kv=8, D=128, ctx_fixed=131072, quant=True, num_sink=4),
     "swa": dict(index=7, B=64, H_q=32, H_kv=8, D=128, ctx_range=(4096, 16384), window=4096),
+    "int4_8b": dict(index=8, B=64, H_q=32, H_kv=8, D=128, ctx_range=(512, 4096), kv="int4"),
 }
 
 # Calibration code ranges of the 8-bit formats (largest finite E4M3 value; symmetric int8).
@@ -97,6 +100,13 @@ class Workload:
 
     def kv_elem_bytes(self) -> int:
         return 1 if self.k_dtype != "bf16" else 2
+
+    def kv_row_bytes(self) -> int:
+        """Cache bytes of one (token, KV head) row of K or V: int4 holds 4-bit codes plus one
+        32-bit scale / zero-point word per 32 dims."""
+        if self.k_dtype == "int4":
+            return self.D // 2 + self.D // 32 * 4
+        return self.D * self.kv_elem_bytes()
 
 
 def _randn_bf16(g, shape, chunk_rows=1 << 16):
@@ -201,9 +211,11 @@ def make_workload(name: str, steps: int = 1, **overrides) -> Workload:
         k_scales = (k_abs / E4M3_RANGE).to(torch.float32)
         v_scales = (v_abs / INT8_RANGE).to(torch.float32)
 
+    int4 = cfg.get("kv") == "int4"
     return Workload(
         name=name, seed=seed, B=B, H_q=H_q, H_kv=H_kv, D=D,
-        k_dtype="e4m3" if quant else "bf16", v_dtype="int8" if quant else "bf16",
+        k_dtype="int4" if int4 else ("e4m3" if quant else "bf16"),
+        v_dtype="int4" if int4 else ("int8" if quant else "bf16"),
         num_sink=num_sink, scale=1.0 / math.sqrt(D), num_blocks=num_blocks, max_blocks=max_blocks,
         steps=steps, ctx_old=ctx.astype(np.int32), tables=tables, fill_k=fill_k, fill_v=fill_v,
         fill_seq=fill_seq, fill_pos=fill_pos, q=q, k_new=k_new, v_new=v_new,

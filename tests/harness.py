@@ -21,6 +21,9 @@ from paged_kv_cache_table_gb300.workloads import Workload, bf16_bits
 BF16_NAN = 0x7FC0
 E4M3_NAN = 0x7F
 INT8_OUTSIDE = 0x80
+# int4 pools: every code nibble 15 and every group parameter word all ones (a NaN scale, zero
+# point 255)
+INT4_FILL = 0xFF
 
 ATOL_MAX = 2e-2   # attention: max |gpu - oracle|
 ATOL_MEAN = 2e-3  # attention: mean |gpu - oracle|
@@ -43,6 +46,10 @@ class GpuState:
         if w.k_dtype == "bf16":
             self.k = torch.full(shape, BF16_NAN, dtype=torch.int16, device=device).view(torch.bfloat16)
             self.v = torch.full(shape, BF16_NAN, dtype=torch.int16, device=device).view(torch.bfloat16)
+        elif w.k_dtype == "int4":
+            nbytes = n_slots * w.H_kv * w.kv_row_bytes()
+            self.k = torch.full((nbytes,), INT4_FILL, dtype=torch.uint8, device=device)
+            self.v = torch.full((nbytes,), INT4_FILL, dtype=torch.uint8, device=device)
         else:
             self.k = torch.full(shape, E4M3_NAN, dtype=torch.uint8, device=device)
             self.v = torch.full(shape, INT8_OUTSIDE, dtype=torch.uint8, device=device)
@@ -147,6 +154,11 @@ class OracleState:
         if w.k_dtype == "bf16":
             self.cache.k[:] = BF16_NAN
             self.cache.v[:] = BF16_NAN
+        elif w.k_dtype == "int4":  # what the GPU fill reads as
+            self.cache.k[:] = 15
+            self.cache.v[:] = 15
+            self.cache.k_params[:] = 0xFFFFFFFF
+            self.cache.v_params[:] = 0xFFFFFFFF
         else:
             self.cache.k[:] = E4M3_NAN
             self.cache.v[:] = INT8_OUTSIDE
@@ -223,11 +235,45 @@ def assert_attention_close(gpu: np.ndarray, ref: np.ndarray, what=""):
     return float(err.max()), float(err.mean())
 
 
+def unpack_int4_pool(raw: np.ndarray, n_slots: int, H: int, D: int, tensor: str):
+    """Natural-order codes [slot][head][dim] and params [slot][head][dim/32] of a GPU int4 pool,
+    read by the byte layout the library documents for PA_INT4 (K: word 4c + g holds dims
+    32g + 8c + i at bits 4i; V: byte 8r + m holds dims 16m + r and 16m + r + 8)."""
+    code_bytes = n_slots * H * (D // 2)
+    rows = raw[:code_bytes].reshape(n_slots, H, D // 2)
+    params = raw[code_bytes:code_bytes + n_slots * H * (D // 32) * 4].view(np.uint32).reshape(n_slots, H, D // 32)
+    codes = np.empty((n_slots, H, D), dtype=np.uint8)
+    if tensor == "k":
+        words = rows.view(np.uint32)  # [slot][head][16]
+        for c in range(4):
+            for g in range(D // 32):
+                w = words[:, :, 4 * c + g]
+                for i in range(8):
+                    codes[:, :, 32 * g + 8 * c + i] = (w >> (4 * i)) & 0xF
+    else:
+        for r in range(8):
+            for m in range(D // 16):
+                b = rows[:, :, 8 * r + m]
+                codes[:, :, 16 * m + r] = b & 0xF
+                codes[:, :, 16 * m + r + 8] = b >> 4
+    return codes, params
+
+
 def assert_pools_equal(gpu: GpuState, ora: OracleState):
     gk, gv, gks, gvs = gpu.pools()
     assert np.array_equal(gpu.tables, ora.tables.astype(np.int32)), "block tables differ"
-    assert np.array_equal(gk, ora.cache.k), "K pool differs"
-    assert np.array_equal(gv, ora.cache.v), "V pool differs"
+    if gpu.w.k_dtype == "int4":
+        w = gpu.w
+        n_slots = w.num_blocks * 16
+        kc, kp = unpack_int4_pool(gk, n_slots, w.H_kv, w.D, "k")
+        vc, vp = unpack_int4_pool(gv, n_slots, w.H_kv, w.D, "v")
+        assert np.array_equal(kc, ora.cache.k), "K codes differ"
+        assert np.array_equal(kp, ora.cache.k_params), "K group parameters differ"
+        assert np.array_equal(vc, ora.cache.v), "V codes differ"
+        assert np.array_equal(vp, ora.cache.v_params), "V group parameters differ"
+    else:
+        assert np.array_equal(gk, ora.cache.k), "K pool differs"
+        assert np.array_equal(gv, ora.cache.v), "V pool differs"
     if gks is not None:
         assert np.array_equal(gks, ora.cache.k_sink), "K sink buffer differs"
         assert np.array_equal(gvs, ora.cache.v_sink), "V sink buffer differs"
@@ -270,6 +316,10 @@ def reference_row(w: Workload, s: int, h: int, step: int, kb: np.ndarray, vb: np
     if w.k_dtype == "bf16":
         K[ns:, 0] = O.bf16_bits_to_f64(kb[ns:, kv])
         V[ns:, 0] = O.bf16_bits_to_f64(vb[ns:, kv])
+    elif w.k_dtype == "int4":
+        for t in range(ns, ctx):
+            K[t, 0] = O.int4_decode_row(*O.int4_encode_row(kb[t, kv]))
+            V[t, 0] = O.int4_decode_row(*O.int4_encode_row(vb[t, kv]))
     else:
         ks = np.float32(w.k_scales[kv].item())
         vs = np.float32(w.v_scales[kv].item())

@@ -10,7 +10,7 @@ import torch
 import oracle as O
 from paged_kv_cache_table_gb300.workloads import bf16_bits, make_workload
 
-from harness import ATOL_MAX, ATOL_MEAN, GpuState, logical_tokens, reference_row, to_f64
+from harness import ATOL_MAX, ATOL_MEAN, GpuState, logical_tokens, reference_row, to_f64, unpack_int4_pool
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -26,6 +26,10 @@ def _samples(w, n=10, seed=0):
 def _check_appended_slots(g, w, step=0):
     """Every appended token's slot holds the oracle's encoding of its K and V rows."""
     gk, gv, gks, gvs = g.pools()
+    if w.k_dtype == "int4":
+        n_slots = w.num_blocks * 16
+        gk = unpack_int4_pool(gk, n_slots, w.H_kv, w.D, "k")
+        gv = unpack_int4_pool(gv, n_slots, w.H_kv, w.D, "v")
     pos = w.positions(step)
     kb, vb = bf16_bits(w.k_new[step]), bf16_bits(w.v_new[step])
     for s in range(w.B):
@@ -36,6 +40,11 @@ def _check_appended_slots(g, w, step=0):
         slot = O.locate(g.tables[s], p)
         if w.k_dtype == "bf16":
             assert np.array_equal(gk[slot], kb[s]) and np.array_equal(gv[slot], vb[s])
+        elif w.k_dtype == "int4":
+            for h in range(w.H_kv):
+                for pool, bits in ((gk, kb), (gv, vb)):
+                    codes, params = O.int4_encode_row(bits[s, h])
+                    assert np.array_equal(pool[0][slot, h], codes) and np.array_equal(pool[1][slot, h], params)
         else:
             for h in range(w.H_kv):
                 ks = np.float32(w.k_scales[h].item())
@@ -54,7 +63,7 @@ def _check_rows(out, w, rows):
     assert np.all(np.isfinite(out))
 
 
-@pytest.mark.parametrize("name", ["8b", "70b", "long_quant"])
+@pytest.mark.parametrize("name", ["8b", "70b", "long_quant", "int4_8b", "swa"])
 def test_full_size_step(name):
     w = make_workload(name, steps=1)
     g = GpuState(w)
