@@ -40,8 +40,9 @@ WINDOW = 64
 # ncu captures summarised in profiles/decode_kernel_<workload>.md.  Reported only while the
 # kernel sources hash to the version the counters were taken on; null otherwise.
 NCU_TRAFFIC = {
-    "sources_sha256_16": "a96f1864419759e5",
-    "8b": 553_093_120, "70b": 543_519_488, "long_quant": 1_077_270_416, "prefix_cow": 284_664_064,
+    "sources_sha256_16": "64d7526d389f185d",
+    "8b": 552_450_816, "70b": 543_420_672, "long_quant": 1_076_937_216, "prefix_cow": 282_450_944,
+    "int4_8b": 189_920_000, "swa": 1_082_065_408,
 }
 KERNEL_SOURCES = ["paged_kv_cache_table_gb300/csrc/decode_attention.cu",
                   "paged_kv_cache_table_gb300/csrc/pa_device.cuh",

@@ -51,6 +51,15 @@ constexpr int kFixedFallbackPartition = 512;
 #ifndef PA_MAX_STAGES
 #define PA_MAX_STAGES 8
 #endif
+// INT4: at most this many KV heads per CTA, and this many consumer warps per CTA (blocks per
+// stage = warps / heads).  The 4-bit path is bound by its dequantising arithmetic, so it
+// trades heads per CTA for more warps in flight.
+#ifndef PA_I4_MAX_HG
+#define PA_I4_MAX_HG 8
+#endif
+#ifndef PA_I4_WARPS
+#define PA_I4_WARPS 8
+#endif
 constexpr int kMaxStages = PA_MAX_STAGES;
 constexpr int kSmemLimit = (PA_CTAS_PER_SM == 1 ? 227 * 1024 : (228 * 1024) / PA_CTAS_PER_SM - 1024);
 constexpr float kNegInf = -INFINITY;
@@ -914,10 +923,16 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
   pl->nc = int4 ? 1 : row_bytes / 128;
   int hg = 1;
   for (int c = 1; c <= d->num_kv_heads; ++c)
-    if (d->num_kv_heads % c == 0 && c * row_bytes <= PA_GROUP_BYTES && (!int4 || c % 2 == 0)) hg = c;
+    if (d->num_kv_heads % c == 0 && c * row_bytes <= PA_GROUP_BYTES && (!int4 || (c % 2 == 0 && c <= PA_I4_MAX_HG)))
+      hg = c;
+  if (int4 && hg % 2 != 0) return PA_ERR_UNSUPPORTED;
   pl->hg = hg;
   pl->n_hg = d->num_kv_heads / hg;
-  pl->nbs = std::max(1, 8 / hg);
+  // Blocks per stage: a power of two, so that a stage never straddles the 32-entry chunks in
+  // which the producer warp resolves table entries (one lane per block).
+  int nbs = std::max(1, (int4 ? PA_I4_WARPS : 8) / hg);
+  while (32 % nbs != 0) --nbs;
+  pl->nbs = nbs;
   pl->warps_c = hg * pl->nbs;
   if (pl->warps_c > kMaxConsumerWarps) return PA_ERR_UNSUPPORTED;
   pl->threads = (pl->warps_c + 1) * 32;
@@ -962,8 +977,14 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
 template <int D, int KIND>
 pa_status launch(const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mkp,
                  const CUtensorMap& mvp, const DecodeParams& p, cudaStream_t stream) {
-  // 9-warp CTAs get the register budget of a 288-thread launch; wider ones a 544-thread one
-  auto kern = pl.warps_c <= 8 ? decode_kernel<D, KIND, 8> : decode_kernel<D, KIND, kMaxConsumerWarps>;
+  // 9-warp CTAs get the register budget of a 288-thread launch; wider ones a 416-thread (INT4
+  // only: four warps per scheduler, 128 registers) or a 544-thread one
+  auto kern = decode_kernel<D, KIND, kMaxConsumerWarps>;
+  if (pl.warps_c <= 8) {
+    kern = decode_kernel<D, KIND, 8>;
+  } else if constexpr (KIND == 2) {
+    if (pl.warps_c <= 12) kern = decode_kernel<D, KIND, 12>;
+  }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(pl.smem_bytes)) != cudaSuccess)
     return PA_ERR_CUDA;
