@@ -328,6 +328,12 @@ extern "C" pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, 
     return PA_ERR_INVALID_ARG;
   if (desc->num_seqs > 65535 || desc->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
   const int D = desc->head_dim;
+  const int G = desc->num_q_heads / desc->num_kv_heads;
+#ifndef PA_PREFILL_WARP_MMA_ONLY
+  if (D == 128 && (G & (G - 1)) == 0)  // the tensor-core (tcgen05) kernel
+    return pa::launch_prefill_tc(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
+                                 scale, err_flag, pa::as_stream(stream));
+#endif
   const int nc = D * 2 / 128;
   const long long slots = static_cast<long long>(desc->num_blocks) * PA_BLOCK_SIZE;
   CUtensorMap mk, mv;
