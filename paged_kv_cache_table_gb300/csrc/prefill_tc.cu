@@ -8,19 +8,29 @@
 //
 // Design (head_dim 128, G = 1, 2, 4 or 8 query heads per KV head):
 //  * One CTA per (256 query rows, sequence, KV head): two query tiles of 128 rows, a row being
-//    (token, query head), share every K/V tile.  A 128-key tile is 8 scattered physical blocks and
-//    the canonical operand layout needs one TMA box per block and 64-dim half (32 boxes per K+V
-//    tile); sharing it between two query tiles halves the boxes per flop, which is what bounds the
-//    copy engine here.
+//    (token, query head), share every K/V tile.  Two such CTAs of the same sequence and KV head
+//    form a cluster and load each K/V tile once: every CTA copies half of the tile's boxes with
+//    TMA multicast into both CTAs' shared memory.  Measured, one SM ingests only about 15-30
+//    bytes per cycle of scattered 2 KB blocks (copy engine or cp.async alike), so halving what
+//    each SM fetches per flop is what feeds the tensor core.
 //  * S = Q·Kᵀ and O += P·V are tcgen05.mma (kind::f16, bf16 operands, M = N = 128, fp32
-//    accumulators in TMEM: S0, S1, O0, O1 in 4 x 128 columns), issued by one thread; the next
-//    tile's S is issued as soon as the softmax has read this one, ahead of this tile's P·V.
-//    Q, K, P are K-major and V is MN-major shared-memory operands with the 128-byte swizzle.
-//  * A producer warp streams K through a two-stage ring and V through one stage.
+//    accumulators in TMEM: S0, S1, O0, O1 in 4 x 128 columns), issued by one thread.  Q and K are
+//    K-major and V MN-major shared-memory operands with the 128-byte swizzle; P goes back into
+//    TMEM over the S columns it came from (bf16 pairs) and is the A operand of P·V from there, so
+//    the tensor core reads only Q, K and V from shared memory, whose bandwidth bounds it here.  A
+//    group's next S is issued after its P·V (the tensor pipe runs one thread's products in order,
+//    so P is read before it is overwritten); the two groups interleave on the tensor core.
+//  * One copy warp streams K through a two-stage ring of 128-key tiles and another V through a
+//    three-stage ring: a V tile is needed only at P·V, after the softmax, so V is fetched two tiles
+//    ahead, and on its own warp its waits never hold back the next K tile.  A stage is released to the copy warps
+//    by a multicast tcgen05.commit from each CTA's MMA thread, so it is refilled only when both
+//    CTAs are done with it.
+//  * Clusters are dispatched last query tiles first: under the causal mask the late tiles of a
+//    chunk see the most keys, so the long clusters start early and the short ones fill the tail.
 //  * Two softmax warpgroups (one per query tile) own one query row per thread through TMEM
 //    lanes: they read S, mask (causal, window), keep the running maximum (moved only when a score
-//    exceeds it by 2^8), write P as bf16 into their swizzled P tile, rescale O in TMEM when the
-//    maximum moved, and finally normalise O into the output.  V rows of keys that are not loaded
+//    exceeds it by 2^8), write P as bf16 into TMEM, rescale O in TMEM when the maximum moved (O is
+//    complete by then: its P·V was issued before this S), and finally normalise O into the output.  V rows of keys that are not loaded
 //    or lie beyond the context are zeroed before P·V reads them, so bits left in unused slots (NaN
 //    included) cannot leak.
 //  * Every wait is bounded; TMEM is released on every path.
@@ -34,14 +44,14 @@
 namespace pa {
 namespace {
 
-constexpr int kTcThreads = 320;                 // 10 warps: producer, MMA, 2 x 4 softmax
+constexpr int kTcThreads = 352;                 // 11 warps: K copies, MMA, 2 x 4 softmax, V copies
 constexpr int kHalf = 128 * 128;                // 128 rows x 128 bytes (64 bf16): one K-half
 constexpr int kTile = 2 * kHalf;                // a 128 x 128 bf16 operand tile
 constexpr int kQOff = 0;                        // Q0, Q1
 constexpr int kKOff = kQOff + 2 * kTile;        // K stages 0, 1
-constexpr int kVOff = kKOff + 2 * kTile;        // V (one stage)
-constexpr int kPOff = kVOff + kTile;            // P0, P1
-constexpr int kBarOff = kPOff + 2 * kTile;
+constexpr int kVOff = kKOff + 2 * kTile;        // V stages 0, 1, 2
+constexpr int kVStages = 3;
+constexpr int kBarOff = kVOff + kVStages * kTile;
 constexpr int kTcSmem = kBarOff + 256 + 1024;   // barriers, and slack for 1024-byte alignment
 constexpr uint32_t kTmemCols = 512;             // S0 0..127, S1 128..255, O0 256..383, O1 384..511
 constexpr float kNegInfTc = -INFINITY;
@@ -97,6 +107,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// As tc_mma with the A operand in TMEM (M lanes x K/2 columns of bf16 pairs) instead of shared memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // This warp's 32 TMEM lanes x 32 consecutive fp32 columns: thread i gets lane base + i.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -115,6 +134,38 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// 16 bytes global -> shared without registers; `valid` false fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Both CTAs of the cluster: every thread arrives, then waits for every thread of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// TMA box copied into the same shared-memory offset of every CTA in `mask`, each of whose
+// mbarrier at `bar`'s offset receives the bytes.
+__device__ __forceinline__ void tma_load_3d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                               int c2, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(mask), "l"(policy)
+      : "memory");
+}
+// tcgen05.commit arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const TcParams p) {
@@ -125,19 +176,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;   // [2]
   uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;
-  uint64_t* v_empty = bars + 6;
-  uint64_t* s_full = bars + 7;   // [2] per query tile
-  uint64_t* s_free = bars + 9;   // [2]
-  uint64_t* p_full = bars + 11;  // [2]
-  uint64_t* o_done = bars + 13;  // [2]
-  uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  int* flags = reinterpret_cast<int*>(bars + 17);  // [0] a bad block id, [1] a wait gave up
+  uint64_t* v_full = bars + 5;   // [3] per V stage
+  uint64_t* v_empty = bars + 8;  // [3]
+  uint64_t* s_full = bars + 11;  // [2] per query tile
+  uint64_t* p_full = bars + 13;  // [2]
+  uint64_t* o_done = bars + 15;  // [2]
+  uint64_t* drain = bars + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  int* flags = reinterpret_cast<int*>(bars + 19);  // [0] a bad block id, [1] a wait gave up
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int s = blockIdx.y, h_kv = blockIdx.z, tile = blockIdx.x;
+  // Clusters of two CTAs along x.  Dispatch order: clusters start in linear order, so the linear
+  // cluster index walks every (sequence, KV head) at the last query tiles first.
+  const int rank = blockIdx.x & 1;
+  const int nclx = gridDim.x >> 1;
+  const int pairs = gridDim.y * gridDim.z;
+  const int lc = (blockIdx.x >> 1) + nclx * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int ctile = nclx - 1 - lc / pairs;
+  const int s = (lc % pairs) % gridDim.y, h_kv = (lc % pairs) / gridDim.y;
+  const int tile = 2 * ctile + rank;
   const int tpc = 2 * p.tpq;  // tokens per CTA
+  constexpr uint16_t kBoth = 0x3;
   // launched with programmatic dependent launch: the previous kernel may still write any input
   grid_dep_wait();
   const int qs = p.q_start[s];
@@ -152,13 +211,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         p.out[(static_cast<size_t>(qs + t) * p.H_q + h_kv * p.G) * D + i] = __float2bfloat16_rn(0.f);
     return;
   }
+  // the whole cluster works or leaves together: both CTAs take part in every tile's copies
+  const int tc0 = 2 * ctile * tpc;  // first token of the cluster
+  if (tc0 >= n) return;
   const int t0 = tile * tpc;
-  if (t0 >= n) return;
-  const bool has1 = t0 + p.tpq < n;  // the second query tile holds tokens
+  const bool has0 = t0 < n, has1 = t0 + p.tpq < n;  // this CTA's query tiles that hold tokens
   const int first_pos = ctx - n;
   const int t_end = min(n, t0 + tpc);
-  const int kv_end = first_pos + t_end;  // keys [kv_lo, kv_end) are visible to this CTA
-  const int kv_lo = p.window > 0 ? max(0, first_pos + t0 - p.window + 1) : 0;
+  // keys [kv_lo, kv_end) are visible to some row of the cluster
+  const int kv_end = first_pos + min(n, tc0 + 2 * tpc);
+  const int kv_lo = p.window > 0 ? max(0, first_pos + tc0 - p.window + 1) : 0;
   const int kb0 = kv_lo / PA_BLOCK_SIZE;
   const int kb_end = (kv_end + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
   const int n_tiles = (kb_end - kb0 + 7) / 8;
@@ -166,16 +228,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (tid == 0) {
     mbar_init(q_full, 256);
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 2);  // released by the MMA threads of both CTAs
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
+      mbar_init(&k_empty[i], 2);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
     }
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
     mbar_init(drain, 1);
     flags[0] = flags[1] = 0;
     fence_mbar_init();
@@ -186,23 +249,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------ producer ------------------------------
+  if (warp == 0 || warp == 10) {
+    // ---------------------- copy warps: K (warp 0), V (warp 10) ----------------------
     const int32_t* row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
-    const int i = lane >> 1, half = lane & 1;  // lanes 0..15: block i of the tile, 64-dim half
     uint64_t policy;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
-    // one K or V tile: 16 boxes of 16 slots x 128 bytes; returns false when a wait gave up
-    auto load = [&](int k, const CUtensorMap* map, uint64_t* full, uint64_t* empty, uint32_t parity,
-                    uint8_t* dst) -> bool {
+    // Table entries live in registers, 32 consecutive blocks per chunk and one per lane, for
+    // chunks c0, c0 + 1 and c0 + 2: the accesses only move forward, so a chunk is loaded two
+    // chunks before it is first needed and its latency is hidden.
+    auto entry = [&](int c) { const int kb = kb0 + 32 * c + lane; return kb < kb_end ? row[kb] : -1; };
+    int c0 = 0, e0 = entry(0), e1 = entry(1), e2 = entry(2);
+    auto table = [&](int b) -> int {  // entry of block kb0 + b; b is in the same chunk on every lane
+      const int cb = __shfl_sync(0xffffffffu, b, 0) >> 5;
+      while (cb > c0 + 1) {
+        e0 = e1;
+        e1 = e2;
+        e2 = entry(c0 + 3);
+        ++c0;
+      }
+      const int v0 = __shfl_sync(0xffffffffu, e0, b & 31), v1 = __shfl_sync(0xffffffffu, e1, b & 31);
+      return cb == c0 ? v0 : v1;
+    };
+    // nblk blocks from tile-relative block blk0, boxes of 16 slots x 128 bytes, one per lane:
+    // block lane / 2, 64-dim half lane % 2.  Both CTAs count every box of the tile; each copies
+    // the half of the blocks that its rank owns, to both.  Returns false when a wait gave up.
+    auto load = [&](int nblk, int blk0, const CUtensorMap* map, uint64_t* full, uint64_t* empty, uint32_t parity,
+                    uint8_t* dst, int half_bytes) -> bool {
       if (!warp_wait(empty, parity)) return false;
-      const int kb = kb0 + 8 * k + i;
+      const int bi = lane >> 1, half = lane & 1;
+      const int kb = kb0 + blk0 + bi;
+      const int ent = table(blk0 + min(bi, nblk - 1));
       int pb = -1;
-      if (lane < 16 && kb < kb_end) {
-        pb = row[kb];
+      if (bi < nblk && kb < kb_end) {
+        pb = ent;
         if (pb < 0 || pb >= p.num_blocks) {
           if (half == 0) {
             flags[0] = 1;
@@ -218,38 +301,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         else mbar_arrive(full);
       }
       __syncwarp();
-      if (pb >= 0)
-        tma_load_3d(dst + half * kHalf + i * 2048, map, full, 0, h_kv * 2 + half, pb * PA_BLOCK_SIZE, policy);
+      if (pb >= 0 && bi * 2 / nblk == rank)
+        tma_load_3d_mc(dst + half * half_bytes + bi * 2048, map, full, 0, h_kv * 2 + half, pb * PA_BLOCK_SIZE, kBoth,
+                       policy);
       return true;
     };
-    auto load_k = [&](int k) {
-      return load(k, &tmK, &k_full[k & 1], &k_empty[k & 1], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u,
-                  sm + kKOff + (k & 1) * kTile);
-    };
-    auto load_v = [&](int k) {
-      return load(k, &tmV, v_full, v_empty, (static_cast<uint32_t>(k) & 1u) ^ 1u, sm + kVOff);
-    };
-    // K runs one tile ahead of V (V has a single stage and is freed last)
-    int nk = 0, nv = 0;
-    bool ok = load_k(0);
-    nk += ok;
-    if (ok && n_tiles > 1) nk += (ok = load_k(1));
-    if (ok) nv += (ok = load_v(0));
-    for (int k = 1; ok && k < n_tiles; ++k) {
-      if (k + 1 < n_tiles) {
-        if (!(ok = load_k(k + 1))) break;
-        ++nk;
+    bool ok = true;
+    for (int k = 0; ok && k < n_tiles; ++k) {
+      if (warp == 0) {
+        ok = load(8, 8 * k, &tmK, &k_full[k & 1], &k_empty[k & 1], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u,
+                  sm + kKOff + (k & 1) * kTile, kHalf);
+      } else {
+        const int st = k % kVStages;
+        ok = load(8, 8 * k, &tmV, &v_full[st], &v_empty[st], (static_cast<uint32_t>(k / kVStages) & 1u) ^ 1u,
+                  sm + kVOff + st * kTile, kHalf);
       }
-      if (!(ok = load_v(k))) break;
-      ++nv;
     }
     if (!ok && lane == 0) flags[1] = 1;
-    // do not leave while a copy into shared memory may still be in flight
-    for (int st = 0; st < 2 && st < nk; ++st) {
-      const int last = st + 2 * ((nk - 1 - st) / 2);
-      if (!warp_wait(&k_full[st], static_cast<uint32_t>(last >> 1) & 1u) && lane == 0) flags[1] = 1;
-    }
-    if (nv > 0 && !warp_wait(v_full, static_cast<uint32_t>(nv - 1) & 1u) && lane == 0) flags[1] = 1;
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
@@ -264,48 +332,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_commit(&s_full[w]);
       };
       auto issue_pv = [&](int w, int k) {  // O_w += P_w V of tile k
-        const uint32_t pbuf = smem_u32(sm + kPOff + w * kTile);
-        const uint32_t vbuf = smem_u32(sm + kVOff);
+        const uint32_t vbuf = smem_u32(sm + kVOff + (k % kVStages) * kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;  // P: keys 16kk .. 16kk+15
-          const uint32_t boff = kk * 16 * 128;                      // V: key rows 16kk .. of both halves
-          tc_mma(tmem + 256 + w * 128, sw128_desc(pbuf + aoff, 16, 1024), sw128_desc(vbuf + boff, kHalf, 1024),
-                 kIdescPV, (k > 0 || kk > 0) ? 1u : 0u);
+          // P: keys 16kk .. 16kk+15 = TMEM columns 8kk .. 8kk+7 of S_w; V: key rows 16kk .. of both halves
+          tc_mma_ts(tmem + 256 + w * 128, tmem + w * 128 + 8 * kk, sw128_desc(vbuf + kk * 16 * 128, kHalf, 1024),
+                    kIdescPV, (k > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&o_done[w]);
       };
+      // groups of this CTA with rows (a CTA without any still joins every copy and release)
+      const int groups = has1 ? 2 : (has0 ? 1 : 0);
+      // A stage is released (in both CTAs) only when a later copy waits for it: every such
+      // arrival is consumed before either CTA can finish, so none lands in a CTA that has left.
+      // The K stage of tile m is refilled with tile m + 2; the V stage of tile k with tile k + 3.
       bool ok = mbar_wait(q_full, 0) && mbar_wait(&k_full[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        if (has1) issue_s(1, 0);
-        tc_commit(&k_empty[0]);
+        for (int w = 0; w < groups; ++w) issue_s(w, 0);
+        if (n_tiles > 2) tc_commit_mc(&k_empty[0], kBoth);
       }
       for (int k = 0; ok && k < n_tiles; ++k) {
         const uint32_t ph = static_cast<uint32_t>(k) & 1u;
-        // S of the next tile as soon as each softmax group has read this one
-        if (k + 1 < n_tiles) {
-          ok = mbar_wait(&s_free[0], ph) && mbar_wait(&k_full[(k + 1) & 1], static_cast<uint32_t>((k + 1) >> 1) & 1u);
-          if (!ok) break;
+        const bool next = k + 1 < n_tiles;
+        if (next && !(ok = mbar_wait(&k_full[(k + 1) & 1], static_cast<uint32_t>((k + 1) >> 1) & 1u))) break;
+        const int vs = k % kVStages;
+        if (!(ok = mbar_wait(&v_full[vs], static_cast<uint32_t>(k / kVStages) & 1u))) break;
+        // per group: P·V of this tile, then the group's S of the next tile
+        for (int w = 0; ok && w < groups; ++w) {
+          if (!(ok = mbar_wait(&p_full[w], ph))) break;
           tc_fence_after();
-          issue_s(0, k + 1);
-          if (has1) {
-            if (!(ok = mbar_wait(&s_free[1], ph))) break;
-            tc_fence_after();
-            issue_s(1, k + 1);
-          }
-          tc_commit(&k_empty[(k + 1) & 1]);
+          issue_pv(w, k);
+          tc_commit(&o_done[w]);
+          if (next) issue_s(w, k + 1);
         }
-        if (!(ok = mbar_wait(v_full, ph) && mbar_wait(&p_full[0], ph))) break;
-        tc_fence_after();
-        issue_pv(0, k);
-        if (has1) {
-          if (!(ok = mbar_wait(&p_full[1], ph))) break;
-          tc_fence_after();
-          issue_pv(1, k);
-        }
-        tc_commit(v_empty);
+        if (!ok) break;
+        if (k + kVStages < n_tiles) tc_commit_mc(&v_empty[vs], kBoth);
+        if (k + 3 < n_tiles) tc_commit_mc(&k_empty[(k + 1) & 1], kBoth);
       }
       if (!ok) {
         flags[1] = 1;
@@ -327,19 +389,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row_pos = first_pos + tq0 + tok;
     const int row_lo = p.window > 0 ? max(0, row_pos - p.window + 1) : 0;
     uint8_t* qtile = sm + kQOff + wg * kTile;
-    uint8_t* ptile = sm + kPOff + wg * kTile;
-    {  // Q row -> swizzled Q tile
-      const uint4* qrow = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<size_t>(qs + (row_ok ? tq0 + tok : t0)) * p.H_q + h_kv * p.G + hh) * D);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = row_ok ? qrow[c] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qtile + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+    {  // this warp's 32 Q rows -> swizzled Q tile; two 256-byte rows per instruction, so that
+       // the lanes of a row read it whole (16 bytes each) and the loads coalesce
+      const int c = lane & 15;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int rr = quad * 32 + 2 * i + (lane >> 4);
+        const int tk = rr / p.G;
+        const bool ok_r = tq0 + tk < t_end;
+        const __nv_bfloat16* src =
+            ok_r ? p.q + (static_cast<size_t>(qs + tq0 + tk) * p.H_q + h_kv * p.G + (rr - tk * p.G)) * D + c * 8 : p.q;
+        cp_async16(qtile + (c >> 3) * kHalf + rr * 128 + (((c & 7) ^ (rr & 7)) << 4), src, ok_r);
       }
+      cp_async_wait_all();
       fence_proxy_async();
       mbar_arrive(q_full);
     }
-    const bool active = wg == 0 || has1;
+    const bool active = wg == 0 ? has0 : has1;
     float m_run = kNegInfTc, l_run = 0.f;
     bool ok = true;
     for (int k = 0; active && k < n_tiles; ++k) {
@@ -353,8 +419,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_free[wg]);
       const int kbase = (kb0 + 8 * k) * PA_BLOCK_SIZE;
       // scores stay raw (the scale is positive, so the maximum commutes with it); only tiles
       // that cross a row's causal or window edge take the per-key mask
@@ -373,29 +437,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float m_new = (m_run == kNegInfTc || mx > m_run + 8.f) ? fmaxf(m_run, mx) : m_run;
       const float ms = m_new == kNegInfTc ? 0.f : m_new;
       const float alpha = ex2(m_run - ms);
-      // P·V of the previous tile must be done: P is rewritten and O may be rescaled
-      if (k > 0) {
-        if (!warp_wait(&o_done[wg], ph ^ 1u)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
+      // P (bf16 pairs) over the S columns just read: column c holds keys 2c and 2c + 1
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};
       const float sl = p.scale_log2;
 #pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        uint32_t w[4];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pw[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = ex2(fmaf(__uint_as_float(sv[c + 2 * e]), sl, -ms));
-          const float b = ex2(fmaf(__uint_as_float(sv[c + 2 * e + 1]), sl, -ms));
-          ls4[e] += a + b;
-          w[e] = pack_bf16(a, b);
+        for (int e = 0; e < 32; ++e) {
+          const float a = ex2(fmaf(__uint_as_float(sv[64 * h + 2 * e]), sl, -ms));
+          const float b = ex2(fmaf(__uint_as_float(sv[64 * h + 2 * e + 1]), sl, -ms));
+          ls4[e & 3] += a + b;
+          pw[e] = pack_bf16(a, b);
         }
-        *reinterpret_cast<uint4*>(ptile + (c >> 6) * kHalf + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        tmem_st32(tS + 32 * h, pw);
       }
+      tmem_wait_st();
       l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
       if (k > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
 #pragma unroll
@@ -414,14 +471,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // same zeros; each must see them before its own P·V)
       const int kp_r = kbase + r;
       const bool zero_row = kp_r < kv_lo || kp_r >= loaded_end;
+      const int vs = k % kVStages;
       if (__any_sync(0xffffffffu, zero_row)) {
-        if (!warp_wait(v_full, ph)) {  // the tile's copies must have landed first
+        // the stage's copies must have landed first
+        if (!warp_wait(&v_full[vs], static_cast<uint32_t>(k / kVStages) & 1u)) {
           ok = false;
           break;
         }
       }
       if (zero_row) {
-        uint8_t* vrow = sm + kVOff + r * 128;
+        uint8_t* vrow = sm + kVOff + vs * kTile + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
@@ -439,23 +498,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float inv = (!ok || !(l_run > 0.f)) ? 0.f : 1.f / l_run;
     uint4* orow = reinterpret_cast<uint4*>(
         p.out + (static_cast<size_t>(qs + (row_ok ? tq0 + tok : t0)) * p.H_q + h_kv * p.G + hh) * D);
-    if (active) {
+    if (active && ok) {
+      // Every product has completed (o_done of the last tile follows them all), so the Q tile is
+      // idle: the warp stages its 32 rows there as bf16 (16-byte chunk j of row i at j ^ (i & 15),
+      // conflict-free both ways) and stores them two rows per instruction, coalesced.
+      uint8_t* stage = qtile + quad * 32 * 256;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
         tmem_ld32(tO + 32 * c, ov);
         tmem_wait_ld();
-        if (row_ok) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t w[4];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16(__uint_as_float(ov[8 * q4 + 2 * e]) * inv, __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
-            orow[4 * c + q4] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__uint_as_float(ov[8 * q4 + 2 * e]) * inv, __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
+          *reinterpret_cast<uint4*>(stage + lane * 256 + (((4 * c + q4) ^ (lane & 15)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
+      __syncwarp();
+      const int c = lane & 15;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int ri = 2 * i + (lane >> 4);
+        const int rr = quad * 32 + ri;
+        const int tk = rr / p.G;
+        if (tq0 + tk < t_end)
+          reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(qs + tq0 + tk) * p.H_q + h_kv * p.G + (rr - tk * p.G)) *
+                                               D)[c] = *reinterpret_cast<const uint4*>(stage + ri * 256 + ((c ^ (ri & 15)) << 4));
+      }
+    } else if (active && row_ok) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0, 0, 0, 0);
     }
     tc_fence_before();
     __syncthreads();  // (1) every role is done: the flags are final
@@ -465,11 +541,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (tid == 64 && flags[1] != 0) set_error(p.err, PA_EFLAG_TIMEOUT);
   }
-  if (warp < 2) {
+  if (warp < 2 || warp == 10) {
     tc_fence_before();
     __syncthreads();  // (1)
   }
   __syncthreads();  // (2) no TMEM access is pending
+  // neither CTA leaves while the other may still copy into its shared memory or release a stage
+  cluster_sync();
   // ------------------------------ teardown ------------------------------
   if (warp == 1) {
     tc_fence_after();
@@ -508,8 +586,23 @@ pa_status launch_prefill_tc(const pa_cache_desc* desc, void* out, const void* q,
   p.err = err_flag;
   if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
     return PA_ERR_CUDA;
-  const dim3 grid((max_query_len + 2 * p.tpq - 1) / (2 * p.tpq), p.B, p.H_kv);
-  return launch_overlapped(prefill_tc_kernel, grid, dim3(kTcThreads), kTcSmem, stream, mk, mv, p);
+  const int ctas_x = (max_query_len + 2 * p.tpq - 1) / (2 * p.tpq);
+  const dim3 grid(2 * ((ctas_x + 1) / 2), p.B, p.H_kv);  // whole clusters of two along x
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kTcSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, mk, mv, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa
