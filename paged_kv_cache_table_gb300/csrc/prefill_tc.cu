@@ -144,6 +144,12 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Both CTAs of the cluster: every thread arrives, then waits for every thread of the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -429,10 +435,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!(row_ok && kp <= row_pos && kp >= row_lo)) sv[c] = __float_as_uint(kNegInfTc);
         }
       }
-      float mx4[4] = {kNegInfTc, kNegInfTc, kNegInfTc, kNegInfTc};
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(sv[c]));
-      const float mraw = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      for (int j = 0; j < 8; ++j) mx8[j] = kNegInfTc;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2)
+        mx8[(c >> 1) & 7] = max3f(mx8[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+      const float mraw = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
       const float mx = mraw == kNegInfTc ? kNegInfTc : mraw * p.scale_log2;
       const float m_new = (m_run == kNegInfTc || mx > m_run + 8.f) ? fmaxf(m_run, mx) : m_run;
       const float ms = m_new == kNegInfTc ? 0.f : m_new;
@@ -478,16 +487,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = false;
           break;
         }
-      }
-      if (zero_row) {
-        uint8_t* vrow = sm + kVOff + vs * kTile + r * 128;
+        if (zero_row) {
+          uint8_t* vrow = sm + kVOff + vs * kTile + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = make_uint4(0, 0, 0, 0);
+          }
         }
+        fence_proxy_async();  // the zeros, before the tensor core reads the stage
       }
-      fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&p_full[wg]);
     }
