@@ -25,8 +25,11 @@
 //    ahead, and on its own warp its waits never hold back the next K tile.  A stage is released to the copy warps
 //    by a multicast tcgen05.commit from each CTA's MMA thread, so it is refilled only when both
 //    CTAs are done with it.
-//  * Clusters are dispatched last query tiles first: under the causal mask the late tiles of a
-//    chunk see the most keys, so the long clusters start early and the short ones fill the tail.
+//  * Clusters start longest first.  A cluster's work grows with the last key it reads, which for
+//    the c-th cluster of a sequence is first_pos + min(n, (c + 1) W) (W query tokens per cluster):
+//    an arithmetic progression per sequence.  So the number of clusters whose last key is at
+//    least X has a closed form per sequence, and each cluster finds its own item, the one at its
+//    launch position in that order, by a 32-way search over X in one warp; no sort, no scratch.
 //  * Two softmax warpgroups (one per query tile) own one query row per thread through TMEM
 //    lanes: they read S, mask (causal, window), keep the running maximum (moved only when a score
 //    exceeds it by 2^8), write P as bf16 into TMEM, rescale O in TMEM when the maximum moved (O is
@@ -150,6 +153,80 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return d;
 }
 
+// Query rows of sequence s in clusters of W = 2^lw tokens: fp = first new position, n rows (those
+// of an invalid sequence are only zeroed), nc clusters.
+struct alignas(16) SeqGeo {
+  int fp, n, nc, valid;
+};
+constexpr int kMaxOrderSeqs = 2 * kTile / static_cast<int>(sizeof(SeqGeo));  // staged in the K ring
+__device__ __forceinline__ SeqGeo seq_geo(const TcParams& p, int s, int lw) {
+  const int n = p.q_start[s + 1] - p.q_start[s], ctx = p.context_lens[s];
+  SeqGeo g;
+  g.valid = n >= 0 && n <= ctx && n <= p.max_q && ctx <= p.max_blocks * PA_BLOCK_SIZE;
+  g.n = g.valid ? n : min(max(n, 0), p.max_q);
+  g.fp = ctx - n;
+  g.nc = (g.n + (1 << lw) - 1) >> lw;
+  return g;
+}
+// Clusters of one sequence whose key is >= X (X >= 1).  The key of cluster c, strictly increasing
+// in c, is the last key it reads, fp + min(n, (c + 1) W), or c + 1 for an invalid sequence.
+__device__ __forceinline__ int count_ge(const SeqGeo& g, int X, int lw) {
+  if (!g.valid) return min(g.nc, max(g.nc - (X - 1), 0));
+  if (g.nc == 0 || X > g.fp + g.n) return 0;
+  const int d = X - g.fp;  // clusters c < nc - 1 with fp + (c + 1) W < X lie below X
+  const int below = d <= 0 ? 0 : min(((d + (1 << lw) - 1) >> lw) - 1, g.nc - 1);
+  return g.nc - below;
+}
+// The work item at launch position i when the clusters of all sequences are sorted by key, largest
+// first, equal keys by sequence; false past the last one.  geo: every sequence's SeqGeo in shared
+// memory.  Called by all lanes of a warp.
+__device__ bool cluster_item(const SeqGeo* geo, int B, int key_max, int lw, int i, int lane, int& s_out,
+                             int& c_out) {
+  int total = 0;
+  for (int s = lane; s < B; s += 32) total += count_ge(geo[s], 1, lw);
+  total = __reduce_add_sync(0xffffffffu, total);
+  if (i >= total) return false;
+  // largest key K with count_ge(K) > i: keep count_ge(lo) > i >= count_ge(hi), keys in [1, key_max]
+  int lo = 1, hi = key_max + 1;
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 32) >> 5;  // >= 1; candidates lo + step, lo + 2 step, ... below hi
+    const int X = min(lo + step * (lane + 1), hi - 1);
+    int cnt = 0;
+    for (int s = 0; s < B; ++s) cnt += count_ge(geo[s], X, lw);
+    const unsigned pm = __ballot_sync(0xffffffffu, cnt > i);  // X non-decreasing in lane: a prefix
+    const int nt = __popc(pm);
+    const int x_true = __shfl_sync(0xffffffffu, X, max(nt - 1, 0));
+    const int x_false = __shfl_sync(0xffffffffu, X, min(nt, 31));
+    if (nt > 0) lo = max(lo, x_true);
+    if (nt < 32) hi = min(hi, x_false);
+  }
+  // the r-th sequence (in order) that has a cluster with key lo
+  int above = 0;
+  for (int s = lane; s < B; s += 32) above += count_ge(geo[s], lo + 1, lw);
+  int r = i - __reduce_add_sync(0xffffffffu, above);
+  for (int base = 0; base < B; base += 32) {
+    const int s = base + lane;
+    int has = 0, c = 0;
+    if (s < B) {
+      const SeqGeo g = geo[s];
+      const int ge = count_ge(g, lo, lw);
+      has = ge - count_ge(g, lo + 1, lw);
+      c = g.nc - ge;
+    }
+    const unsigned hm = __ballot_sync(0xffffffffu, has != 0);
+    if (r < __popc(hm)) {
+      unsigned m = hm;
+      for (int k = 0; k < r; ++k) m &= m - 1;  // drop the r lowest set lanes
+      const int src = __ffs(m) - 1;
+      s_out = base + src;
+      c_out = __shfl_sync(0xffffffffu, c, src);
+      return true;
+    }
+    r -= __popc(hm);
+  }
+  return false;
+}
+
 // Both CTAs of the cluster: every thread arrives, then waits for every thread of the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -192,19 +269,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int* flags = reinterpret_cast<int*>(bars + 19);  // [0] a bad block id, [1] a wait gave up
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Clusters of two CTAs along x.  Dispatch order: clusters start in linear order, so the linear
-  // cluster index walks every (sequence, KV head) at the last query tiles first.
+  // Clusters of two CTAs along x; clusters start in linear order, and the linear cluster index
+  // is the launch position: KV heads innermost, work items longest first.
   const int rank = blockIdx.x & 1;
-  const int nclx = gridDim.x >> 1;
-  const int pairs = gridDim.y * gridDim.z;
-  const int lc = (blockIdx.x >> 1) + nclx * (blockIdx.y + gridDim.y * blockIdx.z);
-  const int ctile = nclx - 1 - lc / pairs;
-  const int s = (lc % pairs) % gridDim.y, h_kv = (lc % pairs) / gridDim.y;
-  const int tile = 2 * ctile + rank;
+  const int lc = (blockIdx.x >> 1) + (gridDim.x >> 1) * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int h_kv = lc % p.H_kv;
   const int tpc = 2 * p.tpq;  // tokens per CTA
   constexpr uint16_t kBoth = 0x3;
   // launched with programmatic dependent launch: the previous kernel may still write any input
   grid_dep_wait();
+  int s = 0, ctile = 0;
+  {
+    const int lw = 31 - __clz(2 * tpc);  // W = 2 tpc = 512 / G query tokens per cluster
+    bool have;
+    if (p.B <= kMaxOrderSeqs) {
+      // the K ring is idle until the cluster barrier below, which no copy into it precedes
+      SeqGeo* geo = reinterpret_cast<SeqGeo*>(sm + kKOff);
+      int* pick = reinterpret_cast<int*>(sm + kVOff);
+      for (int q = tid; q < p.B; q += kTcThreads) geo[q] = seq_geo(p, q, lw);
+      __syncthreads();
+      if (warp == 0) {  // one warp searches, the others wait
+        const int key_max = max(p.max_blocks * PA_BLOCK_SIZE, (p.max_q + (1 << lw) - 1) >> lw);
+        const bool h = cluster_item(geo, p.B, key_max, lw, lc / p.H_kv, lane, s, ctile);
+        if (lane == 0) {
+          pick[0] = h;
+          pick[1] = s;
+          pick[2] = ctile;
+        }
+      }
+      __syncthreads();
+      have = pick[0] != 0;
+      s = pick[1];
+      ctile = pick[2];
+    } else {  // many sequences: last query tiles first, sequences in order
+      const int nclx = gridDim.x >> 1, per = lc / p.H_kv;
+      ctile = nclx - 1 - per / p.B;
+      s = per % p.B;
+      have = true;
+    }
+    if (!have) return;  // past the last item: both CTAs leave
+  }
+  const int tile = 2 * ctile + rank;
   const int qs = p.q_start[s];
   const int n = p.q_start[s + 1] - qs;
   const int ctx = p.context_lens[s];
