@@ -38,6 +38,10 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int ro
 // boxes of `box_heads` heads x 16 slots, no swizzle (tensor_map.cpp).
 bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots);
 
+// TMA descriptor of bf16 queries [T][heads][128] viewed as (64 dims, half, head, token) with boxes
+// of one half x G heads x tokens_per_box tokens, 128-byte swizzle (tensor_map.cpp).
+bool encode_query_map(CUtensorMap* map, const void* base, int heads, int G, int tokens_per_box, long long tokens);
+
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // The tcgen05 chunked-prefill kernel (prefill_tc.cu): head_dim 128 and a power-of-two number of

@@ -47,7 +47,7 @@
 namespace pa {
 namespace {
 
-constexpr int kTcThreads = 352;                 // 11 warps: K copies, MMA, 2 x 4 softmax, V copies
+constexpr int kTcThreads = 384;                 // 12 warps: K, MMA, V, Q copies; 2 x 4 softmax
 constexpr int kHalf = 128 * 128;                // 128 rows x 128 bytes (64 bf16): one K-half
 constexpr int kTile = 2 * kHalf;                // a 128 x 128 bf16 operand tile
 constexpr int kQOff = 0;                        // Q0, Q1
@@ -55,7 +55,10 @@ constexpr int kKOff = kQOff + 2 * kTile;        // K stages 0, 1
 constexpr int kVOff = kKOff + 2 * kTile;        // V stages 0, 1, 2
 constexpr int kVStages = 3;
 constexpr int kBarOff = kVOff + kVStages * kTile;
-constexpr int kTcSmem = kBarOff + 256 + 1024;   // barriers, and slack for 1024-byte alignment
+constexpr int kMaxItems = 64;                   // work items of one cluster (the launch makes enough clusters)
+constexpr int kListOff = kBarOff + 256;         // barriers, then the cluster's item list
+constexpr int kTcSmem = kListOff + kMaxItems * 24 + 1024;  // and slack for 1024-byte alignment
+constexpr int kQMapTokens = 1 << 24;            // token extent of the Q tensor map (rows past it: plain copies)
 constexpr uint32_t kTmemCols = 512;             // S0 0..127, S1 128..255, O0 256..383, O1 384..511
 constexpr float kNegInfTc = -INFINITY;
 
@@ -129,6 +132,10 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]) : "memory");
 }
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -152,6 +159,37 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+
+// A 4-D TMA box into this CTA's shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// A 4-D TMA box from this CTA's shared memory to global memory (bulk async group of this thread).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* smem_src, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(smem_src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's bulk stores have read their shared memory (reads) or completed (all).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Arrive on the mbarrier at `bar`'s offset in the CTA of the cluster with the given rank.
+__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, int cta_rank) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
+      "r"(cta_rank)
+      : "memory");
+}
+__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
 // Query rows of sequence s in clusters of W = 2^lw tokens: fp = first new position, n rows (those
 // of an invalid sequence are only zeroed), nc clusters.
@@ -177,56 +215,6 @@ __device__ __forceinline__ int count_ge(const SeqGeo& g, int X, int lw) {
   const int below = d <= 0 ? 0 : min(((d + (1 << lw) - 1) >> lw) - 1, g.nc - 1);
   return g.nc - below;
 }
-// The work item at launch position i when the clusters of all sequences are sorted by key, largest
-// first, equal keys by sequence; false past the last one.  geo: every sequence's SeqGeo in shared
-// memory.  Called by all lanes of a warp.
-__device__ bool cluster_item(const SeqGeo* geo, int B, int key_max, int lw, int i, int lane, int& s_out,
-                             int& c_out) {
-  int total = 0;
-  for (int s = lane; s < B; s += 32) total += count_ge(geo[s], 1, lw);
-  total = __reduce_add_sync(0xffffffffu, total);
-  if (i >= total) return false;
-  // largest key K with count_ge(K) > i: keep count_ge(lo) > i >= count_ge(hi), keys in [1, key_max]
-  int lo = 1, hi = key_max + 1;
-  while (hi - lo > 1) {
-    const int step = (hi - lo + 32) >> 5;  // >= 1; candidates lo + step, lo + 2 step, ... below hi
-    const int X = min(lo + step * (lane + 1), hi - 1);
-    int cnt = 0;
-    for (int s = 0; s < B; ++s) cnt += count_ge(geo[s], X, lw);
-    const unsigned pm = __ballot_sync(0xffffffffu, cnt > i);  // X non-decreasing in lane: a prefix
-    const int nt = __popc(pm);
-    const int x_true = __shfl_sync(0xffffffffu, X, max(nt - 1, 0));
-    const int x_false = __shfl_sync(0xffffffffu, X, min(nt, 31));
-    if (nt > 0) lo = max(lo, x_true);
-    if (nt < 32) hi = min(hi, x_false);
-  }
-  // the r-th sequence (in order) that has a cluster with key lo
-  int above = 0;
-  for (int s = lane; s < B; s += 32) above += count_ge(geo[s], lo + 1, lw);
-  int r = i - __reduce_add_sync(0xffffffffu, above);
-  for (int base = 0; base < B; base += 32) {
-    const int s = base + lane;
-    int has = 0, c = 0;
-    if (s < B) {
-      const SeqGeo g = geo[s];
-      const int ge = count_ge(g, lo, lw);
-      has = ge - count_ge(g, lo + 1, lw);
-      c = g.nc - ge;
-    }
-    const unsigned hm = __ballot_sync(0xffffffffu, has != 0);
-    if (r < __popc(hm)) {
-      unsigned m = hm;
-      for (int k = 0; k < r; ++k) m &= m - 1;  // drop the r lowest set lanes
-      const int src = __ffs(m) - 1;
-      s_out = base + src;
-      c_out = __shfl_sync(0xffffffffu, c, src);
-      return true;
-    }
-    r -= __popc(hm);
-  }
-  return false;
-}
-
 // Both CTAs of the cluster: every thread arrives, then waits for every thread of the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -249,96 +237,97 @@ __device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
                : "memory");
 }
 
+// One work item of a cluster: the query rows of cluster tile c of sequence s (tokens
+// [2 tpc c, 2 tpc (c + 1)), tpc tokens per CTA) against KV head h_kv.  This CTA holds tokens
+// [t0, t_end) in two query tiles of tpq tokens; the cluster reads the keys [kv_lo, kv_end),
+// blocks [kb0, kb_end), in n_tiles tiles of 8 blocks.
+struct Item {
+  int s, h_kv, tile, qs, n, t0, t_end, first_pos, kv_lo, kb0, kb_end, n_tiles, loaded_end;
+  bool valid, has0, has1;
+};
+// An entry of a cluster's item list (shared memory): the sequence, the cluster tile and KV head
+// (c << 16 | h), and the sequence's first query row, query rows and context length.
+struct ItemRec {
+  int s, ch, qs, n, ctx, pad;
+};
+__device__ __forceinline__ ItemRec item_rec(const TcParams& p, int s, int c, int h) {
+  ItemRec e;
+  e.s = s;
+  e.ch = (c << 16) | h;
+  e.qs = p.q_start[s];
+  e.n = p.q_start[s + 1] - e.qs;
+  e.ctx = p.context_lens[s];
+  e.pad = 0;
+  return e;
+}
+__device__ __forceinline__ Item make_item(const TcParams& p, const ItemRec& e, int rank) {
+  Item it;
+  it.s = e.s;
+  const int ctile = e.ch >> 16;
+  it.h_kv = e.ch & 0xFFFF;
+  const int tpc = 2 * p.tpq;
+  it.tile = 2 * ctile + rank;
+  it.qs = e.qs;
+  it.n = e.n;
+  const int ctx = e.ctx;
+  it.valid = it.n >= 0 && it.n <= ctx && it.n <= p.max_q && ctx <= p.max_blocks * PA_BLOCK_SIZE;
+  const int tc0 = 2 * ctile * tpc;
+  it.t0 = it.tile * tpc;
+  it.has0 = it.valid && it.t0 < it.n;
+  it.has1 = it.valid && it.t0 + p.tpq < it.n;
+  it.first_pos = ctx - it.n;
+  it.t_end = min(it.n, it.t0 + tpc);
+  it.kv_lo = it.kb0 = it.kb_end = it.n_tiles = it.loaded_end = 0;
+  if (it.valid && tc0 < it.n) {
+    const int kv_end = it.first_pos + min(it.n, tc0 + 2 * tpc);
+    it.kv_lo = p.window > 0 ? max(0, it.first_pos + tc0 - p.window + 1) : 0;
+    it.kb0 = it.kv_lo / PA_BLOCK_SIZE;
+    it.kb_end = (kv_end + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+    it.n_tiles = (it.kb_end - it.kb0 + 7) / 8;
+    it.loaded_end = min(ctx, it.kb_end * PA_BLOCK_SIZE);  // keys past this hold no loaded data
+  }
+  return it;
+}
+
+// Launch position pos of round r of a cluster: rounds deal NC positions each, alternately in
+// cluster order and in reverse, so that the longest items of one round and the shortest of the
+// next land on the same cluster.
+__device__ __forceinline__ int round_pos(int r, int NC, int cid) { return r * NC + ((r & 1) ? NC - 1 - cid : cid); }
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
                       const TcParams p) {
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBarOff);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;   // [3] per V stage
-  uint64_t* v_empty = bars + 8;  // [3]
-  uint64_t* s_full = bars + 11;  // [2] per query tile
-  uint64_t* p_full = bars + 13;  // [2]
-  uint64_t* o_done = bars + 15;  // [2]
-  uint64_t* drain = bars + 17;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
-  int* flags = reinterpret_cast<int*>(bars + 19);  // [0] a bad block id, [1] a wait gave up
+  uint64_t* q_empty = bars + 2;
+  uint64_t* k_full = bars + 4;   // [2]
+  uint64_t* k_empty = bars + 6;  // [2]
+  uint64_t* v_full = bars + 8;   // [3] per V stage
+  uint64_t* v_empty = bars + 11; // [3]
+  uint64_t* s_full = bars + 14;  // [2] per query tile
+  uint64_t* p_full = bars + 16;  // [2]
+  uint64_t* o_done = bars + 18;  // [2]
+  uint64_t* drain = bars + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
+  int* flags = reinterpret_cast<int*>(bars + 22);  // [0] work items of all clusters, [1] a wait gave up
+  ItemRec* list = reinterpret_cast<ItemRec*>(sm + kListOff);  // this cluster's items, in order
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Clusters of two CTAs along x; clusters start in linear order, and the linear cluster index
-  // is the launch position: KV heads innermost, work items longest first.
-  const int rank = blockIdx.x & 1;
-  const int lc = (blockIdx.x >> 1) + (gridDim.x >> 1) * (blockIdx.y + gridDim.y * blockIdx.z);
-  const int h_kv = lc % p.H_kv;
-  const int tpc = 2 * p.tpq;  // tokens per CTA
+  const int rank = blockIdx.x & 1, cid = blockIdx.x >> 1, NC = gridDim.x >> 1;
+  const int tpc = 2 * p.tpq;                 // tokens per CTA
+  const int lw = 31 - __clz(2 * tpc);        // W = 2 tpc = 512 / G query tokens per cluster tile
+  const int nclx = (p.max_q + (1 << lw) - 1) >> lw;
+  const bool lpt = p.B <= kMaxOrderSeqs;
   constexpr uint16_t kBoth = 0x3;
-  // launched with programmatic dependent launch: the previous kernel may still write any input
-  grid_dep_wait();
-  int s = 0, ctile = 0;
-  {
-    const int lw = 31 - __clz(2 * tpc);  // W = 2 tpc = 512 / G query tokens per cluster
-    bool have;
-    if (p.B <= kMaxOrderSeqs) {
-      // the K ring is idle until the cluster barrier below, which no copy into it precedes
-      SeqGeo* geo = reinterpret_cast<SeqGeo*>(sm + kKOff);
-      int* pick = reinterpret_cast<int*>(sm + kVOff);
-      for (int q = tid; q < p.B; q += kTcThreads) geo[q] = seq_geo(p, q, lw);
-      __syncthreads();
-      if (warp == 0) {  // one warp searches, the others wait
-        const int key_max = max(p.max_blocks * PA_BLOCK_SIZE, (p.max_q + (1 << lw) - 1) >> lw);
-        const bool h = cluster_item(geo, p.B, key_max, lw, lc / p.H_kv, lane, s, ctile);
-        if (lane == 0) {
-          pick[0] = h;
-          pick[1] = s;
-          pick[2] = ctile;
-        }
-      }
-      __syncthreads();
-      have = pick[0] != 0;
-      s = pick[1];
-      ctile = pick[2];
-    } else {  // many sequences: last query tiles first, sequences in order
-      const int nclx = gridDim.x >> 1, per = lc / p.H_kv;
-      ctile = nclx - 1 - per / p.B;
-      s = per % p.B;
-      have = true;
-    }
-    if (!have) return;  // past the last item: both CTAs leave
-  }
-  const int tile = 2 * ctile + rank;
-  const int qs = p.q_start[s];
-  const int n = p.q_start[s + 1] - qs;
-  const int ctx = p.context_lens[s];
-  const bool valid = n >= 0 && n <= ctx && n <= p.max_q && ctx <= p.max_blocks * PA_BLOCK_SIZE;
-  if (!valid) {
-    if (tile == 0 && h_kv == 0 && tid == 0) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
-    const int rows = min(max(n, 0), p.max_q);
-    for (int t = tile * tpc + warp; t < min(rows, (tile + 1) * tpc); t += kTcThreads / 32)
-      for (int i = lane; i < p.G * D; i += 32)
-        p.out[(static_cast<size_t>(qs + t) * p.H_q + h_kv * p.G) * D + i] = __float2bfloat16_rn(0.f);
-    return;
-  }
-  // the whole cluster works or leaves together: both CTAs take part in every tile's copies
-  const int tc0 = 2 * ctile * tpc;  // first token of the cluster
-  if (tc0 >= n) return;
-  const int t0 = tile * tpc;
-  const bool has0 = t0 < n, has1 = t0 + p.tpq < n;  // this CTA's query tiles that hold tokens
-  const int first_pos = ctx - n;
-  const int t_end = min(n, t0 + tpc);
-  // keys [kv_lo, kv_end) are visible to some row of the cluster
-  const int kv_end = first_pos + min(n, tc0 + 2 * tpc);
-  const int kv_lo = p.window > 0 ? max(0, first_pos + tc0 - p.window + 1) : 0;
-  const int kb0 = kv_lo / PA_BLOCK_SIZE;
-  const int kb_end = (kv_end + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
-  const int n_tiles = (kb_end - kb0 + 7) / 8;
-  const int loaded_end = min(ctx, kb_end * PA_BLOCK_SIZE);  // keys past this hold no loaded data
+  SeqGeo* geo = reinterpret_cast<SeqGeo*>(sm + kKOff);  // scratch: the K ring is idle until the cluster barrier
 
   if (tid == 0) {
-    mbar_init(q_full, 256);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 2);  // released by the MMA threads of both CTAs
@@ -358,83 +347,182 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  // launched with programmatic dependent launch: the previous kernel may still write any input
+  grid_dep_wait();
+  if (lpt)
+    for (int q = tid; q < p.B; q += kTcThreads) geo[q] = seq_geo(p, q, lw);
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  if (lpt) {
+    int part = 0;
+    for (int q = tid; q < p.B; q += kTcThreads) part += geo[q].nc;
+    part = __reduce_add_sync(0xffffffffu, part);
+    if (lane == 0 && part) atomicAdd(&flags[0], part);
+  }
+  __syncthreads();
+  // Work items longest first: item (s, c) of key k sits at rank = #items of larger key + #items of
+  // key k in earlier sequences; with KV heads innermost, launch position = rank * H_kv + h.
+  // Many sequences: last cluster tiles first, sequences in order (slots past a sequence are empty).
+  const int p_tot = lpt ? flags[0] * p.H_kv : p.B * nclx * p.H_kv;
+  const int rounds = (p_tot + NC - 1) / NC;
+  const int n_items = min(kMaxItems, rounds == 0 ? 0 : rounds - 1 + (round_pos(rounds - 1, NC, cid) < p_tot ? 1 : 0));
+  if (lpt) {
+    for (int j = tid; j < p.B * nclx; j += kTcThreads) {
+      const int s = j / nclx, c = j - s * nclx;
+      const SeqGeo g = geo[s];
+      if (c >= g.nc) continue;
+      const int key = g.valid ? g.fp + min(g.n, (c + 1) << lw) : c + 1;
+      int rk = 0;
+      for (int q = 0; q < p.B; ++q) {
+        const SeqGeo gq = geo[q];
+        const int above = count_ge(gq, key + 1, lw);
+        rk += above + (q < s ? count_ge(gq, key, lw) - above : 0);
+      }
+      for (int h = 0; h < p.H_kv; ++h) {
+        const int pos = rk * p.H_kv + h, r = pos / NC, w = pos - r * NC;
+        if (((r & 1) ? NC - 1 - w : w) == cid && r < kMaxItems) list[r] = item_rec(p, s, c, h);
+      }
+    }
+  } else {
+    for (int r = tid; r < n_items; r += kTcThreads) {
+      const int pos = round_pos(r, NC, cid), slot = pos / p.H_kv, h = pos - slot * p.H_kv;
+      list[r] = item_rec(p, slot % p.B, nclx - 1 - slot / p.B, h);
+    }
+  }
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before any multicast reaches them; scratch is done
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 || warp == 10) {
-    // ---------------------- copy warps: K (warp 0), V (warp 10) ----------------------
-    const int32_t* row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+  if (warp == 0 || warp == 2) {
+    // ---------------------- copy warps: K (warp 0), V (warp 2) ----------------------
     uint64_t policy;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
-    // Table entries live in registers, 32 consecutive blocks per chunk and one per lane, for
-    // chunks c0, c0 + 1 and c0 + 2: the accesses only move forward, so a chunk is loaded two
-    // chunks before it is first needed and its latency is hidden.
-    auto entry = [&](int c) { const int kb = kb0 + 32 * c + lane; return kb < kb_end ? row[kb] : -1; };
-    int c0 = 0, e0 = entry(0), e1 = entry(1), e2 = entry(2);
-    auto table = [&](int b) -> int {  // entry of block kb0 + b; b is in the same chunk on every lane
-      const int cb = __shfl_sync(0xffffffffu, b, 0) >> 5;
-      while (cb > c0 + 1) {
-        e0 = e1;
-        e1 = e2;
-        e2 = entry(c0 + 3);
-        ++c0;
-      }
-      const int v0 = __shfl_sync(0xffffffffu, e0, b & 31), v1 = __shfl_sync(0xffffffffu, e1, b & 31);
-      return cb == c0 ? v0 : v1;
-    };
-    // nblk blocks from tile-relative block blk0, boxes of 16 slots x 128 bytes, one per lane:
-    // block lane / 2, 64-dim half lane % 2.  Both CTAs count every box of the tile; each copies
-    // the half of the blocks that its rank owns, to both.  Returns false when a wait gave up.
-    auto load = [&](int nblk, int blk0, const CUtensorMap* map, uint64_t* full, uint64_t* empty, uint32_t parity,
-                    uint8_t* dst, int half_bytes) -> bool {
-      if (!warp_wait(empty, parity)) return false;
-      const int bi = lane >> 1, half = lane & 1;
-      const int kb = kb0 + blk0 + bi;
-      const int ent = table(blk0 + min(bi, nblk - 1));
-      int pb = -1;
-      if (bi < nblk && kb < kb_end) {
-        pb = ent;
-        if (pb < 0 || pb >= p.num_blocks) {
-          if (half == 0) {
-            flags[0] = 1;
-            set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
+    bool ok = true;
+    int g = 0;  // tiles of the cluster so far: ring stage and phase
+    for (int ii = 0; ok && ii < n_items; ++ii) {
+      const Item it = make_item(p, list[ii], rank);
+      if (it.n_tiles == 0) continue;
+      const int32_t* row = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks;
+      const int kb0 = it.kb0, kb_end = it.kb_end;
+      // Table entries live in registers, 32 consecutive blocks per chunk and one per lane, for
+      // chunks c0, c0 + 1 and c0 + 2: the accesses only move forward, so a chunk is loaded two
+      // chunks before it is first needed and its latency is hidden.
+      auto entry = [&](int c) { const int kb = kb0 + 32 * c + lane; return kb < kb_end ? row[kb] : -1; };
+      int c0 = 0, e0 = entry(0), e1 = entry(1), e2 = entry(2);
+      auto table = [&](int b) -> int {  // entry of block kb0 + b; b is in the same chunk on every lane
+        const int cb = __shfl_sync(0xffffffffu, b, 0) >> 5;
+        while (cb > c0 + 1) {
+          e0 = e1;
+          e1 = e2;
+          e2 = entry(c0 + 3);
+          ++c0;
+        }
+        const int v0 = __shfl_sync(0xffffffffu, e0, b & 31), v1 = __shfl_sync(0xffffffffu, e1, b & 31);
+        return cb == c0 ? v0 : v1;
+      };
+      // 8 blocks from tile-relative block blk0, boxes of 16 slots x 128 bytes, one per lane:
+      // block lane / 2, 64-dim half lane % 2.  Both CTAs count every box of the tile; each copies
+      // the half of the blocks that its rank owns, to both.  Returns false when a wait gave up.
+      auto load = [&](int blk0, const CUtensorMap* map, uint64_t* full, uint64_t* empty, uint32_t parity,
+                      uint8_t* dst) -> bool {
+        if (!warp_wait(empty, parity)) return false;
+        const int bi = lane >> 1, half = lane & 1;
+        const int kb = kb0 + blk0 + bi;
+        const int ent = table(blk0 + min(bi, 7));
+        int pb = -1;
+        if (bi < 8 && kb < kb_end) {
+          pb = ent;
+          if (pb < 0 || pb >= p.num_blocks) {
+            if (half == 0) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
+            pb = -1;
           }
-          pb = -1;
+        }
+        const unsigned loads = __ballot_sync(0xffffffffu, pb >= 0);
+        if (lane == 0) {
+          const uint32_t bytes = __popc(loads) * 2048u;
+          if (bytes) mbar_arrive_expect_tx(full, bytes);
+          else mbar_arrive(full);
+        }
+        __syncwarp();
+        if (pb >= 0 && bi / 4 == rank)
+          tma_load_3d_mc(dst + half * kHalf + bi * 2048, map, full, 0, it.h_kv * 2 + half, pb * PA_BLOCK_SIZE, kBoth,
+                         policy);
+        return true;
+      };
+      for (int k = 0; ok && k < it.n_tiles; ++k, ++g) {
+        if (warp == 0) {
+          ok = load(8 * k, &tmK, &k_full[g & 1], &k_empty[g & 1], (static_cast<uint32_t>(g >> 1) & 1u) ^ 1u,
+                    sm + kKOff + (g & 1) * kTile);
+        } else {
+          const int st = g % kVStages;
+          ok = load(8 * k, &tmV, &v_full[st], &v_empty[st], (static_cast<uint32_t>(g / kVStages) & 1u) ^ 1u,
+                    sm + kVOff + st * kTile);
         }
       }
-      const unsigned loads = __ballot_sync(0xffffffffu, pb >= 0);
-      if (lane == 0) {
-        const uint32_t bytes = __popc(loads) * 2048u;
-        if (bytes) mbar_arrive_expect_tx(full, bytes);
-        else mbar_arrive(full);
-      }
-      __syncwarp();
-      if (pb >= 0 && bi * 2 / nblk == rank)
-        tma_load_3d_mc(dst + half * half_bytes + bi * 2048, map, full, 0, h_kv * 2 + half, pb * PA_BLOCK_SIZE, kBoth,
-                       policy);
-      return true;
-    };
+    }
+    if (!ok && lane == 0) flags[1] = 1;
+  } else if (warp == 3) {
+    // ------------------- Q copies: each item's two query tiles -------------------
+    // The tiles of the next item are copied as soon as every product of the current one that
+    // reads them has completed (q_empty), while its last tiles and output are still under way.
+    // A tile is one TMA box per 64-dim half (tpq tokens x G heads x 128 bytes, landing as the
+    // swizzled K-major operand); rows past the sequence are other sequences' queries, masked
+    // later.  Only a box that would reach past the last query row q_start[B] (which the caller
+    // need not have allocated) is copied row by row instead, zero-filled.
+    const uint64_t policy = l2_evict_first_policy();
+    const int q_rows = min(p.q_start[p.B], kQMapTokens);
     bool ok = true;
-    for (int k = 0; ok && k < n_tiles; ++k) {
-      if (warp == 0) {
-        ok = load(8, 8 * k, &tmK, &k_full[k & 1], &k_empty[k & 1], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u,
-                  sm + kKOff + (k & 1) * kTile, kHalf);
-      } else {
-        const int st = k % kVStages;
-        ok = load(8, 8 * k, &tmV, &v_full[st], &v_empty[st], (static_cast<uint32_t>(k / kVStages) & 1u) ^ 1u,
-                  sm + kVOff + st * kTile, kHalf);
+    int qi = 0;
+    const int c = lane & 15;
+    for (int ii = 0; ok && ii < n_items; ++ii) {
+      const Item it = make_item(p, list[ii], rank);
+      if (it.n_tiles == 0) continue;
+      if (!(ok = warp_wait(q_empty, (static_cast<uint32_t>(qi) & 1u) ^ 1u))) break;
+      ++qi;
+      uint32_t boxes = 0;  // tiles copied by TMA
+      for (int w = 0; w < 2; ++w) {
+        const int tq0 = it.t0 + w * p.tpq;
+        if (tq0 >= it.t_end) continue;  // no rows: its products are not issued
+        if (it.qs + tq0 + p.tpq <= q_rows) {
+          boxes |= 1u << w;
+          continue;
+        }
+        uint8_t* qtile = sm + kQOff + w * kTile;
+#pragma unroll 4
+        for (int i = 0; i < 64; ++i) {  // two 256-byte rows per instruction, 16 bytes per lane
+          const int rr = 2 * i + (lane >> 4);
+          const int tk = rr / p.G;
+          const bool ok_r = tq0 + tk < it.t_end;
+          const __nv_bfloat16* src =
+              ok_r ? p.q + (static_cast<size_t>(it.qs + tq0 + tk) * p.H_q + it.h_kv * p.G + (rr - tk * p.G)) * D + c * 8
+                   : p.q;
+          cp_async16(qtile + (c >> 3) * kHalf + rr * 128 + (((c & 7) ^ (rr & 7)) << 4), src, ok_r);
+        }
+      }
+      cp_async_wait_all();
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        if (boxes) {
+          mbar_arrive_expect_tx(q_full, __popc(boxes) * static_cast<uint32_t>(kTile));
+          for (int w = 0; w < 2; ++w)
+            if (boxes >> w & 1u)
+              for (int half = 0; half < 2; ++half)
+                tma_load_4d(sm + kQOff + w * kTile + half * kHalf, &tmQ, q_full, 0, half, it.h_kv * p.G,
+                            it.qs + it.t0 + w * p.tpq, policy);
+        } else {
+          mbar_arrive(q_full);
+        }
       }
     }
     if (!ok && lane == 0) flags[1] = 1;
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
-      auto issue_s = [&](int w, int k) {  // S_w = Q_w K^T of tile k
+      auto issue_s = [&](int w, int kst) {  // S_w = Q_w K^T of the tile in K stage kst
         const uint32_t qb = smem_u32(sm + kQOff + w * kTile);
-        const uint32_t kbuf = smem_u32(sm + kKOff + (k & 1) * kTile);
+        const uint32_t kbuf = smem_u32(sm + kKOff + kst * kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -442,43 +530,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_commit(&s_full[w]);
       };
-      auto issue_pv = [&](int w, int k) {  // O_w += P_w V of tile k
-        const uint32_t vbuf = smem_u32(sm + kVOff + (k % kVStages) * kTile);
+      auto issue_pv = [&](int w, int vst, bool first) {  // O_w (+)= P_w V of the tile in V stage vst
+        const uint32_t vbuf = smem_u32(sm + kVOff + vst * kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           // P: keys 16kk .. 16kk+15 = TMEM columns 8kk .. 8kk+7 of S_w; V: key rows 16kk .. of both halves
           tc_mma_ts(tmem + 256 + w * 128, tmem + w * 128 + 8 * kk, sw128_desc(vbuf + kk * 16 * 128, kHalf, 1024),
-                    kIdescPV, (k > 0 || kk > 0) ? 1u : 0u);
+                    kIdescPV, (!first || kk > 0) ? 1u : 0u);
         }
       };
-      // groups of this CTA with rows (a CTA without any still joins every copy and release)
-      const int groups = has1 ? 2 : (has0 ? 1 : 0);
-      // A stage is released (in both CTAs) only when a later copy waits for it: every such
-      // arrival is consumed before either CTA can finish, so none lands in a CTA that has left.
-      // The K stage of tile m is refilled with tile m + 2; the V stage of tile k with tile k + 3.
-      bool ok = mbar_wait(q_full, 0) && mbar_wait(&k_full[0], 0);
-      if (ok) {
-        tc_fence_after();
-        for (int w = 0; w < groups; ++w) issue_s(w, 0);
-        if (n_tiles > 2) tc_commit_mc(&k_empty[0], kBoth);
-      }
-      for (int k = 0; ok && k < n_tiles; ++k) {
-        const uint32_t ph = static_cast<uint32_t>(k) & 1u;
-        const bool next = k + 1 < n_tiles;
-        if (next && !(ok = mbar_wait(&k_full[(k + 1) & 1], static_cast<uint32_t>((k + 1) >> 1) & 1u))) break;
-        const int vs = k % kVStages;
-        if (!(ok = mbar_wait(&v_full[vs], static_cast<uint32_t>(k / kVStages) & 1u))) break;
-        // per group: P·V of this tile, then the group's S of the next tile
-        for (int w = 0; ok && w < groups; ++w) {
-          if (!(ok = mbar_wait(&p_full[w], ph))) break;
-          tc_fence_after();
-          issue_pv(w, k);
-          tc_commit(&o_done[w]);
-          if (next) issue_s(w, k + 1);
-        }
+      // A ring stage is released (in both CTAs) only when a later copy of the cluster waits for
+      // it: every such arrival is consumed before either CTA can finish, so none lands in a CTA
+      // that has left.  The K stage of tile m is refilled with tile m + 2, the V stage of tile m
+      // with tile m + 3, counting the tiles of all the cluster's items in order.  The K and V
+      // stages of an item's last tile stage the output of query tiles 0 and 1 when those hold
+      // rows, and their groups release them after it has left; otherwise they are released here.
+      int g_tot = 0;
+      for (int ii = 0; ii < n_items; ++ii) g_tot += make_item(p, list[ii], rank).n_tiles;
+      bool ok = true;
+      int g = 0, qi = 0;
+      uint32_t sp[2] = {0u, 0u};  // tiles of each query tile so far: s_full / p_full / o_done phase
+      for (int ii = 0; ok && ii < n_items; ++ii) {
+        const Item it = make_item(p, list[ii], rank);
+        const int nt = it.n_tiles;
+        if (nt == 0) continue;
+        // query tiles of this CTA with rows (a CTA without any still joins every copy and release)
+        const int groups = it.has1 ? 2 : (it.has0 ? 1 : 0);
+        ok = mbar_wait(q_full, static_cast<uint32_t>(qi) & 1u) &&
+             mbar_wait(&k_full[g & 1], static_cast<uint32_t>(g >> 1) & 1u);
+        ++qi;
         if (!ok) break;
-        if (k + kVStages < n_tiles) tc_commit_mc(&v_empty[vs], kBoth);
-        if (k + 3 < n_tiles) tc_commit_mc(&k_empty[(k + 1) & 1], kBoth);
+        tc_fence_after();
+        for (int w = 0; w < groups; ++w) issue_s(w, g & 1);
+        if (nt == 1) tc_commit(q_empty);  // the item's last products that read Q are issued
+        if (g + 2 < g_tot && (nt > 1 || groups == 0)) tc_commit_mc(&k_empty[g & 1], kBoth);
+        for (int k = 0; k < nt; ++k) {
+          const int gk = g + k;
+          const bool next = k + 1 < nt;
+          if (next && !(ok = mbar_wait(&k_full[(gk + 1) & 1], static_cast<uint32_t>((gk + 1) >> 1) & 1u))) break;
+          const int vs = gk % kVStages;
+          if (!(ok = mbar_wait(&v_full[vs], static_cast<uint32_t>(gk / kVStages) & 1u))) break;
+          // per query tile: P·V of this tile, then its S of the next tile
+          for (int w = 0; ok && w < groups; ++w) {
+            if (!(ok = mbar_wait(&p_full[w], sp[w] & 1u))) break;
+            ++sp[w];
+            tc_fence_after();
+            issue_pv(w, vs, k == 0);
+            tc_commit(&o_done[w]);
+            if (next) issue_s(w, (gk + 1) & 1);
+          }
+          if (!ok) break;
+          if (k == nt - 2) tc_commit(q_empty);
+          if (gk + kVStages < g_tot && (next || groups < 2)) tc_commit_mc(&v_empty[vs], kBoth);
+          if (next && gk + 3 < g_tot && (k + 2 < nt || groups == 0)) tc_commit_mc(&k_empty[(gk + 1) & 1], kBoth);
+        }
+        g += nt;
       }
       if (!ok) {
         flags[1] = 1;
@@ -489,184 +595,242 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------ softmax warpgroups ------------------------------
-    const int wg = (warp - 2) >> 2;  // query tile of this group
+    const int wg = (warp - 4) >> 2;  // query tile of this group
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // this thread's row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + wg * 128 + lane_off, tO = tmem + 256 + wg * 128 + lane_off;
-    const int tq0 = t0 + wg * p.tpq;  // first token of this query tile
     const int tok = r / p.G, hh = r - tok * p.G;
-    const bool row_ok = tq0 + tok < t_end;
-    const int row_pos = first_pos + tq0 + tok;
-    const int row_lo = p.window > 0 ? max(0, row_pos - p.window + 1) : 0;
-    uint8_t* qtile = sm + kQOff + wg * kTile;
-    {  // this warp's 32 Q rows -> swizzled Q tile; two 256-byte rows per instruction, so that
-       // the lanes of a row read it whole (16 bytes each) and the loads coalesce
-      const int c = lane & 15;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int rr = quad * 32 + 2 * i + (lane >> 4);
-        const int tk = rr / p.G;
-        const bool ok_r = tq0 + tk < t_end;
-        const __nv_bfloat16* src =
-            ok_r ? p.q + (static_cast<size_t>(qs + tq0 + tk) * p.H_q + h_kv * p.G + (rr - tk * p.G)) * D + c * 8 : p.q;
-        cp_async16(qtile + (c >> 3) * kHalf + rr * 128 + (((c & 7) ^ (rr & 7)) << 4), src, ok_r);
-      }
-      cp_async_wait_all();
-      fence_proxy_async();
-      mbar_arrive(q_full);
-    }
-    const bool active = wg == 0 ? has0 : has1;
-    float m_run = kNegInfTc, l_run = 0.f;
     bool ok = true;
-    for (int k = 0; active && k < n_tiles; ++k) {
-      const uint32_t ph = static_cast<uint32_t>(k) & 1u;
-      if (!warp_wait(&s_full[wg], ph)) {
-        ok = false;
-        break;
+    int g = 0;        // tiles of the cluster so far (V stage and phase)
+    uint32_t sp = 0;  // tiles of this query tile so far
+    int g_tot = 0;    // tiles of all the cluster's items (whether a later copy waits for a stage)
+    for (int ii = 0; ii < n_items; ++ii) g_tot += make_item(p, list[ii], rank).n_tiles;
+    for (int ii = 0; ii < n_items; ++ii) {
+      const Item it = make_item(p, list[ii], rank);
+      const int tq0 = it.t0 + wg * p.tpq;  // first token of this query tile
+      uint4* orow = reinterpret_cast<uint4*>(
+          p.out + (static_cast<size_t>(it.qs + tq0 + tok) * p.H_q + it.h_kv * p.G + hh) * D);
+      if (!it.valid) {  // zero rows, within the rows the caller declared
+        if (it.tile == 0 && it.h_kv == 0 && wg == 0 && r == 0) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
+        if (tq0 + tok < min(min(max(it.n, 0), p.max_q), tq0 + p.tpq))
+#pragma unroll
+          for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+        continue;
       }
-      tc_fence_after();
-      uint32_t sv[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
-      tmem_wait_ld();
-      const int kbase = (kb0 + 8 * k) * PA_BLOCK_SIZE;
-      // scores stay raw (the scale is positive, so the maximum commutes with it); only tiles
-      // that cross a row's causal or window edge take the per-key mask
-      if (!__all_sync(0xffffffffu, row_ok && kbase + 127 <= row_pos && kbase >= row_lo)) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int kp = kbase + c;
-          if (!(row_ok && kp <= row_pos && kp >= row_lo)) sv[c] = __float_as_uint(kNegInfTc);
-        }
+      const int nt = it.n_tiles;
+      if (nt == 0 || !(wg == 0 ? it.has0 : it.has1)) {
+        g += nt;
+        continue;
       }
-      float mx8[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) mx8[j] = kNegInfTc;
-#pragma unroll
-      for (int c = 0; c < 128; c += 2)
-        mx8[(c >> 1) & 7] = max3f(mx8[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-      const float mraw = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-      const float mx = mraw == kNegInfTc ? kNegInfTc : mraw * p.scale_log2;
-      const float m_new = (m_run == kNegInfTc || mx > m_run + 8.f) ? fmaxf(m_run, mx) : m_run;
-      const float ms = m_new == kNegInfTc ? 0.f : m_new;
-      const float alpha = ex2(m_run - ms);
-      // P (bf16 pairs) over the S columns just read: column c holds keys 2c and 2c + 1
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-      const float sl = p.scale_log2;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pw[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float a = ex2(fmaf(__uint_as_float(sv[64 * h + 2 * e]), sl, -ms));
-          const float b = ex2(fmaf(__uint_as_float(sv[64 * h + 2 * e + 1]), sl, -ms));
-          ls4[e & 3] += a + b;
-          pw[e] = pack_bf16(a, b);
-        }
-        tmem_st32(tS + 32 * h, pw);
-      }
-      tmem_wait_st();
-      l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
-      if (k > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tO + 32 * c, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32(tO + 32 * c, ov);
-        }
-        tmem_wait_st();
-      }
-      m_run = m_new;
-      // key row r of V: zero it when it holds no loaded in-context data (both groups write the
-      // same zeros; each must see them before its own P·V)
-      const int kp_r = kbase + r;
-      const bool zero_row = kp_r < kv_lo || kp_r >= loaded_end;
-      const int vs = k % kVStages;
-      if (__any_sync(0xffffffffu, zero_row)) {
-        // the stage's copies must have landed first
-        if (!warp_wait(&v_full[vs], static_cast<uint32_t>(k / kVStages) & 1u)) {
+      const bool row_ok = tq0 + tok < it.t_end;
+      const int row_pos = it.first_pos + tq0 + tok;
+      const int row_lo = p.window > 0 ? max(0, row_pos - p.window + 1) : 0;
+      float m_run = kNegInfTc, l_run = 0.f;
+      for (int k = 0; ok && k < nt; ++k) {
+        if (!warp_wait(&s_full[wg], sp & 1u)) {
           ok = false;
           break;
         }
-        if (zero_row) {
-          uint8_t* vrow = sm + kVOff + vs * kTile + r * 128;
+        ++sp;
+        tc_fence_after();
+        uint32_t sv[128];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
+        tmem_wait_ld();
+        const int kbase = (it.kb0 + 8 * k) * PA_BLOCK_SIZE;
+        // scores stay raw (the scale is positive, so the maximum commutes with it); only tiles
+        // that cross a row's causal or window edge take the per-key mask
+        if (!__all_sync(0xffffffffu, row_ok && kbase + 127 <= row_pos && kbase >= row_lo)) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int kp = kbase + c;
+            if (!(row_ok && kp <= row_pos && kp >= row_lo)) sv[c] = __float_as_uint(kNegInfTc);
           }
         }
-        fence_proxy_async();  // the zeros, before the tensor core reads the stage
+        float mx4[4] = {kNegInfTc, kNegInfTc, kNegInfTc, kNegInfTc};
+#pragma unroll
+        for (int c = 0; c < 128; c += 2)
+          mx4[(c >> 1) & 3] = max3f(mx4[(c >> 1) & 3], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        const float mraw = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]);
+        const float mx = mraw == kNegInfTc ? kNegInfTc : mraw * p.scale_log2;
+        const float m_new = (m_run == kNegInfTc || mx > m_run + 8.f) ? fmaxf(m_run, mx) : m_run;
+        const float ms = m_new == kNegInfTc ? 0.f : m_new;
+        const float alpha = ex2(m_run - ms);
+        // P (bf16 pairs) over the S columns just read: column c holds keys 2c and 2c + 1
+        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+        const float sl = p.scale_log2;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {  // a quarter (32 keys, 16 columns) at a time
+          uint32_t pw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e]), sl, -ms));
+            const float b = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e + 1]), sl, -ms));
+            ls4[e & 3] += a + b;
+            pw[e] = pack_bf16(a, b);
+          }
+          tmem_st16(tS + 16 * h, pw);
+        }
+        tmem_wait_st();
+        l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+        if (k > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + 32 * c, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(tO + 32 * c, ov);
+          }
+          tmem_wait_st();
+        }
+        m_run = m_new;
+        // key row r of V: zero it when it holds no loaded in-context data (both groups write the
+        // same zeros; each must see them before its own P·V)
+        const int kp_r = kbase + r;
+        const bool zero_row = kp_r < it.kv_lo || kp_r >= it.loaded_end;
+        const int gk = g + k, vs = gk % kVStages;
+        if (__any_sync(0xffffffffu, zero_row)) {
+          // the stage's copies must have landed first
+          if (!warp_wait(&v_full[vs], static_cast<uint32_t>(gk / kVStages) & 1u)) {
+            ok = false;
+            break;
+          }
+          if (zero_row) {
+            uint8_t* vrow = sm + kVOff + vs * kTile + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async();  // the zeros, before the tensor core reads the stage
+        }
+        tc_fence_before();
+        mbar_arrive(&p_full[wg]);
       }
-      tc_fence_before();
-      mbar_arrive(&p_full[wg]);
-    }
-    // epilogue: O / l -> bf16 output row, 32 columns at a time
-    if (active && ok && n_tiles > 0) ok = warp_wait(&o_done[wg], static_cast<uint32_t>(n_tiles - 1) & 1u);
-    if (!ok && lane == 0) flags[1] = 1;
-    tc_fence_after();
-    const float inv = (!ok || !(l_run > 0.f)) ? 0.f : 1.f / l_run;
-    uint4* orow = reinterpret_cast<uint4*>(
-        p.out + (static_cast<size_t>(qs + (row_ok ? tq0 + tok : t0)) * p.H_q + h_kv * p.G + hh) * D);
-    if (active && ok) {
-      // Every product has completed (o_done of the last tile follows them all), so the Q tile is
-      // idle: the warp stages its 32 rows there as bf16 (16-byte chunk j of row i at j ^ (i & 15),
-      // conflict-free both ways) and stores them two rows per instruction, coalesced.
-      uint8_t* stage = qtile + quad * 32 * 256;
+      g += nt;
+      // a table entry of the item's keys outside the pool: its rows become zero (read while the
+      // last P·V runs)
+      bool bad = false;
+      {
+        const int32_t* trow = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks;
+        for (int kb = it.kb0 + lane; kb < it.kb_end; kb += 32) {
+          const int e = trow[kb];
+          bad |= e < 0 || e >= p.num_blocks;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+      }
+      // output: O / l as bf16 (zeros when a wait gave up or a block id was bad), staged in the
+      // ring stage of the item's last tile that this group owns: K for query tile 0, V for 1.
+      // o_done of the last tile follows every product of the CTA that reads either, so both are
+      // idle.  One thread stores the tile with two TMA boxes (the copy engine, not the load/store
+      // unit, moves the bytes), waits until they have been read and releases the stage to the
+      // copies of both CTAs.  A tile that holds rows past its sequence is stored row by row
+      // instead (coalesced).
+      if (ok) ok = warp_wait(&o_done[wg], (sp - 1u) & 1u);
+      tc_fence_after();
+      const float inv = (!ok || bad || !(l_run > 0.f)) ? 0.f : 1.f / l_run;
+      const int g_last = g - 1;
+      uint8_t* stile = wg == 0 ? sm + kKOff + (g_last & 1) * kTile : sm + kVOff + (g_last % kVStages) * kTile;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
-        tmem_ld32(tO + 32 * c, ov);
-        tmem_wait_ld();
+        if (ok) {
+          tmem_ld32(tO + 32 * c, ov);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte chunk j = 4c + q4 of row r (dims 8j .. 8j + 7)
+          const int j = 4 * c + q4;
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             w[e] = pack_bf16(__uint_as_float(ov[8 * q4 + 2 * e]) * inv, __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
-          *reinterpret_cast<uint4*>(stage + lane * 256 + (((4 * c + q4) ^ (lane & 15)) << 4)) =
+          *reinterpret_cast<uint4*>(stile + (j >> 3) * kHalf + r * 128 + (((j & 7) ^ (r & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      __syncwarp();
-      const int c = lane & 15;
+      tc_fence_before();
+      fence_proxy_async();  // the staged rows, before the copy engine reads them
+      group_sync(1 + wg);
+      const bool release = wg == 0 ? g_last + 2 < g_tot : g_last + kVStages < g_tot;
+      uint64_t* rel = wg == 0 ? &k_empty[g_last & 1] : &v_empty[g_last % kVStages];
+      if (tq0 + p.tpq <= it.t_end) {
+        if (quad == 0 && lane == 0) {
+          for (int half = 0; half < 2; ++half)
+            tma_store_4d(&tmO, stile + half * kHalf, 0, half, it.h_kv * p.G, it.qs + tq0);
+          bulk_commit();
+          bulk_wait_read();
+          if (release) {
+            mbar_arrive_cluster(rel, 0);
+            mbar_arrive_cluster(rel, 1);
+          }
+        }
+      } else {
+        const int c = lane & 15;
 #pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int ri = 2 * i + (lane >> 4);
-        const int rr = quad * 32 + ri;
-        const int tk = rr / p.G;
-        if (tq0 + tk < t_end)
-          reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(qs + tq0 + tk) * p.H_q + h_kv * p.G + (rr - tk * p.G)) *
-                                               D)[c] = *reinterpret_cast<const uint4*>(stage + ri * 256 + ((c ^ (ri & 15)) << 4));
+        for (int i = 0; i < 16; ++i) {  // this warp's rows, two per instruction
+          const int rr = quad * 32 + 2 * i + (lane >> 4);
+          const int tk = rr / p.G;
+          if (tq0 + tk < it.t_end)
+            reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(it.qs + tq0 + tk) * p.H_q + it.h_kv * p.G +
+                                              (rr - tk * p.G)) * D)[c] =
+                *reinterpret_cast<const uint4*>(stile + (c >> 3) * kHalf + rr * 128 + (((c & 7) ^ (rr & 7)) << 4));
+        }
+        group_sync(1 + wg);  // every row has been read back before the stage is released
+        if (quad == 0 && lane == 0 && release) {
+          mbar_arrive_cluster(rel, 0);
+          mbar_arrive_cluster(rel, 1);
+        }
       }
-    } else if (active && row_ok) {
-#pragma unroll
-      for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0, 0, 0, 0);
     }
-    tc_fence_before();
-    __syncthreads();  // (1) every role is done: the flags are final
-    if ((flags[0] != 0 || flags[1] != 0) && row_ok) {
-#pragma unroll
-      for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0, 0, 0, 0);
-    }
-    if (tid == 64 && flags[1] != 0) set_error(p.err, PA_EFLAG_TIMEOUT);
+    bulk_wait_all();  // this thread's output stores are complete
+    if (!ok && lane == 0) flags[1] = 1;
   }
-  if (warp < 2 || warp == 10) {
-    tc_fence_before();
-    __syncthreads();  // (1)
-  }
-  __syncthreads();  // (2) no TMEM access is pending
+  // ------------------------------ teardown ------------------------------
+  tc_fence_before();
+  __syncthreads();  // no TMEM access is pending
+  if (tid == 64 && flags[1] != 0) set_error(p.err, PA_EFLAG_TIMEOUT);
   // neither CTA leaves while the other may still copy into its shared memory or release a stage
   cluster_sync();
-  // ------------------------------ teardown ------------------------------
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Clusters of two that can run at once on the current device (persistent grid size).
+int resident_clusters() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kTcSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    n = sms / 2;
+  }
+  if (dev < 64) cached[dev] = n;
+  return n;
 }
 
 }  // namespace
@@ -677,9 +841,12 @@ pa_status launch_prefill_tc(const pa_cache_desc* desc, void* out, const void* q,
                             const int32_t* context_lens, int max_query_len, float scale, int32_t* err_flag,
                             cudaStream_t stream) {
   const long long slots = static_cast<long long>(desc->num_blocks) * PA_BLOCK_SIZE;
-  CUtensorMap mk, mv;
+  CUtensorMap mk, mv, mq, mo;
+  const int G = desc->num_q_heads / desc->num_kv_heads;
   if (!encode_cache_map(&mk, k_cache, 2, desc->num_kv_heads * 2, 1, slots) ||
-      !encode_cache_map(&mv, v_cache, 2, desc->num_kv_heads * 2, 1, slots))
+      !encode_cache_map(&mv, v_cache, 2, desc->num_kv_heads * 2, 1, slots) ||
+      !encode_query_map(&mq, q, desc->num_q_heads, G, 128 / G, kQMapTokens) ||
+      !encode_query_map(&mo, out, desc->num_q_heads, G, 128 / G, kQMapTokens))
     return PA_ERR_CUDA;
   TcParams p;
   p.B = desc->num_seqs;
@@ -700,10 +867,16 @@ pa_status launch_prefill_tc(const pa_cache_desc* desc, void* out, const void* q,
   p.err = err_flag;
   if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
     return PA_ERR_CUDA;
-  const int ctas_x = (max_query_len + 2 * p.tpq - 1) / (2 * p.tpq);
-  const dim3 grid(2 * ((ctas_x + 1) / 2), p.B, p.H_kv);  // whole clusters of two along x
+  // Persistent clusters: as many as run at once, but no more than there are work items, and
+  // enough that none holds more than kMaxItems of them.
+  const long long w_tokens = 4LL * p.tpq;  // query tokens of one cluster tile
+  const long long items = static_cast<long long>(p.B) * ((max_query_len + w_tokens - 1) / w_tokens) * p.H_kv;
+  if (items > (1LL << 30)) return PA_ERR_UNSUPPORTED;
+  long long nc = std::min<long long>(items, std::max(1, resident_clusters()));
+  nc = std::max(nc, (items + kMaxItems - 1) / kMaxItems);
+  nc = std::max(nc, 1LL);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * nc));
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = kTcSmem;
   cfg.stream = stream;
@@ -716,7 +889,7 @@ pa_status launch_prefill_tc(const pa_cache_desc* desc, void* out, const void* q,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, mk, mv, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, mk, mv, mq, mo, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa

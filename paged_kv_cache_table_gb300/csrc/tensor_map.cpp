@@ -57,4 +57,20 @@ bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_hea
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Queries [T][H_q][128] bf16 as a 4-D tensor (64 dims of a half row, half, query head, token) with
+// boxes of one half x G heads x tokens_per_box tokens: a box lands as tokens_per_box * G rows of
+// 128 bytes, row (token, head), with the 128-byte swizzle.  `tokens` is the extent of the token
+// dimension; boxes must stay inside the rows the caller allocated.
+bool encode_query_map(CUtensorMap* map, const void* base, int heads, int G, int tokens_per_box, long long tokens) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {64, 2, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[3] = {128, 256, static_cast<cuuint64_t>(heads) * 256};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(tokens_per_box)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace pa
