@@ -552,6 +552,26 @@ class PrefillBench:
         torch.cuda.synchronize()
         return t0.elapsed_time(t1) / 1e3 / steps
 
+    def run_attention(self, steps, warmup):
+        """Seconds per prefill-attention call alone (the cache already holds the chunk), timed with
+        CUDA events on the stream the kernel is launched on."""
+        torch, N, w = self.torch, self.N, self.w
+        sid = torch.cuda.current_stream().cuda_stream
+
+        def call():
+            N.pa_prefill_attention(self.desc, self.out, self.q, self.k, self.v, self.tables, self.q_start, self.ctx,
+                                   self.max_q, w.scale, self.err, sid)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            call()
+        t1.record()
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / 1e3 / steps
+
 
 def prefix_cache_row(device, warmup):
     """Prefix-cache row: host cost of a lookup (hash chain + match + release through the binding)
@@ -789,12 +809,16 @@ def run_native(args):
     if rank == 0 and not args.no_next:
         pb = PrefillBench(device)
         sec = pb.run(max(20, args.steps // 50), args.warmup)
+        a_sec = pb.run_attention(max(50, args.steps // 20), args.warmup)
         bf16_peak = _bf16_peak()
         next_rows["chunked_prefill"] = {
             "workload": f"{pb.w.B} sequences, cached U[0..3584], chunk {pb.max_q} tokens, "
                         f"{pb.w.H_q}/{pb.w.H_kv} heads, d {pb.w.D}, bf16",
             "ms_per_step": round(sec * 1e3, 4), "tflops": round(pb.flops / sec / 1e12, 1),
             "frac_of_bf16_peak": round(pb.flops / sec / 1e12 / bf16_peak, 4),
+            "attention_ms_per_call": round(a_sec * 1e3, 4),
+            "attention_tflops": round(pb.flops / a_sec / 1e12, 1),
+            "attention_frac_of_bf16_peak": round(pb.flops / a_sec / 1e12 / bf16_peak, 4),
             "prefill_tokens_per_s_per_layer": round(pb.tokens / sec, 1), "err_flag": int(pb.err.item())}
         del pb
         torch.cuda.empty_cache()
@@ -890,10 +914,27 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per attention call of this build (null when unknown)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the chunked-prefill row (append + prefill attention steps) and print it; "
+                         "for profiling that kernel")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.prefill_only:
+        return run_prefill_only(args)
     return run_native(args)
+
+
+def run_prefill_only(args):
+    """--steps chunked-prefill steps after --warmup, then one JSON line with the step time."""
+    import torch
+    device = torch.device("cuda", 0)
+    pb = PrefillBench(device)
+    sec = pb.run(max(1, args.steps), max(0, args.warmup))
+    print(json.dumps({"row": "chunked_prefill", "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": round(sec * 1e3, 4), "tflops": round(pb.flops / sec / 1e12, 1),
+                      "err_flag": int(pb.err.item())}))
+    return 0 if int(pb.err.item()) == 0 else 1
 
 
 if __name__ == "__main__":
