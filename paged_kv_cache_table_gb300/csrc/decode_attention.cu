@@ -627,11 +627,12 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     // ------------------------------- producer -------------------------------
     // Every lane owns one block of the current 32-block chunk: its table entry is loaded one
     // chunk ahead and its stage metadata is packed once when the chunk becomes current, so a
-    // stage costs one shuffle, one shared store and one TMA per (tensor, head) box.  Each box
-    // is a whole head row (all 128-byte chunks) of the block's 16 slots.
-    // INT4 stages take four boxes per block: K and V codes of all the group's heads (128-byte
-    // rows of two heads), then K and V group parameters.
-    const int ops_per_block = KIND == 2 ? 4 : 2 * p.hg;
+    // stage costs one shuffle, one shared store and one TMA per box.  A block takes one box per
+    // tensor: the whole head rows of the group's heads for the block's 16 slots, head-major.
+    // (Measured, issuing a box costs about 90 cycles whatever its size, so fewer, larger boxes
+    // keep the producer ahead of HBM.)  INT4 stages take four boxes per block: K and V codes of
+    // all the group's heads (128-byte rows of two heads), then K and V group parameters.
+    const int ops_per_block = KIND == 2 ? 4 : 2;
     const int n_ops = nbs * ops_per_block;  // <= 32
     const uint64_t policy = l2_evict_first_policy();
     // this lane's op (fixed for every stage): block jj of the stage, tensor, head
@@ -647,11 +648,10 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       my_dst = static_cast<size_t>(my_jj) * p.block_bytes +
                (prm ? 2 * p.hg * 1024 + t * p.hg * 256 : t * p.hg * 1024);
     } else {
-      const int my_t = my_op / p.hg;
-      const int my_h = my_op - my_t * p.hg;
+      const int my_t = my_op;
       my_map = my_t ? &tmV : &tmK;
-      my_row = (hgi * p.hg + my_h) * p.nc;
-      my_dst = static_cast<size_t>((my_jj * 2 + my_t) * p.hg + my_h) * p.nc * kTileBytes;
+      my_row = hgi * p.hg;  // first head of the box
+      my_dst = static_cast<size_t>(my_jj * 2 + my_t) * p.hg * p.nc * kTileBytes;
     }
     // logical block of list entry u of sequence s (the visited blocks start at the window)
     auto logical = [&](int s, int u) { return window_lo(p, sm.ctxs[s]) / PA_BLOCK_SIZE + (u - sm.cum[s]); };
@@ -708,9 +708,14 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
         else mbar_arrive(&sm.full[st]);
       }
       __syncwarp();
-      if (lane < n_ops && ((live >> my_jj) & 1u))
-        tma_load_3d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], 0,
-                    my_row, pb * PA_BLOCK_SIZE, policy);
+      if (lane < n_ops && ((live >> my_jj) & 1u)) {
+        if constexpr (KIND == 2)
+          tma_load_3d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], 0,
+                      my_row, pb * PA_BLOCK_SIZE, policy);
+        else
+          tma_load_4d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], 0, 0,
+                      pb * PA_BLOCK_SIZE, my_row, policy);
+      }
     }
     // do not leave while a copy into this CTA's shared memory may still be in flight
     for (int st = 0; st < S && st < k; ++st) {
@@ -1038,8 +1043,8 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, c
         !pa::encode_param_map(&mvp, static_cast<const uint8_t*>(v_cache) + po, desc->num_kv_heads, pl.hg, slots))
       return PA_ERR_CUDA;
   } else {
-    if (!pa::encode_cache_map(&mk, k_cache, e, desc->num_kv_heads * pl.nc, pl.nc, slots) ||
-        !pa::encode_cache_map(&mv, v_cache, e, desc->num_kv_heads * pl.nc, pl.nc, slots))
+    if (!pa::encode_cache_map_heads(&mk, k_cache, e, desc->num_kv_heads, pl.nc, pl.hg, slots) ||
+        !pa::encode_cache_map_heads(&mv, v_cache, e, desc->num_kv_heads, pl.nc, pl.hg, slots))
       return PA_ERR_CUDA;
     mkp = mk;  // unused by the bf16 and 8-bit kernels
     mvp = mv;

@@ -34,6 +34,11 @@ pa_status validate_desc(const pa_cache_desc* d);
 bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int rows, int box_rows,
                       long long slots);
 
+// TMA descriptor of a bf16 or 8-bit cache pool viewed as (128-byte chunk elements, chunk, slot,
+// kv_head) with boxes of nc chunks x 16 slots x box_heads heads, landing head-major (tensor_map.cpp).
+bool encode_cache_map_heads(CUtensorMap* map, const void* base, int elem_bytes, int heads, int nc, int box_heads,
+                            long long slots);
+
 // TMA descriptor of the INT4 group parameters viewed as (16-byte head row, kv_head, slot) with
 // boxes of `box_heads` heads x 16 slots, no swizzle (tensor_map.cpp).
 bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots);

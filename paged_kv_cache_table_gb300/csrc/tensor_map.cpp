@@ -45,6 +45,27 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int ro
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The cache as a 4-D tensor (elements of a 128-byte chunk, chunk of the head row, slot, KV head)
+// with boxes of every chunk x 16 slots x `box_heads` heads.  The box runs heads outermost, so it
+// lands as [head][slot][chunk][128 B] with the 128-byte swizzle: each head's rows of a block form
+// the same contiguous tile that a one-head box gives, and one box carries a block of many heads.
+bool encode_cache_map_heads(CUtensorMap* map, const void* base, int elem_bytes, int heads, int nc, int box_heads,
+                            long long slots) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(128 / elem_bytes), static_cast<cuuint64_t>(nc),
+                        static_cast<cuuint64_t>(slots), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(heads) * nc * 128, static_cast<cuuint64_t>(nc) * 128};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(nc), PA_BLOCK_SIZE,
+                       static_cast<cuuint32_t>(box_heads)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots) {
   auto fn = tensor_map_encoder();
   if (!fn) return false;
