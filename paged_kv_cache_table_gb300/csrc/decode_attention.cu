@@ -376,19 +376,13 @@ struct Consumer {
     }
   }
 
-  // One 16-token block: scores, online softmax update, P·V.
-  // Tokens first .. ntok-1 of the block are attended; those below `first` are sink positions
-  // (read from the bf16 sink buffer by the merge) or lie before the sliding window.
-  __device__ __forceinline__ void block(const uint8_t* stage, int first, int ntok) {
-    if constexpr (I4) {
-      block_i4(stage, first, ntok);
-      return;
-    }
+  // q·Kᵀ of one 16-token block for this warp's head: acc rows = tokens t4, t4 + 8, columns =
+  // query heads 2tq, 2tq + 1, not yet scaled.  Two independent accumulation chains halve the
+  // dependent-MMA latency.
+  __device__ __forceinline__ void scores(const uint8_t* stage, float (&acc)[4]) const {
     const uint8_t* kbase = stage + kofs;
-    const uint8_t* vbase = stage + vofs;
-    // two independent accumulation chains halve the dependent-MMA latency of q·Kᵀ
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     const int tokA = (lane & 7) + ((lane >> 3) & 1) * 8;
     if constexpr (!QUANT) {
       const int halfA = lane >> 4;
@@ -416,11 +410,71 @@ struct Consumer {
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
-    float p00, p01, p10, p11;
-    softmax(acc, first, ntok, p00, p01, p10, p11);
+  }
+
+  // Online-softmax update over NB blocks' scores at once (one maximum, one rescale check);
+  // pr[b] = this lane's unnormalised probabilities {row t4: head 2tq, 2tq+1; row t4+8: same}.
+  template <int NB>
+  __device__ __forceinline__ void softmax_n(const float (&acc)[NB][4], const int (&first)[NB], const int (&ntok)[NB],
+                                            float (&pr)[NB][4]) {
+    float s[NB][4];
+    float bm0 = kNegInf, bm1 = kNegInf;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const bool v0 = t4 < ntok[b] && t4 >= first[b];
+      const bool v1 = t4 + 8 < ntok[b] && t4 + 8 >= first[b];
+      s[b][0] = v0 ? acc[b][0] * sl[0] : kNegInf;
+      s[b][1] = v0 ? acc[b][1] * sl[1] : kNegInf;
+      s[b][2] = v1 ? acc[b][2] * sl[0] : kNegInf;
+      s[b][3] = v1 ? acc[b][3] * sl[1] : kNegInf;
+      bm0 = fmaxf(bm0, fmaxf(s[b][0], s[b][2]));
+      bm1 = fmaxf(bm1, fmaxf(s[b][1], s[b][3]));
+    }
+#pragma unroll
+    for (int mask = 4; mask <= 16; mask <<= 1) {
+      bm0 = warp_max_xor(bm0, mask);
+      bm1 = warp_max_xor(bm1, mask);
+    }
+    // The reference maximum only moves when a score exceeds it by more than 2^8 (exact: the
+    // final division by l uses the same reference), so most blocks skip the rescale of o.
+    const float mn0 = (m[0] == kNegInf || bm0 > m[0] + 8.f) ? fmaxf(m[0], bm0) : m[0];
+    const float mn1 = (m[1] == kNegInf || bm1 > m[1] + 8.f) ? fmaxf(m[1], bm1) : m[1];
+    const float ms0 = mn0 == kNegInf ? 0.f : mn0;
+    const float ms1 = mn1 == kNegInf ? 0.f : mn1;
+    float add0 = 0.f, add1 = 0.f;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      pr[b][0] = ex2(s[b][0] - ms0);
+      pr[b][1] = ex2(s[b][1] - ms1);
+      pr[b][2] = ex2(s[b][2] - ms0);
+      pr[b][3] = ex2(s[b][3] - ms1);
+      add0 += pr[b][0] + pr[b][2];
+      add1 += pr[b][1] + pr[b][3];
+    }
+    if (__any_sync(0xffffffffu, mn0 != m[0] || mn1 != m[1])) {
+      const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
+      l[0] *= al0;
+      l[1] *= al1;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
+    l[0] += add0;
+    l[1] += add1;
+    m[0] = mn0;
+    m[1] = mn1;
+  }
+
+  // O += P·V of one block, P = pr (this lane's probabilities, tokens x heads).
+  __device__ __forceinline__ void pv(const uint8_t* stage, const float (&pr)[4], int first, int ntok) {
+    const uint8_t* vbase = stage + vofs;
     // P (tokens x heads) -> B operand (K = tokens, N = heads) of P·V
-    const uint32_t x0 = QUANT ? pack_f16(p00, p01) : pack_bf16(p00, p01);
-    const uint32_t x1 = QUANT ? pack_f16(p10, p11) : pack_bf16(p10, p11);
+    const uint32_t x0 = QUANT ? pack_f16(pr[0], pr[1]) : pack_bf16(pr[0], pr[1]);
+    const uint32_t x1 = QUANT ? pack_f16(pr[2], pr[3]) : pack_bf16(pr[2], pr[3]);
     const uint32_t b0 = movmatrix_t(x0), b1 = movmatrix_t(x1);
     if constexpr (!QUANT) {
       // Slots outside the attended range (tail of the last block, sink positions, positions
@@ -446,7 +500,9 @@ struct Consumer {
       }
     } else {
       // int8 V: a transposed 8x8 load of 16-bit pairs gives each lane two d values of two
-      // tokens; output row m = t4 holds d = 16mt + 2t4 and row m = t4+8 holds d + 1.
+      // tokens; output row m = t4 holds d = 16mt + 2t4 and row m = t4+8 holds d + 1.  Codes are
+      // finite, so tokens outside the attended range (P = 0) need no masking.
+      const int tokA = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
       for (int mp = 0; mp < KT / 2; ++mp) {
         const int ch16 = 2 * mp + (lane >> 4);
@@ -463,6 +519,34 @@ struct Consumer {
                 i8x2_to_f16x2(r3, 0x4240), i8x2_to_f16x2(r3, 0x4341), b0, b1);
       }
     }
+  }
+
+  // One 16-token block: scores, online softmax update, P·V.
+  // Tokens first .. ntok-1 of the block are attended; those below `first` are sink positions
+  // (read from the bf16 sink buffer by the merge) or lie before the sliding window.
+  __device__ __forceinline__ void block(const uint8_t* stage, int first, int ntok) {
+    if constexpr (I4) {
+      block_i4(stage, first, ntok);
+      return;
+    } else {
+      float acc[1][4], pr[1][4];
+      const int f[1] = {first}, n[1] = {ntok};
+      scores(stage, acc[0]);
+      softmax_n<1>(acc, f, n, pr);
+      pv(stage, pr[0], first, ntok);
+    }
+  }
+
+  // Two consecutive blocks of one sequence as one 32-token step: four independent q·Kᵀ chains,
+  // one maximum and one rescale check for both, then both P·V products.
+  __device__ __forceinline__ void block2(const uint8_t* s0, int f0, int n0, const uint8_t* s1, int f1, int n1) {
+    float acc[2][4], pr[2][4];
+    const int f[2] = {f0, f1}, n[2] = {n0, n1};
+    scores(s0, acc[0]);
+    scores(s1, acc[1]);
+    softmax_n<2>(acc, f, n, pr);
+    pv(s0, pr[0], f0, n0);
+    pv(s1, pr[1], f1, n1);
   }
 
   // d index of accumulator element (mt, e): e = 0,1 -> row t4; e = 2,3 -> row t4 + 8.
@@ -751,6 +835,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       return;
     }
     const int u = u0 + k * nbs + j;
+    bool paired = false;
     if (u < u1) {
       const int4 mt = sm.meta[st * nbs + j];
       if (mt.x != cur) {
@@ -768,11 +853,34 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
         c.bad = true;
       } else {
         const uint8_t* stage = sm.stages + static_cast<size_t>(st) * p.stage_bytes;
-        c.block(stage, mt.y, mt.z);
+        if constexpr (KIND != 2 && MAXW <= 8) {
+          // one block per stage: take the next stage too when its block belongs to the same
+          // sequence, and run both as one 32-token step (every warp decides alike: the
+          // metadata is the stage's).  Only with 4 or more stages, so that holding two still
+          // leaves the copies room ahead (measured: with 3 stages of 64 KiB it is slower); wider
+          // CTAs lack the registers for it.
+          if (nbs == 1 && S >= 4 && k + 1 < n_iters) {
+            const int st1 = (k + 1) % S;
+            if (!mbar_wait(&sm.full[st1], static_cast<uint32_t>((k + 1) / S) & 1u)) {
+              if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
+              return;
+            }
+            const int4 mt1 = sm.meta[st1];
+            if (mt1.x == mt.x && !mt1.w) {
+              c.block2(stage, mt.y, mt.z, sm.stages + static_cast<size_t>(st1) * p.stage_bytes, mt1.y, mt1.z);
+              paired = true;
+            }
+          }
+        }
+        if (!paired) c.block(stage, mt.y, mt.z);
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[st]);
+    if (lane == 0) {
+      mbar_arrive(&sm.empty[st]);
+      if (paired) mbar_arrive(&sm.empty[(k + 1) % S]);
+    }
+    if (paired) ++k;
   }
   c.flush(seq_base + cur, slot_of(cur), p.direct_ok && covers(cur) && q_loaded);
   for (int s = cur + 1; s <= s_last; ++s) c.flush_empty(slot_of(s));
