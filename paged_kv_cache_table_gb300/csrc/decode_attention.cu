@@ -155,6 +155,10 @@ struct Consumer {
   float o[KT][4];
   float m[2], l[2], sl[2];
   float vsc;
+  // INT4 zero points, applied per 32-dim group instead of per code: qz[g][c] = sum of q over
+  // group g for query head 2tq + c; cz[g][c] = running sum over tokens of p * s * (128 + z), the
+  // part of P·V that the offset codes add to every dim of group g
+  float qz[4][2], cz[4][2];
   bool bad;
   int lane, t4, tq, h_kv, j, h_loc;
   uint32_t kofs, vofs, kpofs, vpofs;  // this warp's tiles inside a stage
@@ -183,6 +187,10 @@ struct Consumer {
     bad = false;
 #pragma unroll
     for (int i = 0; i < KT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    if constexpr (I4) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) cz[g][0] = cz[g][1] = 0.f;
+    }
   }
 
   // B fragments of q for this KV head's G query heads (N = head, K = head_dim).
@@ -199,6 +207,16 @@ struct Consumer {
         qf[2 * g][1] = prmt(x.x, x.z, 0x7632);
         qf[2 * g + 1][0] = prmt(x.y, x.w, 0x5410);
         qf[2 * g + 1][1] = prmt(x.y, x.w, 0x7632);
+        // sum of the group's 32 q values of head t4 (8 here, then over the four tq lanes)
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        float sg = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sg += __uint_as_float(xw[e] << 16) + __uint_as_float(xw[e] & 0xFFFF0000u);
+        sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+        sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+        // this lane's score columns are heads 2tq, 2tq + 1: lanes 8tq and 8tq + 4 hold them
+        qz[g][0] = __shfl_sync(0xffffffffu, sg, 8 * tq);
+        qz[g][1] = __shfl_sync(0xffffffffu, sg, 8 * tq + 4);
       }
       sl[0] = sl[1] = p.scale_log2;
       vsc = 1.f;
@@ -249,51 +267,6 @@ struct Consumer {
     }
   }
 
-  // Online-softmax update for the block's scores acc (rows = tokens t4, t4+8; columns = query
-  // heads 2tq, 2tq+1, not yet scaled); returns this lane's unnormalised probabilities.
-  __device__ __forceinline__ void softmax(const float (&acc)[4], int first, int ntok, float& p00, float& p01,
-                                          float& p10, float& p11) {
-    // rows t4 and t4+8 of the block; columns = query heads 2tq, 2tq+1
-    const bool v0 = t4 < ntok && t4 >= first;
-    const bool v1 = t4 + 8 < ntok && t4 + 8 >= first;
-    const float s00 = v0 ? acc[0] * sl[0] : kNegInf;
-    const float s01 = v0 ? acc[1] * sl[1] : kNegInf;
-    const float s10 = v1 ? acc[2] * sl[0] : kNegInf;
-    const float s11 = v1 ? acc[3] * sl[1] : kNegInf;
-    float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
-#pragma unroll
-    for (int mask = 4; mask <= 16; mask <<= 1) {
-      bm0 = warp_max_xor(bm0, mask);
-      bm1 = warp_max_xor(bm1, mask);
-    }
-    // The reference maximum only moves when a score exceeds it by more than 2^8 (exact: the
-    // final division by l uses the same reference), so most blocks skip the rescale of o.
-    const float mn0 = (m[0] == kNegInf || bm0 > m[0] + 8.f) ? fmaxf(m[0], bm0) : m[0];
-    const float mn1 = (m[1] == kNegInf || bm1 > m[1] + 8.f) ? fmaxf(m[1], bm1) : m[1];
-    const float ms0 = mn0 == kNegInf ? 0.f : mn0;
-    const float ms1 = mn1 == kNegInf ? 0.f : mn1;
-    p00 = ex2(s00 - ms0);
-    p10 = ex2(s10 - ms0);
-    p01 = ex2(s01 - ms1);
-    p11 = ex2(s11 - ms1);
-    if (__any_sync(0xffffffffu, mn0 != m[0] || mn1 != m[1])) {
-      const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
-      l[0] *= al0;
-      l[1] *= al1;
-#pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
-      }
-    }
-    l[0] += p00 + p10;
-    l[1] += p01 + p11;
-    m[0] = mn0;
-    m[1] = mn1;
-  }
-
   // INT4: byte x (0..63) of this warp's head row in slot `slot` of a codes tile, whose 128-byte
   // rows hold two heads each and carry the 128-byte swizzle of the TMA box.
   __device__ __forceinline__ const uint8_t* i4_code(const uint8_t* tile, int slot, int x) const {
@@ -310,48 +283,44 @@ struct Consumer {
   // tq's K words hold whole 32-dim groups, so the two k-steps of group g accumulate apart and
   // the group's scale multiplies the fp32 sum.  P·V: the MMA sums over tokens, so each token's
   // group scale goes into P before the transpose; the output rows are dims 16mt + t4 (+8).
-  __device__ __forceinline__ void block_i4(const uint8_t* stage, int first, int ntok) {
-    constexpr uint32_t kOne = 0x3F803F80u;  // bf16 pair (1, 1)
+  __device__ __forceinline__ void scores_i4(const uint8_t* stage, float (&acc)[4]) const {
     const uint8_t* kc = stage + kofs;
-    const uint8_t* vc = stage + vofs;
     const uint8_t* kp = stage + kpofs;
-    const uint8_t* vp = stage + vpofs;
     const uint4 kw0 = *reinterpret_cast<const uint4*>(i4_code(kc, t4, tq * 16));
     const uint4 kw1 = *reinterpret_cast<const uint4*>(i4_code(kc, t4 + 8, tq * 16));
     const uint4 kq0 = i4_param(kp, t4), kq1 = i4_param(kp, t4 + 8);
     const uint32_t w0[4] = {kw0.x, kw0.y, kw0.z, kw0.w}, w1[4] = {kw1.x, kw1.y, kw1.z, kw1.w};
     const uint32_t q0[4] = {kq0.x, kq0.y, kq0.z, kq0.w}, q1[4] = {kq1.x, kq1.y, kq1.z, kq1.w};
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      const uint32_t z0 = (((q0[g] >> 16) & 0xFFu) * 0x00010001u) | 0xC300C300u;  // -(128 + z), twice
-      const uint32_t z1 = (((q1[g] >> 16) & 0xFFu) * 0x00010001u) | 0xC300C300u;
+      // q·(128 + n) over the group's 32 dims, then - (128 + z) * sum(q) and * scale
       float ag[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_bf16(ag, fma_bf16x2(nib_pair(w0[g], 0), kOne, z0), fma_bf16x2(nib_pair(w1[g], 0), kOne, z1),
-               fma_bf16x2(nib_pair(w0[g], 1), kOne, z0), fma_bf16x2(nib_pair(w1[g], 1), kOne, z1),
-               qf[2 * g][0], qf[2 * g][1]);
-      mma_bf16(ag, fma_bf16x2(nib_pair(w0[g], 2), kOne, z0), fma_bf16x2(nib_pair(w1[g], 2), kOne, z1),
-               fma_bf16x2(nib_pair(w0[g], 3), kOne, z0), fma_bf16x2(nib_pair(w1[g], 3), kOne, z1),
+      mma_bf16(ag, nib_pair(w0[g], 0), nib_pair(w1[g], 0), nib_pair(w0[g], 1), nib_pair(w1[g], 1), qf[2 * g][0],
+               qf[2 * g][1]);
+      mma_bf16(ag, nib_pair(w0[g], 2), nib_pair(w1[g], 2), nib_pair(w0[g], 3), nib_pair(w1[g], 3),
                qf[2 * g + 1][0], qf[2 * g + 1][1]);
+      const float c0 = __uint_as_float(0x43000000u | (q0[g] & 0x00FF0000u));  // 128 + z (z < 16)
+      const float c1 = __uint_as_float(0x43000000u | (q1[g] & 0x00FF0000u));
       const float s0 = __uint_as_float(q0[g] << 16), s1 = __uint_as_float(q1[g] << 16);
-      acc[0] = fmaf(s0, ag[0], acc[0]);
-      acc[1] = fmaf(s0, ag[1], acc[1]);
-      acc[2] = fmaf(s1, ag[2], acc[2]);
-      acc[3] = fmaf(s1, ag[3], acc[3]);
+      acc[0] = fmaf(s0, fmaf(-c0, qz[g][0], ag[0]), acc[0]);
+      acc[1] = fmaf(s0, fmaf(-c0, qz[g][1], ag[1]), acc[1]);
+      acc[2] = fmaf(s1, fmaf(-c1, qz[g][0], ag[2]), acc[2]);
+      acc[3] = fmaf(s1, fmaf(-c1, qz[g][1], ag[3]), acc[3]);
     }
-    float p00, p01, p10, p11;
-    softmax(acc, first, ntok, p00, p01, p10, p11);
+  }
+
+  __device__ __forceinline__ void pv_i4(const uint8_t* stage, const float (&pr)[4], int first, int ntok) {
+    const uint8_t* vc = stage + vofs;
+    const uint8_t* vp = stage + vpofs;
+    const float p00 = pr[0], p01 = pr[1], p10 = pr[2], p11 = pr[3];
     // scales of the P rows (tokens t4, t4 + 8); a masked token's slot may hold any bits, so its
     // scale is replaced by 0 rather than multiplied in
     const bool v0 = t4 < ntok && t4 >= first;
     const bool v1 = t4 + 8 < ntok && t4 + 8 >= first;
     const uint4 vs0 = i4_param(vp, t4), vs1 = i4_param(vp, t4 + 8);
     const uint32_t sv0w[4] = {vs0.x, vs0.y, vs0.z, vs0.w}, sv1w[4] = {vs1.x, vs1.y, vs1.z, vs1.w};
-    // zero points and codes of the A columns: tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
-    const uint4 zA = i4_param(vp, 2 * tq), zB = i4_param(vp, 2 * tq + 1);
-    const uint4 zC = i4_param(vp, 2 * tq + 8), zD = i4_param(vp, 2 * tq + 9);
-    const uint32_t zAw[4] = {zA.x, zA.y, zA.z, zA.w}, zBw[4] = {zB.x, zB.y, zB.z, zB.w};
-    const uint32_t zCw[4] = {zC.x, zC.y, zC.z, zC.w}, zDw[4] = {zD.x, zD.y, zD.z, zD.w};
+    // codes of the A columns: tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
     const uint2 cA = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq, t4 * 8));
     const uint2 cB = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq + 1, t4 * 8));
     const uint2 cC = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq + 8, t4 * 8));
@@ -360,18 +329,21 @@ struct Consumer {
     for (int g = 0; g < 4; ++g) {
       const float sv0 = v0 ? __uint_as_float(sv0w[g] << 16) : 0.f;
       const float sv1 = v1 ? __uint_as_float(sv1w[g] << 16) : 0.f;
-      const uint32_t b0 = movmatrix_t(pack_bf16(p00 * sv0, p01 * sv0));
-      const uint32_t b1 = movmatrix_t(pack_bf16(p10 * sv1, p11 * sv1));
-      const uint32_t zAB = (prmt(zAw[g], zBw[g], 0x0602) & 0x00FF00FFu) | 0xC300C300u;
-      const uint32_t zCD = (prmt(zCw[g], zDw[g], 0x0602) & 0x00FF00FFu) | 0xC300C300u;
+      // P * s as bf16, exactly as the MMA takes it; the offset codes add sum_t p s (128 + z) to
+      // every dim of the group, kept in cz and removed when the output is written
+      const uint32_t x0 = pack_bf16(p00 * sv0, p01 * sv0), x1 = pack_bf16(p10 * sv1, p11 * sv1);
+      const float c0 = __uint_as_float(0x43000000u | (sv0w[g] & 0x00FF0000u));  // 128 + z
+      const float c1 = __uint_as_float(0x43000000u | (sv1w[g] & 0x00FF0000u));
+      cz[g][0] = fmaf(__uint_as_float(x0 << 16), c0, fmaf(__uint_as_float(x1 << 16), c1, cz[g][0]));
+      cz[g][1] = fmaf(__uint_as_float(x0 & 0xFFFF0000u), c0, fmaf(__uint_as_float(x1 & 0xFFFF0000u), c1, cz[g][1]));
+      const uint32_t b0 = movmatrix_t(x0), b1 = movmatrix_t(x1);
 #pragma unroll
       for (int mm = 0; mm < 2; ++mm) {
         const int mt = 2 * g + mm, k = mt & 3;
         const uint32_t sel = static_cast<uint32_t>(k | ((k + 4) << 8));  // byte k of each token
         const uint32_t tAB = prmt(mt < 4 ? cA.x : cA.y, mt < 4 ? cB.x : cB.y, sel);
         const uint32_t tCD = prmt(mt < 4 ? cC.x : cC.y, mt < 4 ? cD.x : cD.y, sel);
-        mma_bf16(o[mt], fma_bf16x2(nib_pair(tAB, 0), kOne, zAB), fma_bf16x2(nib_pair(tAB, 1), kOne, zAB),
-                 fma_bf16x2(nib_pair(tCD, 0), kOne, zCD), fma_bf16x2(nib_pair(tCD, 1), kOne, zCD), b0, b1);
+        mma_bf16(o[mt], nib_pair(tAB, 0), nib_pair(tAB, 1), nib_pair(tCD, 0), nib_pair(tCD, 1), b0, b1);
       }
     }
   }
@@ -462,6 +434,13 @@ struct Consumer {
         o[mt][2] *= al0;
         o[mt][3] *= al1;
       }
+      if constexpr (I4) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          cz[g][0] *= al0;
+          cz[g][1] *= al1;
+        }
+      }
     }
     l[0] += add0;
     l[1] += add1;
@@ -525,12 +504,13 @@ struct Consumer {
   // Tokens first .. ntok-1 of the block are attended; those below `first` are sink positions
   // (read from the bf16 sink buffer by the merge) or lie before the sliding window.
   __device__ __forceinline__ void block(const uint8_t* stage, int first, int ntok) {
+    float acc[1][4], pr[1][4];
+    const int f[1] = {first}, n[1] = {ntok};
     if constexpr (I4) {
-      block_i4(stage, first, ntok);
-      return;
+      scores_i4(stage, acc[0]);
+      softmax_n<1>(acc, f, n, pr);
+      pv_i4(stage, pr[0], first, ntok);
     } else {
-      float acc[1][4], pr[1][4];
-      const int f[1] = {first}, n[1] = {ntok};
       scores(stage, acc[0]);
       softmax_n<1>(acc, f, n, pr);
       pv(stage, pr[0], first, ntok);
@@ -542,11 +522,19 @@ struct Consumer {
   __device__ __forceinline__ void block2(const uint8_t* s0, int f0, int n0, const uint8_t* s1, int f1, int n1) {
     float acc[2][4], pr[2][4];
     const int f[2] = {f0, f1}, n[2] = {n0, n1};
-    scores(s0, acc[0]);
-    scores(s1, acc[1]);
-    softmax_n<2>(acc, f, n, pr);
-    pv(s0, pr[0], f0, n0);
-    pv(s1, pr[1], f1, n1);
+    if constexpr (I4) {
+      scores_i4(s0, acc[0]);
+      scores_i4(s1, acc[1]);
+      softmax_n<2>(acc, f, n, pr);
+      pv_i4(s0, pr[0], f0, n0);
+      pv_i4(s1, pr[1], f1, n1);
+    } else {
+      scores(s0, acc[0]);
+      scores(s1, acc[1]);
+      softmax_n<2>(acc, f, n, pr);
+      pv(s0, pr[0], f0, n0);
+      pv(s1, pr[1], f1, n1);
+    }
   }
 
   // d index of accumulator element (mt, e): e = 0,1 -> row t4; e = 2,3 -> row t4 + 8.
@@ -557,6 +545,22 @@ struct Consumer {
 
   // Emit this warp's state for sequence s (global index).
   __device__ void flush(int s, size_t slot, bool direct) {
+    if constexpr (I4) {
+      // every token's part of cz, then o[dim][head] -= cz[group of dim][head]
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int mask = 4; mask <= 16; mask <<= 1) cz[g][c] += __shfl_xor_sync(0xffffffffu, cz[g][c], mask);
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        o[mt][0] -= cz[mt >> 1][0];
+        o[mt][1] -= cz[mt >> 1][1];
+        o[mt][2] -= cz[mt >> 1][0];
+        o[mt][3] -= cz[mt >> 1][1];
+      }
+    }
     float lt0 = l[0], lt1 = l[1];
 #pragma unroll
     for (int mask = 4; mask <= 16; mask <<= 1) {
@@ -853,7 +857,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
         c.bad = true;
       } else {
         const uint8_t* stage = sm.stages + static_cast<size_t>(st) * p.stage_bytes;
-        if constexpr (KIND != 2 && MAXW <= 8) {
+        if constexpr (MAXW <= 8) {
           // one block per stage: take the next stage too when its block belongs to the same
           // sequence, and run both as one 32-token step (every warp decides alike: the
           // metadata is the stage's).  Only with 4 or more stages, so that holding two still
