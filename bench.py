@@ -40,9 +40,9 @@ WINDOW = 64
 # ncu captures summarised in profiles/decode_kernel_<workload>.md.  Reported only while the
 # kernel sources hash to the version the counters were taken on; null otherwise.
 NCU_TRAFFIC = {
-    "sources_sha256_16": "64d7526d389f185d",
-    "8b": 552_450_816, "70b": 543_420_672, "long_quant": 1_076_937_216, "prefix_cow": 282_450_944,
-    "int4_8b": 189_920_000, "swa": 1_082_065_408,
+    "sources_sha256_16": "cfd18f129e65fa9d",
+    "8b": 552_086_784, "70b": 543_323_392, "long_quant": 1_077_113_600, "prefix_cow": 282_323_456,
+    "int4_8b": 190_098_944, "swa": 1_082_448_896,
 }
 KERNEL_SOURCES = ["paged_kv_cache_table_gb300/csrc/decode_attention.cu",
                   "paged_kv_cache_table_gb300/csrc/pa_device.cuh",
@@ -914,6 +914,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per attention call of this build (null when unknown)")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="with --config: one decode step, then --warmup + --steps decode-attention calls on the "
+                         "same inputs, one JSON line; for profiling the decode kernel")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the chunked-prefill row (append + prefill attention steps) and print it; "
                          "for profiling that kernel")
@@ -922,7 +925,36 @@ def main(argv=None):
         return run_reference(args)
     if args.prefill_only:
         return run_prefill_only(args)
+    if args.attention_only:
+        return run_attention_only(args)
     return run_native(args)
+
+
+def run_attention_only(args):
+    """One decode step on --config (append + attention), then --warmup + --steps attention calls on the
+    step's inputs; prints the mean call time."""
+    import torch
+    from paged_kv_cache_table_gb300 import native as N
+    b = DecodeBench(args.config, torch.device("cuda", 0), args.partition)
+    s = torch.cuda.current_stream().cuda_stream
+    b.step(0, s)
+
+    def call():
+        N.pa_decode_attention(b.desc, b.out, b.q[0], b.k, b.v, b.tables_dev, b.ctx_dev[0], b.max_ctx, b.w.scale,
+                              args.partition, b.ws, b.ws_bytes, b.err, s)
+    for _ in range(max(0, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(max(1, args.steps)):
+        call()
+    t1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"row": "decode_attention", "config": args.config, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_call": round(t0.elapsed_time(t1) / max(1, args.steps), 5),
+                      "err_flag": int(b.err.item())}))
+    return 0 if int(b.err.item()) == 0 else 1
 
 
 def run_prefill_only(args):
