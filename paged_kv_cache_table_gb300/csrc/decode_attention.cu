@@ -903,6 +903,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
   const int lane = threadIdx.x & 31;
   if (h >= p.H_q) return;
   const int h_kv = h / p.G;
+  // Every input is read after the wait: this launch may begin while the decode kernel (and, through
+  // it, whatever kernel wrote q or the context lengths) still runs; the wait covers them all.
+  grid_dep_wait();  // the decode kernel's partials and prefix sums are complete from here on
   const int ctx = p.context_lens[s];
   const int nb = seq_span(p, ctx);
   // sink positions inside the attended range [window_lo, ctx)
@@ -914,7 +917,6 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
 #pragma unroll
     for (int e = 0; e < E; ++e) qv[e] = __bfloat162float(qrow[e]);
   }
-  grid_dep_wait();  // the decode kernel's partials and prefix sums are complete from here on
   __nv_bfloat16* orow = p.out + (static_cast<size_t>(s) * p.H_q + h) * D;
 
   int c_first = 0, c_last = -1;
