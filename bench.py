@@ -325,13 +325,16 @@ class DecodeBench:
         out = P["out"]
         if buf is not None:
             q, kn, vn, out = self.ptr_e2e[buf]
+        if ev is None:
+            # the step as one call: the append overlaps the attention's streaming of other blocks
+            N.pa_decode_step(self.desc, out, q, P["k"], P["v"], kn, vn, P["tab"], pos, ctx, self.max_ctx, w.scale,
+                             self.partition, P["ws"], self.ws_bytes, P["err"], stream)
+            return
         N.pa_kv_append(self.desc, P["k"], P["v"], kn, vn, P["tab"], pos, P["err"], stream)
-        if ev is not None:
-            ev[0].record()
+        ev[0].record()
         N.pa_decode_attention(self.desc, out, q, P["k"], P["v"], P["tab"], ctx, self.max_ctx, w.scale,
                               self.partition, P["ws"], self.ws_bytes, P["err"], stream)
-        if ev is not None:
-            ev[1].record()
+        ev[1].record()
 
     def run(self, steps, warmup, per_call_events=False):
         """Device-resident steps.  Returns (elapsed_s, attention_ms_per_call or None, bytes)."""
@@ -466,12 +469,14 @@ class SlidingBench(DecodeBench):
         q, kn, vn = self.ptr_step[j][:3]
         pos = self.pos_all_dev[t].data_ptr()
         ctx = self.ctx_all_dev[t].data_ptr()
-        N.pa_kv_append(self.desc, P["k"], P["v"], kn, vn, P["tab"], pos, P["err"], stream)
-        if ev is not None:
+        if ev is None:
+            N.pa_decode_step(self.desc, P["out"], q, P["k"], P["v"], kn, vn, P["tab"], pos, ctx, self.max_ctx,
+                             w.scale, 0, P["ws"], self.ws_bytes, P["err"], stream)
+        else:
+            N.pa_kv_append(self.desc, P["k"], P["v"], kn, vn, P["tab"], pos, P["err"], stream)
             ev[0].record()
-        N.pa_decode_attention(self.desc, P["out"], q, P["k"], P["v"], P["tab"], ctx, self.max_ctx, w.scale,
-                              0, P["ws"], self.ws_bytes, P["err"], stream)
-        if ev is not None:
+            N.pa_decode_attention(self.desc, P["out"], q, P["k"], P["v"], P["tab"], ctx, self.max_ctx, w.scale,
+                                  0, P["ws"], self.ws_bytes, P["err"], stream)
             ev[1].record()
         released, _ = self.bm.slide_window(self.tables, self.ctx_all[t], w.window)
         self.dirty = released > 0

@@ -249,6 +249,27 @@ pa_status pa_decode_attention_noalloc(const pa_cache_desc* desc, void* out, cons
                                       int max_context_len, float scale, int partition_size,
                                       int32_t* err_flag, void* stream);
 
+/* One decode step: pa_kv_append of one token per sequence, then pa_decode_attention, enqueued
+ * together (显存账本 §四: the step appends the new token's K/V into the sequence's last block and
+ * attends over the context; ldpk §4.3).  The result is what the two calls give one after the
+ * other.  What differs is the overlap: the attention kernel waits for the append only before it
+ * loads a block that holds one of `positions`, so the append runs while every other block
+ * streams.  That is exact because the append writes nothing else the attention reads: it writes
+ * the K/V (and for 8-bit or INT4 caches the codes and parameters) of slot positions[s], and the
+ * bf16 sink rows when positions[s] < num_sink, which the attention reads only after the step's
+ * kernels have all waited for the append.
+ *   Arguments: those of pa_kv_append (k_new, v_new, positions) and of pa_decode_attention,
+ *   with the same meaning, layouts and rules; q, block_tables, positions and context_lens must
+ *   not be written by the append (they are not).  Every argument is checked before anything is
+ *   enqueued.
+ * Host errors: those of pa_kv_append and pa_decode_attention. */
+pa_status pa_decode_step(const pa_cache_desc* desc, void* out, const void* q, void* k_cache,
+                         void* v_cache, const void* k_new, const void* v_new,
+                         const int32_t* block_tables, const int32_t* positions,
+                         const int32_t* context_lens, int max_context_len, float scale,
+                         int partition_size, void* workspace, size_t workspace_bytes,
+                         int32_t* err_flag, void* stream);
+
 /* ---------------------------------------------------------------------------------
  * Host block manager: the physical block pool with a free list and reference counts
  * (显存账本 §四: equal-size blocks, any free one usable; AI内存系统 §3.2: reference counts,

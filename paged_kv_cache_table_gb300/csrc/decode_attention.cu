@@ -85,6 +85,10 @@ struct DecodeParams {
   float* partials;
   int32_t* ws_meta;
   int32_t* err;
+  // Positions of the tokens that the append kernel launched just before this one writes, one per
+  // sequence (a decode step), or null.  With them the kernel waits for that kernel only before
+  // loading a block that holds such a position; without them it waits before reading anything.
+  const int32_t* append_pos;
 };
 
 // Blocks of a sequence with ctx tokens; -1 for an invalid context.
@@ -626,8 +630,13 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
   // This kernel may have been launched while the previous kernel of the stream still runs
   // (programmatic dependent launch); whatever that kernel is, it may have produced any input
   // read below (q, context lengths, tables, the cache), so wait for it first.  What overlaps is
-  // the launch and the CTA set-up.
-  grid_dep_wait();
+  // the launch and the CTA set-up.  In a decode step the previous kernel is the append of one
+  // token per sequence (append_pos), which writes only the block holding each new position: the
+  // producer waits before loading such a block, so the append runs alongside the streaming of
+  // every other block, and every CTA waits before it leaves, so that this grid never completes
+  // before the append.
+  const bool step = p.append_pos != nullptr;
+  if (!step) grid_dep_wait();
 
   // ---- this CTA's range [u0, u1) of the (sequence, logical block) list ----
   int hgi, seq_base, nseq, u0, u1;
@@ -678,11 +687,13 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       for (int i = tid; i <= p.B; i += nthreads) p.ws_meta[i] = sm.cum[i];
       if (tid == 0) p.ws_meta[p.B + 1] = T;
     }
-    if (T == 0) return;
     const int W = (T + gridDim.x - 1) / gridDim.x;
     u0 = blockIdx.x * W;
     u1 = min(T, u0 + W);
-    if (u0 >= u1) return;
+    if (T == 0 || u0 >= u1) {
+      if (step) grid_dep_wait();
+      return;
+    }
   } else {
     hgi = blockIdx.z;
     seq_base = blockIdx.y;
@@ -698,7 +709,10 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     }
     u0 = blockIdx.x * p.ppb;
     u1 = min(nbv, u0 + p.ppb);
-    if (u0 >= u1) return;
+    if (u0 >= u1) {
+      if (step) grid_dep_wait();
+      return;
+    }
   }
 
   if (tid == 0) {
@@ -752,7 +766,8 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     int cur_pb = load_entry(base + lane);
     int nxt_pb = load_entry(base + 32 + lane);
     int4 my_meta;
-    unsigned live_mask;
+    unsigned live_mask, wait_mask;
+    bool waited = !step;
     auto pack = [&]() {
       const int u = base + lane;
       const bool valid = u < u1;
@@ -767,6 +782,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       my_meta = valid ? make_int4(s, first, min(PA_BLOCK_SIZE, sm.ctxs[s] - lb * PA_BLOCK_SIZE), bad ? 1 : 0)
                       : make_int4(-1, 0, 0, 1);
       live_mask = __ballot_sync(0xffffffffu, valid && !bad);
+      // blocks that receive this step's appended token (the append's position of the sequence)
+      const int ap = (valid && step) ? p.append_pos[seq_base + s] : -1;
+      wait_mask = __ballot_sync(0xffffffffu, ap >= 0 && ap / PA_BLOCK_SIZE == lb);
     };
     pack();
     const int n_iters = (u1 - u0 + nbs - 1) / nbs;
@@ -788,6 +806,10 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       if (!mbar_wait(&sm.empty[st], ph ^ 1u)) {
         if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
         break;
+      }
+      if (!waited && ((wait_mask >> i) & stage_bits)) {  // a block the append writes: wait for it
+        grid_dep_wait();
+        waited = true;
       }
       if (lane >= i && lane < i + nbs) sm.meta[st * nbs + (lane - i)] = my_meta;
       if (lane == 0) {
@@ -812,6 +834,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
         if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
       }
     }
+    if (!waited) grid_dep_wait();  // nor before the append of this step has completed
     return;
   }
   if (warp > p.warps_c) return;
@@ -1125,12 +1148,13 @@ extern "C" size_t pa_decode_workspace_size(const pa_cache_desc* desc, int max_co
   return pl.ws_bytes;
 }
 
-extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, const void* q,
-                                         const void* k_cache, const void* v_cache,
-                                         const int32_t* block_tables, const int32_t* context_lens,
-                                         int max_context_len, float scale, int partition_size,
-                                         void* workspace, size_t workspace_bytes, int32_t* err_flag,
-                                         void* stream) {
+namespace pa {
+namespace {
+// pa_decode_attention, and the attention half of pa_decode_step (append_pos non-null).
+pa_status decode_attention_impl(const pa_cache_desc* desc, void* out, const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                                int max_context_len, float scale, int partition_size, void* workspace,
+                                size_t workspace_bytes, int32_t* err_flag, void* stream, const int32_t* append_pos) {
   pa::Plan pl;
   pa_status st = pa::make_plan(desc, max_context_len, partition_size, &pl);
   if (st != PA_OK) return st;
@@ -1197,6 +1221,7 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, c
   p.ws_meta = static_cast<int32_t*>(workspace);
   p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.meta_bytes);
   p.err = err_flag;
+  p.append_pos = append_pos;
 
   cudaStream_t s = pa::as_stream(stream);
   const bool quant = pa::is_quantized(desc);
@@ -1205,6 +1230,42 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, c
            : quant ? pa::launch<128, 1>(pl, mk, mv, mkp, mvp, p, s)
                    : pa::launch<128, 0>(pl, mk, mv, mkp, mvp, p, s);
   return pa::launch<64, 0>(pl, mk, mv, mkp, mvp, p, s);
+}
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, const void* q,
+                                         const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         int max_context_len, float scale, int partition_size,
+                                         void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                         void* stream) {
+  return pa::decode_attention_impl(desc, out, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                                   scale, partition_size, workspace, workspace_bytes, err_flag, stream, nullptr);
+}
+
+extern "C" pa_status pa_decode_step(const pa_cache_desc* desc, void* out, const void* q, void* k_cache,
+                                    void* v_cache, const void* k_new, const void* v_new,
+                                    const int32_t* block_tables, const int32_t* positions,
+                                    const int32_t* context_lens, int max_context_len, float scale,
+                                    int partition_size, void* workspace, size_t workspace_bytes,
+                                    int32_t* err_flag, void* stream) {
+  // every argument of the attention half is checked before anything is enqueued
+  pa::Plan pl;
+  pa_status st = pa::make_plan(desc, max_context_len, partition_size, &pl);
+  if (st != PA_OK) return st;
+  if (desc->num_seqs == 0) return PA_OK;
+  if (!positions || !workspace || !out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+       reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u)
+    return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < pl.ws_bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+  st = pa_kv_append(desc, k_cache, v_cache, k_new, v_new, block_tables, positions, err_flag, stream);
+  if (st != PA_OK) return st;
+  return pa::decode_attention_impl(desc, out, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                                   scale, partition_size, workspace, workspace_bytes, err_flag, stream, positions);
 }
 
 // ------------------------------------------------------------------------------------

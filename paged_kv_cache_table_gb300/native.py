@@ -39,7 +39,8 @@ _DTYPES = {"bf16": PA_BF16, "fp8_e4m3": PA_FP8_E4M3, "e4m3": PA_FP8_E4M3, "int8"
 # Every symbol the header declares, for load checks.
 EXPORTED = [
     "pa_status_string", "pa_kv_append", "pa_kv_append_tokens", "pa_block_copy",
-    "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_noalloc", "pa_prefill_attention",
+    "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_noalloc", "pa_decode_step",
+    "pa_prefill_attention",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_alloc", "pa_bm_claim", "pa_bm_incref", "pa_bm_decref",
     "pa_bm_refcount", "pa_bm_num_free", "pa_bm_fork", "pa_bm_release", "pa_bm_prepare_step",
     "pa_bm_slide_window",
@@ -115,6 +116,9 @@ def lib() -> ctypes.CDLL:
         L.pa_prefill_attention.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, c_int, ctypes.c_float, vp, vp]
         L.pa_decode_attention_noalloc.restype = c_int
         L.pa_decode_attention_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp, c_int, ctypes.c_float, c_int, vp, vp]
+        L.pa_decode_step.restype = c_int
+        L.pa_decode_step.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, ctypes.c_float, c_int, vp,
+                                     ctypes.c_size_t, vp, vp]
         L.pa_bm_create.restype = vp
         L.pa_bm_create.argtypes = [c_int, c_int]
         L.pa_bm_destroy.restype = None
@@ -226,6 +230,19 @@ def pa_decode_attention(desc, out, q, k_cache, v_cache, block_tables, context_le
                                      float(scale), int(partition_size), _ptr(workspace),
                                      int(workspace_bytes), _ptr(err_flag), _stream(stream)),
            "pa_decode_attention")
+
+
+def pa_decode_step(desc, out, q, k_cache, v_cache, k_new, v_new, block_tables, positions, context_lens,
+                   max_context_len, scale, partition_size, workspace, workspace_bytes=None, err_flag=None,
+                   stream=None):
+    """pa_kv_append of one token per sequence, then pa_decode_attention, as one step (see pa.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_step(ctypes.byref(desc), _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(positions),
+                                _ptr(context_lens), int(max_context_len), float(scale), int(partition_size),
+                                _ptr(workspace), int(workspace_bytes), _ptr(err_flag), _stream(stream)),
+           "pa_decode_step")
 
 
 def pa_prefill_attention(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
