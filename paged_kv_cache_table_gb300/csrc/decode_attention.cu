@@ -166,6 +166,10 @@ struct Consumer {
   bool bad;
   int lane, t4, tq, h_kv, j, h_loc;
   uint32_t kofs, vofs, kpofs, vpofs;  // this warp's tiles inside a stage
+  // INT4: this lane's byte offsets inside a stage (they depend only on the lane and the head):
+  // K codes of tokens t4, t4 + 8; V codes of tokens 2tq, 2tq+1, 2tq+8, 2tq+9; K and V group
+  // parameters of tokens t4, t4 + 8
+  uint32_t ik[2], iv[4], ikp[2], ivp[2];
 
   __device__ Consumer(const DecodeParams& p_, int lane_, int h_kv_, int j_, int h_loc_)
       : p(p_), vsc(1.f), lane(lane_), t4(lane_ >> 2), tq(lane_ & 3), h_kv(h_kv_), j(j_), h_loc(h_loc_) {
@@ -177,6 +181,16 @@ struct Consumer {
       vofs = kofs + p_.hg * 1024;
       kpofs = kofs + 2 * p_.hg * 1024;
       vpofs = kpofs + p_.hg * 256;
+      ik[0] = kofs + i4_code_off(t4, tq * 16);
+      ik[1] = kofs + i4_code_off(t4 + 8, tq * 16);
+      iv[0] = vofs + i4_code_off(2 * tq, t4 * 8);
+      iv[1] = vofs + i4_code_off(2 * tq + 1, t4 * 8);
+      iv[2] = vofs + i4_code_off(2 * tq + 8, t4 * 8);
+      iv[3] = vofs + i4_code_off(2 * tq + 9, t4 * 8);
+      ikp[0] = kpofs + (t4 * p_.hg + h_loc_) * 16;
+      ikp[1] = kpofs + ((t4 + 8) * p_.hg + h_loc_) * 16;
+      ivp[0] = vpofs + (t4 * p_.hg + h_loc_) * 16;
+      ivp[1] = vpofs + ((t4 + 8) * p_.hg + h_loc_) * 16;
     } else {
       kofs = ((j * 2 + 0) * p_.hg * p_.nc + h_loc_ * p_.nc) * kTileBytes;
       vofs = ((j * 2 + 1) * p_.hg * p_.nc + h_loc_ * p_.nc) * kTileBytes;
@@ -273,26 +287,22 @@ struct Consumer {
 
   // INT4: byte x (0..63) of this warp's head row in slot `slot` of a codes tile, whose 128-byte
   // rows hold two heads each and carry the 128-byte swizzle of the TMA box.
-  __device__ __forceinline__ const uint8_t* i4_code(const uint8_t* tile, int slot, int x) const {
+  __device__ __forceinline__ uint32_t i4_code_off(int slot, int x) const {
     const int R = slot * (p.hg >> 1) + (h_loc >> 1);
     const int xb = ((h_loc & 1) << 6) + x;
-    return tile + R * 128 + ((((xb >> 4) ^ (R & 7)) << 4) | (xb & 15));
+    return static_cast<uint32_t>(R * 128 + ((((xb >> 4) ^ (R & 7)) << 4) | (xb & 15)));
   }
-  // INT4: the four group parameter words of this warp's head in slot `slot`.
-  __device__ __forceinline__ uint4 i4_param(const uint8_t* tile, int slot) const {
-    return *reinterpret_cast<const uint4*>(tile + (slot * p.hg + h_loc) * 16);
-  }
+
 
   // INT4 block.  Codes become exact bf16 integers (128 + n) - (128 + z) = n - z.  Scores: lane
   // tq's K words hold whole 32-dim groups, so the two k-steps of group g accumulate apart and
   // the group's scale multiplies the fp32 sum.  P·V: the MMA sums over tokens, so each token's
   // group scale goes into P before the transpose; the output rows are dims 16mt + t4 (+8).
   __device__ __forceinline__ void scores_i4(const uint8_t* stage, float (&acc)[4]) const {
-    const uint8_t* kc = stage + kofs;
-    const uint8_t* kp = stage + kpofs;
-    const uint4 kw0 = *reinterpret_cast<const uint4*>(i4_code(kc, t4, tq * 16));
-    const uint4 kw1 = *reinterpret_cast<const uint4*>(i4_code(kc, t4 + 8, tq * 16));
-    const uint4 kq0 = i4_param(kp, t4), kq1 = i4_param(kp, t4 + 8);
+    const uint4 kw0 = *reinterpret_cast<const uint4*>(stage + ik[0]);
+    const uint4 kw1 = *reinterpret_cast<const uint4*>(stage + ik[1]);
+    const uint4 kq0 = *reinterpret_cast<const uint4*>(stage + ikp[0]);
+    const uint4 kq1 = *reinterpret_cast<const uint4*>(stage + ikp[1]);
     const uint32_t w0[4] = {kw0.x, kw0.y, kw0.z, kw0.w}, w1[4] = {kw1.x, kw1.y, kw1.z, kw1.w};
     const uint32_t q0[4] = {kq0.x, kq0.y, kq0.z, kq0.w}, q1[4] = {kq1.x, kq1.y, kq1.z, kq1.w};
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
@@ -315,20 +325,19 @@ struct Consumer {
   }
 
   __device__ __forceinline__ void pv_i4(const uint8_t* stage, const float (&pr)[4], int first, int ntok) {
-    const uint8_t* vc = stage + vofs;
-    const uint8_t* vp = stage + vpofs;
     const float p00 = pr[0], p01 = pr[1], p10 = pr[2], p11 = pr[3];
     // scales of the P rows (tokens t4, t4 + 8); a masked token's slot may hold any bits, so its
     // scale is replaced by 0 rather than multiplied in
     const bool v0 = t4 < ntok && t4 >= first;
     const bool v1 = t4 + 8 < ntok && t4 + 8 >= first;
-    const uint4 vs0 = i4_param(vp, t4), vs1 = i4_param(vp, t4 + 8);
+    const uint4 vs0 = *reinterpret_cast<const uint4*>(stage + ivp[0]);
+    const uint4 vs1 = *reinterpret_cast<const uint4*>(stage + ivp[1]);
     const uint32_t sv0w[4] = {vs0.x, vs0.y, vs0.z, vs0.w}, sv1w[4] = {vs1.x, vs1.y, vs1.z, vs1.w};
     // codes of the A columns: tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
-    const uint2 cA = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq, t4 * 8));
-    const uint2 cB = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq + 1, t4 * 8));
-    const uint2 cC = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq + 8, t4 * 8));
-    const uint2 cD = *reinterpret_cast<const uint2*>(i4_code(vc, 2 * tq + 9, t4 * 8));
+    const uint2 cA = *reinterpret_cast<const uint2*>(stage + iv[0]);
+    const uint2 cB = *reinterpret_cast<const uint2*>(stage + iv[1]);
+    const uint2 cC = *reinterpret_cast<const uint2*>(stage + iv[2]);
+    const uint2 cD = *reinterpret_cast<const uint2*>(stage + iv[3]);
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const float sv0 = v0 ? __uint_as_float(sv0w[g] << 16) : 0.f;
