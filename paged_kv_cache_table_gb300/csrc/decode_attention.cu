@@ -924,16 +924,20 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
 
 // ------------------------------------------------------------------------------------
 // Merge: out = Σ_p e^{m_p - M} o_p / Σ_p e^{m_p - M} l_p (plus the bf16 sink tokens).
-// One warp per (sequence, query head).
+// WPR = 1: one warp per (sequence, query head).  WPR = 4, for launches with few (sequence, head)
+// rows: four warps per row, each merging a quarter of the partials (the first also the sinks),
+// combined through shared memory by the same log-sum-exp rule.
 // ------------------------------------------------------------------------------------
-template <int D>
+template <int D, int WPR>
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int grid_x) {
   constexpr int E = D / 32;  // dims per lane
   constexpr int CH = 8;      // partials per round of loads
   const int s = blockIdx.x;
-  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
+  const int wid = threadIdx.x >> 5;
+  const int h = WPR == 1 ? blockIdx.y * 4 + wid : blockIdx.y;
+  const int part = WPR == 1 ? 0 : wid;  // this warp's share of the row's partials
   const int lane = threadIdx.x & 31;
-  if (h >= p.H_q) return;
+  if (h >= p.H_q) return;  // (WPR = 4: h is the CTA's, so the CTA leaves together)
   const int h_kv = h / p.G;
   // Every input is read after the wait: this launch may begin while the decode kernel (and, through
   // it, whatever kernel wrote q or the context lengths) still runs; the wait covers them all.
@@ -942,7 +946,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
   const int nb = seq_span(p, ctx);
   // sink positions inside the attended range [window_lo, ctx)
   const int sink_lo = window_lo(p, ctx);
-  const int n_sink = nb < 0 ? 0 : min(p.num_sink, ctx);
+  const int n_sink = (nb < 0 || part != 0) ? 0 : min(p.num_sink, ctx);
   float qv[E];
   if (n_sink > sink_lo) {
     const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(s) * p.H_q + h) * D + lane * E;
@@ -964,6 +968,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
     if (p.direct_ok && c_first == c_last) return;  // the main kernel wrote this row
   }
   const int n_parts = (c_last - c_first + 1) * p.nbs;
+  const int share = (n_parts + WPR - 1) / WPR;
+  const int i_begin = min(n_parts, part * share), i_end = min(n_parts, i_begin + share);
   auto row_of = [&](int i) -> const float* {
     const int c = c_first + i / p.nbs, jj = i % p.nbs;
     const size_t slot = p.mode == 0 ? static_cast<size_t>(s + c) : static_cast<size_t>(s) * p.max_parts + c;
@@ -978,8 +984,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   bool bad = false;
-  for (int base = 0; base < n_parts; base += CH) {
-    const int n = min(CH, n_parts - base);
+  for (int base = i_begin; base < i_end; base += CH) {
+    const int n = min(CH, i_end - base);
     float mi = kNegInf, li = 0.f;
     if (lane < n) {
       const float* r = row_of(base + lane);
@@ -1041,6 +1047,36 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = acc[e] * sc + w * __bfloat162float(p.v_sink[off + e]);
     M = newM;
+  }
+  if constexpr (WPR > 1) {
+    // the warps' (M, L, acc) -> one row: weights e^{M_w - max M}, warps without a partial weigh 0
+    __shared__ float sh_m[WPR], sh_l[WPR], sh_acc[WPR][D];
+    __shared__ int sh_bad[WPR];
+    if (lane == 0) {
+      sh_m[wid] = M;
+      sh_l[wid] = L;
+      sh_bad[wid] = bad ? 1 : 0;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) sh_acc[wid][lane * E + e] = acc[e];
+    __syncthreads();
+    if (wid != 0) return;
+    float Mt = kNegInf;
+#pragma unroll
+    for (int w = 0; w < WPR; ++w) Mt = fmaxf(Mt, sh_m[w]);
+    L = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    bad = false;
+#pragma unroll
+    for (int w = 0; w < WPR; ++w) {
+      bad = bad || sh_bad[w] != 0;
+      if (sh_m[w] == kNegInf) continue;
+      const float sc = ex2(sh_m[w] - Mt);
+      L += sc * sh_l[w];
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += sc * sh_acc[w][lane * E + e];
+    }
   }
   const float inv = (bad || nb <= 0 || !(L > 0.f)) ? 0.f : 1.f / L;
 #pragma unroll
@@ -1144,7 +1180,10 @@ pa_status launch(const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv, c
   // append; the merge launch overlaps the decode tail); each waits before reading its inputs.
   if (launch_overlapped(kern, grid, dim3(pl.threads), pl.smem_bytes, stream, mk, mv, mkp, mvp, p) != PA_OK)
     return PA_ERR_CUDA;
-  return launch_overlapped(merge_kernel<D>, dim3(p.B, (p.H_q + 3) / 4), dim3(128), 0, stream, p, pl.grid_x);
+  // few (sequence, head) rows for the SMs (long contexts, small batches): four warps per row
+  if (static_cast<long long>(p.B) * p.H_q < 4LL * std::max(1, num_sms_current()))
+    return launch_overlapped(merge_kernel<D, 4>, dim3(p.B, p.H_q), dim3(128), 0, stream, p, pl.grid_x);
+  return launch_overlapped(merge_kernel<D, 1>, dim3(p.B, (p.H_q + 3) / 4), dim3(128), 0, stream, p, pl.grid_x);
 }
 
 }  // namespace
