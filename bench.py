@@ -40,9 +40,9 @@ WINDOW = 64
 # ncu captures summarised in profiles/decode_kernel_<workload>.md.  Reported only while the
 # kernel sources hash to the version the counters were taken on; null otherwise.
 NCU_TRAFFIC = {
-    "sources_sha256_16": "cfd18f129e65fa9d",
-    "8b": 552_086_784, "70b": 543_323_392, "long_quant": 1_077_113_600, "prefix_cow": 282_323_456,
-    "int4_8b": 190_098_944, "swa": 1_082_448_896,
+    "sources_sha256_16": "8eec9f82dd2e5b2b",
+    "8b": 552_238_848, "70b": 543_540_736, "long_quant": 1_077_185_024, "prefix_cow": 282_092_288,
+    "int4_8b": 190_453_248, "swa": 1_081_732_096,
 }
 KERNEL_SOURCES = ["paged_kv_cache_table_gb300/csrc/decode_attention.cu",
                   "paged_kv_cache_table_gb300/csrc/pa_device.cuh",
