@@ -7,35 +7,43 @@
 // window (ldpk §5.3).
 //
 // Design (head_dim 128, G = 1, 2, 4 or 8 query heads per KV head):
-//  * One CTA per (256 query rows, sequence, KV head): two query tiles of 128 rows, a row being
-//    (token, query head), share every K/V tile.  Two such CTAs of the same sequence and KV head
-//    form a cluster and load each K/V tile once: every CTA copies half of the tile's boxes with
-//    TMA multicast into both CTAs' shared memory.  Measured, one SM ingests only about 15-30
-//    bytes per cycle of scattered 2 KB blocks (copy engine or cp.async alike), so halving what
-//    each SM fetches per flop is what feeds the tensor core.
+//  * Work items.  An item is (sequence, cluster tile c, KV head): the query rows of 2 x 2 query
+//    tiles of 128 rows, a row being (token, query head), held by a cluster of two CTAs; a CTA's
+//    two query tiles share every K/V tile, and the cluster loads each K/V tile once: every CTA
+//    copies half of the tile's boxes with TMA multicast into both CTAs' shared memory.  Measured,
+//    one SM ingests only about 15-30 bytes per cycle of scattered 2 KB blocks (copy engine or
+//    cp.async alike), so halving what each SM fetches per flop is what feeds the tensor core.
+//  * Persistent clusters, longest first.  The grid is as many clusters as can be resident, each
+//    walking its own list of items.  An item's work grows with the last key it reads, which for
+//    the c-th cluster tile of a sequence is first_pos + min(n, (c + 1) W) (W query tokens per
+//    cluster tile): an arithmetic progression per sequence.  So the number of items whose last
+//    key is at least X has a closed form per sequence, every item's rank in the longest-first
+//    order is a sum over sequences, and the clusters rank all items in parallel at start-up
+//    (no sort, no scratch memory), dealing the ranks to clusters round by round, alternately in
+//    order and in reverse.  Barriers, TMEM and the ring phases carry across items.
 //  * S = Q·Kᵀ and O += P·V are tcgen05.mma (kind::f16, bf16 operands, M = N = 128, fp32
 //    accumulators in TMEM: S0, S1, O0, O1 in 4 x 128 columns), issued by one thread.  Q and K are
 //    K-major and V MN-major shared-memory operands with the 128-byte swizzle; P goes back into
 //    TMEM over the S columns it came from (bf16 pairs) and is the A operand of P·V from there, so
-//    the tensor core reads only Q, K and V from shared memory, whose bandwidth bounds it here.  A
-//    group's next S is issued after its P·V (the tensor pipe runs one thread's products in order,
-//    so P is read before it is overwritten); the two groups interleave on the tensor core.
-//  * One copy warp streams K through a two-stage ring of 128-key tiles and another V through a
-//    three-stage ring: a V tile is needed only at P·V, after the softmax, so V is fetched two tiles
-//    ahead, and on its own warp its waits never hold back the next K tile.  A stage is released to the copy warps
-//    by a multicast tcgen05.commit from each CTA's MMA thread, so it is refilled only when both
-//    CTAs are done with it.
-//  * Clusters start longest first.  A cluster's work grows with the last key it reads, which for
-//    the c-th cluster of a sequence is first_pos + min(n, (c + 1) W) (W query tokens per cluster):
-//    an arithmetic progression per sequence.  So the number of clusters whose last key is at
-//    least X has a closed form per sequence, and each cluster finds its own item, the one at its
-//    launch position in that order, by a 32-way search over X in one warp; no sort, no scratch.
+//    the tensor core reads only Q, K and V from shared memory.  A query tile's next S is issued
+//    after its P·V (the tensor pipe runs one thread's products in order, so P is read before it
+//    is overwritten); the two query tiles interleave on the tensor core.
+//  * Copies: one warp streams K through a two-stage ring of 128-key tiles, another V through a
+//    three-stage ring (a V tile is needed only at P·V, after the softmax, so V is fetched further
+//    ahead, and on its own warp its waits never hold back the next K tile), and a third loads the
+//    next item's query tiles by TMA (a 4-D map over q) as soon as the current item's last S
+//    products have completed.  A ring stage is released to the copy warps of both CTAs by a
+//    multicast tcgen05.commit from each CTA's MMA thread, so it is refilled only when both CTAs are
+//    done with it, and only when a later copy waits for it.
 //  * Two softmax warpgroups (one per query tile) own one query row per thread through TMEM
-//    lanes: they read S, mask (causal, window), keep the running maximum (moved only when a score
-//    exceeds it by 2^8), write P as bf16 into TMEM, rescale O in TMEM when the maximum moved (O is
-//    complete by then: its P·V was issued before this S), and finally normalise O into the output.  V rows of keys that are not loaded
-//    or lie beyond the context are zeroed before P·V reads them, so bits left in unused slots (NaN
-//    included) cannot leak.
+//    lanes: they read S, mask (causal, window) only on tiles that cross a row's edge, keep the
+//    running maximum (moved only when a score exceeds it by 2^8), write P as bf16 into TMEM, and
+//    rescale O in TMEM when the maximum moved (O is complete by then: its P·V was issued before
+//    this S).  V rows of keys that are not loaded or lie beyond the context are zeroed before P·V
+//    reads them, so bits left in unused slots (NaN included) cannot leak.
+//  * Output: O / l as bf16 is staged in the idle ring stage of the item's last tile (K for query
+//    tile 0, V for query tile 1) and stored by TMA; the stage is then released to both CTAs'
+//    copy warps.  Only a tile holding rows past its sequence is stored row by row.
 //  * Every wait is bounded; TMEM is released on every path.
 
 #include <algorithm>
