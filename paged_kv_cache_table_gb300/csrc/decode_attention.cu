@@ -15,15 +15,18 @@
 //    fixed mode each CTA owns one partition of partition_size tokens of one sequence.
 //  * A producer warp resolves block-table entries and streams every block with TMA
 //    (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared-memory stages guarded by
-//    mbarriers.  The slot-major cache keeps each (slot, kv-head) row contiguous, and the TMA box
-//    is 16 slots x 128 bytes of one head, so a stage holds whole blocks for all heads of the
-//    group and no byte is fetched twice.
+//    mbarriers.  The slot-major cache keeps each block's rows of all heads contiguous; one box per
+//    tensor carries the block for all heads of the group, head-major (each head's 16 slots form a
+//    tile), so a stage holds whole blocks and no byte is fetched twice.
 //  * One consumer warp per (KV head, block of the stage).  q·Kᵀ for the G query heads of the KV
 //    head and the 16 tokens of the block is an m16n8k16 tensor-core product (tokens = M, query
 //    heads = N); the probabilities are transposed in registers (movmatrix) into the B operand
 //    of P·V (head_dim = M).  The softmax is the online (running max) form in fp32 with warp
-//    shuffles; partial (m, l, o) go to the workspace and a merge kernel combines them by
-//    log-sum-exp.  A warp that saw a whole sequence writes the bf16 output directly.
+//    shuffles; with enough stages a warp takes two blocks of one sequence as one 32-token step.
+//    Partial (m, l, o) go to the workspace and a merge kernel combines them by log-sum-exp; a warp
+//    that saw a whole sequence writes the bf16 output directly.
+//  * In a decode step (pa_decode_step) the kernel overlaps the append launched just before it and
+//    waits for it only before the blocks that receive the appended tokens.
 //  * Every wait is bounded; invalid table entries and contexts set error bits and zero rows.
 
 #include <algorithm>
