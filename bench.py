@@ -40,7 +40,7 @@ WINDOW = 64
 # ncu captures summarised in profiles/decode_kernel_<workload>.md.  Reported only while the
 # kernel sources hash to the version the counters were taken on; null otherwise.
 NCU_TRAFFIC = {
-    "sources_sha256_16": "8eec9f82dd2e5b2b",
+    "sources_sha256_16": "8d8afddf5dd31680",
     "8b": 552_238_848, "70b": 543_540_736, "long_quant": 1_077_185_024, "prefix_cow": 282_092_288,
     "int4_8b": 190_453_248, "swa": 1_081_732_096,
 }
@@ -68,13 +68,23 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def ncu_traffic(workload: str):
+def kernel_sources_hash() -> str:
+    """First 16 hex digits of the sha256 of the kernel sources with comments and whitespace removed
+    (so that documentation edits keep the counters; any code change drops them)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest()[:16] != NCU_TRAFFIC["sources_sha256_16"]:
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update("".join(src.split()).encode())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    if kernel_sources_hash() != NCU_TRAFFIC["sources_sha256_16"]:
         return None
     return NCU_TRAFFIC.get(workload)
 
