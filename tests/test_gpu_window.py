@@ -91,10 +91,8 @@ def _oracle_prefill_window(w, window):
     return out
 
 
-@pytest.mark.parametrize("window", [1, 7, 16, 45, 200])
-@pytest.mark.parametrize("H_q,H_kv,D", [(8, 2, 64), (32, 8, 128), (8, 8, 128)])
-def test_sliding_prefill_matches_oracle(window, H_q, H_kv, D):
-    w = make_prefill_workload(H_q=H_q, H_kv=H_kv, D=D, cached_list=[0, 17, 100, 300], chunk_list=[5, 16, 33, 70])
+def _windowed_prefill(w, window):
+    """A PrefillGpu for workload w under window W, its pool as the previous step's release left it."""
     g = PrefillGpu(w)
     g.desc = N.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks, sliding_window=window)
     # What the previous step's release left: blocks wholly before position ctx_old - W are gone
@@ -114,6 +112,27 @@ def test_sliding_prefill_matches_oracle(window, H_q, H_kv, D):
         N.pa_kv_append_tokens(g.desc, g.k, g.v, rows, rows, len(nan_seq),
                               torch.tensor(nan_seq, dtype=torch.int32).cuda(),
                               torch.tensor(nan_pos, dtype=torch.int32).cuda(), g.tables, g.err)
+    return g
+
+
+@pytest.mark.parametrize("window", [1, 7, 16, 45, 200])
+@pytest.mark.parametrize("H_q,H_kv,D", [(8, 2, 64), (32, 8, 128), (8, 8, 128)])
+def test_sliding_prefill_matches_oracle(window, H_q, H_kv, D):
+    w = make_prefill_workload(H_q=H_q, H_kv=H_kv, D=D, cached_list=[0, 17, 100, 300], chunk_list=[5, 16, 33, 70])
+    g = _windowed_prefill(w, window)
     out = g.run()
     assert int(g.err.item()) == 0
     assert_attention_close(out, _oracle_prefill_window(w, window), f"prefill window {window}")
+
+
+@pytest.mark.parametrize("window", [64, 200, 600])
+@pytest.mark.parametrize("H_q,H_kv", [(32, 8), (64, 8), (16, 16)])
+def test_sliding_prefill_long_chunks(window, H_q, H_kv):
+    """Chunks spanning several tensor-core cluster tiles (d 128): later tiles start their keys
+    inside the window, the first key tile partly before it."""
+    w = make_prefill_workload(H_q=H_q, H_kv=H_kv, D=128, cached_list=[0, 500, 1000, 37],
+                              chunk_list=[300, 257, 129, 411], seed=21)
+    g = _windowed_prefill(w, window)
+    out = g.run()
+    assert int(g.err.item()) == 0
+    assert_attention_close(out, _oracle_prefill_window(w, window), f"prefill window {window}, long chunks")
