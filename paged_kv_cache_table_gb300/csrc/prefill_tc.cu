@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* s_full = bars + 14;  // [2] per query tile
   uint64_t* p_full = bars + 16;  // [2]
   uint64_t* o_done = bars + 18;  // [2]
+  uint64_t* p_half = bars + 24;  // [2] P of the tile's first 64 keys is in TMEM
   uint64_t* drain = bars + 20;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
   int* flags = reinterpret_cast<int*>(bars + 22);  // [0] work items of all clusters, [1] a wait gave up
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&k_empty[i], 2);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
+      mbar_init(&p_half[i], 128);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(drain, 1);
@@ -538,10 +540,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_commit(&s_full[w]);
       };
-      auto issue_pv = [&](int w, int vst, bool first) {  // O_w (+)= P_w V of the tile in V stage vst
+      // O_w (+)= P_w V over keys 64 half .. 64 half + 63 of the tile in V stage vst
+      auto issue_pv = [&](int w, int vst, bool first, int half) {
         const uint32_t vbuf = smem_u32(sm + kVOff + vst * kTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 4 * half; kk < 4 * half + 4; ++kk) {
           // P: keys 16kk .. 16kk+15 = TMEM columns 8kk .. 8kk+7 of S_w; V: key rows 16kk .. of both halves
           tc_mma_ts(tmem + 256 + w * 128, tmem + w * 128 + 8 * kk, sw128_desc(vbuf + kk * 16 * 128, kHalf, 1024),
                     kIdescPV, (!first || kk > 0) ? 1u : 0u);
@@ -578,12 +581,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (next && !(ok = mbar_wait(&k_full[(gk + 1) & 1], static_cast<uint32_t>((gk + 1) >> 1) & 1u))) break;
           const int vs = gk % kVStages;
           if (!(ok = mbar_wait(&v_full[vs], static_cast<uint32_t>(gk / kVStages) & 1u))) break;
-          // per query tile: P·V of this tile, then its S of the next tile
+          // per query tile: P·V of this tile (the first 64 keys as soon as their P is written, the
+          // rest when the whole of P is), then its S of the next tile
           for (int w = 0; ok && w < groups; ++w) {
+            if (!(ok = mbar_wait(&p_half[w], sp[w] & 1u))) break;
+            tc_fence_after();
+            issue_pv(w, vs, k == 0, 0);
             if (!(ok = mbar_wait(&p_full[w], sp[w] & 1u))) break;
             ++sp[w];
             tc_fence_after();
-            issue_pv(w, vs, k == 0);
+            issue_pv(w, vs, k == 0, 1);
             tc_commit(&o_done[w]);
             if (next) issue_s(w, (gk + 1) & 1);
           }
@@ -665,35 +672,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float m_new = (m_run == kNegInfTc || mx > m_run + 8.f) ? fmaxf(m_run, mx) : m_run;
         const float ms = m_new == kNegInfTc ? 0.f : m_new;
         const float alpha = ex2(m_run - ms);
-        // P (bf16 pairs) over the S columns just read: column c holds keys 2c and 2c + 1
-        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-        const float sl = p.scale_log2;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {  // a quarter (32 keys, 16 columns) at a time
-          uint32_t pw[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float a = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e]), sl, -ms));
-            const float b = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e + 1]), sl, -ms));
-            ls4[e & 3] += a + b;
-            pw[e] = pack_bf16(a, b);
-          }
-          tmem_st16(tS + 16 * h, pw);
-        }
-        tmem_wait_st();
-        l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
-        if (k > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + 32 * c, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(tO + 32 * c, ov);
-          }
-          tmem_wait_st();
-        }
+        const bool moved = k > 0 && __any_sync(0xffffffffu, m_new != m_run);
         m_run = m_new;
         // key row r of V: zero it when it holds no loaded in-context data (both groups write the
         // same zeros; each must see them before its own P·V)
@@ -715,6 +694,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
           fence_proxy_async();  // the zeros, before the tensor core reads the stage
+        }
+        // P (bf16 pairs) over the S columns just read: column c holds keys 2c and 2c + 1.  The
+        // first half (keys 0-63) is handed to the MMA thread as soon as it is written, so its
+        // P·V runs while the second half is computed; when the maximum moved, O is rescaled
+        // first and both halves go together.
+        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+        const float sl = p.scale_log2;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {  // a quarter (32 keys, 16 columns) at a time
+          uint32_t pw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e]), sl, -ms));
+            const float b = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e + 1]), sl, -ms));
+            ls4[e & 3] += a + b;
+            pw[e] = pack_bf16(a, b);
+          }
+          tmem_st16(tS + 16 * h, pw);
+          if (h == 1 && !moved) {
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_half[wg]);
+          }
+        }
+        tmem_wait_st();
+        l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+        if (moved) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + 32 * c, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(tO + 32 * c, ov);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&p_half[wg]);
         }
         tc_fence_before();
         mbar_arrive(&p_full[wg]);
