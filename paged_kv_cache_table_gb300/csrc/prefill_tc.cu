@@ -25,9 +25,11 @@
 //    accumulators in TMEM: S0, S1, O0, O1 in 4 x 128 columns), issued by one thread.  Q and K are
 //    K-major and V MN-major shared-memory operands with the 128-byte swizzle; P goes back into
 //    TMEM over the S columns it came from (bf16 pairs) and is the A operand of P·V from there, so
-//    the tensor core reads only Q, K and V from shared memory.  A query tile's next S is issued
-//    after its P·V (the tensor pipe runs one thread's products in order, so P is read before it
-//    is overwritten); the two query tiles interleave on the tensor core.
+//    the tensor core reads only Q, K and V from shared memory.  P·V is issued in two halves of
+//    64 keys: the first as soon as the softmax has written that half of P (p_half), so that it
+//    runs while the exponentials of the second half are computed, the second on p_full.  A query
+//    tile's next S is issued after its P·V (the tensor pipe runs one thread's products in order,
+//    so P is read before it is overwritten); the two query tiles interleave on the tensor core.
 //  * Copies: one warp streams K through a two-stage ring of 128-key tiles, another V through a
 //    three-stage ring (a V tile is needed only at P·V, after the softmax, so V is fetched further
 //    ahead, and on its own warp its waits never hold back the next K tile), and a third loads the
@@ -38,9 +40,10 @@
 //  * Two softmax warpgroups (one per query tile) own one query row per thread through TMEM
 //    lanes: they read S, mask (causal, window) only on tiles that cross a row's edge, keep the
 //    running maximum (moved only when a score exceeds it by 2^8), write P as bf16 into TMEM, and
-//    rescale O in TMEM when the maximum moved (O is complete by then: its P·V was issued before
-//    this S).  V rows of keys that are not loaded or lie beyond the context are zeroed before P·V
-//    reads them, so bits left in unused slots (NaN included) cannot leak.
+//    when the maximum moved rescale O in TMEM before handing any of P over (O is complete by
+//    then: its P·V was issued before this S).  V rows of keys that are not loaded or lie beyond
+//    the context are zeroed before P·V reads them, so bits left in unused slots (NaN included)
+//    cannot leak.
 //  * Output: O / l as bf16 is staged in the idle ring stage of the item's last tile (K for query
 //    tile 0, V for query tile 1) and stored by TMA; the stage is then released to both CTAs'
 //    copy warps.  Only a tile holding rows past its sequence is stored row by row.
