@@ -928,7 +928,7 @@ def main(argv=None):
     ap.add_argument("--no-next", action="store_true", help="skip the rows beyond decode (chunked prefill)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per attention call of this build (null when unknown)")
+                    help="ncu dram bytes per attention call of the current kernel sources (null when unknown)")
     ap.add_argument("--attention-only", action="store_true",
                     help="with --config: one decode step, then --warmup + --steps decode-attention calls on the "
                          "same inputs, one JSON line; for profiling the decode kernel")
