@@ -945,6 +945,14 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
   // Every input is read after the wait: this launch may begin while the decode kernel (and, through
   // it, whatever kernel wrote q or the context lengths) still runs; the wait covers them all.
   grid_dep_wait();  // the decode kernel's partials and prefix sums are complete from here on
+  // the row's extent in the balanced split does not depend on the context length: its loads go
+  // out together with it (one round trip before the partials, not two)
+  int cs = 0, ce = 0, T = 0;
+  if (p.mode == 0) {
+    cs = p.ws_meta[s];
+    ce = p.ws_meta[s + 1];
+    T = p.ws_meta[p.B + 1];
+  }
   const int ctx = p.context_lens[s];
   const int nb = seq_span(p, ctx);
   // sink positions inside the attended range [window_lo, ctx)
@@ -961,7 +969,6 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
   int c_first = 0, c_last = -1;
   if (nb > 0) {
     if (p.mode == 0) {
-      const int cs = p.ws_meta[s], ce = p.ws_meta[s + 1], T = p.ws_meta[p.B + 1];
       const int W = (T + grid_x - 1) / grid_x;
       c_first = cs / W;
       c_last = (ce - 1) / W;
