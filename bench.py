@@ -548,10 +548,9 @@ class PrefillBench:
 
     def step(self, stream):
         N, w = self.N, self.w
-        N.pa_kv_append_tokens(self.desc, self.k, self.v, self.new_k, self.new_v, self.tokens, self.new_seq,
-                              self.new_pos, self.tables, self.err, stream)
-        N.pa_prefill_attention(self.desc, self.out, self.q, self.k, self.v, self.tables, self.q_start, self.ctx,
-                               self.max_q, w.scale, self.err, stream)
+        N.pa_prefill_step(self.desc, self.out, self.q, self.k, self.v, self.new_k, self.new_v, self.tokens,
+                          self.new_seq, self.new_pos, self.tables, self.q_start, self.ctx, self.max_q, w.scale,
+                          self.err, stream)
 
     def run(self, steps, warmup):
         torch = self.torch

@@ -226,6 +226,24 @@ pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, const void*
                                const int32_t* context_lens, int max_query_len, float scale,
                                int32_t* err_flag, void* stream);
 
+/* One chunked-prefill step: pa_kv_append_tokens of the chunk's K/V, then pa_prefill_attention,
+ * enqueued together (ldpk §7: a chunk's K/V join the cache and its queries attend over it).  The
+ * result is what the two calls give one after the other.  What differs is the overlap: on the
+ * tensor-core path the attention kernel's set-up (work ranking, query loads) runs while the
+ * append does, and only its K/V copies wait for the append.  That is exact because the append
+ * writes only the K/V slots of the chunk's tokens, and nothing but those copies reads them.
+ *   Arguments: those of pa_kv_append_tokens (k_new, v_new, num_tokens, token_seq, token_pos) and
+ *   of pa_prefill_attention, with the same meaning, layouts and rules; out must not overlap
+ *   k_new, v_new, token_seq or token_pos.  Every argument is checked before anything is
+ *   enqueued.
+ * Host errors: those of pa_kv_append_tokens and pa_prefill_attention. */
+pa_status pa_prefill_step(const pa_cache_desc* desc, void* out, const void* q, void* k_cache,
+                          void* v_cache, const void* k_new, const void* v_new, int num_tokens,
+                          const int32_t* token_seq, const int32_t* token_pos,
+                          const int32_t* block_tables, const int32_t* q_start,
+                          const int32_t* context_lens, int max_query_len, float scale,
+                          int32_t* err_flag, void* stream);
+
 /* Allocation-free decode attention.  The pages have no counterpart to this entry point: it is
  * pa_decode_attention for callers that cannot allocate device memory when they call it, for
  * example a plugin running inside a host framework that owns every byte of device memory, a

@@ -8,9 +8,11 @@
 // keep a scale and a zero point besides the codes; here one of each per 32 dims of a token's
 // head row (the PA_INT4 rule in pa.h).
 //
-// One CTA per appended row; each thread moves 8 elements (one 16-byte bf16 vector).  The
-// row's kv_heads x head_dim elements are contiguous in the slot-major cache, so the stores
-// are fully coalesced.
+// bf16 and 8-bit caches: one warp per appended row, 8 rows per CTA; a lane moves 16-byte bf16
+// vectors.  The row's K and V are loaded before the table lookup that places them (they do
+// not depend on it), so the two memory round trips overlap.  The row's kv_heads x head_dim
+// elements are contiguous in the slot-major cache, so the stores are fully coalesced.  INT4
+// caches: one CTA per row, one thread per 32-dim group.
 
 #include <cuda_fp8.h>
 
@@ -122,10 +124,80 @@ __device__ __forceinline__ void encode_int4_group(const uint4* src, int h, int g
       sb | (static_cast<uint32_t>(z) << 16);
 }
 
-template <int KIND>  // 0 bf16, 1 fp8 K / int8 V, 2 int4
-__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+template <int KIND>  // 0 bf16, 1 fp8 K / int8 V
+__global__ void __launch_bounds__(256) kv_append_rows_kernel(const AppendParams p) {
   // the decode kernel that usually follows may start its prologue now: it waits for this
   // kernel's completion before it reads the cache
+  grid_dep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= p.num_rows) return;
+  const int vecs = p.H_kv * p.D / 8;  // 16-byte bf16 vectors per row
+  const uint4* kin = p.k_new + static_cast<size_t>(r) * vecs;
+  const uint4* vin = p.v_new + static_cast<size_t>(r) * vecs;
+  const int s = p.token_seq ? p.token_seq[r] : r;
+  const int pos = p.positions[r];
+  constexpr int kAhead = 4;  // vectors per lane loaded ahead of the lookup (a whole row up to 1024 dims)
+  uint4 kv[kAhead], vv[kAhead];
+#pragma unroll
+  for (int j = 0; j < kAhead; ++j) {
+    const int i = lane + 32 * j;
+    if (i < vecs) {
+      kv[j] = kin[i];
+      vv[j] = vin[i];
+    }
+  }
+  if (s < 0 || s >= p.num_seqs) {
+    if (lane == 0) set_error(p.err, PA_EFLAG_BAD_SEQ);
+    return;
+  }
+  if (pos < 0) return;  // padding row
+  if (pos < p.num_sink) {  // sink rows keep bf16 in their own buffer
+    const size_t base = (static_cast<size_t>(s) * p.num_sink + pos) * vecs;
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) {
+      const int i = lane + 32 * j;
+      if (i < vecs) {
+        p.k_sink[base + i] = kv[j];
+        p.v_sink[base + i] = vv[j];
+      }
+    }
+    for (int i = lane + 32 * kAhead; i < vecs; i += 32) {
+      p.k_sink[base + i] = kin[i];
+      p.v_sink[base + i] = vin[i];
+    }
+    return;
+  }
+  const int lb = pos / PA_BLOCK_SIZE;
+  if (lb >= p.max_blocks) {
+    if (lane == 0) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
+    return;
+  }
+  const int pb = p.block_tables[static_cast<size_t>(s) * p.max_blocks + lb];
+  if (pb < 0 || pb >= p.num_blocks) {
+    if (lane == 0) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
+    return;
+  }
+  const size_t slot = static_cast<size_t>(pb) * PA_BLOCK_SIZE + pos % PA_BLOCK_SIZE;
+  auto put = [&](int i, const uint4& k4, const uint4& v4) {
+    if constexpr (KIND == 1) {
+      const int h = (i * 8) / p.D;
+      reinterpret_cast<uint2*>(p.k_cache)[slot * vecs + i] = encode_e4m3x8(k4, p.k_scales[h]);
+      reinterpret_cast<uint2*>(p.v_cache)[slot * vecs + i] = encode_int8x8(v4, p.v_scales[h]);
+    } else {
+      reinterpret_cast<uint4*>(p.k_cache)[slot * vecs + i] = k4;
+      reinterpret_cast<uint4*>(p.v_cache)[slot * vecs + i] = v4;
+    }
+  };
+#pragma unroll
+  for (int j = 0; j < kAhead; ++j) {
+    const int i = lane + 32 * j;
+    if (i < vecs) put(i, kv[j], vv[j]);
+  }
+  for (int i = lane + 32 * kAhead; i < vecs; i += 32) put(i, kin[i], vin[i]);
+}
+
+__global__ void __launch_bounds__(256) kv_append_int4_kernel(const AppendParams p) {
   grid_dep_launch_dependents();
   const int r = blockIdx.x;
   const int s = p.token_seq ? p.token_seq[r] : r;
@@ -138,7 +210,6 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   const int vecs = p.H_kv * p.D / 8;  // 16-byte bf16 vectors per row
   const uint4* kin = p.k_new + static_cast<size_t>(r) * vecs;
   const uint4* vin = p.v_new + static_cast<size_t>(r) * vecs;
-
   if (pos < p.num_sink) {  // sink rows keep bf16 in their own buffer
     const size_t base = (static_cast<size_t>(s) * p.num_sink + pos) * vecs;
     for (int i = threadIdx.x; i < vecs; i += blockDim.x) {
@@ -158,26 +229,11 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
     return;
   }
   const size_t slot = static_cast<size_t>(pb) * PA_BLOCK_SIZE + pos % PA_BLOCK_SIZE;
-  if constexpr (KIND == 2) {
-    const int groups = p.H_kv * 4;  // head_dim 128
-    for (int i = threadIdx.x; i < 2 * groups; i += blockDim.x) {
-      const int tensor = i / groups, h = (i % groups) / 4, g = i % 4;
-      encode_int4_group((tensor ? vin : kin) + h * 16 + g * 4, h, g, tensor, p.H_kv, slot,
-                        static_cast<uint8_t*>(tensor ? p.v_cache : p.k_cache), p.params_offset);
-    }
-    return;
-  }
-  for (int i = threadIdx.x; i < vecs; i += blockDim.x) {
-    const uint4 kv = kin[i];
-    const uint4 vv = vin[i];
-    if constexpr (KIND == 1) {
-      const int h = (i * 8) / p.D;
-      reinterpret_cast<uint2*>(p.k_cache)[slot * vecs + i] = encode_e4m3x8(kv, p.k_scales[h]);
-      reinterpret_cast<uint2*>(p.v_cache)[slot * vecs + i] = encode_int8x8(vv, p.v_scales[h]);
-    } else {
-      reinterpret_cast<uint4*>(p.k_cache)[slot * vecs + i] = kv;
-      reinterpret_cast<uint4*>(p.v_cache)[slot * vecs + i] = vv;
-    }
+  const int groups = p.H_kv * 4;  // head_dim 128
+  for (int i = threadIdx.x; i < 2 * groups; i += blockDim.x) {
+    const int tensor = i / groups, h = (i % groups) / 4, g = i % 4;
+    encode_int4_group((tensor ? vin : kin) + h * 16 + g * 4, h, g, tensor, p.H_kv, slot,
+                      static_cast<uint8_t*>(tensor ? p.v_cache : p.k_cache), p.params_offset);
   }
 }
 
@@ -217,13 +273,14 @@ pa_status append_impl(const pa_cache_desc* d, void* k_cache, void* v_cache, cons
   p.err = err;
   p.params_offset = is_int4(d) ? int4_params_offset(d) : 0;
   const int vecs = p.H_kv * p.D / 8;
-  const int threads = min(256, ((vecs + 31) / 32) * 32);
+  constexpr int kRowsPerCta = 8;
+  const int grid = (num_rows + kRowsPerCta - 1) / kRowsPerCta;
   if (is_int4(d))
-    kv_append_kernel<2><<<num_rows, threads, 0, as_stream(stream)>>>(p);
+    kv_append_int4_kernel<<<num_rows, min(256, ((vecs + 31) / 32) * 32), 0, as_stream(stream)>>>(p);
   else if (is_quantized(d))
-    kv_append_kernel<1><<<num_rows, threads, 0, as_stream(stream)>>>(p);
+    kv_append_rows_kernel<1><<<grid, 32 * kRowsPerCta, 0, as_stream(stream)>>>(p);
   else
-    kv_append_kernel<0><<<num_rows, threads, 0, as_stream(stream)>>>(p);
+    kv_append_rows_kernel<0><<<grid, 32 * kRowsPerCta, 0, as_stream(stream)>>>(p);
   return launch_status();
 }
 

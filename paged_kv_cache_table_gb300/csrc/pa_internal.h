@@ -51,10 +51,12 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 
 // The tcgen05 chunked-prefill kernel (prefill_tc.cu): head_dim 128 and a power-of-two number of
 // query heads per KV head; arguments as pa_prefill_attention after its checks.
+// step: the previous kernel on the stream is the append of this prefill step (it writes only
+// K/V slots), so only the K/V copies wait for it.
 pa_status launch_prefill_tc(const pa_cache_desc* desc, void* out, const void* q, const void* k_cache,
                             const void* v_cache, const int32_t* block_tables, const int32_t* q_start,
                             const int32_t* context_lens, int max_query_len, float scale, int32_t* err_flag,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool step);
 
 inline pa_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;

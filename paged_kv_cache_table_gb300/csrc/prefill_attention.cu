@@ -311,14 +311,16 @@ __global__ void __launch_bounds__(kPfThreads)
 }  // namespace
 }  // namespace pa
 
-extern "C" pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, const void* q,
-                                          const void* k_cache, const void* v_cache,
-                                          const int32_t* block_tables, const int32_t* q_start,
-                                          const int32_t* context_lens, int max_query_len, float scale,
-                                          int32_t* err_flag, void* stream) {
-  pa_status st = pa::validate_desc(desc);
+namespace pa {
+namespace {
+// Host checks of pa_prefill_attention; *work = false when there is nothing to enqueue.
+pa_status prefill_check(const pa_cache_desc* desc, const void* out, const void* q, const void* k_cache,
+                        const void* v_cache, const int32_t* block_tables, const int32_t* q_start,
+                        const int32_t* context_lens, int max_query_len, float scale, bool* work) {
+  *work = false;
+  pa_status st = validate_desc(desc);
   if (st != PA_OK) return st;
-  if (pa::is_quantized(desc) || desc->num_sink > 0) return PA_ERR_UNSUPPORTED;
+  if (is_quantized(desc) || desc->num_sink > 0) return PA_ERR_UNSUPPORTED;
   if (max_query_len < 0 || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (desc->num_seqs == 0 || max_query_len == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !q_start || !context_lens)
@@ -327,20 +329,30 @@ extern "C" pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, 
        reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u)
     return PA_ERR_INVALID_ARG;
   if (desc->num_seqs > 65535 || desc->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  *work = true;
+  return PA_OK;
+}
+
+// pa_prefill_attention after its checks; step: the previous kernel is this step's append.
+pa_status prefill_launch(const pa_cache_desc* desc, void* out, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* block_tables, const int32_t* q_start,
+                         const int32_t* context_lens, int max_query_len, float scale, int32_t* err_flag,
+                         void* stream, bool step) {
   const int D = desc->head_dim;
   const int G = desc->num_q_heads / desc->num_kv_heads;
 #ifndef PA_PREFILL_WARP_MMA_ONLY
   if (D == 128 && (G & (G - 1)) == 0)  // the tensor-core (tcgen05) kernel
-    return pa::launch_prefill_tc(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
-                                 scale, err_flag, pa::as_stream(stream));
+    return launch_prefill_tc(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
+                             scale, err_flag, as_stream(stream), step);
 #endif
+  (void)step;  // the warp-MMA kernel waits for its predecessor before it starts
   const int nc = D * 2 / 128;
   const long long slots = static_cast<long long>(desc->num_blocks) * PA_BLOCK_SIZE;
   CUtensorMap mk, mv;
-  if (!pa::encode_cache_map(&mk, k_cache, 2, desc->num_kv_heads * nc, 1, slots) ||
-      !pa::encode_cache_map(&mv, v_cache, 2, desc->num_kv_heads * nc, 1, slots))
+  if (!encode_cache_map(&mk, k_cache, 2, desc->num_kv_heads * nc, 1, slots) ||
+      !encode_cache_map(&mv, v_cache, 2, desc->num_kv_heads * nc, 1, slots))
     return PA_ERR_CUDA;
-  pa::PrefillParams p;
+  PrefillParams p;
   p.B = desc->num_seqs;
   p.H_q = desc->num_q_heads;
   p.H_kv = desc->num_kv_heads;
@@ -350,7 +362,7 @@ extern "C" pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, 
   p.max_q = max_query_len;
   p.window = desc->sliding_window;
   p.tpw = 16 / p.G;
-  p.q_tile = pa::kPfWarps * p.tpw;
+  p.q_tile = kPfWarps * p.tpw;
   p.nc = nc;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.q_start = q_start;
@@ -360,8 +372,41 @@ extern "C" pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, 
   p.out = static_cast<__nv_bfloat16*>(out);
   p.err = err_flag;
   const dim3 grid((max_query_len + p.q_tile - 1) / p.q_tile, p.B, p.H_kv);
-  cudaStream_t s = pa::as_stream(stream);
+  cudaStream_t s = as_stream(stream);
   if (D == 128)
-    return pa::launch_overlapped(pa::prefill_kernel<128>, grid, dim3(pa::kPfThreads), 0, s, mk, mv, p);
-  return pa::launch_overlapped(pa::prefill_kernel<64>, grid, dim3(pa::kPfThreads), 0, s, mk, mv, p);
+    return launch_overlapped(prefill_kernel<128>, grid, dim3(kPfThreads), 0, s, mk, mv, p);
+  return launch_overlapped(prefill_kernel<64>, grid, dim3(kPfThreads), 0, s, mk, mv, p);
+}
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, const int32_t* q_start,
+                                          const int32_t* context_lens, int max_query_len, float scale,
+                                          int32_t* err_flag, void* stream) {
+  bool work = false;
+  const pa_status st = pa::prefill_check(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens,
+                                         max_query_len, scale, &work);
+  if (st != PA_OK || !work) return st;
+  return pa::prefill_launch(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
+                            scale, err_flag, stream, false);
+}
+
+extern "C" pa_status pa_prefill_step(const pa_cache_desc* desc, void* out, const void* q, void* k_cache,
+                                     void* v_cache, const void* k_new, const void* v_new, int num_tokens,
+                                     const int32_t* token_seq, const int32_t* token_pos,
+                                     const int32_t* block_tables, const int32_t* q_start,
+                                     const int32_t* context_lens, int max_query_len, float scale,
+                                     int32_t* err_flag, void* stream) {
+  // every argument of the attention half is checked before the append is enqueued
+  bool work = false;
+  const pa_status st = pa::prefill_check(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens,
+                                         max_query_len, scale, &work);
+  if (st != PA_OK) return st;
+  const pa_status sa = pa_kv_append_tokens(desc, k_cache, v_cache, k_new, v_new, num_tokens, token_seq,
+                                           token_pos, block_tables, err_flag, stream);
+  if (sa != PA_OK || !work) return sa;
+  return pa::prefill_launch(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
+                            scale, err_flag, stream, num_tokens > 0);
 }

@@ -82,6 +82,7 @@ constexpr uint32_t kIdescPV = kIdescS | (1u << 16);
 struct TcParams {
   int B, H_q, H_kv, G, num_blocks, max_blocks, max_q, window;
   int tpq;  // tokens per query tile: 128 / G (a CTA holds two tiles)
+  int step;  // the previous kernel is this step's append: only the K/V copies wait for it
   float scale_log2;
   const int32_t* q_start;
   const int32_t* context_lens;
@@ -360,8 +361,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  // launched with programmatic dependent launch: the previous kernel may still write any input
-  grid_dep_wait();
+  // Launched with programmatic dependent launch: the previous kernel may still write any input,
+  // so everything waits for it here.  In a prefill step the previous kernel is the append of the
+  // chunk, which writes only K/V slots; then only the K/V copy warps wait (before their first
+  // copy, in every CTA, so that this grid never completes before the append), and the set-up
+  // and the query copies overlap the append.
+  if (!p.step) grid_dep_wait();
   if (lpt)
     for (int q = tid; q < p.B; q += kTcThreads) geo[q] = seq_geo(p, q, lw);
   tc_fence_before();
@@ -409,6 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0 || warp == 2) {
     // ---------------------- copy warps: K (warp 0), V (warp 2) ----------------------
+    if (p.step) grid_dep_wait();
     uint64_t policy;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
     bool ok = true;
@@ -868,7 +874,7 @@ int resident_clusters() {
 pa_status launch_prefill_tc(const pa_cache_desc* desc, void* out, const void* q, const void* k_cache,
                             const void* v_cache, const int32_t* block_tables, const int32_t* q_start,
                             const int32_t* context_lens, int max_query_len, float scale, int32_t* err_flag,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool step) {
   const long long slots = static_cast<long long>(desc->num_blocks) * PA_BLOCK_SIZE;
   CUtensorMap mk, mv, mq, mo;
   const int G = desc->num_q_heads / desc->num_kv_heads;
@@ -887,6 +893,7 @@ pa_status launch_prefill_tc(const pa_cache_desc* desc, void* out, const void* q,
   p.max_q = max_query_len;
   p.window = desc->sliding_window;
   p.tpq = 128 / p.G;
+  p.step = step ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.q_start = q_start;
   p.context_lens = context_lens;
