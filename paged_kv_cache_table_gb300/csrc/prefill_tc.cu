@@ -47,6 +47,9 @@
 //  * Output: O / l as bf16 is staged in the idle ring stage of the item's last tile (K for query
 //    tile 0, V for query tile 1) and stored by TMA; the stage is then released to both CTAs'
 //    copy warps.  Only a tile holding rows past its sequence is stored row by row.
+//  * Launched with programmatic dependent launch.  In a prefill step (pa_prefill_step) the
+//    previous kernel is the chunk's append, which writes only K/V slots, so only the K/V copy
+//    warps wait for it; the work ranking and the query copies run alongside it.
 //  * Every wait is bounded; TMEM is released on every path.
 
 #include <algorithm>
