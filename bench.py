@@ -40,9 +40,9 @@ WINDOW = 64
 # ncu captures summarised in profiles/decode_kernel_<workload>.md.  Reported only while the
 # kernel sources hash to the version the counters were taken on; null otherwise.
 NCU_TRAFFIC = {
-    "sources_sha256_16": "dd3ccdf378ffcbc2",
-    "8b": 552_204_288, "70b": 543_349_504, "long_quant": 1_077_334_272, "prefix_cow": 282_273_792,
-    "int4_8b": 190_674_944, "swa": 1_082_582_528,
+    "sources_sha256_16": "81eb5caebcbe4597",
+    "8b": 552_557_056, "70b": 543_515_904, "long_quant": 1_076_951_808, "prefix_cow": 282_210_560,
+    "int4_8b": 190_876_416, "swa": 1_082_485_504,
 }
 KERNEL_SOURCES = ["paged_kv_cache_table_gb300/csrc/decode_attention.cu",
                   "paged_kv_cache_table_gb300/csrc/pa_device.cuh",
