@@ -51,6 +51,19 @@ def _desc(**kw):
 FAKE = 1 << 20  # never dereferenced: every call below returns before launching
 
 
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except ImportError:
+        return True
+
+
+# Calls with fake device addresses are made only where no GPU is visible: should a host check
+# ever go missing, such a call must not reach a device.
+host_only = pytest.mark.skipif(not _no_gpu(), reason="fake device addresses: run without a GPU")
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=96), N.PA_ERR_UNSUPPORTED),
     (dict(block_size=32), N.PA_ERR_UNSUPPORTED),
@@ -63,6 +76,7 @@ FAKE = 1 << 20  # never dereferenced: every call below returns before launching
     (dict(k_dtype=7), N.PA_ERR_INVALID_ARG),
     (dict(num_sink=4), N.PA_ERR_INVALID_ARG),  # sinks without buffers
 ])
+@host_only
 def test_bad_descriptions_are_rejected_on_the_host(kw, status):
     d = _desc(**kw)
     with pytest.raises(N.PaError) as e:
@@ -74,6 +88,7 @@ def test_bad_descriptions_are_rejected_on_the_host(kw, status):
     assert N.pa_decode_workspace_size(d, 100, 32) == 0
 
 
+@host_only
 def test_null_and_misaligned_pointers_are_rejected():
     d = _desc()
     with pytest.raises(N.PaError) as e:
@@ -91,6 +106,61 @@ def test_null_and_misaligned_pointers_are_rejected():
     # zero rows / pairs: nothing to enqueue
     N.pa_kv_append_tokens(d, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, FAKE, None, 0)
     N.pa_block_copy(d, FAKE, FAKE, 0, 0, None, 0)
+
+
+@host_only
+def test_step_and_prefill_calls_reject_bad_arguments_on_the_host():
+    """The combined calls check every argument (attention and append alike) before anything is
+    enqueued; every call below returns from those checks (no device work, no CUDA call)."""
+    nan = float("nan")
+    pf = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128)
+    # pa_prefill_step(desc, out, q, k, v, k_new, v_new, n, seq, pos, tables, q_start, ctx, max_q, scale)
+    good = dict(out=FAKE, q=FAKE, k_new=FAKE, v_new=FAKE, n=5, seq=FAKE, pos=FAKE, max_q=16, scale=0.1)
+    bad = [
+        (dict(scale=nan), N.PA_ERR_INVALID_ARG),
+        (dict(max_q=-1), N.PA_ERR_INVALID_ARG),
+        (dict(out=0), N.PA_ERR_INVALID_ARG),
+        (dict(q=FAKE + 8), N.PA_ERR_INVALID_ARG),
+        (dict(k_new=0), N.PA_ERR_INVALID_ARG),      # an append argument
+        (dict(seq=0), N.PA_ERR_INVALID_ARG),
+        (dict(n=-1), N.PA_ERR_INVALID_ARG),
+    ]
+    for kw, status in bad:
+        a = dict(good, **kw)
+        with pytest.raises(N.PaError) as e:
+            N.pa_prefill_step(pf, a["out"], a["q"], FAKE, FAKE, a["k_new"], a["v_new"], a["n"], a["seq"], a["pos"],
+                              FAKE, FAKE, FAKE, a["max_q"], a["scale"], None, 0)
+        assert e.value.status == status, kw
+    quant = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, k_dtype="e4m3", v_dtype="int8",
+                  k_scales=FAKE, v_scales=FAKE)
+    for call in (lambda d: N.pa_prefill_step(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 5, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                             16, 0.1, None, 0),
+                 lambda d: N.pa_prefill_attention(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 0.1, None, 0)):
+        with pytest.raises(N.PaError) as e:
+            call(quant)
+        assert e.value.status == N.PA_ERR_UNSUPPORTED
+    # pa_decode_step with fixed partitions (its plan needs no device query)
+    dd = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, num_seqs=4)
+    ws = N.pa_decode_workspace_size(dd, 1000, 512)
+    assert ws > 0
+    ws_ptr = 1 << 24  # 256-byte aligned
+    # pa_decode_step(desc, out, q, k, v, k_new, v_new, tables, positions, ctx, max_ctx, scale, part, ws, bytes)
+    good = dict(q=FAKE, pos=FAKE, scale=0.1, part=512, ws=ws_ptr, nbytes=ws, k_new=FAKE)
+    bad = [
+        (dict(scale=nan), N.PA_ERR_INVALID_ARG),
+        (dict(pos=0), N.PA_ERR_INVALID_ARG),
+        (dict(q=FAKE + 8), N.PA_ERR_INVALID_ARG),
+        (dict(part=100), N.PA_ERR_INVALID_ARG),     # not a multiple of 16
+        (dict(ws=ws_ptr + 16), N.PA_ERR_INVALID_ARG),
+        (dict(nbytes=ws - 1), N.PA_ERR_WORKSPACE_TOO_SMALL),
+        (dict(k_new=0), N.PA_ERR_INVALID_ARG),      # an append argument
+    ]
+    for kw, status in bad:
+        a = dict(good, **kw)
+        with pytest.raises(N.PaError) as e:
+            N.pa_decode_step(dd, FAKE, a["q"], FAKE, FAKE, a["k_new"], FAKE, FAKE, a["pos"], FAKE, 1000, a["scale"],
+                             a["part"], a["ws"], a["nbytes"], None, 0)
+        assert e.value.status == status, kw
 
 
 def test_workspace_size_fixed_partitions():
