@@ -75,6 +75,9 @@ host_only = pytest.mark.skipif(not _no_gpu(), reason="fake device addresses: run
     (dict(k_dtype="bf16", v_dtype="int8"), N.PA_ERR_UNSUPPORTED),
     (dict(k_dtype=7), N.PA_ERR_INVALID_ARG),
     (dict(num_sink=4), N.PA_ERR_INVALID_ARG),  # sinks without buffers
+    # INT4 needs head_dim 128 and an even number of KV heads
+    (dict(k_dtype=N.PA_INT4, v_dtype=N.PA_INT4, num_q_heads=6, num_kv_heads=3, head_dim=128), N.PA_ERR_UNSUPPORTED),
+    (dict(k_dtype=N.PA_INT4, v_dtype=N.PA_INT4, head_dim=64), N.PA_ERR_UNSUPPORTED),
 ])
 @host_only
 def test_bad_descriptions_are_rejected_on_the_host(kw, status):

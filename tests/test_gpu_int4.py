@@ -77,13 +77,3 @@ def test_int4_copy_on_write_carries_parameters():
     assert_pools_equal(g, o)
 
 
-def test_int4_unsupported_shapes_are_rejected():
-    for kw in (dict(num_kv_heads=3, num_q_heads=6), dict(head_dim=64)):
-        base = dict(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, num_blocks=8, max_blocks_per_seq=4,
-                    k_dtype=N.PA_INT4, v_dtype=N.PA_INT4)
-        base.update(kw)
-        d = N.make_desc(**base)
-        assert N.pa_decode_workspace_size(d, 16, 0) == 0
-        with pytest.raises(N.PaError) as e:
-            N.pa_kv_append(d, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, None, 0)
-        assert e.value.status == N.PA_ERR_UNSUPPORTED
