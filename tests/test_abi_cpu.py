@@ -36,6 +36,20 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, name), name
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/pa.h is a C header: it compiles as strict C99 on its own (no C++, no CUDA types)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "pa.h"\nint main(void) { pa_cache_desc d; (void)d; return 0; }\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_status_strings():
     assert N.status_string(0) == "PA_OK"
     assert N.status_string(3) == "PA_ERR_WORKSPACE_TOO_SMALL"
