@@ -70,6 +70,16 @@ const Sha256Consts& sha256_consts() {
 
 inline uint32_t rotr(uint32_t x, int n) { return (x >> n) | (x << (32 - n)); }
 
+// One round of FIPS 180-4 §6.2.2 step 3 with the working variables renamed instead of shifted:
+// the caller rotates the argument order, so only d and h change (d += T1, h = T1 + T2).
+inline void sha256_round(uint32_t a, uint32_t b, uint32_t c, uint32_t& d, uint32_t e, uint32_t f, uint32_t g,
+                         uint32_t& h, uint32_t kw) {
+  const uint32_t t1 = h + (rotr(e, 6) ^ rotr(e, 11) ^ rotr(e, 25)) + ((e & f) ^ (~e & g)) + kw;
+  const uint32_t t2 = (rotr(a, 2) ^ rotr(a, 13) ^ rotr(a, 22)) + ((a & b) ^ (a & c) ^ (b & c));
+  d += t1;
+  h = t1 + t2;
+}
+
 void sha256_block(uint32_t st[8], const uint8_t* blk, const uint32_t* k) {
   uint32_t w[64];
   for (int t = 0; t < 16; ++t)
@@ -81,21 +91,15 @@ void sha256_block(uint32_t st[8], const uint8_t* blk, const uint32_t* k) {
     w[t] = s1 + w[t - 7] + s0 + w[t - 16];
   }
   uint32_t a = st[0], b = st[1], c = st[2], d = st[3], e = st[4], f = st[5], g = st[6], h = st[7];
-  for (int t = 0; t < 64; ++t) {
-    const uint32_t S1 = rotr(e, 6) ^ rotr(e, 11) ^ rotr(e, 25);
-    const uint32_t ch = (e & f) ^ (~e & g);
-    const uint32_t t1 = h + S1 + ch + k[t] + w[t];
-    const uint32_t S0 = rotr(a, 2) ^ rotr(a, 13) ^ rotr(a, 22);
-    const uint32_t maj = (a & b) ^ (a & c) ^ (b & c);
-    const uint32_t t2 = S0 + maj;
-    h = g;
-    g = f;
-    f = e;
-    e = d + t1;
-    d = c;
-    c = b;
-    b = a;
-    a = t1 + t2;
+  for (int t = 0; t < 64; t += 8) {  // eight rounds bring the names back to their places
+    sha256_round(a, b, c, d, e, f, g, h, k[t] + w[t]);
+    sha256_round(h, a, b, c, d, e, f, g, k[t + 1] + w[t + 1]);
+    sha256_round(g, h, a, b, c, d, e, f, k[t + 2] + w[t + 2]);
+    sha256_round(f, g, h, a, b, c, d, e, k[t + 3] + w[t + 3]);
+    sha256_round(e, f, g, h, a, b, c, d, k[t + 4] + w[t + 4]);
+    sha256_round(d, e, f, g, h, a, b, c, k[t + 5] + w[t + 5]);
+    sha256_round(c, d, e, f, g, h, a, b, k[t + 6] + w[t + 6]);
+    sha256_round(b, c, d, e, f, g, h, a, k[t + 7] + w[t + 7]);
   }
   st[0] += a; st[1] += b; st[2] += c; st[3] += d;
   st[4] += e; st[5] += f; st[6] += g; st[7] += h;
