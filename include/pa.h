@@ -252,8 +252,11 @@ pa_status pa_prefill_step(const pa_cache_desc* desc, void* out, const void* q, v
  * decode step.  It takes the same arguments minus the workspace, and runs the same kernels with
  * their scratch in a static 8 MiB device array that every GPU which loads this library holds
  * until the process exits.
- *   - The first call on a device looks the array's address up (cudaGetSymbolAddress, with that
- *     device current); make that first call before any stream capture on the device.
+ *   - The first call in a context looks the array's address up (cudaGetSymbolAddress, with that
+ *     device current) and keeps it under the context's unique id; make that first call before any
+ *     stream capture on the device.  A new context on the device (after cudaDeviceReset, or
+ *     another context made current) gets its own lookup on its first call, never an address
+ *     kept from an earlier one.
  *   - A problem whose pa_decode_workspace_size() exceeds 8 MiB (8388608 bytes) is rejected
  *     with PA_ERR_WORKSPACE_TOO_SMALL and nothing is enqueued.
  *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library routine.

@@ -1,9 +1,80 @@
-// Status strings and cache-description checks shared by every entry point.
+// Status strings, cache-description checks and per-device launch state shared by every entry point.
+#include <cudaTypedefs.h>
+
 #include <climits>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "pa_internal.h"
 
 namespace pa {
+
+namespace {
+
+// The driver's context calls, through the runtime's entry-point lookup (no link to libcuda).
+struct CtxCalls {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+
+const CtxCalls& ctx_calls() {
+  static CtxCalls calls;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      calls.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      calls.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(ptr);
+  });
+  return calls;
+}
+
+std::mutex g_launch_mu;
+std::map<int, std::pair<unsigned long long, int>> g_sms;                         // device -> (context, SMs)
+std::map<std::pair<const void*, unsigned long long>, size_t> g_smem_set;          // (kernel, context) -> bytes
+
+}  // namespace
+
+unsigned long long current_ctx_id() {
+  const CtxCalls& c = ctx_calls();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!c.get_current || !c.get_id || c.get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (c.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+int sm_count_current() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const unsigned long long ctx = current_ctx_id();
+  std::lock_guard<std::mutex> lock(g_launch_mu);
+  auto it = g_sms.find(dev);
+  if (ctx != 0 && it != g_sms.end() && it->second.first == ctx) return it->second.second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (ctx != 0) g_sms[dev] = {ctx, n};
+  return n;
+}
+
+bool ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  const unsigned long long ctx = current_ctx_id();
+  std::lock_guard<std::mutex> lock(g_launch_mu);
+  if (ctx != 0) {
+    auto it = g_smem_set.find({kernel, ctx});
+    if (it != g_smem_set.end() && it->second >= bytes) return true;
+  }
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+      cudaSuccess)
+    return false;
+  if (ctx != 0) g_smem_set[{kernel, ctx}] = bytes;
+  return true;
+}
 
 pa_status validate_desc(const pa_cache_desc* d) {
   if (!d) return PA_ERR_INVALID_ARG;

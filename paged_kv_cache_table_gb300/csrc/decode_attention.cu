@@ -1103,12 +1103,6 @@ struct Plan {
   size_t smem_bytes, meta_bytes, ws_bytes, n_slots;
 };
 
-int num_sms_current() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
 
 pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Plan* pl) {
   pa_status st = validate_desc(d);
@@ -1143,8 +1137,9 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
     pl->ppb = 0;
     pl->max_parts = 0;
     // one wave: every head group gets an equal share of the resident CTAs
-    pl->grid_x = std::max(1, num_sms_current() * PA_CTAS_PER_SM / pl->n_hg);
-    if (num_sms_current() <= 0) return PA_ERR_CUDA;
+    const int sms = sm_count_current();
+    if (sms <= 0) return PA_ERR_CUDA;
+    pl->grid_x = std::max(1, sms * PA_CTAS_PER_SM / pl->n_hg);
     pl->n_slots = static_cast<size_t>(B) + pl->grid_x;
     pl->meta_bytes = ((static_cast<size_t>(B) + 2) * 4 + 255) / 256 * 256;
   } else {
@@ -1182,16 +1177,14 @@ pa_status launch(const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv, c
   } else if constexpr (KIND == 2) {
     if (pl.warps_c <= 12) kern = decode_kernel<D, KIND, 12>;
   }
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(pl.smem_bytes)) != cudaSuccess)
-    return PA_ERR_CUDA;
+  if (!ensure_dynamic_smem(reinterpret_cast<const void*>(kern), pl.smem_bytes)) return PA_ERR_CUDA;
   const dim3 grid = p.mode == 0 ? dim3(pl.grid_x, pl.n_hg, 1) : dim3(pl.max_parts, p.B, pl.n_hg);
   // Both kernels may start while their predecessor drains (the decode prologue overlaps the
   // append; the merge launch overlaps the decode tail); each waits before reading its inputs.
   if (launch_overlapped(kern, grid, dim3(pl.threads), pl.smem_bytes, stream, mk, mv, mkp, mvp, p) != PA_OK)
     return PA_ERR_CUDA;
   // few (sequence, head) rows for the SMs (long contexts, small batches): four warps per row
-  if (static_cast<long long>(p.B) * p.H_q < 4LL * std::max(1, num_sms_current()))
+  if (static_cast<long long>(p.B) * p.H_q < 4LL * std::max(1, sm_count_current()))
     return launch_overlapped(merge_kernel<D, 4>, dim3(p.B, p.H_q), dim3(128), 0, stream, p, pl.grid_x);
   return launch_overlapped(merge_kernel<D, 1>, dim3(p.B, (p.H_q + 3) / 4), dim3(128), 0, stream, p, pl.grid_x);
 }
@@ -1340,20 +1333,32 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id;  // the context the address belongs to
+  void* ptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once per device.
+// Device address of the scratch array in the current context of the current device.  It is looked
+// up (cudaGetSymbolAddress, with the device current) the first time a context is seen and kept
+// under that context's id, so a new context on the device (after cudaDeviceReset, or another
+// context made current) gets a fresh lookup rather than an address of a module that is gone.
 pa_status static_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return PA_ERR_CUDA;
-    g_scratch_addr[dev] = ptr;
+  const unsigned long long id = current_ctx_id();
+  if (id != 0 && g_scratch_addr[dev].ptr && g_scratch_addr[dev].ctx_id == id) {
+    *out = g_scratch_addr[dev].ptr;
+    return PA_OK;
   }
-  *out = g_scratch_addr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return PA_ERR_CUDA;
+  // the lookup makes the device's primary context current if none was: ask again
+  const unsigned long long id_now = id != 0 ? id : current_ctx_id();
+  g_scratch_addr[dev] = {id_now, id_now != 0 ? ptr : nullptr};
+  *out = ptr;
   return PA_OK;
 }
 

@@ -49,6 +49,17 @@ bool encode_query_map(CUtensorMap* map, const void* base, int heads, int G, int 
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Unique id of the calling thread's current CUDA context (never reused within a process), or 0
+// when there is none yet or the driver cannot tell (api.cpp).
+unsigned long long current_ctx_id();
+
+// SMs of the current device, looked up once per context (0 on failure).
+int sm_count_current();
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` in the current context; the
+// runtime call is made only when a (kernel, context) pair needs more than it was given before.
+bool ensure_dynamic_smem(const void* kernel, size_t bytes);
+
 // The tcgen05 chunked-prefill kernel (prefill_tc.cu): head_dim 128 and a power-of-two number of
 // query heads per KV head; arguments as pa_prefill_attention after its checks.
 // step: the previous kernel on the stream is the append of this prefill step (it writes only
