@@ -7,20 +7,19 @@
 // window (ldpk §5.3).
 //
 // Design (head_dim 128, G = 1, 2, 4 or 8 query heads per KV head):
-//  * Work items.  An item is (sequence, cluster tile c, KV head): the query rows of 2 x 2 query
-//    tiles of 128 rows, a row being (token, query head), held by a cluster of two CTAs; a CTA's
-//    two query tiles share every K/V tile, and the cluster loads each K/V tile once: every CTA
-//    copies half of the tile's boxes with TMA multicast into both CTAs' shared memory.  Measured,
-//    one SM ingests only about 15-30 bytes per cycle of scattered 2 KB blocks (copy engine or
-//    cp.async alike), so halving what each SM fetches per flop is what feeds the tensor core.
-//  * Persistent clusters, longest first.  The grid is as many clusters as can be resident, each
-//    walking its own list of items.  An item's work grows with the last key it reads, which for
-//    the c-th cluster tile of a sequence is first_pos + min(n, (c + 1) W) (W query tokens per
-//    cluster tile): an arithmetic progression per sequence.  So the number of items whose last
-//    key is at least X has a closed form per sequence, every item's rank in the longest-first
-//    order is a sum over sequences, and the clusters rank all items in parallel at start-up
-//    (no sort, no scratch memory), dealing the ranks to clusters round by round, alternately in
-//    order and in reverse.  Barriers, TMEM and the ring phases carry across items.
+//  * Work items.  An item is (sequence, tile c, KV head): the query rows of two query tiles of
+//    128 rows, a row being (token, query head), i.e. 256 / G query tokens, held by one CTA.  Both
+//    query tiles share every K/V tile the CTA loads, so each 32 KiB K or V tile feeds four
+//    128 x 128 x 128 products.  Each CTA loads its own tiles from its own GPU's pool with plain
+//    TMA boxes; the CTAs that read the same keys (the tiles of one sequence) meet in L2.
+//  * Persistent CTAs, longest first.  The grid is as many CTAs as can be resident, each walking
+//    its own list of items.  An item's work grows with the last key it reads, which for the c-th
+//    tile of a sequence is first_pos + min(n, (c + 1) W) (W query tokens per tile): an
+//    arithmetic progression per sequence.  So the number of items whose last key is at least X
+//    has a closed form per sequence, every item's rank in the longest-first order is a sum over
+//    sequences, and the CTAs rank all items in parallel at start-up (no sort, no scratch
+//    memory), dealing the ranks to CTAs round by round, alternately in order and in reverse.
+//    Barriers, TMEM and the ring phases carry across items.
 //  * S = Q·Kᵀ and O += P·V are tcgen05.mma (kind::f16, bf16 operands, M = N = 128, fp32
 //    accumulators in TMEM: S0, S1, O0, O1 in 4 x 128 columns), issued by one thread.  Q and K are
 //    K-major and V MN-major shared-memory operands with the 128-byte swizzle; P goes back into
@@ -34,9 +33,8 @@
 //    three-stage ring (a V tile is needed only at P·V, after the softmax, so V is fetched further
 //    ahead, and on its own warp its waits never hold back the next K tile), and a third loads the
 //    next item's query tiles by TMA (a 4-D map over q) as soon as the current item's last S
-//    products have completed.  A ring stage is released to the copy warps of both CTAs by a
-//    multicast tcgen05.commit from each CTA's MMA thread, so it is refilled only when both CTAs are
-//    done with it, and only when a later copy waits for it.
+//    products have completed.  A ring stage is released to its copy warp by a tcgen05.commit of
+//    the MMA thread once every product reading it has completed.
 //  * Two softmax warpgroups (one per query tile) own one query row per thread through TMEM
 //    lanes: they read S, mask (causal, window) only on tiles that cross a row's edge, keep the
 //    running maximum (moved only when a score exceeds it by 2^8), write P as bf16 into TMEM, and
@@ -45,12 +43,13 @@
 //    the context are zeroed before P·V reads them, so bits left in unused slots (NaN included)
 //    cannot leak.
 //  * Output: O / l as bf16 is staged in the idle ring stage of the item's last tile (K for query
-//    tile 0, V for query tile 1) and stored by TMA; the stage is then released to both CTAs'
-//    copy warps.  Only a tile holding rows past its sequence is stored row by row.
+//    tile 0, V for query tile 1) and stored by TMA; the stage is then released to its copy warp.
+//    Only a tile holding rows past its sequence is stored row by row.
 //  * Launched with programmatic dependent launch.  In a prefill step (pa_prefill_step) the
 //    previous kernel is the chunk's append, which writes only K/V slots, so only the K/V copy
 //    warps wait for it; the work ranking and the query copies run alongside it.
-//  * Every wait is bounded; TMEM is released on every path.
+//  * Every wait is bounded; TMEM is released on every path, and no warp leaves while a copy it
+//    issued into this CTA's shared memory may still be in flight.
 
 #include <algorithm>
 #include <cmath>
@@ -69,8 +68,8 @@ constexpr int kKOff = kQOff + 2 * kTile;        // K stages 0, 1
 constexpr int kVOff = kKOff + 2 * kTile;        // V stages 0, 1, 2
 constexpr int kVStages = 3;
 constexpr int kBarOff = kVOff + kVStages * kTile;
-constexpr int kMaxItems = 64;                   // work items of one cluster (the launch makes enough clusters)
-constexpr int kListOff = kBarOff + 256;         // barriers, then the cluster's item list
+constexpr int kMaxItems = 64;                   // work items of one CTA (the launch makes enough CTAs)
+constexpr int kListOff = kBarOff + 256;         // barriers, then the CTA's item list
 constexpr int kTcSmem = kListOff + kMaxItems * 24 + 1024;  // and slack for 1024-byte alignment
 constexpr int kQMapTokens = 1 << 24;            // token extent of the Q tensor map (rows past it: plain copies)
 constexpr uint32_t kTmemCols = 512;             // S0 0..127, S1 128..255, O0 256..383, O1 384..511
@@ -196,18 +195,10 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // This thread's bulk stores have read their shared memory (reads) or completed (all).
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Arrive on the mbarrier at `bar`'s offset in the CTA of the cluster with the given rank.
-__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, int cta_rank) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, %1;\n\t"
-      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
-      "r"(cta_rank)
-      : "memory");
-}
 __device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
-// Query rows of sequence s in clusters of W = 2^lw tokens: fp = first new position, n rows (those
-// of an invalid sequence are only zeroed), nc clusters.
+// Query rows of sequence s in tiles of W = 2^lw tokens: fp = first new position, n rows (those
+// of an invalid sequence are only zeroed), nc tiles.
 struct alignas(16) SeqGeo {
   int fp, n, nc, valid;
 };
@@ -221,46 +212,23 @@ __device__ __forceinline__ SeqGeo seq_geo(const TcParams& p, int s, int lw) {
   g.nc = (g.n + (1 << lw) - 1) >> lw;
   return g;
 }
-// Clusters of one sequence whose key is >= X (X >= 1).  The key of cluster c, strictly increasing
-// in c, is the last key it reads, fp + min(n, (c + 1) W), or c + 1 for an invalid sequence.
+// Tiles of one sequence whose key is >= X (X >= 1).  The key of tile c, strictly increasing in c,
+// is the last key it reads, fp + min(n, (c + 1) W), or c + 1 for an invalid sequence.
 __device__ __forceinline__ int count_ge(const SeqGeo& g, int X, int lw) {
   if (!g.valid) return min(g.nc, max(g.nc - (X - 1), 0));
   if (g.nc == 0 || X > g.fp + g.n) return 0;
-  const int d = X - g.fp;  // clusters c < nc - 1 with fp + (c + 1) W < X lie below X
+  const int d = X - g.fp;  // tiles c < nc - 1 with fp + (c + 1) W < X lie below X
   const int below = d <= 0 ? 0 : min(((d + (1 << lw) - 1) >> lw) - 1, g.nc - 1);
   return g.nc - below;
 }
-// Both CTAs of the cluster: every thread arrives, then waits for every thread of the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// TMA box copied into the same shared-memory offset of every CTA in `mask`, each of whose
-// mbarrier at `bar`'s offset receives the bytes.
-__device__ __forceinline__ void tma_load_3d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                               int c2, uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(mask), "l"(policy)
-      : "memory");
-}
-// tcgen05.commit arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   smem_u32(bar)),
-               "h"(mask)
-               : "memory");
-}
-
-// One work item of a cluster: the query rows of cluster tile c of sequence s (tokens
-// [2 tpc c, 2 tpc (c + 1)), tpc tokens per CTA) against KV head h_kv.  This CTA holds tokens
-// [t0, t_end) in two query tiles of tpq tokens; the cluster reads the keys [kv_lo, kv_end),
-// blocks [kb0, kb_end), in n_tiles tiles of 8 blocks.
+// One work item of a CTA: the query rows of tile c of sequence s (tokens [t0, t_end) with
+// t0 = c tpc, tpc = 2 tpq tokens per tile) against KV head h_kv, in two query tiles of tpq tokens;
+// the CTA reads the keys [kv_lo, kv_end), blocks [kb0, kb_end), in n_tiles tiles of 8 blocks.
 struct Item {
   int s, h_kv, tile, qs, n, t0, t_end, first_pos, kv_lo, kb0, kb_end, n_tiles, loaded_end;
   bool valid, has0, has1;
 };
-// An entry of a cluster's item list (shared memory): the sequence, the cluster tile and KV head
+// An entry of a CTA's item list (shared memory): the sequence, the tile and KV head
 // (c << 16 | h), and the sequence's first query row, query rows and context length.
 struct ItemRec {
   int s, ch, qs, n, ctx, pad;
@@ -275,27 +243,25 @@ __device__ __forceinline__ ItemRec item_rec(const TcParams& p, int s, int c, int
   e.pad = 0;
   return e;
 }
-__device__ __forceinline__ Item make_item(const TcParams& p, const ItemRec& e, int rank) {
+__device__ __forceinline__ Item make_item(const TcParams& p, const ItemRec& e) {
   Item it;
   it.s = e.s;
-  const int ctile = e.ch >> 16;
+  it.tile = e.ch >> 16;
   it.h_kv = e.ch & 0xFFFF;
   const int tpc = 2 * p.tpq;
-  it.tile = 2 * ctile + rank;
   it.qs = e.qs;
   it.n = e.n;
   const int ctx = e.ctx;
   it.valid = it.n >= 0 && it.n <= ctx && it.n <= p.max_q && ctx <= p.max_blocks * PA_BLOCK_SIZE;
-  const int tc0 = 2 * ctile * tpc;
   it.t0 = it.tile * tpc;
   it.has0 = it.valid && it.t0 < it.n;
   it.has1 = it.valid && it.t0 + p.tpq < it.n;
   it.first_pos = ctx - it.n;
   it.t_end = min(it.n, it.t0 + tpc);
   it.kv_lo = it.kb0 = it.kb_end = it.n_tiles = it.loaded_end = 0;
-  if (it.valid && tc0 < it.n) {
-    const int kv_end = it.first_pos + min(it.n, tc0 + 2 * tpc);
-    it.kv_lo = p.window > 0 ? max(0, it.first_pos + tc0 - p.window + 1) : 0;
+  if (it.has0) {
+    const int kv_end = it.first_pos + it.t_end;
+    it.kv_lo = p.window > 0 ? max(0, it.first_pos + it.t0 - p.window + 1) : 0;
     it.kb0 = it.kv_lo / PA_BLOCK_SIZE;
     it.kb_end = (kv_end + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
     it.n_tiles = (it.kb_end - it.kb0 + 7) / 8;
@@ -304,9 +270,9 @@ __device__ __forceinline__ Item make_item(const TcParams& p, const ItemRec& e, i
   return it;
 }
 
-// Launch position pos of round r of a cluster: rounds deal NC positions each, alternately in
-// cluster order and in reverse, so that the longest items of one round and the shortest of the
-// next land on the same cluster.
+// Launch position pos of round r of a CTA: rounds deal NC positions each, alternately in CTA
+// order and in reverse, so that the longest items of one round and the shortest of the next land
+// on the same CTA.
 __device__ __forceinline__ int round_pos(int r, int NC, int cid) { return r * NC + ((r & 1) ? NC - 1 - cid : cid); }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -329,28 +295,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* p_half = bars + 24;  // [2] P of the tile's first 64 keys is in TMEM
   uint64_t* drain = bars + 20;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
-  int* flags = reinterpret_cast<int*>(bars + 22);  // [0] work items of all clusters, [1] a wait gave up
-  ItemRec* list = reinterpret_cast<ItemRec*>(sm + kListOff);  // this cluster's items, in order
+  int* flags = reinterpret_cast<int*>(bars + 22);  // [0] tiles of all sequences, [1] a wait gave up
+  ItemRec* list = reinterpret_cast<ItemRec*>(sm + kListOff);  // this CTA's items, in order
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rank = blockIdx.x & 1, cid = blockIdx.x >> 1, NC = gridDim.x >> 1;
-  const int tpc = 2 * p.tpq;                 // tokens per CTA
-  const int lw = 31 - __clz(2 * tpc);        // W = 2 tpc = 512 / G query tokens per cluster tile
+  const int cid = blockIdx.x, NC = gridDim.x;
+  const int tpc = 2 * p.tpq;                 // W = tpc = 256 / G query tokens per tile (a power of two)
+  const int lw = 31 - __clz(tpc);
   const int nclx = (p.max_q + (1 << lw) - 1) >> lw;
   const bool lpt = p.B <= kMaxOrderSeqs;
-  constexpr uint16_t kBoth = 0x3;
-  SeqGeo* geo = reinterpret_cast<SeqGeo*>(sm + kKOff);  // scratch: the K ring is idle until the cluster barrier
+  SeqGeo* geo = reinterpret_cast<SeqGeo*>(sm + kKOff);  // scratch: the K ring is idle until the items are listed
 
   if (tid == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 2);  // released by the MMA threads of both CTAs
+      mbar_init(&v_empty[i], 1);  // released by the MMA thread (or the output's store)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 2);
+      mbar_init(&k_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&p_half[i], 128);
@@ -383,7 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   // Work items longest first: item (s, c) of key k sits at rank = #items of larger key + #items of
   // key k in earlier sequences; with KV heads innermost, launch position = rank * H_kv + h.
-  // Many sequences: last cluster tiles first, sequences in order (slots past a sequence are empty).
+  // Many sequences: last tiles first, sequences in order (slots past a sequence are empty).
   const int p_tot = lpt ? flags[0] * p.H_kv : p.B * nclx * p.H_kv;
   const int rounds = (p_tot + NC - 1) / NC;
   const int n_items = min(kMaxItems, rounds == 0 ? 0 : rounds - 1 + (round_pos(rounds - 1, NC, cid) < p_tot ? 1 : 0));
@@ -410,8 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       list[r] = item_rec(p, slot % p.B, nclx - 1 - slot / p.B, h);
     }
   }
-  __syncthreads();
-  cluster_sync();  // the peer's barriers exist before any multicast reaches them; scratch is done
+  __syncthreads();  // the list is complete and the K ring is free again
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -421,9 +385,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t policy;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
     bool ok = true;
-    int g = 0;  // tiles of the cluster so far: ring stage and phase
+    int g = 0;  // tiles of this CTA so far: ring stage and phase
     for (int ii = 0; ok && ii < n_items; ++ii) {
-      const Item it = make_item(p, list[ii], rank);
+      const Item it = make_item(p, list[ii]);
       if (it.n_tiles == 0) continue;
       const int32_t* row = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks;
       const int kb0 = it.kb0, kb_end = it.kb_end;
@@ -444,8 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return cb == c0 ? v0 : v1;
       };
       // 8 blocks from tile-relative block blk0, boxes of 16 slots x 128 bytes, one per lane:
-      // block lane / 2, 64-dim half lane % 2.  Both CTAs count every box of the tile; each copies
-      // the half of the blocks that its rank owns, to both.  Returns false when a wait gave up.
+      // block lane / 2, 64-dim half lane % 2.  Returns false when a wait gave up.
       auto load = [&](int blk0, const CUtensorMap* map, uint64_t* full, uint64_t* empty, uint32_t parity,
                       uint8_t* dst) -> bool {
         if (!warp_wait(empty, parity)) return false;
@@ -467,12 +430,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           else mbar_arrive(full);
         }
         __syncwarp();
-        if (pb >= 0 && bi / 4 == rank)
-          tma_load_3d_mc(dst + half * kHalf + bi * 2048, map, full, 0, it.h_kv * 2 + half, pb * PA_BLOCK_SIZE, kBoth,
-                         policy);
+        if (pb >= 0) tma_load_3d(dst + half * kHalf + bi * 2048, map, full, 0, it.h_kv * 2 + half, pb * PA_BLOCK_SIZE, policy);
         return true;
       };
-      for (int k = 0; ok && k < it.n_tiles; ++k, ++g) {
+      for (int k = 0; ok && k < it.n_tiles; ++k) {
         if (warp == 0) {
           ok = load(8 * k, &tmK, &k_full[g & 1], &k_empty[g & 1], (static_cast<uint32_t>(g >> 1) & 1u) ^ 1u,
                     sm + kKOff + (g & 1) * kTile);
@@ -481,7 +442,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = load(8 * k, &tmV, &v_full[st], &v_empty[st], (static_cast<uint32_t>(g / kVStages) & 1u) ^ 1u,
                     sm + kVOff + st * kTile);
         }
+        if (ok) ++g;
       }
+    }
+    // do not leave while a copy into this CTA's shared memory may still be in flight (the MMA
+    // thread waits for every tile, unless one of its own waits gave up)
+    const int S = warp == 0 ? 2 : kVStages;
+    uint64_t* full = warp == 0 ? k_full : v_full;
+    for (int st = 0; st < S && st < g; ++st) {
+      const int last = st + S * ((g - 1 - st) / S);
+      if (!warp_wait(&full[st], static_cast<uint32_t>(last / S) & 1u)) ok = false;
     }
     if (!ok && lane == 0) flags[1] = 1;
   } else if (warp == 3) {
@@ -498,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int qi = 0;
     const int c = lane & 15;
     for (int ii = 0; ok && ii < n_items; ++ii) {
-      const Item it = make_item(p, list[ii], rank);
+      const Item it = make_item(p, list[ii]);
       if (it.n_tiles == 0) continue;
       if (!(ok = warp_wait(q_empty, (static_cast<uint32_t>(qi) & 1u) ^ 1u))) break;
       ++qi;
@@ -538,6 +508,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
+    // the last query copies have landed before the warp leaves
+    if (qi > 0 && !warp_wait(q_full, static_cast<uint32_t>(qi - 1) & 1u)) ok = false;
     if (!ok && lane == 0) flags[1] = 1;
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
@@ -562,23 +534,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     kIdescPV, (!first || kk > 0) ? 1u : 0u);
         }
       };
-      // A ring stage is released (in both CTAs) only when a later copy of the cluster waits for
-      // it: every such arrival is consumed before either CTA can finish, so none lands in a CTA
-      // that has left.  The K stage of tile m is refilled with tile m + 2, the V stage of tile m
-      // with tile m + 3, counting the tiles of all the cluster's items in order.  The K and V
-      // stages of an item's last tile stage the output of query tiles 0 and 1 when those hold
-      // rows, and their groups release them after it has left; otherwise they are released here.
+      // A ring stage is released only when a later copy waits for it.  The K stage of tile m is
+      // refilled with tile m + 2, the V stage of tile m with tile m + 3, counting the tiles of all
+      // the CTA's items in order.  The K and V stages of an item's last tile stage the output of
+      // query tiles 0 and 1 when those hold rows, and their groups release them after it has
+      // left; otherwise they are released here.
       int g_tot = 0;
-      for (int ii = 0; ii < n_items; ++ii) g_tot += make_item(p, list[ii], rank).n_tiles;
+      for (int ii = 0; ii < n_items; ++ii) g_tot += make_item(p, list[ii]).n_tiles;
       bool ok = true;
       int g = 0, qi = 0;
       uint32_t sp[2] = {0u, 0u};  // tiles of each query tile so far: s_full / p_full / o_done phase
       for (int ii = 0; ok && ii < n_items; ++ii) {
-        const Item it = make_item(p, list[ii], rank);
+        const Item it = make_item(p, list[ii]);
         const int nt = it.n_tiles;
         if (nt == 0) continue;
-        // query tiles of this CTA with rows (a CTA without any still joins every copy and release)
-        const int groups = it.has1 ? 2 : (it.has0 ? 1 : 0);
+        const int groups = it.has1 ? 2 : 1;  // query tiles with rows (an item with tiles has rows)
         ok = mbar_wait(q_full, static_cast<uint32_t>(qi) & 1u) &&
              mbar_wait(&k_full[g & 1], static_cast<uint32_t>(g >> 1) & 1u);
         ++qi;
@@ -586,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         for (int w = 0; w < groups; ++w) issue_s(w, g & 1);
         if (nt == 1) tc_commit(q_empty);  // the item's last products that read Q are issued
-        if (g + 2 < g_tot && (nt > 1 || groups == 0)) tc_commit_mc(&k_empty[g & 1], kBoth);
+        if (g + 2 < g_tot && nt > 1) tc_commit(&k_empty[g & 1]);
         for (int k = 0; k < nt; ++k) {
           const int gk = g + k;
           const bool next = k + 1 < nt;
@@ -608,8 +578,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           if (!ok) break;
           if (k == nt - 2) tc_commit(q_empty);
-          if (gk + kVStages < g_tot && (next || groups < 2)) tc_commit_mc(&v_empty[vs], kBoth);
-          if (next && gk + 3 < g_tot && (k + 2 < nt || groups == 0)) tc_commit_mc(&k_empty[(gk + 1) & 1], kBoth);
+          if (gk + kVStages < g_tot && (next || groups < 2)) tc_commit(&v_empty[vs]);
+          if (next && gk + 3 < g_tot && k + 2 < nt) tc_commit(&k_empty[(gk + 1) & 1]);
         }
         g += nt;
       }
@@ -629,12 +599,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tS = tmem + wg * 128 + lane_off, tO = tmem + 256 + wg * 128 + lane_off;
     const int tok = r / p.G, hh = r - tok * p.G;
     bool ok = true;
-    int g = 0;        // tiles of the cluster so far (V stage and phase)
+    int g = 0;        // tiles of this CTA so far (V stage and phase)
     uint32_t sp = 0;  // tiles of this query tile so far
-    int g_tot = 0;    // tiles of all the cluster's items (whether a later copy waits for a stage)
-    for (int ii = 0; ii < n_items; ++ii) g_tot += make_item(p, list[ii], rank).n_tiles;
+    int g_tot = 0;    // tiles of all the CTA's items (whether a later copy waits for a stage)
+    for (int ii = 0; ii < n_items; ++ii) g_tot += make_item(p, list[ii]).n_tiles;
     for (int ii = 0; ii < n_items; ++ii) {
-      const Item it = make_item(p, list[ii], rank);
+      const Item it = make_item(p, list[ii]);
       const int tq0 = it.t0 + wg * p.tpq;  // first token of this query tile
       uint4* orow = reinterpret_cast<uint4*>(
           p.out + (static_cast<size_t>(it.qs + tq0 + tok) * p.H_q + it.h_kv * p.G + hh) * D);
@@ -765,9 +735,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ring stage of the item's last tile that this group owns: K for query tile 0, V for 1.
       // o_done of the last tile follows every product of the CTA that reads either, so both are
       // idle.  One thread stores the tile with two TMA boxes (the copy engine, not the load/store
-      // unit, moves the bytes), waits until they have been read and releases the stage to the
-      // copies of both CTAs.  A tile that holds rows past its sequence is stored row by row
-      // instead (coalesced).
+      // unit, moves the bytes), waits until they have been read and releases the stage to its
+      // copy warp.  A tile that holds rows past its sequence is stored row by row instead
+      // (coalesced).
       if (ok) ok = warp_wait(&o_done[wg], (sp - 1u) & 1u);
       tc_fence_after();
       const float inv = (!ok || bad || !(l_run > 0.f)) ? 0.f : 1.f / l_run;
@@ -805,10 +775,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_store_4d(&tmO, stile + half * kHalf, 0, half, it.h_kv * p.G, it.qs + tq0);
           bulk_commit();
           bulk_wait_read();
-          if (release) {
-            mbar_arrive_cluster(rel, 0);
-            mbar_arrive_cluster(rel, 1);
-          }
+          if (release) mbar_arrive(rel);
         }
       } else {
         const int c = lane & 15;
@@ -822,10 +789,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 *reinterpret_cast<const uint4*>(stile + (c >> 3) * kHalf + rr * 128 + (((c & 7) ^ (rr & 7)) << 4));
         }
         group_sync(1 + wg);  // every row has been read back before the stage is released
-        if (quad == 0 && lane == 0 && release) {
-          mbar_arrive_cluster(rel, 0);
-          mbar_arrive_cluster(rel, 1);
-        }
+        if (quad == 0 && lane == 0 && release) mbar_arrive(rel);
       }
     }
     bulk_wait_all();  // this thread's output stores are complete
@@ -835,38 +799,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();  // no TMEM access is pending
   if (tid == 64 && flags[1] != 0) set_error(p.err, PA_EFLAG_TIMEOUT);
-  // neither CTA leaves while the other may still copy into its shared memory or release a stage
-  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-// Clusters of two that can run at once on the current device (persistent grid size).
-int resident_clusters() {
+// CTAs that can run at once on the current device (persistent grid size).
+int resident_ctas() {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
   if (dev < 64 && cached[dev] > 0) return cached[dev];
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = kTcSmem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_tc_kernel, kTcThreads, kTcSmem) != cudaSuccess ||
+      per_sm <= 0) {
     cudaGetLastError();
-    int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    n = sms / 2;
+    per_sm = 1;
   }
+  const int n = sms * per_sm;
   if (dev < 64) cached[dev] = n;
   return n;
 }
@@ -904,30 +856,26 @@ pa_status launch_prefill_tc(const pa_cache_desc* desc, void* out, const void* q,
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.err = err_flag;
-  if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
-    return PA_ERR_CUDA;
-  // Persistent clusters: as many as run at once, but no more than there are work items, and
-  // enough that none holds more than kMaxItems of them.
-  const long long w_tokens = 4LL * p.tpq;  // query tokens of one cluster tile
+  if (!ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_tc_kernel), kTcSmem)) return PA_ERR_CUDA;
+  // Persistent CTAs: as many as run at once, but no more than there are work items, and enough
+  // that none holds more than kMaxItems of them.
+  const long long w_tokens = 2LL * p.tpq;  // query tokens of one tile
   const long long items = static_cast<long long>(p.B) * ((max_query_len + w_tokens - 1) / w_tokens) * p.H_kv;
   if (items > (1LL << 30)) return PA_ERR_UNSUPPORTED;
-  long long nc = std::min<long long>(items, std::max(1, resident_clusters()));
+  long long nc = std::min<long long>(items, std::max(1, resident_ctas()));
   nc = std::max(nc, (items + kMaxItems - 1) / kMaxItems);
   nc = std::max(nc, 1LL);
+  if (nc > 0x7FFFFFFFLL) return PA_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * nc));
+  cfg.gridDim = dim3(static_cast<unsigned>(nc));
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = kTcSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, mk, mv, mq, mo, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -136,7 +136,7 @@ def test_prefill_full_size_sampled():
 
 def test_prefill_tc_invalid_lengths_and_bad_blocks():
     """G = 4, d 128: an invalid sequence is zeroed and flagged; a bad block id zeroes the rows of
-    the cluster tiles whose keys include it and is flagged; other rows are unaffected."""
+    the query tiles whose keys include it and is flagged; other rows are unaffected."""
     w = make_prefill_workload(H_q=32, H_kv=8, D=128, cached_list=[20, 300, 20, 150], chunk_list=[40, 70, 10, 200])
     g = PrefillGpu(w)
     ref = oracle_prefill(w)
@@ -149,7 +149,7 @@ def test_prefill_tc_invalid_lengths_and_bad_blocks():
     keep = np.r_[qs[0]:qs[1], qs[2]:qs[4]]
     assert_attention_close(out[keep], ref[keep], "valid sequences next to an invalid one")
     g.err.zero_()
-    g.tables[3, 0] = w.num_blocks + 3  # block 0 is read by every cluster tile of sequence 3
+    g.tables[3, 0] = w.num_blocks + 3  # block 0 is read by every query tile of sequence 3
     out = g.run()
     assert int(g.err.item()) & N.PA_EFLAG_BAD_BLOCK_ID
     assert np.all(out[qs[3]:qs[4]] == 0)
@@ -157,7 +157,7 @@ def test_prefill_tc_invalid_lengths_and_bad_blocks():
 
 
 def test_prefill_tc_many_ragged_items():
-    """40 sequences, G = 8 (64 query tokens per cluster tile), chunks of 0..300 tokens over 0..500
+    """40 sequences, G = 8 (32 query tokens per work item), chunks of 0..300 tokens over 0..500
     cached: the longest-first item list with ragged tiles, empty chunks and one-token chunks;
     every row against the oracle."""
     rng = np.random.default_rng(11)
@@ -172,22 +172,22 @@ def test_prefill_tc_many_ragged_items():
     assert_attention_close(out, oracle_prefill(w), "40 ragged sequences")
 
 
-def test_prefill_tc_more_items_than_resident_clusters():
-    """700 sequences x 8 KV heads = 5600 work items: more than one cluster list holds for every
-    resident cluster, so the launch adds clusters that start as others finish."""
+def test_prefill_tc_more_items_than_resident_ctas():
+    """1300 sequences x 8 KV heads = 10400 work items: more than one CTA's list holds (64) for
+    every resident CTA (one per SM), so the launch adds CTAs that start as others finish."""
     rng = np.random.default_rng(12)
-    B = 700
+    B = 1300
     w = make_prefill_workload(H_q=64, H_kv=8, D=128, cached_list=rng.integers(0, 61, B).tolist(),
                               chunk_list=rng.integers(1, 4, B).tolist(), seed=12)
     g = PrefillGpu(w)
     out = g.run()
     assert int(g.err.item()) == 0
-    assert_attention_close(out, oracle_prefill(w), "700 sequences")
+    assert_attention_close(out, oracle_prefill(w), "1300 sequences")
 
 
 def test_prefill_tc_over_4096_sequences():
-    """4200 sequences: beyond the 4096 whose geometry the kernel ranks in shared memory, cluster
-    tiles run in their plain order (last tiles first, sequences in order); every row checked."""
+    """4200 sequences: beyond the 4096 whose geometry the kernel ranks in shared memory, work
+    items run in their plain order (last tiles first, sequences in order); every row checked."""
     rng = np.random.default_rng(13)
     B = 4200
     w = make_prefill_workload(H_q=32, H_kv=8, D=128, cached_list=rng.integers(0, 31, B).tolist(),

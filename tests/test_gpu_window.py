@@ -128,7 +128,7 @@ def test_sliding_prefill_matches_oracle(window, H_q, H_kv, D):
 @pytest.mark.parametrize("window", [64, 200, 600])
 @pytest.mark.parametrize("H_q,H_kv", [(32, 8), (64, 8), (16, 16)])
 def test_sliding_prefill_long_chunks(window, H_q, H_kv):
-    """Chunks spanning several tensor-core cluster tiles (d 128): later tiles start their keys
+    """Chunks spanning several tensor-core work items (d 128): later tiles start their keys
     inside the window, the first key tile partly before it."""
     w = make_prefill_workload(H_q=H_q, H_kv=H_kv, D=128, cached_list=[0, 500, 1000, 37],
                               chunk_list=[300, 257, 129, 411], seed=21)
