@@ -253,38 +253,43 @@ INT4_LEVELS = 15  # codes 0 .. 15
 
 
 def int4_encode_group(x_bf16_bits):
-    """One group of 32 bf16 values -> (codes uint8[32] in 0..15, bf16 scale bits, zero point).
+    """Groups of 32 bf16 values [..., 32] -> (codes uint8 [..., 32] in 0..15, bf16 scale bits
+    [...], zero points [...]); one group (a 1-D input) gives the scale bits and the zero point
+    as Python ints.
 
     ldpk §5.2: int4 keeps a scale and a zero point per quantisation group; the group here is
     32 consecutive dims of one token's head row (per-token granularity, so an outlier channel
     of another token cannot squeeze this one).  The range always contains 0, so 0 encodes
     exactly (q = z).  Every arithmetic step is IEEE fp32 and the scale is rounded to bf16
-    before it is used, so that encoding and decoding use the same stored scale.
+    before it is used, so that encoding and decoding use the same stored scale.  Each group is
+    encoded on its own; the leading axes only batch independent groups.
     """
-    x = bf16_bits_to_f64(np.asarray(x_bf16_bits, dtype=np.uint16)).astype(np.float32)
-    lo = np.minimum(np.float32(0), x.min())
-    hi = np.maximum(np.float32(0), x.max())
-    s = np.float32(np.float32(hi - lo) / np.float32(INT4_LEVELS))
-    sb = int(f32_to_bf16_bits(np.array([s], dtype=np.float32))[0])
-    if sb & 0x7FFF == 0:
-        sb = 0x3F80  # an all-zero group: any scale works, take 1
-    sf = np.float32(bf16_bits_to_f64(np.array([sb], dtype=np.uint16))[0])
-    z = int(np.clip(np.rint(np.float32(-lo) / sf), 0, INT4_LEVELS))
-    q = np.clip(np.rint((x / sf).astype(np.float32)) + z, 0, INT4_LEVELS).astype(np.uint8)
+    bits = np.asarray(x_bf16_bits, dtype=np.uint16)
+    x = bf16_bits_to_f64(bits).astype(np.float32)
+    lo = np.minimum(np.float32(0), x.min(axis=-1))
+    hi = np.maximum(np.float32(0), x.max(axis=-1))
+    s = (np.asarray(hi - lo, dtype=np.float32) / np.float32(INT4_LEVELS)).astype(np.float32)
+    sb = f32_to_bf16_bits(s).astype(np.uint16)
+    sb = np.where((sb & 0x7FFF) == 0, np.uint16(0x3F80), sb)  # an all-zero group: any scale works, take 1
+    sf = bf16_bits_to_f64(sb).astype(np.float32)
+    z = np.clip(np.rint((np.asarray(-lo, dtype=np.float32) / sf).astype(np.float32)), 0, INT4_LEVELS)
+    q = np.clip(np.rint((x / sf[..., None]).astype(np.float32)) + z[..., None], 0, INT4_LEVELS).astype(np.uint8)
+    z = z.astype(np.int64)
+    if bits.ndim == 1:
+        return q, int(sb), int(z)
     return q, sb, z
 
 
 def int4_encode_row(x_bf16_bits):
-    """A head row of d values -> (codes uint8[d], params uint32[d / 32]) with each params word
-    holding the group's bf16 scale in bits 0-15 and its zero point in bits 16-23."""
+    """Head rows [..., d] -> (codes uint8 [..., d], params uint32 [..., d / 32]) with each params
+    word holding its group's bf16 scale in bits 0-15 and its zero point in bits 16-23; the groups
+    are dims 32g .. 32g + 31 of each row."""
     x = np.asarray(x_bf16_bits, dtype=np.uint16)
-    d = len(x)
-    codes = np.empty(d, dtype=np.uint8)
-    params = np.empty(d // INT4_GROUP, dtype=np.uint32)
-    for g in range(d // INT4_GROUP):
-        q, sb, z = int4_encode_group(x[g * INT4_GROUP:(g + 1) * INT4_GROUP])
-        codes[g * INT4_GROUP:(g + 1) * INT4_GROUP] = q
-        params[g] = np.uint32(sb | (z << 16))
+    d = x.shape[-1]
+    groups = x.reshape(x.shape[:-1] + (d // INT4_GROUP, INT4_GROUP))
+    q, sb, z = int4_encode_group(groups)
+    codes = q.reshape(x.shape)
+    params = (np.asarray(sb).astype(np.uint32) | (np.asarray(z).astype(np.uint32) << np.uint32(16))).astype(np.uint32)
     return codes, params
 
 

@@ -164,3 +164,21 @@ def test_planted_int4_mistakes_are_caught():
     assert any(not np.array_equal(unrounded_scale(b), O.int4_encode_group(b)[0]) for b in groups)
     assert any(np.any(range_without_zero(b)[_f32(b) == 0] != 0) for b in groups)
     assert any(not np.array_equal(truncating(b), O.int4_encode_group(b)[0]) for b in groups)
+
+
+def test_batched_rows_encode_each_group_on_its_own():
+    """The encoder takes rows with leading axes ([tokens][heads][d]) only as a batch of
+    independent groups: every row equals its own one-group-at-a-time encoding, including rows
+    whose groups differ wildly in range (a group's scale never depends on another group)."""
+    gs = _groups(7, 240)
+    rows = np.stack([np.concatenate(gs[i:i + 4]) for i in range(0, 240, 4)])  # 60 rows of d = 128
+    batch = rows.reshape(6, 10, 128)
+    codes, params = O.int4_encode_row(batch)
+    assert codes.shape == (6, 10, 128) and params.shape == (6, 10, 4)
+    for t in range(6):
+        for h in range(10):
+            row = batch[t, h]
+            for g in range(4):
+                q, sb, z = O.int4_encode_group(row[32 * g:32 * g + 32])
+                assert np.array_equal(codes[t, h, 32 * g:32 * g + 32], q)
+                assert int(params[t, h, g]) == sb | (z << 16)
