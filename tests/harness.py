@@ -108,6 +108,32 @@ class GpuState:
                               self.err)
         return out
 
+    def decode_step(self, k_new, v_new, q, positions, context_lens, partition=0, max_ctx=None):
+        """pa_decode_step: the append of one token per sequence and the attention in one call
+        (the entry point the benchmark times).  The slots must be writable (prepare first)."""
+        w = self.w
+        pos = np.ascontiguousarray(positions, dtype=np.int32)
+        ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+        max_ctx = int(ctx.max()) if max_ctx is None else int(max_ctx)
+        out = torch.full((w.B, w.H_q, w.D), float("nan"), dtype=torch.bfloat16, device=self.dev)
+        nbytes = P.pa_decode_workspace_size(self.desc, max_ctx, partition)
+        assert nbytes > 0
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+        P.pa_decode_step(self.desc, out, q.to(self.dev), self.k, self.v, k_new.to(self.dev), v_new.to(self.dev),
+                         self.tables_dev, torch.from_numpy(pos).to(self.dev), torch.from_numpy(ctx).to(self.dev),
+                         max_ctx, w.scale, partition, ws, nbytes, self.err)
+        return out
+
+    def attend_noalloc(self, q, context_lens, partition=0, max_ctx=None):
+        """pa_decode_attention_noalloc: the same attention with the library's static scratch."""
+        w = self.w
+        ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+        max_ctx = int(ctx.max()) if max_ctx is None else int(max_ctx)
+        out = torch.full((w.B, w.H_q, w.D), float("nan"), dtype=torch.bfloat16, device=self.dev)
+        P.pa_decode_attention_noalloc(self.desc, out, q.to(self.dev), self.k, self.v, self.tables_dev,
+                                      torch.from_numpy(ctx).to(self.dev), max_ctx, w.scale, partition, self.err)
+        return out
+
     def slide(self, context_lens):
         """Sliding window: release the blocks behind every sequence's window (host tables, then
         the device copy)."""
@@ -280,13 +306,17 @@ def assert_pools_equal(gpu: GpuState, ora: OracleState):
 
 
 # ----------------------------------------------------------------------------------
-# Full-size sampled checks: the oracle computes single (sequence, head) rows from the
-# workload's logical token stream, without building a whole pool.
+# Full-size checks: the oracle computes each sequence's rows from the workload's logical token
+# stream (the K/V rows of the positions a step attends, in position order), without building a
+# whole pool.
 # ----------------------------------------------------------------------------------
 def logical_tokens(w: Workload, s: int, step: int):
-    """bf16 bit rows [ctx][H_kv][D] of sequence s as attended at `step` (positions 0..ctx-1)."""
+    """bf16 bit rows [n][H_kv][D] of the positions sequence s attends at `step`, in order, and the
+    position of the first one.  Positions a workload never wrote (before a sliding window) are
+    not part of it: the rows start at the first cached position."""
     parts_k, parts_v = [], []
     if w.prefix:
+        pos0 = 0
         parts_k.append(bf16_bits(w.fill_k))
         parts_v.append(bf16_bits(w.fill_v))
         off = int(w.suffix_len[:s].sum())
@@ -296,34 +326,87 @@ def logical_tokens(w: Workload, s: int, step: int):
     else:
         idx = np.nonzero(w.fill_seq == s)[0]
         order = idx[np.argsort(w.fill_pos[idx])]
+        pos0 = int(w.fill_pos[order[0]]) if len(order) else int(w.ctx_old[s])
         parts_k.append(bf16_bits(w.fill_k[torch.from_numpy(order)]))
         parts_v.append(bf16_bits(w.fill_v[torch.from_numpy(order)]))
     for i in range(step + 1):
         parts_k.append(bf16_bits(w.k_new[i, s:s + 1]))
         parts_v.append(bf16_bits(w.v_new[i, s:s + 1]))
-    return np.concatenate(parts_k), np.concatenate(parts_v)
+    return np.concatenate(parts_k), np.concatenate(parts_v), pos0
+
+
+def _decode_head(k_dtype, num_sink, ks, vs, kb, vb, pos0):
+    """fp64 K and V [n][D] of one KV head's logical rows kb/vb (positions pos0 ..) as the cache
+    stores them: sink positions in bf16, the others through the oracle's encoder and decoder for
+    the cache kind (ks/vs: that head's 8-bit scales)."""
+    n = kb.shape[0]
+    ns = max(0, min(pos0 + n, num_sink) - pos0)
+    K = np.empty(kb.shape)
+    V = np.empty(vb.shape)
+    K[:ns] = O.bf16_bits_to_f64(kb[:ns])
+    V[:ns] = O.bf16_bits_to_f64(vb[:ns])
+    if k_dtype == "bf16":
+        K[ns:] = O.bf16_bits_to_f64(kb[ns:])
+        V[ns:] = O.bf16_bits_to_f64(vb[ns:])
+    elif k_dtype == "int4":
+        K[ns:] = O.int4_decode_row(*O.int4_encode_row(kb[ns:]))
+        V[ns:] = O.int4_decode_row(*O.int4_encode_row(vb[ns:]))
+    else:
+        K[ns:] = O.e4m3_decode(O.quantize_row(kb[ns:], ks, "e4m3")) * float(ks)
+        V[ns:] = O.int8_decode(O.quantize_row(vb[ns:], vs, "int8").view(np.int8)) * float(vs)
+    return K, V
+
+
+def _head_scales(w: Workload, h: int):
+    if w.k_scales is None:
+        return None, None
+    return np.float32(w.k_scales[h].item()), np.float32(w.v_scales[h].item())
+
+
+def _head_task(args):
+    """Oracle rows [G][D] of the G query heads of one KV head of one sequence (pool worker)."""
+    k_dtype, num_sink, ks, vs, kb, vb, pos0, q, scale, window = args
+    K, V = _decode_head(k_dtype, num_sink, ks, vs, kb, vb, pos0)
+    return O.decode_attention(q, K[:, None, :], V[:, None, :], scale, window=window)
+
+
+def _seq_tasks(w: Workload, s: int, step: int, kb: np.ndarray, vb: np.ndarray, pos0: int):
+    q = O.bf16_bits_to_f64(bf16_bits(w.q[step, s]))
+    for h in range(w.H_kv):
+        ks, vs = _head_scales(w, h)
+        yield (w.k_dtype, w.num_sink, ks, vs, np.ascontiguousarray(kb[:, h]), np.ascontiguousarray(vb[:, h]), pos0,
+               q[h * w.G:(h + 1) * w.G], w.scale, w.window)
+
+
+def reference_seq(w: Workload, s: int, step: int, kb: np.ndarray, vb: np.ndarray, pos0: int = 0) -> np.ndarray:
+    """Oracle output [H_q][D] of every query head of sequence s at `step`; kb/vb are the logical
+    bf16 rows of positions pos0 .. ctx-1 (the window start or 0 up to the new token)."""
+    return np.concatenate([_head_task(t) for t in _seq_tasks(w, s, step, kb, vb, pos0)])
+
+
+def reference_all(w: Workload, step: int = 0, processes: int = 0) -> np.ndarray:
+    """Oracle output [B][H_q][D] of every (sequence, query head) row of a decode step.  With
+    processes > 1 the (sequence, KV head) pieces run in a pool of spawned processes (each piece is
+    the same oracle call; only where it runs differs)."""
+    out = np.zeros((w.B, w.H_q, w.D))
+    if processes <= 1:
+        for s in range(w.B):
+            kb, vb, pos0 = logical_tokens(w, s, step)
+            out[s] = reference_seq(w, s, step, kb, vb, pos0)
+        return out
+    import multiprocessing as mp
+
+    def tasks():
+        for s in range(w.B):
+            kb, vb, pos0 = logical_tokens(w, s, step)
+            yield from _seq_tasks(w, s, step, kb, vb, pos0)
+    with mp.get_context("spawn").Pool(processes) as pool:
+        for i, rows in enumerate(pool.imap(_head_task, tasks())):
+            s, h = divmod(i, w.H_kv)
+            out[s, h * w.G:(h + 1) * w.G] = rows
+    return out
 
 
 def reference_row(w: Workload, s: int, h: int, step: int, kb: np.ndarray, vb: np.ndarray) -> np.ndarray:
-    """Oracle output of query head h of sequence s (kb/vb: logical bf16 bit rows)."""
-    kv = h // w.G
-    ctx = kb.shape[0]
-    K = np.empty((ctx, 1, w.D))
-    V = np.empty((ctx, 1, w.D))
-    ns = min(ctx, w.num_sink)
-    K[:ns, 0] = O.bf16_bits_to_f64(kb[:ns, kv])
-    V[:ns, 0] = O.bf16_bits_to_f64(vb[:ns, kv])
-    if w.k_dtype == "bf16":
-        K[ns:, 0] = O.bf16_bits_to_f64(kb[ns:, kv])
-        V[ns:, 0] = O.bf16_bits_to_f64(vb[ns:, kv])
-    elif w.k_dtype == "int4":
-        for t in range(ns, ctx):
-            K[t, 0] = O.int4_decode_row(*O.int4_encode_row(kb[t, kv]))
-            V[t, 0] = O.int4_decode_row(*O.int4_encode_row(vb[t, kv]))
-    else:
-        ks = np.float32(w.k_scales[kv].item())
-        vs = np.float32(w.v_scales[kv].item())
-        K[ns:, 0] = O.e4m3_decode(O.quantize_row(kb[ns:, kv], ks, "e4m3")) * float(ks)
-        V[ns:, 0] = O.int8_decode(O.quantize_row(vb[ns:, kv], vs, "int8").view(np.int8)) * float(vs)
-    q = O.bf16_bits_to_f64(bf16_bits(w.q[step, s, h:h + 1]))
-    return O.decode_attention(q, K, V, w.scale)[0]
+    """Oracle output of query head h of sequence s (kb/vb: logical bf16 bit rows from position 0)."""
+    return reference_seq(w, s, step, kb, vb)[h]
