@@ -36,9 +36,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 WINDOW = 64
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per decode_kernel launch, from the
-# ncu captures summarised in profiles/decode_kernel_<workload>.md.  Reported only while the
-# kernel sources hash to the version the counters were taken on; null otherwise.
+E2E_RING = 4          # e2e: device input/output slots in flight (copies of step k overlap steps k-3 .. k-1)
+WARM_SECONDS = 0.25   # warm-up runs at least this long (and at least --warmup steps) right before timing
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per decode_kernel launch, from one
+# ncu capture of each workload's attention call.  Reported only while the kernel sources hash to
+# the version the counters were taken on; null otherwise.
 NCU_TRAFFIC = {
     "sources_sha256_16": "81eb5caebcbe4597",
     "8b": 552_557_056, "70b": 543_515_904, "long_quant": 1_076_951_808, "prefix_cow": 282_210_560,
@@ -271,11 +273,13 @@ class DecodeBench:
         h_in[:, nq + nk:] = w.v_new.reshape(WINDOW, nk)
         self.h_in = [r for r in h_in.pin_memory()]
         self.h_out = [r for r in torch.empty((WINDOW, w.B, w.H_q, w.D), dtype=torch.bfloat16).pin_memory()]
-        self.d_in = [torch.empty(self.in_elems, dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.d_in = [torch.empty(self.in_elems, dtype=torch.bfloat16, device=device) for _ in range(E2E_RING)]
         self.d_views = [(d[:nq].view(w.B, w.H_q, w.D), d[nq:nq + nk].view(w.B, w.H_kv, w.D),
                          d[nq + nk:].view(w.B, w.H_kv, w.D)) for d in self.d_in]
-        self.d_out = [torch.empty_like(self.out) for _ in range(2)]
+        self.d_out = [torch.empty_like(self.out) for _ in range(E2E_RING)]
         self.host_s = 0.0
+        self.warm_steps = 0
+        self._touch_pinned()
         # raw device pointers for the per-step calls (the binding takes ints as pointers)
         P = lambda t: t.data_ptr()
         self.ptr = dict(k=P(self.k), v=P(self.v), tab=P(self.tables_dev), ws=P(self.ws), err=P(self.err),
@@ -285,6 +289,37 @@ class DecodeBench:
         self.ptr_e2e = [tuple(P(t) for t in v) + (P(o),) for v, o in zip(self.d_views, self.d_out)]
         self.launches_per_step = 3  # append + attention + merge (plus a copy kernel on CoW steps)
         self.cow_launches = 0
+
+    def _touch_pinned(self):
+        """Move every pinned staging slot through a copy once during set-up: the first copy from or
+        to a pinned page costs far more than the later ones (measured, a first pass through the
+        ring slots made the GPU wait on the host), and the timed steps should see the steady
+        state a serving loop reaches after its first steps."""
+        torch = self.torch
+        scratch_tab = torch.empty(self.tables.shape, dtype=torch.int32, device=self.dev)
+        scratch_pairs = torch.empty_like(self.pairs_dev)
+        for j in range(WINDOW):
+            self.tab_ring[j].numpy()[...] = self.tables
+            scratch_tab.copy_(self.tab_ring[j], non_blocking=True)
+            scratch_pairs.copy_(self.pair_ring[j], non_blocking=True)
+            self.d_in[j % E2E_RING].copy_(self.h_in[j], non_blocking=True)
+            self.h_out[j].copy_(self.d_out[j % E2E_RING], non_blocking=True)
+        torch.cuda.synchronize()
+
+    def warm(self, warmup, stream):
+        """Untimed steps right before a timed region: at least `warmup` of them and at least
+        WARM_SECONDS of wall time, so that the timed steps start from steady clocks and a full
+        queue of work rather than from a GPU that has been idle.  Returns the next step index."""
+        i = 0
+        t0 = time.perf_counter()
+        while i < warmup or time.perf_counter() - t0 < WARM_SECONDS:
+            self.step(i, stream)
+            i += 1
+            if i % 64 == 0:
+                self.torch.cuda.synchronize()
+        self.torch.cuda.synchronize()
+        self.warm_steps = i
+        return i
 
     def _fork_and_fill_suffixes(self):
         """Prefix workload set-up: every sequence writes its private suffix after the shared
@@ -350,20 +385,20 @@ class DecodeBench:
         """Device-resident steps.  Returns (elapsed_s, attention_ms_per_call or None, bytes)."""
         torch = self.torch
         sid = torch.cuda.current_stream().cuda_stream
-        for i in range(warmup):
-            self.step(i, sid)
-        torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)] if per_call_events else None
-        barrier(self.dev)
-        torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        first = self.warm(warmup, sid)
+        barrier(self.dev)
+        torch.cuda.synchronize()
+        self.first_step = first
+        self.cow_launches = 0
         t0.record()
         nbytes = 0
         h0 = time.perf_counter()
         for k in range(steps):
-            i = warmup + k
+            i = first + k
             self.step(i, sid, ev=None if evs is None else evs[k])
             nbytes += self.step_bytes[i % WINDOW]
         self.host_s = time.perf_counter() - h0
@@ -376,21 +411,24 @@ class DecodeBench:
 
     def run_e2e(self, steps, warmup):
         """Steps fed from pinned host memory: a copy stream uploads step k's q/k/v into one of
-        two device buffers and downloads step k-2's output while the compute stream runs step
-        k-1; every copy of every timed step is inside the timed region."""
+        E2E_RING device slots and downloads the output of the step that last used that slot,
+        while the compute stream runs the steps before k; every copy of every timed step is
+        inside the timed region, and the region ends when the last output is back in host
+        memory."""
         torch = self.torch
         comp = torch.cuda.current_stream()
         copy = torch.cuda.Stream()
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        done = [torch.cuda.Event() for _ in range(2)]
+        R = E2E_RING
+        in_ready = [torch.cuda.Event() for _ in range(R)]
+        done = [torch.cuda.Event() for _ in range(R)]
         pending = {}
 
         def issue(k, i):
-            b = k % 2
+            b = k % R
             j = i % WINDOW
             with torch.cuda.stream(copy):
-                if k >= 2:
-                    copy.wait_event(done[b])  # step k-2 consumed buffer b and produced out[b]
+                if b in pending:
+                    copy.wait_event(done[b])  # the step that used slot b consumed its input, wrote out[b]
                     self.h_out[pending.pop(b)].copy_(self.d_out[b], non_blocking=True)
                 self.d_in[b].copy_(self.h_in[j], non_blocking=True)
                 in_ready[b].record(copy)
@@ -406,12 +444,18 @@ class DecodeBench:
                     self.h_out[pending[b]].copy_(self.d_out[b], non_blocking=True)
             pending.clear()
 
-        for k in range(warmup):
+        # warm-up through the same pipeline, then the timed steps
+        k, t_w = 0, time.perf_counter()
+        while k < warmup or time.perf_counter() - t_w < WARM_SECONDS:
             issue(k, k)
+            k += 1
+            if k % 64 == 0:
+                drain()
+                torch.cuda.synchronize()
         drain()
         torch.cuda.synchronize()
+        first = k
         barrier(self.dev)
-        torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(comp)
@@ -419,8 +463,8 @@ class DecodeBench:
         nbytes = 0
         h0 = time.perf_counter()
         for k in range(steps):
-            issue(k, warmup + k)
-            nbytes += self.step_bytes[(warmup + k) % WINDOW]
+            issue(k, first + k)
+            nbytes += self.step_bytes[(first + k) % WINDOW]
         drain()
         self.host_s = time.perf_counter() - h0
         comp.wait_stream(copy)
@@ -666,84 +710,164 @@ def prefix_cache_row(device, warmup):
             "prefill_attention_speedup": round(miss_ms / hit_ms, 2), "err_flag": e_hit | e_miss}
 
 
-def cpu_baseline_sample(name, budget_s=15.0, max_seqs=None):
-    """The oracle, as it stands, on a bounded sample of the workload: whole decode steps
-    (append + attention) of the first sequences, on this host's CPU.  Run in a spawned child
-    with BLAS pinned to one thread, so that `cores` is exact."""
+def cpu_model() -> str:
+    """The host CPU's name as /proc/cpuinfo gives it (model name on x86, implementer/part on Arm)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return "unknown"
+    for line in info.splitlines():
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    fields = {}
+    for line in info.splitlines():
+        if ":" in line:
+            k, v = (x.strip() for x in line.split(":", 1))
+            fields.setdefault(k, v)
+    if "CPU implementer" in fields:
+        return f"arm implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return "unknown"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_throughput(name, workers, steps=None, warmup=0, budget_s=None):
+    """The oracle, as it stands, on this host's cores: `workers` spawned processes (one thread each)
+    split the workload's sequences between them (sequence s goes to worker s % workers) and run
+    whole decode steps of their sequences (copy-on-write decision, append, gather through the
+    table, attention of every query head), all at once.
+
+    steps given: `warmup` untimed steps, then `steps` timed steps of every sequence (the same
+    work per step as one GPU step).  budget_s given: sequence-steps, round-robin over the
+    worker's sequences, for about budget_s seconds (a bounded sample).
+    Returns bytes, seconds (the slowest worker's), sequence-steps and the sample's description."""
     import multiprocessing as mp
     ctx = mp.get_context("spawn")
+    start = ctx.Event()
     q = ctx.Queue()
-    p = ctx.Process(target=_oracle_child, args=(name, budget_s, max_seqs, q))
-    p.start()
-    res = q.get(timeout=900)
-    p.join(timeout=60)
-    return res
+    procs = [ctx.Process(target=_oracle_worker, args=(name, w, workers, steps, warmup, budget_s, start, q))
+             for w in range(workers)]
+    for p in procs:
+        p.start()
+    for _ in range(workers):
+        msg = q.get(timeout=900)
+        if msg != "ready":
+            raise RuntimeError(f"oracle worker failed: {msg}")
+    start.set()
+    res = [q.get(timeout=1800) for _ in range(workers)]
+    for p in procs:
+        p.join(timeout=120)
+    bad = [r for r in res if "error" in r]
+    if bad:
+        raise RuntimeError(f"oracle worker failed: {bad[0]['error']}")
+    return {"bytes": sum(r["bytes"] for r in res), "seconds": max(r["seconds"] for r in res),
+            "seq_steps": sum(r["seq_steps"] for r in res), "workers": workers}
 
 
-def _oracle_child(name, budget_s, max_seqs, q):
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[var] = "1"
-    import torch
-    torch.set_num_threads(1)
-    import oracle as O
-    from paged_kv_cache_table_gb300.workloads import bf16_bits, make_workload
-    w = make_workload(name, steps=1)
-    nseq = w.B if max_seqs is None else min(w.B, max_seqs)
-    ks = None if w.k_scales is None else w.k_scales.numpy()
-    vs = None if w.v_scales is None else w.v_scales.numpy()
-    cache = O.PagedKVCache(w.num_blocks, w.H_kv, w.D, k_dtype=w.k_dtype, v_dtype=w.v_dtype, k_scales=ks,
-                           v_scales=vs, num_seqs=w.B, num_sink=w.num_sink)
-    pool = O.BlockPool(w.num_blocks)
-    for b in np.unique(w.tables[w.tables >= 0]):
-        pool.claim(int(b))
-    tables = w.tables.astype(np.int64).copy()
-    kb_all, vb_all = bf16_bits(w.fill_k), bf16_bits(w.fill_v)
-    sel = np.nonzero(w.fill_seq < nseq)[0]
-    for i in sel:
-        s = int(w.fill_seq[i])
-        cache.append(s, tables[s], int(w.fill_pos[i]), kb_all[i], vb_all[i])
-    qv = O.bf16_bits_to_f64(bf16_bits(w.q[0]))
-    kn, vn = bf16_bits(w.k_new[0]), bf16_bits(w.v_new[0])
-    pos, ctx = w.positions(0), w.context_lens(0)
-    done_bytes, done_seqs, t_total = 0, 0, 0.0
-    while t_total < budget_s and done_seqs < 10 * nseq:
-        s = done_seqs % nseq
-        t0 = time.perf_counter()
-        act = pool.prepare_append(tables[s], int(pos[s]))
-        if act[0] == "copy":
-            cache.block_copy(act[1], act[2])
-        cache.append(s, tables[s], int(pos[s]), kn[s], vn[s])
-        K, V = cache.gather(s, tables[s], int(ctx[s]))
-        O.decode_attention(qv[s], K, V, w.scale)
-        t_total += time.perf_counter() - t0
-        done_bytes += seq_bytes(w, int(ctx[s]))
-        done_seqs += 1
-    q.put({"seconds": t_total, "bytes": done_bytes, "seqs": done_seqs, "cores": 1,
-           "sample": f"{done_seqs} sequence-steps (append + attention) of the first {nseq} sequences, "
-                     f"fp64 numpy oracle, 1 thread"})
+def _oracle_worker(name, worker, workers, steps, warmup, budget_s, start, q):
+    try:
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        import torch
+        torch.set_num_threads(1)
+        import oracle as O
+        from paged_kv_cache_table_gb300.workloads import bf16_bits, make_workload
+        n_steps = WINDOW if steps is None else min(WINDOW, steps + warmup)
+        w = make_workload(name, steps=n_steps)
+        if w.prefix:
+            raise ValueError("the oracle baseline covers workloads without a shared prefix")
+        mine = [s for s in range(w.B) if s % workers == worker]
+        ks = None if w.k_scales is None else w.k_scales.numpy()
+        vs = None if w.v_scales is None else w.v_scales.numpy()
+        cache = O.PagedKVCache(w.num_blocks, w.H_kv, w.D, k_dtype=w.k_dtype, v_dtype=w.v_dtype, k_scales=ks,
+                               v_scales=vs, num_seqs=w.B, num_sink=w.num_sink)
+        pool = O.BlockPool(w.num_blocks)
+        for b in np.unique(w.tables[w.tables >= 0]):
+            pool.claim(int(b))
+        tables = w.tables.astype(np.int64).copy()
+        kb_all, vb_all = bf16_bits(w.fill_k), bf16_bits(w.fill_v)
+        for i in np.nonzero(np.isin(w.fill_seq, mine))[0]:
+            s = int(w.fill_seq[i])
+            cache.append(s, tables[s], int(w.fill_pos[i]), kb_all[i], vb_all[i])
+        qs = [O.bf16_bits_to_f64(bf16_bits(w.q[j])) for j in range(n_steps)]
+        kn = [bf16_bits(w.k_new[j]) for j in range(n_steps)]
+        vn = [bf16_bits(w.v_new[j]) for j in range(n_steps)]
+
+        def seq_step(i, s):
+            j = i % n_steps
+            pos, ctx = int(w.ctx_old[s]) + j, int(w.ctx_old[s]) + j + 1
+            act = pool.prepare_append(tables[s], pos)
+            if act[0] == "copy":
+                cache.block_copy(act[1], act[2])
+            cache.append(s, tables[s], pos, kn[j][s], vn[j][s])
+            K, V = cache.gather(s, tables[s], ctx, O.window_start(ctx, w.window))
+            O.decode_attention(qs[j][s], K, V, w.scale)
+            return seq_bytes(w, ctx)
+
+        q.put("ready")
+        start.wait()
+        nbytes, n, secs = 0, 0, 0.0
+        if steps is not None:
+            for i in range(warmup):
+                for s in mine:
+                    seq_step(i, s)
+            t0 = time.perf_counter()
+            for i in range(warmup, warmup + steps):
+                for s in mine:
+                    nbytes += seq_step(i, s)
+                    n += 1
+            secs = time.perf_counter() - t0
+        else:
+            t0 = time.perf_counter()
+            while mine and secs < budget_s:
+                nbytes += seq_step(n // len(mine), mine[n % len(mine)])
+                n += 1
+                secs = time.perf_counter() - t0
+        q.put({"bytes": nbytes, "seconds": secs, "seq_steps": n})
+    except Exception as e:  # reported to the parent, which raises
+        q.put({"error": repr(e)})
+
+
+def cpu_baseline(name, budget_s):
+    """The oracle timed on all host cores and on one, each on a bounded sample of the workload."""
+    cores = host_cores()
+    workers = min(cores, 64)
+    allc = oracle_throughput(name, workers, budget_s=budget_s)
+    one = oracle_throughput(name, 1, budget_s=budget_s)
+    desc = "sequence-steps (copy-on-write decision, append, gather, attention of every query head) of the {} workload, " \
+           "round-robin over its sequences, fp64 numpy oracle, {}"
+    return {"value": round(allc["bytes"] / allc["seconds"] / 1e9, 6), "unit": "GB/s", "cores": workers,
+            "kind": "oracle",
+            "sample": f"{allc['seq_steps']} " + desc.format(name, f"{workers} processes x 1 thread, ~{budget_s:.0f} s"),
+            "single_thread": {"value": round(one["bytes"] / one["seconds"] / 1e9, 6), "unit": "GB/s", "cores": 1,
+                              "sample": f"{one['seq_steps']} " + desc.format(name, f"1 thread, ~{budget_s:.0f} s")},
+            "nproc": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args):
+    """The reference arm: the oracle, as it stands, on every host core, running whole decode steps
+    of the same workload as the GPU arm (every sequence of --config per step)."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
-    vals, secs, tot_bytes, cores, sample = [], 0.0, 0, 1, ""
-    for k in range(args.warmup + args.steps):
-        r = cpu_baseline_sample(args.config, budget_s=min(per_step, 20.0), max_seqs=8)
-        if k >= args.warmup:
-            vals.append(r["bytes"] / r["seconds"] / 1e9)
-            secs += r["seconds"]
-            tot_bytes += r["bytes"]
-        cores, sample = r["cores"], r["sample"]
-    value = tot_bytes / secs / 1e9
+    workers = min(host_cores(), 64)
+    r = oracle_throughput(args.config, workers, steps=args.steps, warmup=args.warmup)
+    value = r["bytes"] / r["seconds"] / 1e9
+    sample = (f"{args.steps} whole decode steps ({r['seq_steps']} sequence-steps) of the {args.config} workload after "
+              f"{args.warmup} untimed ones, fp64 numpy oracle, {workers} processes x 1 thread")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * secs / max(1, args.steps), 3), "higher_is_better": True,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * r["seconds"] / max(1, args.steps), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.config, "oracle": "CPU fp64 numpy"},
-            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+            "config": {"workload": args.config, "oracle": "CPU fp64 numpy", "same_steps_as_gpu_arm": True},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": workers, "kind": "oracle",
+                             "sample": sample, "nproc": os.cpu_count(), "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -772,14 +896,16 @@ def run_native(args):
         elapsed, _, nbytes = b.run(args.steps, args.warmup)
     clocks = cs.summary()
     host_ms = 1e3 * b.host_s / args.steps
+    cow_launches = b.cow_launches
+    warm_steps = b.warm_steps
     # the same steps with CUDA events around every attention call (roofline of the kernel)
-    _, att_ms, _ = b.run(args.steps, args.warmup, per_call_events=True)
+    _, att_ms, nbytes_ev = b.run(args.steps, args.warmup, per_call_events=True)
     el_max, bytes_all = reduce_max_sum(elapsed, nbytes, device)
     value = bytes_all / el_max / 1e9
     ms_per_step = 1e3 * el_max / args.steps
     tok_s_layer = ws * w.B * args.steps / el_max
     att_mean_ms = float(np.mean(att_ms))
-    att_bytes = float(np.mean([b.step_bytes[(args.warmup + k) % WINDOW] for k in range(args.steps)]))
+    att_bytes = nbytes_ev / args.steps
     achieved = att_bytes / (att_mean_ms / 1e3) / 1e9
     # end-to-end through the same API with host buffers
     el_e2e, nbytes_e2e = b.run_e2e(args.steps, args.warmup)
@@ -793,11 +919,11 @@ def run_native(args):
         nb = DecodeBench(name, device, args.partition)
         n2 = max(50, args.steps // 4)
         e2, _, by2 = nb.run(n2, args.warmup)
-        _, a2, _ = nb.run(n2, args.warmup, per_call_events=True)
+        _, a2, by_ev = nb.run(n2, args.warmup, per_call_events=True)
         a_ms = float(np.mean(a2))
-        ab = float(np.mean([nb.step_bytes[(args.warmup + k) % WINDOW] for k in range(len(a2))]))
+        ab = by_ev / len(a2)
         if nb.w.prefix:
-            ub = float(np.mean([nb.unique_bytes(nb.ctx[(args.warmup + k) % WINDOW]) for k in range(len(a2))]))
+            ub = float(np.mean([nb.unique_bytes(nb.ctx[(nb.first_step + k) % WINDOW]) for k in range(len(a2))]))
             extra_prefix = {"unique_bytes_per_call": int(ub),
                             "attention_gbs_unique": round(ub / (a_ms / 1e3) / 1e9, 1),
                             "fork_copy_pairs": nb.fork_pairs}
@@ -867,15 +993,15 @@ def run_native(args):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        r = cpu_baseline_sample(args.config, budget_s=args.cpu_seconds, max_seqs=8)
-        cpu = {"value": round(r["bytes"] / r["seconds"] / 1e9, 6), "unit": "GB/s", "cores": r["cores"],
-               "kind": "oracle", "sample": r["sample"]}
+        cpu = cpu_baseline(args.config, args.cpu_seconds)
 
     if rank == 0:
         kv_bytes = int(sum(b.step_bytes) / WINDOW)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "warmup": args.warmup, "warmup_steps_run": warm_steps,
+            "warmup_note": f"untimed steps right before timing: at least --warmup and at least {WARM_SECONDS} s",
+            "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.k_dtype == "bf16" else "fp8e4m3/int8",
             "data": "synthetic",
             "config": {"workload": f"{args.config}: B={w.B}, H_q={w.H_q}, H_kv={w.H_kv}, d={w.D}, block 16, "
@@ -899,7 +1025,7 @@ def run_native(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * el_e2e / args.steps, 5),
                     "host_ms_per_step": round(host_ms_e2e, 5)},
             "host_ms_per_step": round(host_ms, 5),
-            "gpu_launches": args.steps * b.launches_per_step + b.cow_launches,
+            "gpu_launches": args.steps * b.launches_per_step + cow_launches,
             "clocks": clocks,
             "cpu_baseline": cpu,
             "err_flag": err,
@@ -922,10 +1048,12 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="8b")
     ap.add_argument("--partition", type=int, default=0)
-    ap.add_argument("--also", default="70b")
+    ap.add_argument("--also", default="tiny,70b,prefix_cow,long_quant",
+                    help="more decode workloads reported under 'also' (comma list, or 'none')")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the rows beyond decode (chunked prefill)")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="length of each CPU oracle sample (all cores, then one)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per attention call of the current kernel sources (null when unknown)")
     ap.add_argument("--attention-only", action="store_true",
@@ -935,6 +1063,15 @@ def main(argv=None):
                     help="run only the chunked-prefill row (append + prefill attention steps) and print it; "
                          "for profiling that kernel")
     args = ap.parse_args(argv)
+    ws, _, _ = dist_env()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one process per GPU: start the N replicas under torch.distributed.run
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(29500 + os.getpid() % 1000),
+               os.path.abspath(__file__)] + list(sys.argv[1:] if argv is None else argv)
+        return subprocess.call(cmd)
+    if ws != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but {ws} processes were launched (WORLD_SIZE)")
     if args.impl == "reference":
         return run_reference(args)
     if args.prefill_only:
