@@ -27,6 +27,11 @@ Readings taken where the pages are silent (each repeated where it is used):
     s = bf16((hi - lo) / 15) (1 if that is 0), z = clamp(rint(-lo / s), 0, 15) and
     q = clamp(rint(x / s) + z, 0, 15), divisions in IEEE fp32; a code decodes to s * (q - z);
     with a bf16 scale and the zero point in one 32-bit word that is 0.625 bytes per element;
+  * per-token K scales (ldpk §5.2: K develops outlier channels, so one scale per tensor or per
+    head fails on long contexts and finer granularity is needed): "e4m3_tok" K stores E4M3 codes
+    with one fp32 scale per (token, KV head), s = max|x| / 448 over the token's head row in IEEE
+    fp32 (NaN elements left out of the maximum, an all-zero row takes 1), and codes
+    e4m3(x / s); a code decodes to its value times s;
   * sliding window W (ldpk §5.3): the query at position p attends positions
     max(0, p - W + 1) .. p, i.e. the most recent W tokens with itself included, and W = 0
     means no window; a block is freed once all its positions lie before the window of the
@@ -60,6 +65,8 @@ __all__ = [
     "int8_encode",
     "int8_decode",
     "quantize_row",
+    "e4m3_token_scale",
+    "quantize_token_rows",
     "INT4_GROUP",
     "int4_encode_group",
     "int4_encode_row",
@@ -246,6 +253,33 @@ def quantize_row(x_bf16_bits, scale: np.float32, kind: str) -> np.ndarray:
     if kind == "int8":
         return int8_encode(e).view(np.uint8)
     raise ValueError(kind)
+
+
+def e4m3_token_scale(x_bf16_bits):
+    """Per-token K scale of head rows [..., d] (bf16 bits) -> fp32 [...].
+
+    ldpk §5.2: K carries outlier channels, so a scale shared by a whole tensor or head leaves
+    most tokens with a fraction of the code range; one scale per token's head row adapts to each
+    token.  s = max|x| / 448 (the largest finite E4M3 value) in IEEE fp32, so that the row's
+    largest element maps to the top of the code range; NaN elements are left out of the maximum
+    (it starts from 0), and a row whose maximum is 0 takes s = 1 (any scale encodes it exactly).
+    """
+    x = bf16_bits_to_f64(np.asarray(x_bf16_bits, dtype=np.uint16)).astype(np.float32)
+    a = np.fmax.reduce(np.abs(x), axis=-1, initial=np.float32(0)).astype(np.float32)
+    s = (a / np.float32(E4M3_MAX)).astype(np.float32)
+    return np.where(s == 0, np.float32(1), s).astype(np.float32)
+
+
+def quantize_token_rows(x_bf16_bits):
+    """Head rows [..., d] (bf16 bits) -> (E4M3 codes uint8 [..., d], fp32 scales [...]): each row
+    is divided by its own per-token scale in IEEE fp32 and rounded to E4M3 (nearest, ties to
+    even, saturating), as quantize_row does with a per-head scale."""
+    x = np.asarray(x_bf16_bits, dtype=np.uint16)
+    sc = e4m3_token_scale(x)
+    xf = bf16_bits_to_f64(x).astype(np.float32)
+    with np.errstate(invalid="ignore"):  # inf / inf (a row holding an infinity) is NaN, as in IEEE
+        e = (xf / sc[..., None]).astype(np.float32)
+    return e4m3_encode(e), sc
 
 
 INT4_GROUP = 32   # dims per scale / zero-point group
@@ -437,7 +471,8 @@ class PagedKVCache:
     ``k[slot][kv_head][dim]`` with slot = physical_block * block_size + offset.
     bf16 pools hold uint16 bit patterns; e4m3 / int8 pools hold uint8 codes; int4 pools hold
     one uint8 code (0..15) per element in natural order plus ``k_params`` / ``v_params``
-    [slot][kv_head][dim / 32] uint32 (bf16 scale | zero point << 16).
+    [slot][kv_head][dim / 32] uint32 (bf16 scale | zero point << 16); an "e4m3_tok" K pool holds
+    E4M3 codes plus ``k_tscale`` [slot][kv_head] fp32, one scale per token's head row.
     ``k_sink`` / ``v_sink`` hold the bf16 rows of positions < num_sink per sequence
     (显存账本 §七: attention-sink tokens keep their original precision).
     """
@@ -446,7 +481,7 @@ class PagedKVCache:
     num_kv_heads: int
     head_dim: int
     block_size: int = BLOCK_SIZE
-    k_dtype: str = "bf16"  # "bf16" | "e4m3" | "int4"
+    k_dtype: str = "bf16"  # "bf16" | "e4m3" | "e4m3_tok" | "int4"
     v_dtype: str = "bf16"  # "bf16" | "int8" | "int4"
     k_scales: np.ndarray | None = None  # fp32 [num_kv_heads]
     v_scales: np.ndarray | None = None
@@ -466,14 +501,19 @@ class PagedKVCache:
         pshape = (n_slots, self.num_kv_heads, self.head_dim // INT4_GROUP)
         self.k_params = np.zeros(pshape, dtype=np.uint32) if self.k_dtype == "int4" else None
         self.v_params = np.zeros(pshape, dtype=np.uint32) if self.v_dtype == "int4" else None
+        self.k_tscale = (np.zeros((n_slots, self.num_kv_heads), dtype=np.float32) if self.k_dtype == "e4m3_tok"
+                         else None)
         shape = (self.num_seqs, self.num_sink, self.num_kv_heads, self.head_dim)
         self.k_sink = np.zeros(shape, dtype=np.uint16)
         self.v_sink = np.zeros(shape, dtype=np.uint16)
 
     def _encode(self, bits, kind, scales):
-        """Codes of one token's rows [kv_heads][dim], and its int4 params (else None)."""
+        """Codes of one token's rows [kv_heads][dim], and its int4 params or per-token scales
+        (else None)."""
         if kind == "bf16":
             return np.asarray(bits, dtype=np.uint16), None
+        if kind == "e4m3_tok":
+            return quantize_token_rows(bits)
         out = np.empty(bits.shape, dtype=np.uint8)
         if kind == "int4":
             params = np.empty((self.num_kv_heads, self.head_dim // INT4_GROUP), dtype=np.uint32)
@@ -501,7 +541,9 @@ class PagedKVCache:
         slot = locate(table_row, pos, self.block_size)
         self.k[slot], kp = self._encode(k_bits, self.k_dtype, self.k_scales)
         self.v[slot], vp = self._encode(v_bits, self.v_dtype, self.v_scales)
-        if kp is not None:
+        if kp is not None and self.k_dtype == "e4m3_tok":
+            self.k_tscale[slot] = kp
+        elif kp is not None:
             self.k_params[slot] = kp
         if vp is not None:
             self.v_params[slot] = vp
@@ -511,7 +553,7 @@ class PagedKVCache:
         bs = self.block_size
         self.k[dst * bs:(dst + 1) * bs] = self.k[src * bs:(src + 1) * bs]
         self.v[dst * bs:(dst + 1) * bs] = self.v[src * bs:(src + 1) * bs]
-        for prm in (self.k_params, self.v_params):
+        for prm in (self.k_params, self.v_params, self.k_tscale):
             if prm is not None:
                 prm[dst * bs:(dst + 1) * bs] = prm[src * bs:(src + 1) * bs]
 
@@ -520,6 +562,8 @@ class PagedKVCache:
             return bf16_bits_to_f64(codes)
         if self.k_dtype == "int4":
             return int4_decode_row(codes, self.k_params[slots])
+        if self.k_dtype == "e4m3_tok":
+            return e4m3_decode(codes) * self.k_tscale[slots].astype(np.float64)[..., None]
         vals = e4m3_decode(codes)
         sc = np.asarray(self.k_scales, dtype=np.float32).astype(np.float64)
         return vals * (sc if heads is None else sc[heads])[..., :, None]
