@@ -98,13 +98,14 @@ def seq_bytes(w, ctx_s: int) -> int:
     ctx_s = int(ctx_s)
     lo = max(0, ctx_s - w.window) if w.window else 0
     n_sink = max(0, min(ctx_s, w.num_sink) - lo)
-    kv = (ctx_s - lo - n_sink) * w.H_kv * w.kv_row_bytes() * 2 + n_sink * w.H_kv * w.D * 2 * 2
+    kv = (ctx_s - lo - n_sink) * w.H_kv * (w.k_row_bytes() + w.kv_row_bytes()) + n_sink * w.H_kv * w.D * 2 * 2
     return kv + 2 * w.H_q * w.D * 2 + (-(-ctx_s // 16) - lo // 16) * 4 + 4
 
 
 def attention_bytes(w, ctx: np.ndarray) -> int:
     """Algorithmic bytes of one decode-attention call (what must cross HBM at least once)."""
-    scales = 2 * w.H_kv * 4 if w.k_dtype != "bf16" else 0
+    # per-KV-head fp32 scales read by the call (per-token K scales are in the K row bytes)
+    scales = {"e4m3": 2 * w.H_kv * 4, "e4m3_tok": w.H_kv * 4}.get(w.k_dtype, 0)
     return sum(seq_bytes(w, c) for c in np.asarray(ctx)) + scales
 
 
@@ -212,11 +213,11 @@ class DecodeBench:
         self.w = w
         n_slots = w.num_blocks * 16
         if w.k_dtype == "bf16":
-            shape, kvdt = (n_slots, w.H_kv, w.D), torch.bfloat16
-        else:  # 8-bit codes, or int4 codes followed by the group parameters
-            shape, kvdt = (n_slots, w.H_kv, w.kv_row_bytes()), torch.uint8
-        self.k = torch.empty(shape, dtype=kvdt, device=device)
-        self.v = torch.empty(shape, dtype=kvdt, device=device)
+            self.k = torch.empty((n_slots, w.H_kv, w.D), dtype=torch.bfloat16, device=device)
+            self.v = torch.empty_like(self.k)
+        else:  # 8-bit codes (per-token K: then the scales), or int4 codes followed by the group parameters
+            self.k = torch.empty(n_slots * w.H_kv * w.k_row_bytes(), dtype=torch.uint8, device=device)
+            self.v = torch.empty(n_slots * w.H_kv * w.kv_row_bytes(), dtype=torch.uint8, device=device)
         self.k_scales = None if w.k_scales is None else w.k_scales.to(device)
         self.v_scales = None if w.v_scales is None else w.v_scales.to(device)
         self.k_sink = self.v_sink = None
@@ -1048,7 +1049,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="8b")
     ap.add_argument("--partition", type=int, default=0)
-    ap.add_argument("--also", default="tiny,70b,prefix_cow,long_quant",
+    ap.add_argument("--also", default="tiny,70b,prefix_cow,long_quant,long_quant_tok",
                     help="more decode workloads reported under 'also' (comma list, or 'none')")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the rows beyond decode (chunked prefill)")

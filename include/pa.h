@@ -15,6 +15,9 @@
  *     head h reads KV head h / G, G = num_q_heads / num_kv_heads (显存账本 §二, GQA).
  *   - Optional 8-bit caches store K as FP8 E4M3 and V as INT8 with one fp32 scale per KV
  *     head, and keep the first num_sink positions of every sequence in bf16 (显存账本 §七).
+ *   - Optionally K keeps one fp32 scale per token's head row instead of one per KV head
+ *     (PA_FP8_E4M3_TOKEN; ldpk §5.2: K develops outlier channels, so per-tensor or per-head
+ *     scales fail on long contexts and finer granularity is needed).
  *   - Optional 4-bit caches store K and V as INT4 codes with a scale and a zero point per
  *     group of 32 dims of every token's head row (ldpk §5.2: int4 keeps a scale and a zero
  *     point, about 0.55-0.65 bytes per element; per-token granularity against K's outlier
@@ -38,6 +41,9 @@
  *   INT4 pools        [num_blocks * 16][num_kv_heads][64] code bytes, then (at byte offset
  *                     num_blocks*16*num_kv_heads*64 of the same allocation)
  *                     [num_blocks * 16][num_kv_heads][4] uint32 group parameters; see PA_INT4.
+ *   PA_FP8_E4M3_TOKEN K pools  [num_blocks * 16][num_kv_heads][head_dim] E4M3 codes, then (at
+ *                     byte offset num_blocks*16*num_kv_heads*head_dim of the same allocation)
+ *                     [num_blocks * 16][num_kv_heads] fp32 scales, one per token's head row.
  *
  * Conventions:
  *   - The caller owns every buffer; apart from the static scratch array behind
@@ -78,7 +84,7 @@ typedef enum {
   PA_BF16 = 0,
   PA_FP8_E4M3 = 1, /* OCP FP8 E4M3, round-to-nearest-even, saturating at +-448 */
   PA_INT8 = 2,     /* symmetric int8, round-half-even, clamped to [-127, 127] */
-  PA_INT4 = 3      /* asymmetric 4-bit codes with a bf16 scale and a zero point per 32 dims:
+  PA_INT4 = 3,     /* asymmetric 4-bit codes with a bf16 scale and a zero point per 32 dims:
                     * for each group x[0..31] of a token's head row (head_dim 128: 4 groups)
                     *   lo = min(0, min x), hi = max(0, max x)           (fp32)
                     *   s  = bf16(rn((hi - lo) / 15)), 1.0 if that is +-0
@@ -92,6 +98,12 @@ typedef enum {
                     *   V: byte 8r + m (r, m in 0..7) holds dim 16m + r in bits 0-3 and dim
                     *      16m + r + 8 in bits 4-7.
                     * 64 code bytes + 16 parameter bytes per row: 0.625 bytes per element. */
+  PA_FP8_E4M3_TOKEN = 4 /* K only: OCP FP8 E4M3 codes with one fp32 scale per (token, KV head)
+                         * row: s = max|x| / 448 over the row's head_dim values in IEEE fp32 (NaN
+                         * elements left out of the maximum, which starts from 0; a row whose
+                         * maximum is 0 takes s = 1), code = e4m3(x / s) rounded and saturated as
+                         * PA_FP8_E4M3, value = code * s.  The scale follows the codes in the same
+                         * allocation (see the layout above): head_dim + 4 bytes per row. */
 } pa_dtype;
 
 /* Bits OR-ed into *err_flag by the kernels. */
@@ -102,8 +114,10 @@ typedef enum {
 
 /* One layer's cache description.  Supported: block_size == 16; head_dim 64 or 128;
  * num_q_heads % num_kv_heads == 0 with G = num_q_heads/num_kv_heads <= 8;
- * (k_dtype, v_dtype) = (PA_BF16, PA_BF16), (PA_FP8_E4M3, PA_INT8) or (PA_INT4, PA_INT4), the
- * 8-bit and 4-bit ones with head_dim 128, the 4-bit one with an even num_kv_heads.  k_scales/v_scales are required for 8-bit dtypes and ignored otherwise.
+ * (k_dtype, v_dtype) = (PA_BF16, PA_BF16), (PA_FP8_E4M3, PA_INT8), (PA_FP8_E4M3_TOKEN, PA_INT8)
+ * or (PA_INT4, PA_INT4), the 8-bit and 4-bit ones with head_dim 128, the 4-bit one with an even
+ * num_kv_heads, the per-token one with num_kv_heads a multiple of 4.  k_scales/v_scales are
+ * required for 8-bit dtypes (k_scales is ignored with PA_FP8_E4M3_TOKEN) and ignored otherwise.
  * num_sink > 0 keeps positions < num_sink in k_sink/v_sink (bf16) for any dtype.
  * sliding_window = W > 0 restricts every query to the W most recent positions (ldpk §5.3):
  * a decode query of a ctx-token sequence reads positions max(0, ctx-W) .. ctx-1, a prefill
@@ -143,8 +157,9 @@ const char* pa_status_string(pa_status status);
  *   pos/16 >= max_blocks_per_seq       -> PA_EFLAG_CTX_OVERFLOW, row skipped;
  *   table entry outside [0,num_blocks) -> PA_EFLAG_BAD_BLOCK_ID, row skipped;
  *   otherwise the slot table[s][pos/16]*16 + pos%16 receives the bf16 bits unchanged, or
- *   for 8-bit caches code = round(x / scale[kv_head]) with the division in IEEE fp32, or for
- *   4-bit caches the PA_INT4 codes and group parameters of the row.
+ *   for 8-bit caches code = round(x / scale[kv_head]) with the division in IEEE fp32 (with
+ *   PA_FP8_E4M3_TOKEN the K row's own scale, stored beside it), or for 4-bit caches the
+ *   PA_INT4 codes and group parameters of the row.
  * The caller makes the slot writable first (pa_bm_prepare_step + pa_block_copy) and passes
  * context_lens = positions + 1 to the following pa_decode_attention.
  * Host errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA. */

@@ -90,14 +90,22 @@ pa_status validate_desc(const pa_cache_desc* d) {
   if ((long long)d->num_blocks * PA_BLOCK_SIZE > (long long)INT_MAX) return PA_ERR_INVALID_ARG;
   const bool bf16 = d->k_dtype == PA_BF16 && d->v_dtype == PA_BF16;
   const bool q8 = d->k_dtype == PA_FP8_E4M3 && d->v_dtype == PA_INT8;
+  const bool q8t = d->k_dtype == PA_FP8_E4M3_TOKEN && d->v_dtype == PA_INT8;
   const bool q4 = d->k_dtype == PA_INT4 && d->v_dtype == PA_INT4;
-  if (!bf16 && !q8 && !q4) {
-    auto known = [](pa_dtype t) { return t == PA_BF16 || t == PA_FP8_E4M3 || t == PA_INT8 || t == PA_INT4; };
+  if (!bf16 && !q8 && !q8t && !q4) {
+    auto known = [](pa_dtype t) {
+      return t == PA_BF16 || t == PA_FP8_E4M3 || t == PA_INT8 || t == PA_INT4 || t == PA_FP8_E4M3_TOKEN;
+    };
     return known(d->k_dtype) && known(d->v_dtype) ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
   }
   if (q8) {
     if (d->head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (!d->k_scales || !d->v_scales) return PA_ERR_INVALID_ARG;
+  }
+  if (q8t) {
+    // the scales of a block's heads move as 16-byte TMA rows: num_kv_heads a multiple of 4
+    if (d->head_dim != 128 || d->num_kv_heads % 4 != 0) return PA_ERR_UNSUPPORTED;
+    if (!d->v_scales) return PA_ERR_INVALID_ARG;
   }
   if (q4 && (d->head_dim != 128 || d->num_kv_heads % 2 != 0)) return PA_ERR_UNSUPPORTED;
   if (d->num_sink > 0 && (!d->k_sink || !d->v_sink)) return PA_ERR_INVALID_ARG;

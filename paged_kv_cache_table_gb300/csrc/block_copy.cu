@@ -15,10 +15,11 @@ namespace pa {
 namespace {
 
 // grid.y = tensor (K, V) x region: region 0 is the block's codes (block_vecs vectors per block),
-// region 1 (int4 pools only) its group parameters (param_vecs per block at param_base).
+// region 1 its group parameters (int4 pools) or per-token scales (K of a PA_FP8_E4M3_TOKEN pool):
+// param_vecs per block at param_base, for the tensors whose bit is set in param_mask.
 __global__ void __launch_bounds__(256) block_copy_kernel(const int32_t* pairs, int num_blocks,
                                                          size_t block_vecs, size_t param_base,
-                                                         size_t param_vecs, uint4* k_cache,
+                                                         size_t param_vecs, int param_mask, uint4* k_cache,
                                                          uint4* v_cache, int32_t* err) {
   const int i = blockIdx.x;
   const int src = pairs[2 * i];
@@ -28,6 +29,7 @@ __global__ void __launch_bounds__(256) block_copy_kernel(const int32_t* pairs, i
     return;
   }
   if (src == dst) return;
+  if (blockIdx.y >= 2 && !((param_mask >> (blockIdx.y & 1)) & 1)) return;
   uint4* base = (blockIdx.y & 1) == 0 ? k_cache : v_cache;
   size_t n = block_vecs;
   if (blockIdx.y >= 2) {
@@ -52,14 +54,19 @@ extern "C" pa_status pa_block_copy(const pa_cache_desc* desc, void* k_cache, voi
   if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
     return PA_ERR_INVALID_ARG;
-  const bool int4 = pa::is_int4(desc);
+  const bool int4 = pa::is_int4(desc), tok = pa::has_token_scales(desc);
   const size_t row = int4 ? pa::int4_code_row_bytes(desc)
                           : static_cast<size_t>(desc->head_dim) * pa::dtype_bytes(desc->k_dtype);
   const size_t kbytes = static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * row;
-  const size_t pbytes = int4 ? static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * pa::int4_param_row_bytes(desc)
-                             : 0;
-  pa::block_copy_kernel<<<dim3(n_pairs, int4 ? 4 : 2), 256, 0, pa::as_stream(stream)>>>(
-      src_dst_pairs, desc->num_blocks, kbytes / 16, int4 ? pa::int4_params_offset(desc) / 16 : 0, pbytes / 16,
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), err_flag);
+  // int4: both tensors' group parameters; per-token K: 16 x num_kv_heads fp32 scales (a multiple
+  // of 16 bytes, num_kv_heads being a multiple of 4)
+  const size_t pbytes = int4  ? static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * pa::int4_param_row_bytes(desc)
+                        : tok ? static_cast<size_t>(PA_BLOCK_SIZE) * desc->num_kv_heads * 4
+                              : 0;
+  const size_t pbase = int4 ? pa::int4_params_offset(desc) : (tok ? pa::token_scales_offset(desc) : 0);
+  const int mask = int4 ? 3 : (tok ? 1 : 0);
+  pa::block_copy_kernel<<<dim3(n_pairs, mask ? 4 : 2), 256, 0, pa::as_stream(stream)>>>(
+      src_dst_pairs, desc->num_blocks, kbytes / 16, pbase / 16, pbytes / 16, mask, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), err_flag);
   return pa::launch_status();
 }

@@ -4,7 +4,8 @@
 // row per head against every cached key, softmax(q·Kᵀ·scale)·V.  GQA ("KV Cache 的显存账本：
 // PagedAttention 与连续批处理" §二): every G consecutive query heads read one KV head.  The keys
 // and values are fetched from non-contiguous physical blocks through the block table
-// (ldpk §4.3; 显存账本 §四 locate()).  8-bit caches (显存账本 §七) are decoded in registers.
+// (ldpk §4.3; 显存账本 §四 locate()).  8-bit caches (显存账本 §七) are decoded in registers; with
+// per-token K scales (ldpk §5.2) each token's score takes its own K scale.
 // Under a sliding window (ldpk §5.3) only the blocks holding the last W positions are listed,
 // so the work, the bytes and the table entries read scale with W, not with the context.
 //
@@ -72,6 +73,7 @@ struct DecodeParams {
   int window;  // sliding window in tokens, 0 = whole context
   int hg, nc, nbs, stages, warps_c;
   int block_bytes;  // shared-memory bytes of one block in a stage
+  int block_tx;     // bytes the copies of one block deliver (block_bytes less alignment padding)
   int mode;  // 0 balanced, 1 fixed partitions
   int ppb, max_parts;
   int direct_ok;
@@ -150,10 +152,12 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const DecodeParams& p) {
 // Consumer: one warp = one KV head x one block slot of every stage.
 // ------------------------------------------------------------------------------------
 // KIND 0: bf16 K and V; 1: FP8 E4M3 K and INT8 V with per-head scales; 2: INT4 K and V with a
-// scale and zero point per 32 dims of every token's head row.
+// scale and zero point per 32 dims of every token's head row; 3: as 1, but K with one scale per
+// token's head row (the block's scales follow its K and V tiles in the stage).
 template <int D, int KIND>
 struct Consumer {
-  static constexpr bool QUANT = KIND == 1;
+  static constexpr bool QUANT = KIND == 1 || KIND == 3;
+  static constexpr bool TOKS = KIND == 3;
   static constexpr bool I4 = KIND == 2;
   static constexpr int KT = D / 16;  // k-steps of q·Kᵀ and m-tiles of P·V
   static constexpr int NC = KIND != 0 ? 1 : D * 2 / 128;  // 128-byte chunks per head row
@@ -168,7 +172,7 @@ struct Consumer {
   float qz[4][2], cz[4][2];
   bool bad;
   int lane, t4, tq, h_kv, j, h_loc;
-  uint32_t kofs, vofs, kpofs, vpofs;  // this warp's tiles inside a stage
+  uint32_t kofs, vofs, kpofs, vpofs;  // this warp's tiles inside a stage (kpofs: K scales, KIND 3)
   // INT4: this lane's byte offsets inside a stage (they depend only on the lane and the head):
   // K codes of tokens t4, t4 + 8; V codes of tokens 2tq, 2tq+1, 2tq+8, 2tq+9; K and V group
   // parameters of tokens t4, t4 + 8
@@ -195,9 +199,12 @@ struct Consumer {
       ivp[0] = vpofs + (t4 * p_.hg + h_loc_) * 16;
       ivp[1] = vpofs + ((t4 + 8) * p_.hg + h_loc_) * 16;
     } else {
-      kofs = ((j * 2 + 0) * p_.hg * p_.nc + h_loc_ * p_.nc) * kTileBytes;
-      vofs = ((j * 2 + 1) * p_.hg * p_.nc + h_loc_ * p_.nc) * kTileBytes;
-      kpofs = vpofs = 0;
+      // block j of a stage: [K tiles][V tiles] (hg heads x nc tiles each), then (KIND 3) the
+      // K scales [16 slots][hg heads] fp32
+      kofs = j * p_.block_bytes + h_loc_ * p_.nc * kTileBytes;
+      vofs = kofs + p_.hg * p_.nc * kTileBytes;
+      kpofs = j * p_.block_bytes + 2 * p_.hg * p_.nc * kTileBytes + h_loc_ * 4;
+      vpofs = 0;
     }
     reset();
   }
@@ -281,7 +288,8 @@ struct Consumer {
       }
       const int e_c0 = __shfl_sync(0xffffffffu, e2, 4 * (2 * tq));
       const int e_c1 = __shfl_sync(0xffffffffu, e2, 4 * (2 * tq + 1));
-      const float base = p.scale_log2 * p.k_scales[h_kv];
+      // per-token K scales multiply each token's score in scores() instead
+      const float base = TOKS ? p.scale_log2 : p.scale_log2 * p.k_scales[h_kv];
       sl[0] = base * ldexpf(1.f, -e_c0);
       sl[1] = base * ldexpf(1.f, -e_c1);
       vsc = p.v_scales[h_kv];
@@ -398,6 +406,15 @@ struct Consumer {
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
+    if constexpr (TOKS) {
+      // rows t4 and t4 + 8 of the block: their tokens' K scales ([slot][head] fp32 in the stage)
+      const float s0 = *reinterpret_cast<const float*>(stage + kpofs + t4 * p.hg * 4);
+      const float s1 = *reinterpret_cast<const float*>(stage + kpofs + (t4 + 8) * p.hg * 4);
+      acc[0] *= s0;
+      acc[1] *= s0;
+      acc[2] *= s1;
+      acc[3] *= s1;
+    }
   }
 
   // Online-softmax update over NB blocks' scores at once (one maximum, one rescale check);
@@ -745,8 +762,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     // tensor: the whole head rows of the group's heads for the block's 16 slots, head-major.
     // (Measured, issuing a box costs about 90 cycles whatever its size, so fewer, larger boxes
     // keep the producer ahead of HBM.)  INT4 stages take four boxes per block: K and V codes of
-    // all the group's heads (128-byte rows of two heads), then K and V group parameters.
-    const int ops_per_block = KIND == 2 ? 4 : 2;
+    // all the group's heads (128-byte rows of two heads), then K and V group parameters.  With
+    // per-token K scales a third box per block carries the block's [16 slots][hg heads] scales.
+    const int ops_per_block = KIND == 2 ? 4 : (KIND == 3 ? 3 : 2);
     const int n_ops = nbs * ops_per_block;  // <= 32
     const uint64_t policy = l2_evict_first_policy();
     // this lane's op (fixed for every stage): block jj of the stage, tensor, head
@@ -762,10 +780,10 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       my_dst = static_cast<size_t>(my_jj) * p.block_bytes +
                (prm ? 2 * p.hg * 1024 + t * p.hg * 256 : t * p.hg * 1024);
     } else {
-      const int my_t = my_op;
-      my_map = my_t ? &tmV : &tmK;
+      const int my_t = my_op;  // 0 K, 1 V, 2 K scales
+      my_map = my_t == 2 ? &tmKp : (my_t ? &tmV : &tmK);
       my_row = hgi * p.hg;  // first head of the box
-      my_dst = static_cast<size_t>(my_jj * 2 + my_t) * p.hg * p.nc * kTileBytes;
+      my_dst = static_cast<size_t>(my_jj) * p.block_bytes + static_cast<size_t>(my_t) * p.hg * p.nc * kTileBytes;
     }
     // logical block of list entry u of sequence s (the visited blocks start at the window)
     auto logical = [&](int s, int u) { return window_lo(p, sm.ctxs[s]) / PA_BLOCK_SIZE + (u - sm.cum[s]); };
@@ -825,7 +843,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
       }
       if (lane >= i && lane < i + nbs) sm.meta[st * nbs + (lane - i)] = my_meta;
       if (lane == 0) {
-        const uint32_t bytes = __popc(live) * static_cast<uint32_t>(p.block_bytes);
+        const uint32_t bytes = __popc(live) * static_cast<uint32_t>(p.block_tx);
         if (bytes) mbar_arrive_expect_tx(&sm.full[st], bytes);
         else mbar_arrive(&sm.full[st]);
       }
@@ -834,6 +852,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
         if constexpr (KIND == 2)
           tma_load_3d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], 0,
                       my_row, pb * PA_BLOCK_SIZE, policy);
+        else if (KIND == 3 && my_op == 2)
+          tma_load_2d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], my_row,
+                      pb * PA_BLOCK_SIZE, policy);
         else
           tma_load_4d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], 0, 0,
                       pb * PA_BLOCK_SIZE, my_row, policy);
@@ -1099,7 +1120,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
 struct Plan {
   int hg, n_hg, nc, nbs, warps_c, threads, stages;
   int mode, ppb, max_parts, grid_x;
-  int stage_bytes, block_bytes;
+  int stage_bytes, block_bytes, block_tx;
   size_t smem_bytes, meta_bytes, ws_bytes, n_slots;
 };
 
@@ -1108,15 +1129,18 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
   pa_status st = validate_desc(d);
   if (st != PA_OK) return st;
   if (max_ctx < 0 || partition_size < 0 || partition_size % PA_BLOCK_SIZE != 0) return PA_ERR_INVALID_ARG;
-  const bool int4 = is_int4(d);
+  const bool int4 = is_int4(d), tok = has_token_scales(d);
   const int e = dtype_bytes(d->k_dtype);
   const int row_bytes = int4 ? d->head_dim / 2 : d->head_dim * e;  // 64, 128 or 256
   pl->nc = int4 ? 1 : row_bytes / 128;
+  // per-token K scales travel as a [16 slots][hg heads] fp32 box: hg x 4 bytes a multiple of 16
   int hg = 1;
   for (int c = 1; c <= d->num_kv_heads; ++c)
-    if (d->num_kv_heads % c == 0 && c * row_bytes <= PA_GROUP_BYTES && (!int4 || (c % 2 == 0 && c <= PA_I4_MAX_HG)))
+    if (d->num_kv_heads % c == 0 && c * row_bytes <= PA_GROUP_BYTES && (!int4 || (c % 2 == 0 && c <= PA_I4_MAX_HG)) &&
+        (!tok || c % 4 == 0))
       hg = c;
   if (int4 && hg % 2 != 0) return PA_ERR_UNSUPPORTED;
+  if (tok && hg % 4 != 0) return PA_ERR_UNSUPPORTED;
   pl->hg = hg;
   pl->n_hg = d->num_kv_heads / hg;
   // Blocks per stage: a power of two, so that a stage never straddles the 32-entry chunks in
@@ -1127,8 +1151,11 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
   pl->warps_c = hg * pl->nbs;
   if (pl->warps_c > kMaxConsumerWarps) return PA_ERR_UNSUPPORTED;
   pl->threads = (pl->warps_c + 1) * 32;
-  // int4 block: K and V codes (hg x 1 KiB each) and group parameters (hg x 256 B each)
-  pl->block_bytes = int4 ? 2560 * hg : 2 * hg * pl->nc * kTileBytes;
+  // int4 block: K and V codes (hg x 1 KiB each) and group parameters (hg x 256 B each); a
+  // per-token block: K and V tiles, then the K scales padded to 1 KiB, so that the next block's
+  // swizzled tiles stay 1024-byte aligned
+  pl->block_tx = int4 ? 2560 * hg : 2 * hg * pl->nc * kTileBytes + (tok ? 64 * hg : 0);
+  pl->block_bytes = tok ? 2 * hg * pl->nc * kTileBytes + (64 * hg + 1023) / 1024 * 1024 : pl->block_tx;
   pl->stage_bytes = pl->nbs * pl->block_bytes;
   const int B = d->num_seqs;
   if (B > 65535) return PA_ERR_UNSUPPORTED;  // grid.y of the fixed-partition launch
@@ -1235,8 +1262,12 @@ pa_status decode_attention_impl(const pa_cache_desc* desc, void* out, const void
     if (!pa::encode_cache_map_heads(&mk, k_cache, e, desc->num_kv_heads, pl.nc, pl.hg, slots) ||
         !pa::encode_cache_map_heads(&mv, v_cache, e, desc->num_kv_heads, pl.nc, pl.hg, slots))
       return PA_ERR_CUDA;
-    mkp = mk;  // unused by the bf16 and 8-bit kernels
+    mkp = mk;  // unused by the bf16 and per-head 8-bit kernels
     mvp = mv;
+    if (pa::has_token_scales(desc) &&
+        !pa::encode_scale_map(&mkp, static_cast<const uint8_t*>(k_cache) + pa::token_scales_offset(desc),
+                              desc->num_kv_heads, pl.hg, slots))
+      return PA_ERR_CUDA;
   }
 
   pa::DecodeParams p;
@@ -1260,6 +1291,7 @@ pa_status decode_attention_impl(const pa_cache_desc* desc, void* out, const void
   p.direct_ok = (pl.nbs == 1 && desc->num_sink == 0) ? 1 : 0;
   p.stage_bytes = pl.stage_bytes;
   p.block_bytes = pl.block_bytes;
+  p.block_tx = pl.block_tx;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.block_tables = block_tables;
   p.context_lens = context_lens;
@@ -1277,9 +1309,10 @@ pa_status decode_attention_impl(const pa_cache_desc* desc, void* out, const void
   cudaStream_t s = pa::as_stream(stream);
   const bool quant = pa::is_quantized(desc);
   if (desc->head_dim == 128)
-    return int4    ? pa::launch<128, 2>(pl, mk, mv, mkp, mvp, p, s)
-           : quant ? pa::launch<128, 1>(pl, mk, mv, mkp, mvp, p, s)
-                   : pa::launch<128, 0>(pl, mk, mv, mkp, mvp, p, s);
+    return int4                         ? pa::launch<128, 2>(pl, mk, mv, mkp, mvp, p, s)
+           : pa::has_token_scales(desc) ? pa::launch<128, 3>(pl, mk, mv, mkp, mvp, p, s)
+           : quant                      ? pa::launch<128, 1>(pl, mk, mv, mkp, mvp, p, s)
+                                        : pa::launch<128, 0>(pl, mk, mv, mkp, mvp, p, s);
   return pa::launch<64, 0>(pl, mk, mv, mkp, mvp, p, s);
 }
 }  // namespace

@@ -6,7 +6,8 @@
 // 8-bit caches hold K as FP8 and V as INT8 with one scale per KV head, and sink tokens keep
 // their original precision.  Untitled KV-cache article at ldpk.cn/news/58971 §5.2: 4-bit caches
 // keep a scale and a zero point besides the codes; here one of each per 32 dims of a token's
-// head row (the PA_INT4 rule in pa.h).
+// head row (the PA_INT4 rule in pa.h).  Same section: K's outlier channels call for finer scales
+// than one per head; PA_FP8_E4M3_TOKEN K rows carry their own scale, max|x| / 448.
 //
 // bf16 and 8-bit caches: one warp per appended row, 8 rows per CTA; a lane moves 16-byte bf16
 // vectors.  The row's K and V are loaded before the table lookup that places them (they do
@@ -35,7 +36,8 @@ struct AppendParams {
   const float* v_scales;
   uint4* k_sink;
   uint4* v_sink;
-  size_t params_offset;  // int4: byte offset of the group parameters in each pool
+  size_t params_offset;  // int4: byte offset of the group parameters in each pool; per-token K: of
+                         // the K scales
   int32_t* err;
 };
 
@@ -124,7 +126,7 @@ __device__ __forceinline__ void encode_int4_group(const uint4* src, int h, int g
       sb | (static_cast<uint32_t>(z) << 16);
 }
 
-template <int KIND>  // 0 bf16, 1 fp8 K / int8 V
+template <int KIND>  // 0 bf16, 1 fp8 K / int8 V, 2 fp8 K with per-token scales / int8 V
 __global__ void __launch_bounds__(256) kv_append_rows_kernel(const AppendParams p) {
   // the decode kernel that usually follows may start its prologue now: it waits for this
   // kernel's completion before it reads the cache
@@ -179,8 +181,26 @@ __global__ void __launch_bounds__(256) kv_append_rows_kernel(const AppendParams 
     return;
   }
   const size_t slot = static_cast<size_t>(pb) * PA_BLOCK_SIZE + pos % PA_BLOCK_SIZE;
+  // Every lane of the warp calls put for the same number of vectors (vecs is a multiple of 32 on
+  // the per-token path), so the half-warp reductions below see all their lanes.
   auto put = [&](int i, const uint4& k4, const uint4& v4) {
-    if constexpr (KIND == 1) {
+    if constexpr (KIND == 2) {
+      // head_dim 128: a head row is 16 vectors, held by one half-warp
+      const int h = i >> 4;
+      float x[8];
+      unpack_bf16x8(k4, x);
+      float a = 0.f;  // fmaxf leaves NaN out of the maximum
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(x[e]));
+#pragma unroll
+      for (int m = 1; m < 16; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+      float sc = __fdiv_rn(a, 448.f);
+      if (sc == 0.f) sc = 1.f;  // an all-zero row: any scale encodes it exactly
+      reinterpret_cast<uint2*>(p.k_cache)[slot * vecs + i] = encode_e4m3x8(k4, sc);
+      reinterpret_cast<uint2*>(p.v_cache)[slot * vecs + i] = encode_int8x8(v4, p.v_scales[h]);
+      if ((i & 15) == 0)
+        reinterpret_cast<float*>(static_cast<uint8_t*>(p.k_cache) + p.params_offset)[slot * p.H_kv + h] = sc;
+    } else if constexpr (KIND == 1) {
       const int h = (i * 8) / p.D;
       reinterpret_cast<uint2*>(p.k_cache)[slot * vecs + i] = encode_e4m3x8(k4, p.k_scales[h]);
       reinterpret_cast<uint2*>(p.v_cache)[slot * vecs + i] = encode_int8x8(v4, p.v_scales[h]);
@@ -271,12 +291,14 @@ pa_status append_impl(const pa_cache_desc* d, void* k_cache, void* v_cache, cons
   p.k_sink = static_cast<uint4*>(d->k_sink);
   p.v_sink = static_cast<uint4*>(d->v_sink);
   p.err = err;
-  p.params_offset = is_int4(d) ? int4_params_offset(d) : 0;
+  p.params_offset = is_int4(d) ? int4_params_offset(d) : (has_token_scales(d) ? token_scales_offset(d) : 0);
   const int vecs = p.H_kv * p.D / 8;
   constexpr int kRowsPerCta = 8;
   const int grid = (num_rows + kRowsPerCta - 1) / kRowsPerCta;
   if (is_int4(d))
     kv_append_int4_kernel<<<num_rows, min(256, ((vecs + 31) / 32) * 32), 0, as_stream(stream)>>>(p);
+  else if (has_token_scales(d))
+    kv_append_rows_kernel<2><<<grid, 32 * kRowsPerCta, 0, as_stream(stream)>>>(p);
   else if (is_quantized(d))
     kv_append_rows_kernel<1><<<grid, 32 * kRowsPerCta, 0, as_stream(stream)>>>(p);
   else

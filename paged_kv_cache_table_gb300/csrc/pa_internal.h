@@ -16,6 +16,12 @@ inline bool is_quantized(const pa_cache_desc* d) { return d->k_dtype != PA_BF16;
 
 inline bool is_int4(const pa_cache_desc* d) { return d->k_dtype == PA_INT4; }
 
+// PA_FP8_E4M3_TOKEN: the K pool holds every slot's codes, then an fp32 scale per (slot, head).
+inline bool has_token_scales(const pa_cache_desc* d) { return d->k_dtype == PA_FP8_E4M3_TOKEN; }
+inline size_t token_scales_offset(const pa_cache_desc* d) {
+  return static_cast<size_t>(d->num_blocks) * PA_BLOCK_SIZE * d->num_kv_heads * d->head_dim;
+}
+
 // INT4 pools: code bytes of every slot first, then the group parameter words.
 constexpr int kInt4Group = 32;
 inline size_t int4_code_row_bytes(const pa_cache_desc* d) { return static_cast<size_t>(d->head_dim) / 2; }
@@ -42,6 +48,10 @@ bool encode_cache_map_heads(CUtensorMap* map, const void* base, int elem_bytes, 
 // TMA descriptor of the INT4 group parameters viewed as (16-byte head row, kv_head, slot) with
 // boxes of `box_heads` heads x 16 slots, no swizzle (tensor_map.cpp).
 bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots);
+
+// TMA descriptor of per-token K scales [slots][heads] fp32 with boxes of box_heads heads x 16 slots,
+// no swizzle (tensor_map.cpp).
+bool encode_scale_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots);
 
 // TMA descriptor of bf16 queries [T][heads][128] viewed as (64 dims, half, head, token) with boxes
 // of one half x G heads x tokens_per_box tokens, 128-byte swizzle (tensor_map.cpp).

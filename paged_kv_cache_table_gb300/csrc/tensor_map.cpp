@@ -78,6 +78,21 @@ bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_hea
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Per-token K scales [slots][heads] fp32 as a 2-D tensor with boxes of box_heads heads x 16 slots
+// (one block), no swizzle: a box lands as [slot][head] fp32.  box_heads * 4 and heads * 4 must be
+// multiples of 16 bytes.
+bool encode_scale_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(slots)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_heads), PA_BLOCK_SIZE};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Queries [T][H_q][128] bf16 as a 4-D tensor (64 dims of a half row, half, query head, token) with
 // boxes of one half x G heads x tokens_per_box tokens: a box lands as tokens_per_box * G rows of
 // 128 bytes, row (token, head), with the 128-byte swizzle.  `tokens` is the extent of the token

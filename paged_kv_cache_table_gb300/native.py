@@ -26,6 +26,7 @@ PA_BF16 = 0
 PA_FP8_E4M3 = 1
 PA_INT8 = 2
 PA_INT4 = 3
+PA_FP8_E4M3_TOKEN = 4
 
 PA_EFLAG_BAD_BLOCK_ID = 1
 PA_EFLAG_CTX_OVERFLOW = 2
@@ -34,7 +35,8 @@ PA_EFLAG_TIMEOUT = 8
 
 BLOCK_SIZE = 16
 
-_DTYPES = {"bf16": PA_BF16, "fp8_e4m3": PA_FP8_E4M3, "e4m3": PA_FP8_E4M3, "int8": PA_INT8, "int4": PA_INT4}
+_DTYPES = {"bf16": PA_BF16, "fp8_e4m3": PA_FP8_E4M3, "e4m3": PA_FP8_E4M3, "int8": PA_INT8, "int4": PA_INT4,
+           "e4m3_tok": PA_FP8_E4M3_TOKEN}
 
 # Every symbol the header declares, for load checks.
 EXPORTED = [

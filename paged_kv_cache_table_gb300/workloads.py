@@ -26,6 +26,9 @@ Workloads (seed = 20260 + index):
                   window's positions are written.
   8 "int4_8b"     the 8b shape (64 sequences, cached U[512, 4096], 32 / 8 heads, d 128) with K and V
                   stored as INT4 codes with a scale and zero point per 32 dims of every row.
+  9 "long_quant_tok"  the long_quant shape with K stored FP8 E4M3 with one scale per token's head
+                  row (computed by the cache from each row, so no K calibration scales are
+                  drawn), V INT8 with per-KV-head scales, 4 bf16 sinks.
 Every step appends one token per sequence at position = cached length, then attends over
 cached length + 1 tokens.  All tensors are produced on the CPU with a torch.Generator.
 """
@@ -48,6 +51,8 @@ CONFIGS = {
     "long_quant": dict(index=5, B=4, H_q=32, H_kv=8, D=128, ctx_fixed=131072, quant=True, num_sink=4),
     "swa": dict(index=7, B=64, H_q=32, H_kv=8, D=128, ctx_range=(4096, 16384), window=4096),
     "int4_8b": dict(index=8, B=64, H_q=32, H_kv=8, D=128, ctx_range=(512, 4096), kv="int4"),
+    "long_quant_tok": dict(index=9, B=4, H_q=32, H_kv=8, D=128, ctx_fixed=131072, quant=True, num_sink=4,
+                           kv="e4m3_tok"),
 }
 
 # Calibration code ranges of the 8-bit formats (largest finite E4M3 value; symmetric int8).
@@ -102,11 +107,15 @@ class Workload:
         return 1 if self.k_dtype != "bf16" else 2
 
     def kv_row_bytes(self) -> int:
-        """Cache bytes of one (token, KV head) row of K or V: int4 holds 4-bit codes plus one
-        32-bit scale / zero-point word per 32 dims."""
+        """Cache bytes of one (token, KV head) row of V (and of K, except with per-token K
+        scales): int4 holds 4-bit codes plus one 32-bit scale / zero-point word per 32 dims."""
         if self.k_dtype == "int4":
             return self.D // 2 + self.D // 32 * 4
         return self.D * self.kv_elem_bytes()
+
+    def k_row_bytes(self) -> int:
+        """Cache bytes of one (token, KV head) row of K: per-token K scales add a 4-byte scale."""
+        return self.kv_row_bytes() + (4 if self.k_dtype == "e4m3_tok" else 0)
 
 
 def _randn_bf16(g, shape, chunk_rows=1 << 16):
@@ -198,6 +207,7 @@ def make_workload(name: str, steps: int = 1, **overrides) -> Workload:
     v_new = _randn_bf16(g, (steps * B, H_kv, D)).view(steps, B, H_kv, D)
 
     k_scales = v_scales = None
+    kv = cfg.get("kv")
     if quant:
         keep = torch.from_numpy(fill_pos >= num_sink)
         k_abs = torch.zeros(H_kv)
@@ -208,13 +218,13 @@ def make_workload(name: str, steps: int = 1, **overrides) -> Workload:
             if m.any():
                 k_abs = torch.maximum(k_abs, fill_k[a:a + chunk][m].float().abs().amax(dim=(0, 2)))
                 v_abs = torch.maximum(v_abs, fill_v[a:a + chunk][m].float().abs().amax(dim=(0, 2)))
-        k_scales = (k_abs / E4M3_RANGE).to(torch.float32)
+        k_scales = None if kv == "e4m3_tok" else (k_abs / E4M3_RANGE).to(torch.float32)
         v_scales = (v_abs / INT8_RANGE).to(torch.float32)
 
-    int4 = cfg.get("kv") == "int4"
+    int4 = kv == "int4"
     return Workload(
         name=name, seed=seed, B=B, H_q=H_q, H_kv=H_kv, D=D,
-        k_dtype="int4" if int4 else ("e4m3" if quant else "bf16"),
+        k_dtype="int4" if int4 else (("e4m3_tok" if kv == "e4m3_tok" else "e4m3") if quant else "bf16"),
         v_dtype="int4" if int4 else ("int8" if quant else "bf16"),
         num_sink=num_sink, scale=1.0 / math.sqrt(D), num_blocks=num_blocks, max_blocks=max_blocks,
         steps=steps, ctx_old=ctx.astype(np.int32), tables=tables, fill_k=fill_k, fill_v=fill_v,

@@ -24,6 +24,9 @@ INT8_OUTSIDE = 0x80
 # int4 pools: every code nibble 15 and every group parameter word all ones (a NaN scale, zero
 # point 255)
 INT4_FILL = 0xFF
+# per-token K pools: every byte 0x7F, i.e. NaN codes and never-written scales of 0x7F7F7F7F
+# (3.4e38); an attention that read either would not stay finite
+TOK_FILL = 0x7F
 
 ATOL_MAX = 2e-2   # attention: max |gpu - oracle|
 ATOL_MEAN = 2e-3  # attention: mean |gpu - oracle|
@@ -50,6 +53,9 @@ class GpuState:
             nbytes = n_slots * w.H_kv * w.kv_row_bytes()
             self.k = torch.full((nbytes,), INT4_FILL, dtype=torch.uint8, device=device)
             self.v = torch.full((nbytes,), INT4_FILL, dtype=torch.uint8, device=device)
+        elif w.k_dtype == "e4m3_tok":
+            self.k = torch.full((n_slots * w.H_kv * w.k_row_bytes(),), TOK_FILL, dtype=torch.uint8, device=device)
+            self.v = torch.full(shape, INT8_OUTSIDE, dtype=torch.uint8, device=device)
         else:
             self.k = torch.full(shape, E4M3_NAN, dtype=torch.uint8, device=device)
             self.v = torch.full(shape, INT8_OUTSIDE, dtype=torch.uint8, device=device)
@@ -185,6 +191,10 @@ class OracleState:
             self.cache.v[:] = 15
             self.cache.k_params[:] = 0xFFFFFFFF
             self.cache.v_params[:] = 0xFFFFFFFF
+        elif w.k_dtype == "e4m3_tok":
+            self.cache.k[:] = TOK_FILL
+            self.cache.k_tscale.view(np.uint32)[:] = 0x7F7F7F7F
+            self.cache.v[:] = INT8_OUTSIDE
         else:
             self.cache.k[:] = E4M3_NAN
             self.cache.v[:] = INT8_OUTSIDE
@@ -285,10 +295,25 @@ def unpack_int4_pool(raw: np.ndarray, n_slots: int, H: int, D: int, tensor: str)
     return codes, params
 
 
+def unpack_tok_pool(raw: np.ndarray, n_slots: int, H: int, D: int):
+    """Codes [slot][head][D] and fp32 scales [slot][head] of a GPU per-token K pool, read by the
+    layout the library documents for PA_FP8_E4M3_TOKEN (codes of every slot, then the scales)."""
+    code_bytes = n_slots * H * D
+    codes = raw[:code_bytes].reshape(n_slots, H, D)
+    scales = raw[code_bytes:code_bytes + n_slots * H * 4].view(np.float32).reshape(n_slots, H)
+    return codes, scales
+
+
 def assert_pools_equal(gpu: GpuState, ora: OracleState):
     gk, gv, gks, gvs = gpu.pools()
     assert np.array_equal(gpu.tables, ora.tables.astype(np.int32)), "block tables differ"
-    if gpu.w.k_dtype == "int4":
+    if gpu.w.k_dtype == "e4m3_tok":
+        w = gpu.w
+        kc, ks = unpack_tok_pool(gk, w.num_blocks * 16, w.H_kv, w.D)
+        assert np.array_equal(kc, ora.cache.k), "K codes differ"
+        assert np.array_equal(ks.view(np.uint32), ora.cache.k_tscale.view(np.uint32)), "K token scales differ"
+        assert np.array_equal(gv, ora.cache.v), "V pool differs"
+    elif gpu.w.k_dtype == "int4":
         w = gpu.w
         n_slots = w.num_blocks * 16
         kc, kp = unpack_int4_pool(gk, n_slots, w.H_kv, w.D, "k")
@@ -351,6 +376,10 @@ def _decode_head(k_dtype, num_sink, ks, vs, kb, vb, pos0):
     elif k_dtype == "int4":
         K[ns:] = O.int4_decode_row(*O.int4_encode_row(kb[ns:]))
         V[ns:] = O.int4_decode_row(*O.int4_encode_row(vb[ns:]))
+    elif k_dtype == "e4m3_tok":
+        codes, sc = O.quantize_token_rows(kb[ns:])
+        K[ns:] = O.e4m3_decode(codes) * sc.astype(np.float64)[:, None]
+        V[ns:] = O.int8_decode(O.quantize_row(vb[ns:], vs, "int8").view(np.int8)) * float(vs)
     else:
         K[ns:] = O.e4m3_decode(O.quantize_row(kb[ns:], ks, "e4m3")) * float(ks)
         V[ns:] = O.int8_decode(O.quantize_row(vb[ns:], vs, "int8").view(np.int8)) * float(vs)
@@ -358,9 +387,9 @@ def _decode_head(k_dtype, num_sink, ks, vs, kb, vb, pos0):
 
 
 def _head_scales(w: Workload, h: int):
-    if w.k_scales is None:
-        return None, None
-    return np.float32(w.k_scales[h].item()), np.float32(w.v_scales[h].item())
+    ks = None if w.k_scales is None else np.float32(w.k_scales[h].item())
+    vs = None if w.v_scales is None else np.float32(w.v_scales[h].item())
+    return ks, vs
 
 
 def _head_task(args):

@@ -92,6 +92,13 @@ host_only = pytest.mark.skipif(not _no_gpu(), reason="fake device addresses: run
     # INT4 needs head_dim 128 and an even number of KV heads
     (dict(k_dtype=N.PA_INT4, v_dtype=N.PA_INT4, num_q_heads=6, num_kv_heads=3, head_dim=128), N.PA_ERR_UNSUPPORTED),
     (dict(k_dtype=N.PA_INT4, v_dtype=N.PA_INT4, head_dim=64), N.PA_ERR_UNSUPPORTED),
+    # per-token K scales: head_dim 128, KV heads a multiple of 4, V scales required, V INT8 only
+    (dict(k_dtype="e4m3_tok", v_dtype="int8", head_dim=128, num_kv_heads=4), N.PA_ERR_INVALID_ARG),
+    (dict(k_dtype="e4m3_tok", v_dtype="int8", head_dim=64, v_scales=FAKE), N.PA_ERR_UNSUPPORTED),
+    (dict(k_dtype="e4m3_tok", v_dtype="int8", head_dim=128, num_q_heads=12, num_kv_heads=6, v_scales=FAKE),
+     N.PA_ERR_UNSUPPORTED),
+    (dict(k_dtype="e4m3_tok", v_dtype="bf16", head_dim=128, v_scales=FAKE), N.PA_ERR_UNSUPPORTED),
+    (dict(k_dtype="int8", v_dtype="e4m3_tok"), N.PA_ERR_UNSUPPORTED),
 ])
 @host_only
 def test_bad_descriptions_are_rejected_on_the_host(kw, status):

@@ -19,7 +19,8 @@ import torch
 import oracle as O
 from paged_kv_cache_table_gb300.workloads import bf16_bits, make_workload
 
-from harness import ATOL_MAX, ATOL_MEAN, GpuState, reference_all, reference_seq, to_f64, unpack_int4_pool
+from harness import (ATOL_MAX, ATOL_MEAN, GpuState, reference_all, reference_seq, to_f64, unpack_int4_pool,
+                     unpack_tok_pool)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -31,6 +32,8 @@ def _check_appended_slots(g, w, step=0):
         n_slots = w.num_blocks * 16
         gk = unpack_int4_pool(gk, n_slots, w.H_kv, w.D, "k")
         gv = unpack_int4_pool(gv, n_slots, w.H_kv, w.D, "v")
+    elif w.k_dtype == "e4m3_tok":
+        gk = unpack_tok_pool(gk, w.num_blocks * 16, w.H_kv, w.D)
     pos = w.positions(step)
     kb, vb = bf16_bits(w.k_new[step]), bf16_bits(w.v_new[step])
     for s in range(w.B):
@@ -45,6 +48,12 @@ def _check_appended_slots(g, w, step=0):
             for pool, bits in ((gk, kb), (gv, vb)):
                 codes, params = O.int4_encode_row(bits[s])
                 assert np.array_equal(pool[0][slot], codes) and np.array_equal(pool[1][slot], params)
+        elif w.k_dtype == "e4m3_tok":
+            codes, sc = O.quantize_token_rows(kb[s])
+            assert np.array_equal(gk[0][slot], codes) and np.array_equal(gk[1][slot], sc)
+            for h in range(w.H_kv):
+                vs = np.float32(w.v_scales[h].item())
+                assert np.array_equal(gv[slot, h], O.quantize_row(vb[s, h], vs, "int8"))
         else:
             for h in range(w.H_kv):
                 ks = np.float32(w.k_scales[h].item())
@@ -69,12 +78,13 @@ def _bits(t):
     return t.view(torch.int16).cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["8b", "70b", "long_quant", "int4_8b", "swa"])
+@pytest.mark.parametrize("name", ["8b", "70b", "long_quant", "long_quant_tok", "int4_8b", "swa"])
 def test_full_size_every_row(name):
     w = make_workload(name, steps=1)
     # the longest contexts run the oracle's (sequence, KV head) pieces on all host cores; the pool
     # is spawned and closed before the first GPU call
-    ref = reference_all(w, 0, processes=min(32, os.cpu_count() or 1) if name == "long_quant" else 0)
+    long_ctx = name.startswith("long_quant")
+    ref = reference_all(w, 0, processes=min(32, os.cpu_count() or 1) if long_ctx else 0)
     g = GpuState(w)
     pos, ctx = w.positions(0), w.context_lens(0)
     assert len(g.prepare(pos)) == 0

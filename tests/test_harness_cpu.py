@@ -26,6 +26,7 @@ def test_reference_all_equals_the_oracle_pool():
     paged pool gives after the same step, for bf16, 8-bit with sinks and INT4 caches."""
     for w in (make_workload("tiny", steps=1),
               make_workload("long_quant", B=2, ctx_fixed=70, steps=1),
+              make_workload("long_quant_tok", B=2, ctx_fixed=70, steps=1),
               make_workload("int4_8b", B=3, ctx_range=(1, 90), H_q=8, H_kv=2, steps=1)):
         ora = OracleState(w)
         out, _ = ora.step(0)
