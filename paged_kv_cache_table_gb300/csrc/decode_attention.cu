@@ -65,7 +65,8 @@ constexpr int kFixedFallbackPartition = 512;
 #define PA_I4_WARPS 8
 #endif
 constexpr int kMaxStages = PA_MAX_STAGES;
-constexpr int kSmemLimit = (PA_CTAS_PER_SM == 1 ? 227 * 1024 : (228 * 1024) / PA_CTAS_PER_SM - 1024);
+// shared memory a CTA may use when `ctas` of them share an SM
+constexpr int smem_limit(int ctas) { return ctas == 1 ? 227 * 1024 : (228 * 1024) / ctas - 1024; }
 constexpr float kNegInf = -INFINITY;
 
 struct DecodeParams {
@@ -174,9 +175,10 @@ struct Consumer {
   int lane, t4, tq, h_kv, j, h_loc;
   uint32_t kofs, vofs, kpofs, vpofs;  // this warp's tiles inside a stage (kpofs: K scales, KIND 3)
   // INT4: this lane's byte offsets inside a stage (they depend only on the lane and the head):
-  // K codes of tokens t4, t4 + 8; V codes of tokens 2tq, 2tq+1, 2tq+8, 2tq+9; K and V group
-  // parameters of tokens t4, t4 + 8
-  uint32_t ik[2], iv[4], ikp[2], ivp[2];
+  // K codes of token t4, V codes of tokens 2tq and 2tq+1, K and V group parameters of token t4.
+  // The tokens 8 slots further sit i4_dslot (codes: the same swizzle phase) or i4_dprm
+  // (parameters) bytes later.
+  uint32_t ik0, iv0, iv1, ikp0, ivp0;
 
   __device__ Consumer(const DecodeParams& p_, int lane_, int h_kv_, int j_, int h_loc_)
       : p(p_), vsc(1.f), lane(lane_), t4(lane_ >> 2), tq(lane_ & 3), h_kv(h_kv_), j(j_), h_loc(h_loc_) {
@@ -188,16 +190,11 @@ struct Consumer {
       vofs = kofs + p_.hg * 1024;
       kpofs = kofs + 2 * p_.hg * 1024;
       vpofs = kpofs + p_.hg * 256;
-      ik[0] = kofs + i4_code_off(t4, tq * 16);
-      ik[1] = kofs + i4_code_off(t4 + 8, tq * 16);
-      iv[0] = vofs + i4_code_off(2 * tq, t4 * 8);
-      iv[1] = vofs + i4_code_off(2 * tq + 1, t4 * 8);
-      iv[2] = vofs + i4_code_off(2 * tq + 8, t4 * 8);
-      iv[3] = vofs + i4_code_off(2 * tq + 9, t4 * 8);
-      ikp[0] = kpofs + (t4 * p_.hg + h_loc_) * 16;
-      ikp[1] = kpofs + ((t4 + 8) * p_.hg + h_loc_) * 16;
-      ivp[0] = vpofs + (t4 * p_.hg + h_loc_) * 16;
-      ivp[1] = vpofs + ((t4 + 8) * p_.hg + h_loc_) * 16;
+      ik0 = kofs + i4_code_off(t4, tq * 16);
+      iv0 = vofs + i4_code_off(2 * tq, t4 * 8);
+      iv1 = vofs + i4_code_off(2 * tq + 1, t4 * 8);
+      ikp0 = kpofs + (t4 * p_.hg + h_loc_) * 16;
+      ivp0 = vpofs + (t4 * p_.hg + h_loc_) * 16;
     } else {
       // block j of a stage: [K tiles][V tiles] (hg heads x nc tiles each), then (KIND 3) the
       // K scales [16 slots][hg heads] fp32
@@ -296,6 +293,11 @@ struct Consumer {
     }
   }
 
+  // INT4: 8 slots further in a codes tile (8 x hg/2 rows of 128 bytes, a multiple of the 8-row
+  // swizzle period) and in a parameter tile (8 x hg rows of 16 bytes)
+  __device__ __forceinline__ uint32_t i4_dslot() const { return 8 * (p.hg >> 1) * 128; }
+  __device__ __forceinline__ uint32_t i4_dprm() const { return 8 * p.hg * 16; }
+
   // INT4: byte x (0..63) of this warp's head row in slot `slot` of a codes tile, whose 128-byte
   // rows hold two heads each and carry the 128-byte swizzle of the TMA box.
   __device__ __forceinline__ uint32_t i4_code_off(int slot, int x) const {
@@ -310,10 +312,10 @@ struct Consumer {
   // the group's scale multiplies the fp32 sum.  P·V: the MMA sums over tokens, so each token's
   // group scale goes into P before the transpose; the output rows are dims 16mt + t4 (+8).
   __device__ __forceinline__ void scores_i4(const uint8_t* stage, float (&acc)[4]) const {
-    const uint4 kw0 = *reinterpret_cast<const uint4*>(stage + ik[0]);
-    const uint4 kw1 = *reinterpret_cast<const uint4*>(stage + ik[1]);
-    const uint4 kq0 = *reinterpret_cast<const uint4*>(stage + ikp[0]);
-    const uint4 kq1 = *reinterpret_cast<const uint4*>(stage + ikp[1]);
+    const uint4 kw0 = *reinterpret_cast<const uint4*>(stage + ik0);
+    const uint4 kw1 = *reinterpret_cast<const uint4*>(stage + ik0 + i4_dslot());
+    const uint4 kq0 = *reinterpret_cast<const uint4*>(stage + ikp0);
+    const uint4 kq1 = *reinterpret_cast<const uint4*>(stage + ikp0 + i4_dprm());
     const uint32_t w0[4] = {kw0.x, kw0.y, kw0.z, kw0.w}, w1[4] = {kw1.x, kw1.y, kw1.z, kw1.w};
     const uint32_t q0[4] = {kq0.x, kq0.y, kq0.z, kq0.w}, q1[4] = {kq1.x, kq1.y, kq1.z, kq1.w};
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
@@ -341,14 +343,14 @@ struct Consumer {
     // scale is replaced by 0 rather than multiplied in
     const bool v0 = t4 < ntok && t4 >= first;
     const bool v1 = t4 + 8 < ntok && t4 + 8 >= first;
-    const uint4 vs0 = *reinterpret_cast<const uint4*>(stage + ivp[0]);
-    const uint4 vs1 = *reinterpret_cast<const uint4*>(stage + ivp[1]);
+    const uint4 vs0 = *reinterpret_cast<const uint4*>(stage + ivp0);
+    const uint4 vs1 = *reinterpret_cast<const uint4*>(stage + ivp0 + i4_dprm());
     const uint32_t sv0w[4] = {vs0.x, vs0.y, vs0.z, vs0.w}, sv1w[4] = {vs1.x, vs1.y, vs1.z, vs1.w};
     // codes of the A columns: tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
-    const uint2 cA = *reinterpret_cast<const uint2*>(stage + iv[0]);
-    const uint2 cB = *reinterpret_cast<const uint2*>(stage + iv[1]);
-    const uint2 cC = *reinterpret_cast<const uint2*>(stage + iv[2]);
-    const uint2 cD = *reinterpret_cast<const uint2*>(stage + iv[3]);
+    const uint2 cA = *reinterpret_cast<const uint2*>(stage + iv0);
+    const uint2 cB = *reinterpret_cast<const uint2*>(stage + iv1);
+    const uint2 cC = *reinterpret_cast<const uint2*>(stage + iv0 + i4_dslot());
+    const uint2 cD = *reinterpret_cast<const uint2*>(stage + iv1 + i4_dslot());
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const float sv0 = v0 ? __uint_as_float(sv0w[g] << 16) : 0.f;
@@ -645,6 +647,130 @@ struct Consumer {
   }
 };
 
+// ------------------------------------------------------------------------------------
+// Producer: streams the CTA's blocks into the stage ring.  Every lane owns one block of the
+// current 32-block chunk: its table entry is loaded one chunk ahead and its stage metadata is
+// packed once when the chunk becomes current, so a stage costs one shuffle, one shared store and
+// one TMA per box.  A block takes one box per tensor: the whole head rows of the group's heads for
+// the block's 16 slots, head-major.  (Measured, issuing a box costs about 90 cycles whatever its
+// size, so fewer, larger boxes keep the producer ahead of HBM.)  INT4 stages take four boxes per
+// block: K and V codes of all the group's heads (128-byte rows of two heads), then K and V group
+// parameters.  With per-token K scales a third box per block carries the block's [16 slots][hg
+// heads] scales.  Run by a warp of its own, or (INT4) by consumer warp 0 between its blocks.
+// ------------------------------------------------------------------------------------
+template <int KIND>
+struct Producer {
+  static constexpr int kOps = KIND == 2 ? 4 : (KIND == 3 ? 3 : 2);  // boxes per block
+  // Where the CTA's list lives: sequences [seq_base, seq_base + nseq), entries [u0, u1).
+  struct Range {
+    int seq_base, nseq, u0, u1;
+  };
+  // what persists from stage to stage: the current 32-block chunk (first entry `base`), this
+  // lane's table entries of it and of the next chunk, its block's metadata, the chunk's live and
+  // append-wait masks, and whether the append has been waited for
+  int base, cur_pb, nxt_pb;
+  int4 my_meta;
+  unsigned live_mask, wait_mask;
+  bool waited;
+
+  // logical block of list entry u of sequence s (the visited blocks start at the window)
+  static __device__ __forceinline__ int logical(const DecodeParams& p, const Smem& sm, int s, int u) {
+    return window_lo(p, sm.ctxs[s]) / PA_BLOCK_SIZE + (u - sm.cum[s]);
+  }
+  static __device__ __forceinline__ int load_entry(const DecodeParams& p, const Smem& sm, const Range& r, int u) {
+    if (u >= r.u1) return -1;
+    const int s = find_seq(sm.cum, r.nseq, u);
+    return p.block_tables[static_cast<size_t>(r.seq_base + s) * p.max_blocks + logical(p, sm, s, u)];
+  }
+
+  __device__ __forceinline__ void init(const DecodeParams& p, const Smem& sm, const Range& r, int lane, bool step) {
+    waited = !step;
+    base = r.u0;
+    cur_pb = load_entry(p, sm, r, base + lane);
+    nxt_pb = load_entry(p, sm, r, base + 32 + lane);
+    pack(p, sm, r, lane, step);
+  }
+
+  __device__ __forceinline__ void pack(const DecodeParams& p, const Smem& sm, const Range& r, int lane, bool step) {
+    const int u = base + lane;
+    const bool valid = u < r.u1;
+    const int s = valid ? find_seq(sm.cum, r.nseq, u) : 0;
+    const int lb = valid ? logical(p, sm, s, u) : 0;
+    const bool bad = valid && (cur_pb < 0 || cur_pb >= p.num_blocks);
+    if (bad) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
+    // first attended token of the block: sinks and positions before the window are skipped
+    const int first =
+        valid ? min(PA_BLOCK_SIZE, max(0, max(p.num_sink, window_lo(p, sm.ctxs[s])) - lb * PA_BLOCK_SIZE)) : 0;
+    my_meta = valid ? make_int4(s, first, min(PA_BLOCK_SIZE, sm.ctxs[s] - lb * PA_BLOCK_SIZE), bad ? 1 : 0)
+                    : make_int4(-1, 0, 0, 1);
+    live_mask = __ballot_sync(0xffffffffu, valid && !bad);
+    // blocks that receive this step's appended token (the append's position of the sequence)
+    const int ap = (valid && step) ? p.append_pos[r.seq_base + s] : -1;
+    wait_mask = __ballot_sync(0xffffffffu, ap >= 0 && ap / PA_BLOCK_SIZE == lb);
+  }
+
+  // Fill the stage of iteration k (its previous use must have been released).
+  __device__ __forceinline__ void issue(const DecodeParams& p, const Smem& sm, const Range& r, int lane, bool step,
+                                        int hgi, int k, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                        const CUtensorMap* tmKp, const CUtensorMap* tmVp) {
+    const int S = p.stages, nbs = p.nbs;
+    int i = k * nbs - (base - r.u0);
+    if (i >= 32) {
+      base += 32;
+      i -= 32;
+      cur_pb = nxt_pb;
+      nxt_pb = load_entry(p, sm, r, base + 32 + lane);
+      pack(p, sm, r, lane, step);
+    }
+    // this lane's op: block jj of the stage, tensor (and parameters) of the box
+    const int my_jj = lane / kOps, my_op = lane - my_jj * kOps;
+    const int st = k % S;
+    const unsigned stage_bits = (1u << nbs) - 1u;
+    const int pb = __shfl_sync(0xffffffffu, cur_pb, (i + my_jj) & 31);
+    const unsigned live = (live_mask >> i) & stage_bits;  // i + nbs <= 32 since nbs divides 32
+    if (!waited && ((wait_mask >> i) & stage_bits)) {   // a block the append writes: wait for it
+      grid_dep_wait();
+      waited = true;
+    }
+    if (lane >= i && lane < i + nbs) sm.meta[st * nbs + (lane - i)] = my_meta;
+    if (lane == 0) {
+      const uint32_t bytes = __popc(live) * static_cast<uint32_t>(p.block_tx);
+      if (bytes) mbar_arrive_expect_tx(&sm.full[st], bytes);
+      else mbar_arrive(&sm.full[st]);
+    }
+    __syncwarp();
+    if (lane < nbs * kOps && ((live >> my_jj) & 1u)) {
+      const uint64_t policy = l2_evict_first_policy();
+      uint8_t* stage = sm.stages + static_cast<size_t>(st) * p.stage_bytes + static_cast<size_t>(my_jj) * p.block_bytes;
+      if constexpr (KIND == 2) {
+        const int t = my_op & 1, prm = my_op >> 1;
+        tma_load_3d(stage + (prm ? 2 * p.hg * 1024 + t * p.hg * 256 : t * p.hg * 1024),
+                    prm ? (t ? tmVp : tmKp) : (t ? tmV : tmK), &sm.full[st], 0, prm ? hgi * p.hg : hgi * (p.hg >> 1),
+                    pb * PA_BLOCK_SIZE, policy);
+      } else if (KIND == 3 && my_op == 2) {  // the block's per-token K scales
+        tma_load_2d(stage + 2 * p.hg * p.nc * kTileBytes, tmKp, &sm.full[st], hgi * p.hg, pb * PA_BLOCK_SIZE, policy);
+      } else {  // K (op 0) or V (op 1): every head of the group, head-major
+        tma_load_4d(stage + static_cast<size_t>(my_op) * p.hg * p.nc * kTileBytes, my_op ? tmV : tmK, &sm.full[st], 0,
+                    0, pb * PA_BLOCK_SIZE, hgi * p.hg, policy);
+      }
+    }
+  }
+
+  // The grid must not complete before the append it overlaps (a decode step).
+  __device__ __forceinline__ void finish() {
+    if (!waited) grid_dep_wait();
+  }
+};
+
+// Wait (bounded) until the copies of iterations [from, to) have landed in their stages.
+__device__ __forceinline__ void drain_copies(const Smem& sm, int S, int from, int to, int lane, int32_t* err) {
+  for (int k = max(from, to - S); k < to; ++k) {
+    if (!mbar_wait(&sm.full[k % S], static_cast<uint32_t>(k / S) & 1u)) {
+      if (lane == 0) set_error(err, PA_EFLAG_TIMEOUT);
+    }
+  }
+}
+
 template <int D, int KIND, int MAXW>
 __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -754,120 +880,23 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
   __syncthreads();
 
   const int S = p.stages, nbs = p.nbs;
+  const int n_iters = (u1 - u0 + nbs - 1) / nbs;
+  const typename Producer<KIND>::Range range{seq_base, nseq, u0, u1};
   if (warp == p.warps_c) {
-    // ------------------------------- producer -------------------------------
-    // Every lane owns one block of the current 32-block chunk: its table entry is loaded one
-    // chunk ahead and its stage metadata is packed once when the chunk becomes current, so a
-    // stage costs one shuffle, one shared store and one TMA per box.  A block takes one box per
-    // tensor: the whole head rows of the group's heads for the block's 16 slots, head-major.
-    // (Measured, issuing a box costs about 90 cycles whatever its size, so fewer, larger boxes
-    // keep the producer ahead of HBM.)  INT4 stages take four boxes per block: K and V codes of
-    // all the group's heads (128-byte rows of two heads), then K and V group parameters.  With
-    // per-token K scales a third box per block carries the block's [16 slots][hg heads] scales.
-    const int ops_per_block = KIND == 2 ? 4 : (KIND == 3 ? 3 : 2);
-    const int n_ops = nbs * ops_per_block;  // <= 32
-    const uint64_t policy = l2_evict_first_policy();
-    // this lane's op (fixed for every stage): block jj of the stage, tensor, head
-    const int my_jj = lane / ops_per_block;
-    const int my_op = lane - my_jj * ops_per_block;
-    const CUtensorMap* my_map;
-    int my_row;
-    size_t my_dst;
-    if constexpr (KIND == 2) {
-      const int t = my_op & 1, prm = my_op >> 1;
-      my_map = prm ? (t ? &tmVp : &tmKp) : (t ? &tmV : &tmK);
-      my_row = prm ? hgi * p.hg : hgi * (p.hg >> 1);
-      my_dst = static_cast<size_t>(my_jj) * p.block_bytes +
-               (prm ? 2 * p.hg * 1024 + t * p.hg * 256 : t * p.hg * 1024);
-    } else {
-      const int my_t = my_op;  // 0 K, 1 V, 2 K scales
-      my_map = my_t == 2 ? &tmKp : (my_t ? &tmV : &tmK);
-      my_row = hgi * p.hg;  // first head of the box
-      my_dst = static_cast<size_t>(my_jj) * p.block_bytes + static_cast<size_t>(my_t) * p.hg * p.nc * kTileBytes;
-    }
-    // logical block of list entry u of sequence s (the visited blocks start at the window)
-    auto logical = [&](int s, int u) { return window_lo(p, sm.ctxs[s]) / PA_BLOCK_SIZE + (u - sm.cum[s]); };
-    auto load_entry = [&](int u) -> int {
-      if (u >= u1) return -1;
-      const int s = find_seq(sm.cum, nseq, u);
-      return p.block_tables[static_cast<size_t>(seq_base + s) * p.max_blocks + logical(s, u)];
-    };
-    int base = u0;
-    int cur_pb = load_entry(base + lane);
-    int nxt_pb = load_entry(base + 32 + lane);
-    int4 my_meta;
-    unsigned live_mask, wait_mask;
-    bool waited = !step;
-    auto pack = [&]() {
-      const int u = base + lane;
-      const bool valid = u < u1;
-      const int s = valid ? find_seq(sm.cum, nseq, u) : 0;
-      const int lb = valid ? logical(s, u) : 0;
-      const bool bad = valid && (cur_pb < 0 || cur_pb >= p.num_blocks);
-      if (bad) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
-      // first attended token of the block: sinks and positions before the window are skipped
-      const int first = valid ? min(PA_BLOCK_SIZE, max(0, max(p.num_sink, window_lo(p, sm.ctxs[s])) -
-                                                            lb * PA_BLOCK_SIZE))
-                              : 0;
-      my_meta = valid ? make_int4(s, first, min(PA_BLOCK_SIZE, sm.ctxs[s] - lb * PA_BLOCK_SIZE), bad ? 1 : 0)
-                      : make_int4(-1, 0, 0, 1);
-      live_mask = __ballot_sync(0xffffffffu, valid && !bad);
-      // blocks that receive this step's appended token (the append's position of the sequence)
-      const int ap = (valid && step) ? p.append_pos[seq_base + s] : -1;
-      wait_mask = __ballot_sync(0xffffffffu, ap >= 0 && ap / PA_BLOCK_SIZE == lb);
-    };
-    pack();
-    const int n_iters = (u1 - u0 + nbs - 1) / nbs;
-    const unsigned stage_bits = (1u << nbs) - 1u;
+    // ------------------------------- producer warp -------------------------------
+    Producer<KIND> pr;
+    pr.init(p, sm, range, lane, step);
     int k = 0;
     for (; k < n_iters; ++k) {
-      int i = k * nbs - (base - u0);
-      if (i >= 32) {
-        base += 32;
-        i -= 32;
-        cur_pb = nxt_pb;
-        nxt_pb = load_entry(base + 32 + lane);
-        pack();
-      }
-      const int st = k % S;
-      const uint32_t ph = static_cast<uint32_t>(k / S) & 1u;
-      const int pb = __shfl_sync(0xffffffffu, cur_pb, (i + my_jj) & 31);
-      const unsigned live = (live_mask >> i) & stage_bits;  // i + nbs <= 32 since nbs divides 32
-      if (!mbar_wait(&sm.empty[st], ph ^ 1u)) {
+      if (!mbar_wait(&sm.empty[k % S], (static_cast<uint32_t>(k / S) & 1u) ^ 1u)) {
         if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
         break;
       }
-      if (!waited && ((wait_mask >> i) & stage_bits)) {  // a block the append writes: wait for it
-        grid_dep_wait();
-        waited = true;
-      }
-      if (lane >= i && lane < i + nbs) sm.meta[st * nbs + (lane - i)] = my_meta;
-      if (lane == 0) {
-        const uint32_t bytes = __popc(live) * static_cast<uint32_t>(p.block_tx);
-        if (bytes) mbar_arrive_expect_tx(&sm.full[st], bytes);
-        else mbar_arrive(&sm.full[st]);
-      }
-      __syncwarp();
-      if (lane < n_ops && ((live >> my_jj) & 1u)) {
-        if constexpr (KIND == 2)
-          tma_load_3d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], 0,
-                      my_row, pb * PA_BLOCK_SIZE, policy);
-        else if (KIND == 3 && my_op == 2)
-          tma_load_2d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], my_row,
-                      pb * PA_BLOCK_SIZE, policy);
-        else
-          tma_load_4d(sm.stages + static_cast<size_t>(st) * p.stage_bytes + my_dst, my_map, &sm.full[st], 0, 0,
-                      pb * PA_BLOCK_SIZE, my_row, policy);
-      }
+      pr.issue(p, sm, range, lane, step, hgi, k, &tmK, &tmV, &tmKp, &tmVp);
     }
     // do not leave while a copy into this CTA's shared memory may still be in flight
-    for (int st = 0; st < S && st < k; ++st) {
-      const int last = st + S * ((k - 1 - st) / S);
-      if (!mbar_wait(&sm.full[st], static_cast<uint32_t>(last / S) & 1u)) {
-        if (lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
-      }
-    }
-    if (!waited) grid_dep_wait();  // nor before the append of this step has completed
+    drain_copies(sm, S, 0, k, lane, p.err);
+    pr.finish();  // nor before the append of this step has completed
     return;
   }
   if (warp > p.warps_c) return;
@@ -878,7 +907,6 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
   Consumer<D, KIND> c(p, lane, hgi * p.hg + h_loc, j, h_loc);
   const int s_first = find_seq(sm.cum, nseq, u0);
   const int s_last = find_seq(sm.cum, nseq, u1 - 1);
-  const int n_iters = (u1 - u0 + nbs - 1) / nbs;
   const int cta = blockIdx.x;
   auto slot_of = [&](int s_rel) -> size_t {
     const int s = seq_base + s_rel;
@@ -1181,10 +1209,11 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
     pl->n_slots = static_cast<size_t>(B) * pl->max_parts;
     pl->meta_bytes = 256;
   }
+  const size_t kSmemLimit = smem_limit(PA_CTAS_PER_SM);
   const size_t cum_ints = pl->mode == 0 ? (2 * static_cast<size_t>(B) + 1) : 3;
   const size_t fixed_bytes = 1024 + (cum_ints + 32) * 4;
   const size_t per_stage = pl->stage_bytes + 16 + static_cast<size_t>(pl->nbs) * 16;
-  if (fixed_bytes + 2 * per_stage > static_cast<size_t>(kSmemLimit)) return PA_ERR_UNSUPPORTED;
+  if (fixed_bytes + 2 * per_stage > kSmemLimit) return PA_ERR_UNSUPPORTED;
   pl->stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - fixed_bytes) / per_stage));
   pl->smem_bytes = fixed_bytes + pl->stages * per_stage;
   const size_t partial_bytes =
