@@ -230,8 +230,11 @@ pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, const void* 
  *   q, out            bf16 [T][num_q_heads][head_dim], T >= q_start[num_seqs]
  *   q_start           device int32 [num_seqs + 1], non-decreasing
  *   max_query_len     bounds every n_s (it sizes the grid)
- * Supported: bf16 caches without sinks (anything else returns PA_ERR_UNSUPPORTED).  A sequence
- * with n_s < 0, n_s > ctx, n_s > max_query_len or ctx beyond its table sets
+ * Every cache kind is supported.  bf16 caches without sinks run on the tensor-core paths as they
+ * are; 8-bit, per-token-scaled and INT4 caches and caches with sinks (显存账本 §七) are decoded block
+ * by block (code times scale as fp32, rounded to bf16; sink positions from the sink buffers) and
+ * then take the same bf16 products, so their results carry that extra bf16 rounding of K and V.
+ * A sequence with n_s < 0, n_s > ctx, n_s > max_query_len or ctx beyond its table sets
  * PA_EFLAG_CTX_OVERFLOW and gets zero rows; a table entry outside [0, num_blocks) sets
  * PA_EFLAG_BAD_BLOCK_ID and zeroes the rows of every query tile whose keys include it.
  * Host errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA. */

@@ -155,14 +155,19 @@ def test_step_and_prefill_calls_reject_bad_arguments_on_the_host():
             N.pa_prefill_step(pf, a["out"], a["q"], FAKE, FAKE, a["k_new"], a["v_new"], a["n"], a["seq"], a["pos"],
                               FAKE, FAKE, FAKE, a["max_q"], a["scale"], None, 0)
         assert e.value.status == status, kw
+    # quantised and sink-holding caches take the same argument checks (every cache kind is served)
     quant = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, k_dtype="e4m3", v_dtype="int8",
                   k_scales=FAKE, v_scales=FAKE)
-    for call in (lambda d: N.pa_prefill_step(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 5, FAKE, FAKE, FAKE, FAKE, FAKE,
-                                             16, 0.1, None, 0),
-                 lambda d: N.pa_prefill_attention(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 0.1, None, 0)):
-        with pytest.raises(N.PaError) as e:
-            call(quant)
-        assert e.value.status == N.PA_ERR_UNSUPPORTED
+    int4 = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, k_dtype="int4", v_dtype="int4")
+    sinks = _desc(num_sink=4, k_sink=FAKE, v_sink=FAKE)
+    for d in (quant, int4, sinks):
+        for call in (lambda d: N.pa_prefill_step(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 5, FAKE, FAKE, FAKE, FAKE,
+                                                 FAKE, 16, nan, None, 0),
+                     lambda d: N.pa_prefill_attention(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, nan, None, 0),
+                     lambda d: N.pa_prefill_attention(d, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 0.1, None, 0)):
+            with pytest.raises(N.PaError) as e:
+                call(d)
+            assert e.value.status == N.PA_ERR_INVALID_ARG
     # pa_decode_step with fixed partitions (its plan needs no device query)
     dd = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, num_seqs=4)
     ws = N.pa_decode_workspace_size(dd, 1000, 512)
