@@ -42,9 +42,9 @@ WARM_SECONDS = 0.25   # warm-up runs at least this long (and at least --warmup s
 # ncu capture of each workload's attention call.  Reported only while the kernel sources hash to
 # the version the counters were taken on; null otherwise.
 NCU_TRAFFIC = {
-    "sources_sha256_16": "81eb5caebcbe4597",
-    "8b": 552_557_056, "70b": 543_515_904, "long_quant": 1_076_951_808, "prefix_cow": 282_210_560,
-    "int4_8b": 190_876_416, "swa": 1_082_485_504,
+    "sources_sha256_16": "f470722d1057d36a",
+    "8b": 552_134_400, "70b": 543_439_104, "long_quant": 1_077_082_880, "long_quant_tok": 1_093_661_184,
+    "prefix_cow": 282_154_752, "int4_8b": 190_264_576, "swa": 1_082_067_712, "tiny": 283_136,
 }
 KERNEL_SOURCES = ["paged_kv_cache_table_gb300/csrc/decode_attention.cu",
                   "paged_kv_cache_table_gb300/csrc/pa_device.cuh",
@@ -559,9 +559,10 @@ class SlidingBench(DecodeBench):
 
 class PrefillBench:
     """Chunked-prefill row: each step appends every sequence's chunk of new K/V tokens and runs
-    causal prefill attention of the chunk's queries over the paged cache."""
+    causal prefill attention of the chunk's queries over the paged cache.  kind "fp8": the cache
+    holds E4M3 K / INT8 V with per-head scales from the data's absmax (decoded block by block)."""
 
-    def __init__(self, device):
+    def __init__(self, device, kind="bf16"):
         import torch
         from paged_kv_cache_table_gb300 import native as N
         from paged_kv_cache_table_gb300.workloads import make_prefill_workload
@@ -569,9 +570,18 @@ class PrefillBench:
         w = make_prefill_workload()
         self.w = w
         shape = (w.num_blocks * 16, w.H_kv, w.D)
-        self.k = torch.empty(shape, dtype=torch.bfloat16, device=device)
-        self.v = torch.empty(shape, dtype=torch.bfloat16, device=device)
-        self.desc = N.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks)
+        if kind == "bf16":
+            self.k = torch.empty(shape, dtype=torch.bfloat16, device=device)
+            self.v = torch.empty(shape, dtype=torch.bfloat16, device=device)
+            self.desc = N.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks)
+        else:
+            self.k = torch.empty(shape, dtype=torch.uint8, device=device)
+            self.v = torch.empty(shape, dtype=torch.uint8, device=device)
+            kk, vv = torch.cat([w.fill_k, w.new_k]).float().abs(), torch.cat([w.fill_v, w.new_v]).float().abs()
+            self.k_scales = (kk.amax(dim=(0, 2)) / 448.0).to(device)
+            self.v_scales = (vv.amax(dim=(0, 2)) / 127.0).to(device)
+            self.desc = N.make_desc(w.B, w.H_q, w.H_kv, w.D, w.num_blocks, w.max_blocks, "e4m3", "int8",
+                                    self.k_scales, self.v_scales)
         self.tables = torch.from_numpy(w.tables).to(device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         N.pa_kv_append_tokens(self.desc, self.k, self.v, w.fill_k.to(device), w.fill_v.to(device), len(w.fill_seq),
@@ -931,6 +941,7 @@ def run_native(args):
         else:
             extra_prefix = {}
         r = {**extra_prefix, "value": round(by2 / e2 / 1e9, 1), "unit": "GB/s",
+             "algorithmic_bytes_per_call": int(ab), "ncu_traffic_per_call": ncu_traffic(name),
              "attention_gbs": round(ab / (a_ms / 1e3) / 1e9, 1),
              "attention_frac": round(ab / (a_ms / 1e3) / 1e9 / peak, 4),
              "attention_ms_per_call": round(a_ms, 5),
@@ -962,6 +973,17 @@ def run_native(args):
             "attention_frac_of_bf16_peak": round(pb.flops / a_sec / 1e12 / bf16_peak, 4),
             "prefill_tokens_per_s_per_layer": round(pb.tokens / sec, 1), "err_flag": int(pb.err.item())}
         del pb
+        torch.cuda.empty_cache()
+        pq = PrefillBench(device, kind="fp8")
+        pq.run(1, 0)  # one step appends the chunk's K/V codes
+        q_sec = pq.run_attention(max(50, args.steps // 20), args.warmup)
+        next_rows["chunked_prefill_fp8_cache"] = {
+            "workload": "the chunked-prefill workload over an E4M3 K / INT8 V cache (per-head scales): blocks "
+                        "decoded to bf16 in shared memory, warp-level tensor-core products",
+            "attention_ms_per_call": round(q_sec * 1e3, 4), "attention_tflops": round(pq.flops / q_sec / 1e12, 1),
+            "attention_frac_of_bf16_peak": round(pq.flops / q_sec / 1e12 / bf16_peak, 4),
+            "err_flag": int(pq.err.item())}
+        del pq
         torch.cuda.empty_cache()
         n_sw = max(100, args.steps // 4)
         sb = SlidingBench("swa", device, horizon=2 * (n_sw + args.warmup))
@@ -1063,6 +1085,8 @@ def main(argv=None):
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the chunked-prefill row (append + prefill attention steps) and print it; "
                          "for profiling that kernel")
+    ap.add_argument("--prefill-kind", default="bf16", choices=["bf16", "fp8"],
+                    help="with --prefill-only: the cache the chunk attends over (fp8: E4M3 K / INT8 V)")
     args = ap.parse_args(argv)
     ws, _, _ = dist_env()
     if "WORLD_SIZE" not in os.environ and args.gpus > 1:
@@ -1113,9 +1137,9 @@ def run_prefill_only(args):
     """--steps chunked-prefill steps after --warmup, then one JSON line with the step time."""
     import torch
     device = torch.device("cuda", 0)
-    pb = PrefillBench(device)
+    pb = PrefillBench(device, kind=args.prefill_kind)
     sec = pb.run(max(1, args.steps), max(0, args.warmup))
-    print(json.dumps({"row": "chunked_prefill", "steps": args.steps, "warmup": args.warmup,
+    print(json.dumps({"row": "chunked_prefill", "cache": args.prefill_kind, "steps": args.steps, "warmup": args.warmup,
                       "ms_per_step": round(sec * 1e3, 4), "tflops": round(pb.flops / sec / 1e12, 1),
                       "err_flag": int(pb.err.item())}))
     return 0 if int(pb.err.item()) == 0 else 1
