@@ -24,17 +24,21 @@
 //    accumulators in TMEM: S0, S1, O0, O1 in 4 x 128 columns), issued by one thread.  Q and K are
 //    K-major and V MN-major shared-memory operands with the 128-byte swizzle; P goes back into
 //    TMEM over the S columns it came from (bf16 pairs) and is the A operand of P·V from there, so
-//    the tensor core reads only Q, K and V from shared memory.  P·V is issued in two halves of
-//    64 keys: the first as soon as the softmax has written that half of P (p_half), so that it
-//    runs while the exponentials of the second half are computed, the second on p_full.  A query
-//    tile's next S is issued after its P·V (the tensor pipe runs one thread's products in order,
-//    so P is read before it is overwritten); the two query tiles interleave on the tensor core.
-//  * Copies: one warp streams K through a two-stage ring of 128-key tiles, another V through a
-//    three-stage ring (a V tile is needed only at P·V, after the softmax, so V is fetched further
-//    ahead, and on its own warp its waits never hold back the next K tile), and a third loads the
-//    next item's query tiles by TMA (a 4-D map over q) as soon as the current item's last S
-//    products have completed.  A ring stage is released to its copy warp by a tcgen05.commit of
-//    the MMA thread once every product reading it has completed.
+//    the tensor core reads only Q, K and V from shared memory.  P·V is issued once the softmax
+//    has written all of P (p_full): the issuing thread's waits, not the products, set the pace of
+//    the tile loop (~100-150 cycles per barrier wait; measured, handing over the first 64 keys'
+//    P early cost more in waits than its overlap gained).  A query tile's next S is issued after
+//    its P·V (the tensor pipe runs one thread's products in order, so P is read before it is
+//    overwritten); the two query tiles interleave on the tensor core.
+//  * Copies: two warps, one per 64-dim half, stream K through a three-stage ring of 128-key tiles
+//    and V through a two-stage ring, 8 boxes of 16 slots per warp and tile (a warp issues its
+//    boxes one by one, ~80 cycles each).  A tile's copy takes ~3,500-4,000 cycles from the
+//    release of its stage to its landing, about one tile's time, so K runs one tile ahead of V
+//    (K of tile g + 1 and V of tile g are needed together, when the MMA thread starts tile g) and
+//    K's ring is the deeper one.  A third warp loads the next item's query tiles by TMA (a 4-D
+//    map over q) as soon as the current item's last S products have completed.  A ring stage is
+//    released to the copy warps by a tcgen05.commit of the MMA thread once every product reading
+//    it has completed.
 //  * Two softmax warpgroups (one per query tile) own one query row per thread through TMEM
 //    lanes: they read S, mask (causal, window) only on tiles that cross a row's edge, keep the
 //    running maximum (moved only when a score exceeds it by 2^8), write P as bf16 into TMEM, and
@@ -60,13 +64,14 @@
 namespace pa {
 namespace {
 
-constexpr int kTcThreads = 384;                 // 12 warps: K, MMA, V, Q copies; 2 x 4 softmax
+constexpr int kTcThreads = 384;                 // 12 warps: K/V copies, MMA, K/V copies, Q copies; 2 x 4 softmax
 constexpr int kHalf = 128 * 128;                // 128 rows x 128 bytes (64 bf16): one K-half
 constexpr int kTile = 2 * kHalf;                // a 128 x 128 bf16 operand tile
 constexpr int kQOff = 0;                        // Q0, Q1
-constexpr int kKOff = kQOff + 2 * kTile;        // K stages 0, 1
-constexpr int kVOff = kKOff + 2 * kTile;        // V stages 0, 1, 2
-constexpr int kVStages = 3;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kKOff = kQOff + 2 * kTile;               // K stages
+constexpr int kVOff = kKOff + kKStages * kTile;        // V stages
 constexpr int kBarOff = kVOff + kVStages * kTile;
 constexpr int kMaxItems = 64;                   // work items of one CTA (the launch makes enough CTAs)
 constexpr int kListOff = kBarOff + 256;         // barriers, then the CTA's item list
@@ -285,14 +290,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBarOff);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 2;
-  uint64_t* k_full = bars + 4;   // [2]
-  uint64_t* k_empty = bars + 6;  // [2]
-  uint64_t* v_full = bars + 8;   // [3] per V stage
-  uint64_t* v_empty = bars + 11; // [3]
+  uint64_t* k_full = bars + 4;   // [kKStages] per K stage
+  uint64_t* k_empty = bars + 4 + kKStages;
+  uint64_t* v_full = bars + 4 + 2 * kKStages;  // [kVStages] per V stage
+  uint64_t* v_empty = bars + 4 + 2 * kKStages + kVStages;
   uint64_t* s_full = bars + 14;  // [2] per query tile
   uint64_t* p_full = bars + 16;  // [2]
   uint64_t* o_done = bars + 18;  // [2]
-  uint64_t* p_half = bars + 24;  // [2] P of the tile's first 64 keys is in TMEM
   uint64_t* drain = bars + 20;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
   int* flags = reinterpret_cast<int*>(bars + 22);  // [0] tiles of all sequences, [1] a wait gave up
@@ -310,15 +314,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&v_full[i], 1);
+      mbar_init(&v_full[i], 2);  // one arrival per copy warp
       mbar_init(&v_empty[i], 1);  // released by the MMA thread (or the output's store)
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&k_full[i], 2);  // one arrival per copy warp
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
-      mbar_init(&p_half[i], 128);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(drain, 1);
@@ -380,12 +385,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 || warp == 2) {
-    // ---------------------- copy warps: K (warp 0), V (warp 2) ----------------------
+    // ------------------- K/V copies: warp 0 dims 0-63, warp 2 dims 64-127 -------------------
     if (p.step) grid_dep_wait();
     uint64_t policy;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
     bool ok = true;
-    int g = 0;  // tiles of this CTA so far: ring stage and phase
+    const int half = warp >> 1;
+    // tiles of this CTA whose K (gk) and V (gv) copies have been issued: ring stages and phases.
+    // K runs one tile ahead of V: K of tile g + 1 and V of tile g are needed together (at the
+    // start of the MMA thread's tile g), and K's ring is the deeper one.
+    int gk = 0, gv = 0;
+    int v_pb = -1, v_h = 0;  // the tile whose V copy is still to be issued: its block, KV head
+    unsigned v_loads = 0;
+    // The 8 blocks of this warp's 64-dim half of a tile, boxes of 16 slots x 128 bytes, one per
+    // lane (lanes 0-7).
+    auto issue = [&](const CUtensorMap* map, uint64_t* full, uint64_t* empty, uint32_t parity, uint8_t* dst,
+                     int pb, unsigned loads, int h_kv) -> bool {
+      if (!warp_wait(empty, parity)) return false;
+      if (lane == 0) {
+        const uint32_t bytes = __popc(loads) * 2048u;
+        if (bytes) mbar_arrive_expect_tx(full, bytes);
+        else mbar_arrive(full);
+      }
+      __syncwarp();
+      if (pb >= 0)
+        tma_load_3d(dst + half * kHalf + lane * 2048, map, full, 0, h_kv * 2 + half, pb * PA_BLOCK_SIZE, policy);
+      return true;
+    };
+    auto issue_v = [&]() -> bool {  // V of tile gv (its blocks in v_pb)
+      const int vst = gv % kVStages;
+      const bool r = issue(&tmV, &v_full[vst], &v_empty[vst], (static_cast<uint32_t>(gv / kVStages) & 1u) ^ 1u,
+                           sm + kVOff + vst * kTile, v_pb, v_loads, v_h);
+      if (r) ++gv;
+      return r;
+    };
     for (int ii = 0; ok && ii < n_items; ++ii) {
       const Item it = make_item(p, list[ii]);
       if (it.n_tiles == 0) continue;
@@ -407,16 +440,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int v0 = __shfl_sync(0xffffffffu, e0, b & 31), v1 = __shfl_sync(0xffffffffu, e1, b & 31);
         return cb == c0 ? v0 : v1;
       };
-      // 8 blocks from tile-relative block blk0, boxes of 16 slots x 128 bytes, one per lane:
-      // block lane / 2, 64-dim half lane % 2.  Returns false when a wait gave up.
-      auto load = [&](int blk0, const CUtensorMap* map, uint64_t* full, uint64_t* empty, uint32_t parity,
-                      uint8_t* dst) -> bool {
-        if (!warp_wait(empty, parity)) return false;
-        const int bi = lane >> 1, half = lane & 1;
-        const int kb = kb0 + blk0 + bi;
-        const int ent = table(blk0 + min(bi, 7));
+      for (int k = 0; ok && k < it.n_tiles; ++k) {
+        const int kb = kb0 + 8 * k + lane;
+        const int ent = table(8 * k + min(lane, 7));
         int pb = -1;
-        if (bi < 8 && kb < kb_end) {
+        if (lane < 8 && kb < kb_end) {
           pb = ent;
           if (pb < 0 || pb >= p.num_blocks) {
             if (half == 0) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
@@ -424,34 +452,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         const unsigned loads = __ballot_sync(0xffffffffu, pb >= 0);
-        if (lane == 0) {
-          const uint32_t bytes = __popc(loads) * 2048u;
-          if (bytes) mbar_arrive_expect_tx(full, bytes);
-          else mbar_arrive(full);
-        }
-        __syncwarp();
-        if (pb >= 0) tma_load_3d(dst + half * kHalf + bi * 2048, map, full, 0, it.h_kv * 2 + half, pb * PA_BLOCK_SIZE, policy);
-        return true;
-      };
-      for (int k = 0; ok && k < it.n_tiles; ++k) {
-        if (warp == 0) {
-          ok = load(8 * k, &tmK, &k_full[g & 1], &k_empty[g & 1], (static_cast<uint32_t>(g >> 1) & 1u) ^ 1u,
-                    sm + kKOff + (g & 1) * kTile);
-        } else {
-          const int st = g % kVStages;
-          ok = load(8 * k, &tmV, &v_full[st], &v_empty[st], (static_cast<uint32_t>(g / kVStages) & 1u) ^ 1u,
-                    sm + kVOff + st * kTile);
-        }
-        if (ok) ++g;
+        const int kst = gk % kKStages;
+        ok = issue(&tmK, &k_full[kst], &k_empty[kst], (static_cast<uint32_t>(gk / kKStages) & 1u) ^ 1u,
+                   sm + kKOff + kst * kTile, pb, loads, it.h_kv);
+        if (!ok) break;
+        ++gk;
+        if (gv < gk - 1) ok = issue_v();
+        v_pb = pb;
+        v_loads = loads;
+        v_h = it.h_kv;
       }
     }
+    if (ok && gv < gk) ok = issue_v();
     // do not leave while a copy into this CTA's shared memory may still be in flight (the MMA
     // thread waits for every tile, unless one of its own waits gave up)
-    const int S = warp == 0 ? 2 : kVStages;
-    uint64_t* full = warp == 0 ? k_full : v_full;
-    for (int st = 0; st < S && st < g; ++st) {
-      const int last = st + S * ((g - 1 - st) / S);
-      if (!warp_wait(&full[st], static_cast<uint32_t>(last / S) & 1u)) ok = false;
+    for (int st = 0; st < kKStages && st < gk; ++st) {
+      const int last = st + kKStages * ((gk - 1 - st) / kKStages);
+      if (!warp_wait(&k_full[st], static_cast<uint32_t>(last / kKStages) & 1u)) ok = false;
+    }
+    for (int st = 0; st < kVStages && st < gv; ++st) {
+      const int last = st + kVStages * ((gv - 1 - st) / kVStages);
+      if (!warp_wait(&v_full[st], static_cast<uint32_t>(last / kVStages) & 1u)) ok = false;
     }
     if (!ok && lane == 0) flags[1] = 1;
   } else if (warp == 3) {
@@ -524,21 +545,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_commit(&s_full[w]);
       };
-      // O_w (+)= P_w V over keys 64 half .. 64 half + 63 of the tile in V stage vst
-      auto issue_pv = [&](int w, int vst, bool first, int half) {
+      // O_w (+)= P_w V of the tile in V stage vst
+      auto issue_pv = [&](int w, int vst, bool first) {
         const uint32_t vbuf = smem_u32(sm + kVOff + vst * kTile);
 #pragma unroll
-        for (int kk = 4 * half; kk < 4 * half + 4; ++kk) {
+        for (int kk = 0; kk < 8; ++kk) {
           // P: keys 16kk .. 16kk+15 = TMEM columns 8kk .. 8kk+7 of S_w; V: key rows 16kk .. of both halves
           tc_mma_ts(tmem + 256 + w * 128, tmem + w * 128 + 8 * kk, sw128_desc(vbuf + kk * 16 * 128, kHalf, 1024),
                     kIdescPV, (!first || kk > 0) ? 1u : 0u);
         }
       };
       // A ring stage is released only when a later copy waits for it.  The K stage of tile m is
-      // refilled with tile m + 2, the V stage of tile m with tile m + 3, counting the tiles of all
-      // the CTA's items in order.  The K and V stages of an item's last tile stage the output of
-      // query tiles 0 and 1 when those hold rows, and their groups release them after it has
-      // left; otherwise they are released here.
+      // refilled with tile m + kKStages, the V stage of tile m with tile m + kVStages, counting
+      // the tiles of all the CTA's items in order.  The K and V stages of an item's last tile
+      // stage the output of query tiles 0 and 1 when those hold rows, and their groups release
+      // them after it has left; otherwise they are released here.
       int g_tot = 0;
       for (int ii = 0; ii < n_items; ++ii) g_tot += make_item(p, list[ii]).n_tiles;
       bool ok = true;
@@ -550,36 +571,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (nt == 0) continue;
         const int groups = it.has1 ? 2 : 1;  // query tiles with rows (an item with tiles has rows)
         ok = mbar_wait(q_full, static_cast<uint32_t>(qi) & 1u) &&
-             mbar_wait(&k_full[g & 1], static_cast<uint32_t>(g >> 1) & 1u);
+             mbar_wait(&k_full[g % kKStages], static_cast<uint32_t>(g / kKStages) & 1u);
         ++qi;
         if (!ok) break;
         tc_fence_after();
-        for (int w = 0; w < groups; ++w) issue_s(w, g & 1);
+        for (int w = 0; w < groups; ++w) issue_s(w, g % kKStages);
         if (nt == 1) tc_commit(q_empty);  // the item's last products that read Q are issued
-        if (g + 2 < g_tot && nt > 1) tc_commit(&k_empty[g & 1]);
+        if (g + kKStages < g_tot && nt > 1) tc_commit(&k_empty[g % kKStages]);
         for (int k = 0; k < nt; ++k) {
           const int gk = g + k;
           const bool next = k + 1 < nt;
-          if (next && !(ok = mbar_wait(&k_full[(gk + 1) & 1], static_cast<uint32_t>((gk + 1) >> 1) & 1u))) break;
+          if (next && !(ok = mbar_wait(&k_full[(gk + 1) % kKStages], static_cast<uint32_t>((gk + 1) / kKStages) & 1u)))
+            break;
           const int vs = gk % kVStages;
           if (!(ok = mbar_wait(&v_full[vs], static_cast<uint32_t>(gk / kVStages) & 1u))) break;
-          // per query tile: P·V of this tile (the first 64 keys as soon as their P is written, the
-          // rest when the whole of P is), then its S of the next tile
+          // per query tile: P·V of this tile once its P is written, then its S of the next tile
           for (int w = 0; ok && w < groups; ++w) {
-            if (!(ok = mbar_wait(&p_half[w], sp[w] & 1u))) break;
-            tc_fence_after();
-            issue_pv(w, vs, k == 0, 0);
             if (!(ok = mbar_wait(&p_full[w], sp[w] & 1u))) break;
             ++sp[w];
             tc_fence_after();
-            issue_pv(w, vs, k == 0, 1);
+            issue_pv(w, vs, k == 0);
             tc_commit(&o_done[w]);
-            if (next) issue_s(w, (gk + 1) & 1);
+            if (next) issue_s(w, (gk + 1) % kKStages);
           }
           if (!ok) break;
           if (k == nt - 2) tc_commit(q_empty);
           if (gk + kVStages < g_tot && (next || groups < 2)) tc_commit(&v_empty[vs]);
-          if (next && gk + 3 < g_tot && k + 2 < nt) tc_commit(&k_empty[(gk + 1) & 1]);
+          if (next && gk + 1 + kKStages < g_tot && k + 2 < nt) tc_commit(&k_empty[(gk + 1) % kKStages]);
         }
         g += nt;
       }
@@ -677,10 +695,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           fence_proxy_async();  // the zeros, before the tensor core reads the stage
         }
-        // P (bf16 pairs) over the S columns just read: column c holds keys 2c and 2c + 1.  The
-        // first half (keys 0-63) is handed to the MMA thread as soon as it is written, so its
-        // P·V runs while the second half is computed; when the maximum moved, O is rescaled
-        // first and both halves go together.
+        // P (bf16 pairs) over the S columns just read: column c holds keys 2c and 2c + 1; when the
+        // maximum moved, O is rescaled before P is handed over.
         float ls4[4] = {0.f, 0.f, 0.f, 0.f};
         const float sl = p.scale_log2;
 #pragma unroll
@@ -694,11 +710,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             pw[e] = pack_bf16(a, b);
           }
           tmem_st16(tS + 16 * h, pw);
-          if (h == 1 && !moved) {
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&p_half[wg]);
-          }
         }
         tmem_wait_st();
         l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
@@ -713,8 +724,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tmem_st32(tO + 32 * c, ov);
           }
           tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(&p_half[wg]);
         }
         tc_fence_before();
         mbar_arrive(&p_full[wg]);
@@ -742,7 +751,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const float inv = (!ok || bad || !(l_run > 0.f)) ? 0.f : 1.f / l_run;
       const int g_last = g - 1;
-      uint8_t* stile = wg == 0 ? sm + kKOff + (g_last & 1) * kTile : sm + kVOff + (g_last % kVStages) * kTile;
+      uint8_t* stile =
+          wg == 0 ? sm + kKOff + (g_last % kKStages) * kTile : sm + kVOff + (g_last % kVStages) * kTile;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
@@ -767,8 +777,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       fence_proxy_async();  // the staged rows, before the copy engine reads them
       group_sync(1 + wg);
-      const bool release = wg == 0 ? g_last + 2 < g_tot : g_last + kVStages < g_tot;
-      uint64_t* rel = wg == 0 ? &k_empty[g_last & 1] : &v_empty[g_last % kVStages];
+      const bool release = wg == 0 ? g_last + kKStages < g_tot : g_last + kVStages < g_tot;
+      uint64_t* rel = wg == 0 ? &k_empty[g_last % kKStages] : &v_empty[g_last % kVStages];
       if (tq0 + p.tpq <= it.t_end) {
         if (quad == 0 && lane == 0) {
           for (int half = 0; half < 2; ++half)
