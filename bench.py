@@ -51,6 +51,7 @@ KERNEL_SOURCES = ["paged_kv_cache_table_gb300/csrc/decode_attention.cu",
                   "paged_kv_cache_table_gb300/csrc/pa_internal.h"]
 METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak); decode tokens/s/layer"
 L2_BYTES = 129 * 1024 * 1024
+MODEL_LAYERS = {"8b": 32, "70b": 80}  # decoder layers of the models whose attention shapes these are
 
 
 def _bf16_peak():
@@ -916,6 +917,7 @@ def run_native(args):
     ms_per_step = 1e3 * el_max / args.steps
     tok_s_layer = ws * w.B * args.steps / el_max
     att_mean_ms = float(np.mean(att_ms))
+    att_pct = {k: round(float(np.percentile(att_ms, q)), 5) for k, q in (("p10", 10), ("median", 50), ("p90", 90))}
     att_bytes = nbytes_ev / args.steps
     achieved = att_bytes / (att_mean_ms / 1e3) / 1e9
     # end-to-end through the same API with host buffers
@@ -948,6 +950,9 @@ def run_native(args):
              "ms_per_step": round(1e3 * e2 / len(a2), 4),
              "tokens_per_s_per_layer": round(nb.w.B * len(a2) / e2, 1),
              "err_flag": int(nb.err.item())}
+        layers = MODEL_LAYERS.get(name)
+        if layers:  # the whole model's attention, one such layer after another
+            r[f"tokens_per_s_model_{layers}_layers"] = round(nb.w.B * len(a2) / e2 / layers, 1)
         del nb
         torch.cuda.empty_cache()
         return r
@@ -1034,7 +1039,8 @@ def run_native(args):
                        "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB attended per step vs "
                              f"{L2_BYTES / 1e6:.0f} MB L2)"},
             "tokens_per_s_per_layer": round(tok_s_layer, 1),
-            "tokens_per_s_model_32_layers": round(tok_s_layer / 32, 1),
+            f"tokens_per_s_model_{MODEL_LAYERS.get(args.config, 32)}_layers":
+                round(tok_s_layer / MODEL_LAYERS.get(args.config, 32), 1),
             "pct_of_hbm_peak": round(100 * value / peak, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
@@ -1043,6 +1049,7 @@ def run_native(args):
                                          "whole call (decode_kernel + merge_kernel)",
                          "kernel": "pa_decode_attention (decode_kernel + merge_kernel)",
                          "peak_kind": peak_kind, "ms_per_call": round(att_mean_ms, 5),
+                         "ms_per_call_percentiles": att_pct,
                          "algorithmic_bytes_per_call": int(att_bytes)},
             "e2e": {"value": round(bytes_e2e / el_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * el_e2e / args.steps, 5),
