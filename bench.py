@@ -622,15 +622,23 @@ class PrefillBench:
         torch.cuda.synchronize()
         return t0.elapsed_time(t1) / 1e3 / steps
 
-    def run_attention(self, steps, warmup):
+    def run_attention(self, steps, warmup, ws=False):
         """Seconds per prefill-attention call alone (the cache already holds the chunk), timed with
-        CUDA events on the stream the kernel is launched on."""
+        CUDA events on the stream the kernel is launched on.  ws: through pa_prefill_attention_ws
+        (each attended block decoded once into a workspace, then the bf16 tensor-core path)."""
         torch, N, w = self.torch, self.N, self.w
         sid = torch.cuda.current_stream().cuda_stream
+        max_ctx = int(w.max_blocks * 16)
+        nbytes = N.pa_prefill_workspace_size(self.desc, max_ctx) if ws else 0
+        wsbuf = torch.empty(max(1, nbytes), dtype=torch.uint8, device=self.out.device) if ws else None
 
         def call():
-            N.pa_prefill_attention(self.desc, self.out, self.q, self.k, self.v, self.tables, self.q_start, self.ctx,
-                                   self.max_q, w.scale, self.err, sid)
+            if ws:
+                N.pa_prefill_attention_ws(self.desc, self.out, self.q, self.k, self.v, self.tables, self.q_start,
+                                          self.ctx, self.max_q, max_ctx, w.scale, wsbuf, nbytes, self.err, sid)
+            else:
+                N.pa_prefill_attention(self.desc, self.out, self.q, self.k, self.v, self.tables, self.q_start,
+                                       self.ctx, self.max_q, w.scale, self.err, sid)
         for _ in range(warmup):
             call()
         torch.cuda.synchronize()
@@ -981,12 +989,18 @@ def run_native(args):
         torch.cuda.empty_cache()
         pq = PrefillBench(device, kind="fp8")
         pq.run(1, 0)  # one step appends the chunk's K/V codes
+        x_sec = pq.run_attention(max(50, args.steps // 4), args.warmup, ws=True)
         q_sec = pq.run_attention(max(50, args.steps // 20), args.warmup)
         next_rows["chunked_prefill_fp8_cache"] = {
-            "workload": "the chunked-prefill workload over an E4M3 K / INT8 V cache (per-head scales): blocks "
-                        "decoded to bf16 in shared memory, warp-level tensor-core products",
-            "attention_ms_per_call": round(q_sec * 1e3, 4), "attention_tflops": round(pq.flops / q_sec / 1e12, 1),
-            "attention_frac_of_bf16_peak": round(pq.flops / q_sec / 1e12 / bf16_peak, 4),
+            "workload": "the chunked-prefill workload over an E4M3 K / INT8 V cache (per-head scales)",
+            "path": "pa_prefill_attention_ws: each attended block decoded once into the workspace as bf16, then "
+                    "the tcgen05 kernel",
+            "attention_ms_per_call": round(x_sec * 1e3, 4), "attention_tflops": round(pq.flops / x_sec / 1e12, 1),
+            "attention_frac_of_bf16_peak": round(pq.flops / x_sec / 1e12 / bf16_peak, 4),
+            "no_workspace": {"path": "pa_prefill_attention: blocks decoded per 16-token query tile into shared "
+                                     "memory, warp-level tensor-core products",
+                             "attention_ms_per_call": round(q_sec * 1e3, 4),
+                             "attention_tflops": round(pq.flops / q_sec / 1e12, 1)},
             "err_flag": int(pq.err.item())}
         del pq
         torch.cuda.empty_cache()
@@ -1092,6 +1106,8 @@ def main(argv=None):
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the chunked-prefill row (append + prefill attention steps) and print it; "
                          "for profiling that kernel")
+    ap.add_argument("--prefill-ws", action="store_true",
+                    help="with --prefill-only: time the attention call through pa_prefill_attention_ws")
     ap.add_argument("--prefill-kind", default="bf16", choices=["bf16", "fp8"],
                     help="with --prefill-only: the cache the chunk attends over (fp8: E4M3 K / INT8 V)")
     args = ap.parse_args(argv)
@@ -1145,10 +1161,14 @@ def run_prefill_only(args):
     import torch
     device = torch.device("cuda", 0)
     pb = PrefillBench(device, kind=args.prefill_kind)
-    sec = pb.run(max(1, args.steps), max(0, args.warmup))
-    print(json.dumps({"row": "chunked_prefill", "cache": args.prefill_kind, "steps": args.steps, "warmup": args.warmup,
-                      "ms_per_step": round(sec * 1e3, 4), "tflops": round(pb.flops / sec / 1e12, 1),
-                      "err_flag": int(pb.err.item())}))
+    if args.prefill_ws:  # the attention call alone, through the workspace path, after one step's append
+        pb.run(1, 0)
+        sec = pb.run_attention(max(1, args.steps), max(0, args.warmup), ws=True)
+    else:
+        sec = pb.run(max(1, args.steps), max(0, args.warmup))
+    print(json.dumps({"row": "chunked_prefill", "cache": args.prefill_kind, "workspace_path": bool(args.prefill_ws),
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 4),
+                      "tflops": round(pb.flops / sec / 1e12, 1), "err_flag": int(pb.err.item())}))
     return 0 if int(pb.err.item()) == 0 else 1
 
 

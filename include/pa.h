@@ -262,6 +262,36 @@ pa_status pa_prefill_step(const pa_cache_desc* desc, void* out, const void* q, v
                           const int32_t* context_lens, int max_query_len, float scale,
                           int32_t* err_flag, void* stream);
 
+/* Chunked-prefill attention with a workspace: the computation, layouts, rules and device errors
+ * of pa_prefill_attention, for caches that are decoded (8-bit, per-token-scaled and INT4 caches,
+ * and caches with sinks; 显存账本 §七, ldpk §5.2).  Each logical block that the chunk's queries can
+ * attend (from the first query's window start to the end of the context) is decoded once, into
+ * a bf16 copy in the workspace laid out as a bf16 cache of num_seqs * ceil(max_context_len / 16)
+ * blocks (code times scale in fp32 rounded to bf16, sink positions from the sink buffers: the
+ * values pa_prefill_attention takes), and the tensor-core kernel of bf16 caches then runs over
+ * that copy, instead of every 16-token query tile decoding each block it reads for itself.
+ * Results equal pa_prefill_attention's up to the order in which the products are summed.
+ *   max_context_len   bounds every context_lens[s]; 0 <= max_context_len <= max_blocks_per_seq*16.
+ *                     A sequence with a longer context sets PA_EFLAG_CTX_OVERFLOW and gets zero
+ *                     rows.
+ *   workspace         device memory of at least pa_prefill_workspace_size(desc, max_context_len)
+ *                     bytes, 256-byte aligned, scratch for this call only (its contents need not
+ *                     be initialised).
+ * pa_prefill_workspace_size returns 0 when the call needs no workspace (a bf16 cache without
+ * sinks, head_dim 64, a G that is not a power of two, or more than 2^31 slots in the copy: the
+ * call is then pa_prefill_attention, and workspace may be NULL) and when desc or
+ * max_context_len is invalid (the call then reports the error).
+ * Host errors: those of pa_prefill_attention, PA_ERR_INVALID_ARG for max_context_len out of range
+ * or a missing or misaligned workspace, PA_ERR_WORKSPACE_TOO_SMALL. */
+size_t pa_prefill_workspace_size(const pa_cache_desc* desc, int max_context_len);
+
+pa_status pa_prefill_attention_ws(const pa_cache_desc* desc, void* out, const void* q,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, const int32_t* q_start,
+                                  const int32_t* context_lens, int max_query_len, int max_context_len,
+                                  float scale, void* workspace, size_t workspace_bytes,
+                                  int32_t* err_flag, void* stream);
+
 /* Allocation-free decode attention.  The pages have no counterpart to this entry point: it is
  * pa_decode_attention for callers that cannot allocate device memory when they call it, for
  * example a plugin running inside a host framework that owns every byte of device memory, a

@@ -402,10 +402,8 @@ struct DqPiece {
     }
   }
 
-  // Write the piece's 32 values as bf16 into row `row` of a [16 rows][128 B]-per-chunk tile with
-  // the 128-byte swizzle: dims 32g + 8u .. + 7 form 16-byte unit 4g + u of the row.
-  __device__ __forceinline__ void store(int t, uint8_t* tile, int row, int g) const {
-    uint32_t out[16];
+  // The piece's 32 values as bf16 pairs, dims in order: code times scale in fp32, rounded.
+  __device__ __forceinline__ void decode(int t, uint32_t (&out)[16]) const {
     if (sink || KIND == 0) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) out[i] = w[i];
@@ -446,6 +444,13 @@ struct DqPiece {
 #pragma unroll
       for (int i = 0; i < 16; ++i) out[i] = pack_bf16(s * (x[2 * i] - z), s * (x[2 * i + 1] - z));
     }
+  }
+
+  // Write the piece's 32 values as bf16 into row `row` of a [16 rows][128 B]-per-chunk tile with
+  // the 128-byte swizzle: dims 32g + 8u .. + 7 form 16-byte unit 4g + u of the row.
+  __device__ __forceinline__ void store(int t, uint8_t* tile, int row, int g) const {
+    uint32_t out[16];
+    decode(t, out);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int du = 4 * g + u, c = du >> 3, uu = du & 7;
@@ -531,6 +536,52 @@ __global__ void __launch_bounds__(kPfWarps * 32)
   w.finish(p, qs, h_kv);
 }
 
+// ------------------------------------------------------------------------------------
+// Decoded copy for the tensor-core prefill (pa_prefill_attention_ws).  CTA (b, s) decodes
+// logical block b of sequence s, if the chunk's queries can attend it, into block s * mb + b of
+// a bf16 pool with the cache's slot-major layout (the same DqPiece arithmetic as
+// prefill_dq_kernel: code times scale in fp32 rounded to bf16, sink positions from the sink
+// buffers), and writes the dense table entry dense[s][b]: that block, or -1 for a block no query
+// attends or whose table entry lies outside the pool (the attention kernel then reports it).
+// ------------------------------------------------------------------------------------
+template <int D, int KIND>
+__global__ void __launch_bounds__(256)
+    prefill_expand_kernel(const PrefillParams p, int mb, __nv_bfloat16* kx, __nv_bfloat16* vx, int32_t* dense) {
+  constexpr int GROUPS = D / 32;
+  const int b = blockIdx.x, s = blockIdx.y;
+  grid_dep_wait();  // the previous kernel of the stream may still be writing any input
+  const int n = p.q_start[s + 1] - p.q_start[s];
+  const int ctx = p.context_lens[s];
+  const bool valid = n >= 0 && n <= ctx && n <= p.max_q && ctx <= p.max_blocks * PA_BLOCK_SIZE &&
+                     ctx <= mb * PA_BLOCK_SIZE;
+  // the positions the chunk's queries attend: from the first query's window start to ctx - 1
+  const int lo = p.window > 0 ? max(0, ctx - n - p.window + 1) : 0;
+  int e = -1;  // the block's pool entry (0 for a block of sink positions only: none is read)
+  if (valid && b >= lo / PA_BLOCK_SIZE && b * PA_BLOCK_SIZE < ctx) {
+    if ((b + 1) * PA_BLOCK_SIZE <= p.num_sink) {
+      e = 0;
+    } else {
+      const int t = p.block_tables[static_cast<size_t>(s) * p.max_blocks + b];
+      e = (t < 0 || t >= p.num_blocks) ? -1 : t;
+    }
+  }
+  const size_t xb = static_cast<size_t>(s) * mb + b;  // the block of the bf16 pool
+  if (threadIdx.x == 0) dense[xb] = e >= 0 ? static_cast<int32_t>(xb) : -1;
+  if (e < 0) return;
+  const int pieces = 2 * PA_BLOCK_SIZE * p.H_kv * GROUPS;  // (tensor, slot, head, 32-dim group)
+  for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+    const int g = i % GROUPS, h = (i / GROUPS) % p.H_kv;
+    const int r = (i / (GROUPS * p.H_kv)) % PA_BLOCK_SIZE, t = i / (GROUPS * p.H_kv * PA_BLOCK_SIZE);
+    DqPiece<D, KIND> pc;
+    pc.load(p, t, s, h, b * PA_BLOCK_SIZE + r, static_cast<size_t>(e) * PA_BLOCK_SIZE + r, g);
+    uint32_t out[16];
+    pc.decode(t, out);
+    uint4* dst = reinterpret_cast<uint4*>((t ? vx : kx) + ((xb * PA_BLOCK_SIZE + r) * p.H_kv + h) * D + 32 * g);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) dst[u] = make_uint4(out[4 * u], out[4 * u + 1], out[4 * u + 2], out[4 * u + 3]);
+  }
+}
+
 }  // namespace
 }  // namespace pa
 
@@ -555,6 +606,39 @@ pa_status prefill_check(const pa_cache_desc* desc, const void* out, const void* 
   return PA_OK;
 }
 
+PrefillParams prefill_params(const pa_cache_desc* desc, void* out, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* block_tables, const int32_t* q_start,
+                             const int32_t* context_lens, int max_query_len, float scale, int32_t* err_flag) {
+  PrefillParams p;
+  p.B = desc->num_seqs;
+  p.H_q = desc->num_q_heads;
+  p.H_kv = desc->num_kv_heads;
+  p.G = desc->num_q_heads / desc->num_kv_heads;
+  p.num_blocks = desc->num_blocks;
+  p.max_blocks = desc->max_blocks_per_seq;
+  p.max_q = max_query_len;
+  p.window = desc->sliding_window;
+  p.tpw = 16 / p.G;
+  p.q_tile = kPfWarps * p.tpw;
+  p.nc = desc->head_dim * 2 / 128;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.q_start = q_start;
+  p.context_lens = context_lens;
+  p.block_tables = block_tables;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.err = err_flag;
+  p.num_sink = desc->num_sink;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.k_scales = desc->k_scales;
+  p.v_scales = desc->v_scales;
+  p.k_sink = static_cast<const __nv_bfloat16*>(desc->k_sink);
+  p.v_sink = static_cast<const __nv_bfloat16*>(desc->v_sink);
+  p.extra_offset = is_int4(desc) ? int4_params_offset(desc) : (has_token_scales(desc) ? token_scales_offset(desc) : 0);
+  return p;
+}
+
 // pa_prefill_attention after its checks; step: the previous kernel is this step's append.
 pa_status prefill_launch(const pa_cache_desc* desc, void* out, const void* q, const void* k_cache,
                          const void* v_cache, const int32_t* block_tables, const int32_t* q_start,
@@ -575,33 +659,8 @@ pa_status prefill_launch(const pa_cache_desc* desc, void* out, const void* q, co
   if (!dq && (!encode_cache_map(&mk, k_cache, 2, desc->num_kv_heads * nc, 1, slots) ||
               !encode_cache_map(&mv, v_cache, 2, desc->num_kv_heads * nc, 1, slots)))
     return PA_ERR_CUDA;
-  PrefillParams p;
-  p.B = desc->num_seqs;
-  p.H_q = desc->num_q_heads;
-  p.H_kv = desc->num_kv_heads;
-  p.G = desc->num_q_heads / desc->num_kv_heads;
-  p.num_blocks = desc->num_blocks;
-  p.max_blocks = desc->max_blocks_per_seq;
-  p.max_q = max_query_len;
-  p.window = desc->sliding_window;
-  p.tpw = 16 / p.G;
-  p.q_tile = kPfWarps * p.tpw;
-  p.nc = nc;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.q_start = q_start;
-  p.context_lens = context_lens;
-  p.block_tables = block_tables;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.err = err_flag;
-  p.num_sink = desc->num_sink;
-  p.k_cache = static_cast<const uint8_t*>(k_cache);
-  p.v_cache = static_cast<const uint8_t*>(v_cache);
-  p.k_scales = desc->k_scales;
-  p.v_scales = desc->v_scales;
-  p.k_sink = static_cast<const __nv_bfloat16*>(desc->k_sink);
-  p.v_sink = static_cast<const __nv_bfloat16*>(desc->v_sink);
-  p.extra_offset = is_int4(desc) ? int4_params_offset(desc) : (has_token_scales(desc) ? token_scales_offset(desc) : 0);
+  const PrefillParams p = prefill_params(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens,
+                                         max_query_len, scale, err_flag);
   const dim3 grid((max_query_len + p.q_tile - 1) / p.q_tile, p.B, p.H_kv);
   cudaStream_t s = as_stream(stream);
   if (dq) {  // 8-bit and INT4 caches have head_dim 128 (validate_desc)
@@ -616,8 +675,96 @@ pa_status prefill_launch(const pa_cache_desc* desc, void* out, const void* q, co
     return launch_overlapped(prefill_kernel<128>, grid, dim3(kPfThreads), 0, s, mk, mv, p);
   return launch_overlapped(prefill_kernel<64>, grid, dim3(kPfThreads), 0, s, mk, mv, p);
 }
+
+// Bytes of pa_prefill_attention_ws's workspace (and the bf16 pool's blocks per sequence in *mb):
+// 0 when the call needs none (a bf16 cache without sinks, or a shape the tensor-core kernel does
+// not take) or the arguments are invalid.
+size_t prefill_ws_bytes(const pa_cache_desc* d, int max_ctx, int* mb_out) {
+  if (validate_desc(d) != PA_OK || max_ctx < 0 ||
+      static_cast<long long>(max_ctx) > static_cast<long long>(d->max_blocks_per_seq) * PA_BLOCK_SIZE)
+    return 0;
+#ifdef PA_PREFILL_WARP_MMA_ONLY
+  return 0;
+#else
+  const int G = d->num_q_heads / d->num_kv_heads;
+  const bool dq = is_quantized(d) || d->num_sink > 0;
+  if (!dq || d->head_dim != 128 || (G & (G - 1)) != 0) return 0;
+  const int mb = std::max(1, (max_ctx + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE);
+  // slot indices of the bf16 pool stay within int32 (the tensor maps' coordinates)
+  if (static_cast<long long>(d->num_seqs) * mb * PA_BLOCK_SIZE > 0x7FFFFFFFLL) return 0;
+  if (mb_out) *mb_out = mb;
+  const size_t table = (static_cast<size_t>(d->num_seqs) * mb * 4 + 255) / 256 * 256;
+  const size_t pool = static_cast<size_t>(d->num_seqs) * mb * PA_BLOCK_SIZE * d->num_kv_heads * 128 * 2;
+  return table + 2 * pool;
+#endif
+}
+
+// The expanded path: decode every attended block once into the workspace's bf16 pool, then the
+// tensor-core kernel over that pool and its dense table (as a bf16 cache without sinks).
+pa_status prefill_expanded(const pa_cache_desc* desc, void* out, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_tables, const int32_t* q_start,
+                           const int32_t* context_lens, int max_query_len, float scale, int mb, void* workspace,
+                           int32_t* err_flag, void* stream) {
+  const PrefillParams p = prefill_params(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens,
+                                         max_query_len, scale, err_flag);
+  const size_t table = (static_cast<size_t>(desc->num_seqs) * mb * 4 + 255) / 256 * 256;
+  const size_t pool = static_cast<size_t>(desc->num_seqs) * mb * PA_BLOCK_SIZE * desc->num_kv_heads * 128 * 2;
+  int32_t* dense = static_cast<int32_t*>(workspace);
+  auto* kx = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + table);
+  auto* vx = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + table + pool);
+  cudaStream_t s = as_stream(stream);
+  const dim3 grid(mb, desc->num_seqs), block(256);
+  pa_status st;
+  if (is_int4(desc)) st = launch_overlapped(prefill_expand_kernel<128, 2>, grid, block, 0, s, p, mb, kx, vx, dense);
+  else if (has_token_scales(desc))
+    st = launch_overlapped(prefill_expand_kernel<128, 3>, grid, block, 0, s, p, mb, kx, vx, dense);
+  else if (is_quantized(desc))
+    st = launch_overlapped(prefill_expand_kernel<128, 1>, grid, block, 0, s, p, mb, kx, vx, dense);
+  else st = launch_overlapped(prefill_expand_kernel<128, 0>, grid, block, 0, s, p, mb, kx, vx, dense);
+  if (st != PA_OK) return st;
+  pa_cache_desc x = *desc;  // the bf16 pool: every attended block, sinks included, in place
+  x.k_dtype = x.v_dtype = PA_BF16;
+  x.k_scales = x.v_scales = nullptr;
+  x.k_sink = x.v_sink = nullptr;
+  x.num_sink = 0;
+  x.num_blocks = desc->num_seqs * mb;
+  x.max_blocks_per_seq = mb;
+  return launch_prefill_tc(&x, out, q, kx, vx, dense, q_start, context_lens, max_query_len, scale, err_flag, s,
+                           false);
+}
 }  // namespace
 }  // namespace pa
+
+extern "C" size_t pa_prefill_workspace_size(const pa_cache_desc* desc, int max_context_len) {
+  return pa::prefill_ws_bytes(desc, max_context_len, nullptr);
+}
+
+extern "C" pa_status pa_prefill_attention_ws(const pa_cache_desc* desc, void* out, const void* q,
+                                             const void* k_cache, const void* v_cache,
+                                             const int32_t* block_tables, const int32_t* q_start,
+                                             const int32_t* context_lens, int max_query_len, int max_context_len,
+                                             float scale, void* workspace, size_t workspace_bytes,
+                                             int32_t* err_flag, void* stream) {
+  bool work = false;
+  const pa_status st = pa::prefill_check(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens,
+                                         max_query_len, scale, &work);
+  if (st != PA_OK) return st;
+  if (max_context_len < 0 ||
+      static_cast<long long>(max_context_len) > static_cast<long long>(desc->max_blocks_per_seq) * PA_BLOCK_SIZE)
+    return PA_ERR_INVALID_ARG;
+  int mb = 0;
+  const size_t need = pa::prefill_ws_bytes(desc, max_context_len, &mb);
+  if (need > 0) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  if (!work) return PA_OK;
+  if (need == 0)
+    return pa::prefill_launch(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
+                              scale, err_flag, stream, false);
+  return pa::prefill_expanded(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
+                              scale, mb, workspace, err_flag, stream);
+}
 
 extern "C" pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, const void* q,
                                           const void* k_cache, const void* v_cache,

@@ -749,7 +749,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // (coalesced).
       if (ok) ok = warp_wait(&o_done[wg], (sp - 1u) & 1u);
       tc_fence_after();
-      const float inv = (!ok || bad || !(l_run > 0.f)) ? 0.f : 1.f / l_run;
+      // zero rows are selected, not multiplied: O may hold NaN when a block was not loaded (its
+      // stage keeps earlier bytes) or no key was attended
+      const bool zero_out = !ok || bad || !(l_run > 0.f);
+      const float inv = zero_out ? 0.f : 1.f / l_run;
       const int g_last = g - 1;
       uint8_t* stile =
           wg == 0 ? sm + kKOff + (g_last % kKStages) * kTile : sm + kVOff + (g_last % kVStages) * kTile;
@@ -769,7 +772,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16(__uint_as_float(ov[8 * q4 + 2 * e]) * inv, __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
+            w[e] = zero_out ? 0u
+                            : pack_bf16(__uint_as_float(ov[8 * q4 + 2 * e]) * inv,
+                                        __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
           *reinterpret_cast<uint4*>(stile + (j >> 3) * kHalf + r * 128 + (((j & 7) ^ (r & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }

@@ -378,3 +378,57 @@ def test_release_frees_only_unshared_blocks_and_nothing_leaks():
     assert bm.release(row, 8) == 0  # still held by the fork
     assert bm.release(fork, 8) == 7
     assert bm.num_free() == 32
+
+
+def test_prefill_workspace_size():
+    """The decoded bf16 copy of pa_prefill_attention_ws: a dense table of num_seqs x ceil(max_ctx/16)
+    int32 entries (rounded up to 256 bytes), then K and V pools of that many 16-slot bf16 blocks;
+    none for caches and shapes that keep the plain path."""
+    quant = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, k_dtype="e4m3", v_dtype="int8", k_scales=FAKE,
+                 v_scales=FAKE, max_blocks_per_seq=100)
+    mb = (1000 + 15) // 16
+    table = (4 * mb * 4 + 255) // 256 * 256
+    pool = 4 * mb * 16 * 8 * 128 * 2
+    assert N.pa_prefill_workspace_size(_desc(**quant), 1000) == table + 2 * pool
+    assert N.pa_prefill_workspace_size(_desc(**quant), 0) == 256 + 2 * 4 * 16 * 8 * 128 * 2  # one block each
+    int4 = dict(quant, k_dtype="int4", v_dtype="int4", k_scales=None, v_scales=None)
+    tok = dict(quant, k_dtype="e4m3_tok", k_scales=None)
+    sinks = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, num_sink=4, k_sink=FAKE, v_sink=FAKE,
+                 max_blocks_per_seq=100)
+    for kw in (int4, tok, sinks):
+        assert N.pa_prefill_workspace_size(_desc(**kw), 1000) == table + 2 * pool
+    # the plain path: bf16 without sinks, head_dim 64, G not a power of two
+    assert N.pa_prefill_workspace_size(_desc(num_q_heads=32, num_kv_heads=8, head_dim=128), 1000) == 0
+    assert N.pa_prefill_workspace_size(_desc(num_sink=4, k_sink=FAKE, v_sink=FAKE), 200) == 0
+    assert N.pa_prefill_workspace_size(_desc(**dict(quant, num_q_heads=24)), 1000) == 0
+    # invalid: max_context_len beyond the table, negative, or a bad description
+    assert N.pa_prefill_workspace_size(_desc(**quant), 100 * 16 + 1) == 0
+    assert N.pa_prefill_workspace_size(_desc(**quant), -1) == 0
+    assert N.pa_prefill_workspace_size(_desc(**dict(quant, k_scales=None)), 1000) == 0
+
+
+@host_only
+def test_prefill_ws_rejects_bad_arguments_on_the_host():
+    quant = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, k_dtype="e4m3", v_dtype="int8", k_scales=FAKE,
+                  v_scales=FAKE, max_blocks_per_seq=100)
+    need = N.pa_prefill_workspace_size(quant, 1000)
+    ws = 1 << 24  # 256-byte aligned
+    # pa_prefill_attention_ws(desc, out, q, k, v, tables, q_start, ctx, max_q, max_ctx, scale, ws, bytes)
+    good = dict(out=FAKE, max_q=16, max_ctx=1000, scale=0.1, ws=ws, nbytes=need)
+    bad = [
+        (dict(scale=float("nan")), N.PA_ERR_INVALID_ARG),
+        (dict(out=0), N.PA_ERR_INVALID_ARG),
+        (dict(max_ctx=-1), N.PA_ERR_INVALID_ARG),
+        (dict(max_ctx=100 * 16 + 1), N.PA_ERR_INVALID_ARG),
+        (dict(ws=0), N.PA_ERR_INVALID_ARG),
+        (dict(ws=ws + 128), N.PA_ERR_INVALID_ARG),
+        (dict(nbytes=need - 1), N.PA_ERR_WORKSPACE_TOO_SMALL),
+    ]
+    for kw, status in bad:
+        a = dict(good, **kw)
+        with pytest.raises(N.PaError) as e:
+            N.pa_prefill_attention_ws(quant, a["out"], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["max_q"], a["max_ctx"],
+                                      a["scale"], a["ws"], a["nbytes"], None, 0)
+        assert e.value.status == status, kw
+    # nothing to do (no query rows): checked, then nothing enqueued
+    N.pa_prefill_attention_ws(quant, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1000, 0.1, ws, need, None, 0)

@@ -94,6 +94,21 @@ class QuantPrefill:
                                w.scale, self.err)
         return out
 
+    def attend_ws(self, ctx=None, fill=0):
+        """pa_prefill_attention_ws: every attended block decoded once into the workspace (filled
+        with the byte `fill` first: its contents must not matter), then the bf16 tensor-core path."""
+        w = self.w
+        out = self._out()
+        ctx = w.context_lens() if ctx is None else ctx
+        max_ctx = int(w.max_blocks * 16)
+        nbytes = N.pa_prefill_workspace_size(self.desc, max_ctx)
+        ws = torch.full((max(nbytes, 1),), fill, dtype=torch.uint8, device="cuda") if nbytes else None
+        N.pa_prefill_attention_ws(self.desc, out, w.q.cuda(), self.k, self.v, self.tables,
+                                  torch.from_numpy(w.q_start()).cuda(),
+                                  torch.from_numpy(np.ascontiguousarray(ctx, dtype=np.int32)).cuda(),
+                                  int(w.chunk.max()), max_ctx, w.scale, ws, nbytes, self.err)
+        return out, nbytes
+
     def step(self):
         """pa_prefill_step: the chunk's append and the attention in one call."""
         w = self.w
@@ -233,3 +248,103 @@ def test_one_token_chunks_agree_with_the_decode_path():
     assert int(g.err.item()) == 0
     assert_attention_close(to_f64(pre), ref, "prefill of one token")
     assert_attention_close(to_f64(out), ref, "decode")
+
+
+
+# ---- pa_prefill_attention_ws: each attended block decoded once, then the tcgen05 kernel ----
+
+@pytest.mark.parametrize("kind", ["fp8", "fp8_token", "int4"])
+@pytest.mark.parametrize("H_q,H_kv", [(32, 8), (64, 8), (16, 4)])
+def test_prefill_ws_over_quantized_cache(kind, H_q, H_kv):
+    w = make_prefill_workload(H_q=H_q, H_kv=H_kv, D=128, cached_list=[0, 17, 100, 300], chunk_list=[5, 16, 33, 70],
+                              seed=31)
+    g = QuantPrefill(w, kind)
+    g.append("fill")
+    g.append("new")
+    out, nbytes = g.attend_ws()
+    assert nbytes > 0
+    _check(g, out, f"ws {kind} {H_q}/{H_kv}")
+
+
+@pytest.mark.parametrize("kind", ["fp8", "fp8_token", "int4", "bf16"])
+def test_prefill_ws_with_sinks(kind):
+    w = make_prefill_workload(H_q=32, H_kv=8, D=128, cached_list=[0, 2, 4, 200, 1], chunk_list=[3, 9, 20, 40, 1],
+                              seed=32)
+    g = QuantPrefill(w, kind, num_sink=4)
+    g.append("fill")
+    g.append("new")
+    out, nbytes = g.attend_ws()
+    assert nbytes > 0
+    _check(g, out, f"ws {kind} with sinks")
+
+
+@pytest.mark.parametrize("kind", ["fp8", "int4"])
+def test_prefill_ws_sliding_window(kind):
+    """Blocks before the first query's window are neither decoded nor read."""
+    w = make_prefill_workload(H_q=32, H_kv=8, D=128, cached_list=[0, 300, 60], chunk_list=[100, 50, 77], seed=34)
+    g = QuantPrefill(w, kind, window=64)
+    g.append("fill")
+    g.append("new")
+    out, _ = g.attend_ws()
+    _check(g, out, f"ws {kind} window 64")
+
+
+@pytest.mark.parametrize("kind", ["fp8", "int4"])
+def test_prefill_ws_long_chunks_many_tiles(kind):
+    """Chunks of several 64-token items per sequence over contexts of many 128-key tiles, a
+    workspace full of 0xFF bytes (NaN in bf16) against one of zeros: identical, and both match the
+    oracle and the block-by-block path."""
+    w = make_prefill_workload(H_q=32, H_kv=8, D=128, cached_list=[1500, 40, 700], chunk_list=[300, 130, 257],
+                              seed=38)
+    g = QuantPrefill(w, kind, num_sink=4)
+    g.append("fill")
+    g.append("new")
+    a, _ = g.attend_ws(fill=0)
+    b, _ = g.attend_ws(fill=0xFF)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    _check(g, a, f"ws {kind} long chunks")
+    _check(g, g.attend(), f"block by block {kind} long chunks")
+
+
+def test_prefill_ws_plain_shapes_need_no_workspace():
+    """bf16 without sinks and head_dim 64 with sinks take the plain path: no workspace."""
+    w = make_prefill_workload(H_q=32, H_kv=8, D=128, cached_list=[10, 90], chunk_list=[20, 33], seed=39)
+    g = QuantPrefill(w, "bf16")
+    g.append("fill")
+    g.append("new")
+    out, nbytes = g.attend_ws()
+    assert nbytes == 0
+    _check(g, out, "ws bf16 plain")
+    w = make_prefill_workload(H_q=8, H_kv=2, D=64, cached_list=[0, 6, 90], chunk_list=[12, 30, 7], seed=33)
+    g = QuantPrefill(w, "bf16", num_sink=4)
+    g.append("fill")
+    g.append("new")
+    out, nbytes = g.attend_ws()
+    assert nbytes == 0
+    _check(g, out, "ws bf16 sinks d 64")
+
+
+def test_prefill_ws_invalid_length_and_bad_block():
+    w = make_prefill_workload(H_q=32, H_kv=8, D=128, cached_list=[20, 40, 30], chunk_list=[10, 10, 10], seed=36)
+    g = QuantPrefill(w, "fp8")
+    g.append("fill")
+    g.append("new")
+    ref = g.oracle()
+    ctx = w.context_lens().copy()
+    ctx[1] = 5  # fewer context tokens than queries
+    out, _ = g.attend_ws(ctx)
+    out = to_f64(out)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) & N.PA_EFLAG_CTX_OVERFLOW
+    assert np.all(out[10:20] == 0)
+    keep = np.r_[0:10, 20:30]
+    assert_attention_close(out[keep], ref[keep], "other sequences")
+    g.err.zero_()
+    g.tables[2, 1] = w.num_blocks + 5
+    out, _ = g.attend_ws()
+    out = to_f64(out)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) & N.PA_EFLAG_BAD_BLOCK_ID
+    assert np.all(out[20:30] == 0)
+    assert_attention_close(out[:20], ref[:20], "sequences with valid tables")
