@@ -655,12 +655,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_wait_ld();
         const int kbase = (it.kb0 + 8 * k) * PA_BLOCK_SIZE;
         // scores stay raw (the scale is positive, so the maximum commutes with it); only tiles
-        // that cross a row's causal or window edge take the per-key mask
+        // that cross a row's causal or window edge take the per-key mask, and within them only
+        // the 32-key chunks that some row of the warp does not attend whole (a row attends the
+        // tile's columns lo .. hi; on a diagonal tile a warp's rows, 32 / G tokens, put one or
+        // two of the four chunks across their edges)
         if (!__all_sync(0xffffffffu, row_ok && kbase + 127 <= row_pos && kbase >= row_lo)) {
+          const int lo = row_lo - kbase, hi = row_ok ? row_pos - kbase : -1;
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int kp = kbase + c;
-            if (!(row_ok && kp <= row_pos && kp >= row_lo)) sv[c] = __float_as_uint(kNegInfTc);
+          for (int q = 0; q < 4; ++q) {
+            if (__all_sync(0xffffffffu, lo <= 32 * q && hi >= 32 * q + 31)) continue;
+#pragma unroll
+            for (int c = 32 * q; c < 32 * q + 32; ++c)
+              if (c < lo || c > hi) sv[c] = __float_as_uint(kNegInfTc);
           }
         }
         float mx4[4] = {kNegInfTc, kNegInfTc, kNegInfTc, kNegInfTc};
