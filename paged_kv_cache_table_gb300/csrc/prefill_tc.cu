@@ -656,14 +656,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int kbase = (it.kb0 + 8 * k) * PA_BLOCK_SIZE;
         // scores stay raw (the scale is positive, so the maximum commutes with it); only tiles
         // that cross a row's causal or window edge take the per-key mask, and within them only
-        // the 32-key chunks that some row of the warp does not attend whole (a row attends the
-        // tile's columns lo .. hi; on a diagonal tile a warp's rows, 32 / G tokens, put one or
-        // two of the four chunks across their edges)
+        // the 32-key chunks that some row of the warp attends in part (a row attends the tile's
+        // columns lo .. hi; on a diagonal tile a warp's rows, 32 / G tokens, put one or two of
+        // the four chunks across their edges).  A chunk that no row of the warp attends (`dead`,
+        // the keys past the item's last query on its diagonal tile) takes no maximum and no
+        // exponentials: its P is zero.
+        unsigned dead = 0;
         if (!__all_sync(0xffffffffu, row_ok && kbase + 127 <= row_pos && kbase >= row_lo)) {
           const int lo = row_lo - kbase, hi = row_ok ? row_pos - kbase : -1;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             if (__all_sync(0xffffffffu, lo <= 32 * q && hi >= 32 * q + 31)) continue;
+            if (__all_sync(0xffffffffu, hi < 32 * q || lo > 32 * q + 31)) {
+              dead |= 1u << q;
+              continue;
+            }
 #pragma unroll
             for (int c = 32 * q; c < 32 * q + 32; ++c)
               if (c < lo || c > hi) sv[c] = __float_as_uint(kNegInfTc);
@@ -671,8 +678,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         float mx4[4] = {kNegInfTc, kNegInfTc, kNegInfTc, kNegInfTc};
 #pragma unroll
-        for (int c = 0; c < 128; c += 2)
-          mx4[(c >> 1) & 3] = max3f(mx4[(c >> 1) & 3], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        for (int q = 0; q < 4; ++q) {
+          if ((dead >> q) & 1u) continue;
+#pragma unroll
+          for (int c = 32 * q; c < 32 * q + 32; c += 2)
+            mx4[(c >> 1) & 3] = max3f(mx4[(c >> 1) & 3], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        }
         const float mraw = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]);
         const float mx = mraw == kNegInfTc ? kNegInfTc : mraw * p.scale_log2;
         const float m_new = (m_run == kNegInfTc || mx > m_run + 8.f) ? fmaxf(m_run, mx) : m_run;
@@ -708,12 +719,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int h = 0; h < 4; ++h) {  // a quarter (32 keys, 16 columns) at a time
           uint32_t pw[16];
+          if ((dead >> h) & 1u) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float a = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e]), sl, -ms));
-            const float b = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e + 1]), sl, -ms));
-            ls4[e & 3] += a + b;
-            pw[e] = pack_bf16(a, b);
+            for (int e = 0; e < 16; ++e) pw[e] = 0u;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float a = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e]), sl, -ms));
+              const float b = ex2(fmaf(__uint_as_float(sv[32 * h + 2 * e + 1]), sl, -ms));
+              ls4[e & 3] += a + b;
+              pw[e] = pack_bf16(a, b);
+            }
           }
           tmem_st16(tS + 16 * h, pw);
         }
