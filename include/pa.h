@@ -292,6 +292,20 @@ pa_status pa_prefill_attention_ws(const pa_cache_desc* desc, void* out, const vo
                                   float scale, void* workspace, size_t workspace_bytes,
                                   int32_t* err_flag, void* stream);
 
+/* One chunked-prefill step with the workspace path: pa_kv_append_tokens of the chunk's K/V, then
+ * pa_prefill_attention_ws, enqueued together (ldpk §7).  The result is what the two calls give
+ * one after the other.  Arguments: those of pa_kv_append_tokens and of pa_prefill_attention_ws,
+ * with the same meaning, layouts and rules; out must not overlap k_new, v_new, token_seq or
+ * token_pos.  Every argument is checked before anything is enqueued.
+ * Host errors: those of pa_kv_append_tokens and pa_prefill_attention_ws. */
+pa_status pa_prefill_step_ws(const pa_cache_desc* desc, void* out, const void* q, void* k_cache,
+                             void* v_cache, const void* k_new, const void* v_new, int num_tokens,
+                             const int32_t* token_seq, const int32_t* token_pos,
+                             const int32_t* block_tables, const int32_t* q_start,
+                             const int32_t* context_lens, int max_query_len, int max_context_len,
+                             float scale, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                             void* stream);
+
 /* Allocation-free decode attention.  The pages have no counterpart to this entry point: it is
  * pa_decode_attention for callers that cannot allocate device memory when they call it, for
  * example a plugin running inside a host framework that owns every byte of device memory, a

@@ -766,6 +766,38 @@ extern "C" pa_status pa_prefill_attention_ws(const pa_cache_desc* desc, void* ou
                               scale, mb, workspace, err_flag, stream);
 }
 
+extern "C" pa_status pa_prefill_step_ws(const pa_cache_desc* desc, void* out, const void* q, void* k_cache,
+                                        void* v_cache, const void* k_new, const void* v_new, int num_tokens,
+                                        const int32_t* token_seq, const int32_t* token_pos,
+                                        const int32_t* block_tables, const int32_t* q_start,
+                                        const int32_t* context_lens, int max_query_len, int max_context_len,
+                                        float scale, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                        void* stream) {
+  // every argument of the attention half is checked before the append is enqueued
+  bool work = false;
+  const pa_status st = pa::prefill_check(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens,
+                                         max_query_len, scale, &work);
+  if (st != PA_OK) return st;
+  if (max_context_len < 0 ||
+      static_cast<long long>(max_context_len) > static_cast<long long>(desc->max_blocks_per_seq) * PA_BLOCK_SIZE)
+    return PA_ERR_INVALID_ARG;
+  int mb = 0;
+  const size_t need = pa::prefill_ws_bytes(desc, max_context_len, &mb);
+  if (need > 0) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  const pa_status sa = pa_kv_append_tokens(desc, k_cache, v_cache, k_new, v_new, num_tokens, token_seq,
+                                           token_pos, block_tables, err_flag, stream);
+  if (sa != PA_OK || !work) return sa;
+  if (need == 0)
+    return pa::prefill_launch(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
+                              scale, err_flag, stream, num_tokens > 0);
+  // the expand kernel waits for the append before it reads anything
+  return pa::prefill_expanded(desc, out, q, k_cache, v_cache, block_tables, q_start, context_lens, max_query_len,
+                              scale, mb, workspace, err_flag, stream);
+}
+
 extern "C" pa_status pa_prefill_attention(const pa_cache_desc* desc, void* out, const void* q,
                                           const void* k_cache, const void* v_cache,
                                           const int32_t* block_tables, const int32_t* q_start,

@@ -43,6 +43,7 @@ EXPORTED = [
     "pa_status_string", "pa_kv_append", "pa_kv_append_tokens", "pa_block_copy",
     "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_noalloc", "pa_decode_step",
     "pa_prefill_attention", "pa_prefill_step", "pa_prefill_workspace_size", "pa_prefill_attention_ws",
+    "pa_prefill_step_ws",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_alloc", "pa_bm_claim", "pa_bm_incref", "pa_bm_decref",
     "pa_bm_refcount", "pa_bm_num_free", "pa_bm_fork", "pa_bm_release", "pa_bm_prepare_step",
     "pa_bm_slide_window",
@@ -121,6 +122,9 @@ def lib() -> ctypes.CDLL:
         L.pa_prefill_attention_ws.restype = c_int
         L.pa_prefill_attention_ws.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, ctypes.c_float, vp,
                                               ctypes.c_size_t, vp, vp]
+        L.pa_prefill_step_ws.restype = c_int
+        L.pa_prefill_step_ws.argtypes = [dp, vp, vp, vp, vp, vp, vp, c_int, vp, vp, vp, vp, vp, c_int, c_int,
+                                         ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
         L.pa_prefill_step.restype = c_int
         L.pa_prefill_step.argtypes = [dp, vp, vp, vp, vp, vp, vp, c_int, vp, vp, vp, vp, vp, c_int,
                                       ctypes.c_float, vp, vp]
@@ -277,6 +281,20 @@ def pa_prefill_attention_ws(desc, out, q, k_cache, v_cache, block_tables, q_star
                                          int(max_query_len), int(max_context_len), float(scale), _ptr(workspace),
                                          int(workspace_bytes), _ptr(err_flag), _stream(stream)),
            "pa_prefill_attention_ws")
+
+
+def pa_prefill_step_ws(desc, out, q, k_cache, v_cache, k_new, v_new, num_tokens, token_seq, token_pos, block_tables,
+                       q_start, context_lens, max_query_len, max_context_len, scale, workspace, workspace_bytes=None,
+                       err_flag=None, stream=None):
+    """pa_kv_append_tokens of a chunk, then pa_prefill_attention_ws, as one step (see pa.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_prefill_step_ws(ctypes.byref(desc), _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(k_new), _ptr(v_new), int(num_tokens), _ptr(token_seq), _ptr(token_pos),
+                                    _ptr(block_tables), _ptr(q_start), _ptr(context_lens), int(max_query_len),
+                                    int(max_context_len), float(scale), _ptr(workspace), int(workspace_bytes),
+                                    _ptr(err_flag), _stream(stream)),
+           "pa_prefill_step_ws")
 
 
 def pa_prefill_step(desc, out, q, k_cache, v_cache, k_new, v_new, num_tokens, token_seq, token_pos, block_tables,

@@ -432,3 +432,30 @@ def test_prefill_ws_rejects_bad_arguments_on_the_host():
         assert e.value.status == status, kw
     # nothing to do (no query rows): checked, then nothing enqueued
     N.pa_prefill_attention_ws(quant, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1000, 0.1, ws, need, None, 0)
+
+
+@host_only
+def test_prefill_step_ws_checks_every_argument_first():
+    """The step form checks the attention's workspace and bounds and the append's arguments
+    before it enqueues the append."""
+    quant = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, k_dtype="e4m3", v_dtype="int8", k_scales=FAKE,
+                  v_scales=FAKE, max_blocks_per_seq=100)
+    need = N.pa_prefill_workspace_size(quant, 1000)
+    ws = 1 << 24
+    # pa_prefill_step_ws(desc, out, q, k, v, k_new, v_new, n, seq, pos, tables, q_start, ctx, max_q, max_ctx,
+    #                    scale, ws, bytes)
+    good = dict(k_new=FAKE, n=5, max_ctx=1000, ws=ws, nbytes=need, scale=0.1)
+    bad = [
+        (dict(max_ctx=100 * 16 + 1), N.PA_ERR_INVALID_ARG),
+        (dict(ws=ws + 64), N.PA_ERR_INVALID_ARG),
+        (dict(nbytes=need - 1), N.PA_ERR_WORKSPACE_TOO_SMALL),
+        (dict(k_new=0), N.PA_ERR_INVALID_ARG),      # an append argument
+        (dict(n=-1), N.PA_ERR_INVALID_ARG),
+        (dict(scale=float("nan")), N.PA_ERR_INVALID_ARG),
+    ]
+    for kw, status in bad:
+        a = dict(good, **kw)
+        with pytest.raises(N.PaError) as e:
+            N.pa_prefill_step_ws(quant, FAKE, FAKE, FAKE, FAKE, a["k_new"], FAKE, a["n"], FAKE, FAKE, FAKE, FAKE,
+                                 FAKE, 16, a["max_ctx"], a["scale"], a["ws"], a["nbytes"], None, 0)
+        assert e.value.status == status, kw

@@ -109,6 +109,20 @@ class QuantPrefill:
                                   int(w.chunk.max()), max_ctx, w.scale, ws, nbytes, self.err)
         return out, nbytes
 
+    def step_ws(self):
+        """pa_prefill_step_ws: the chunk's append and the workspace attention in one call."""
+        w = self.w
+        out = self._out()
+        max_ctx = int(w.max_blocks * 16)
+        nbytes = N.pa_prefill_workspace_size(self.desc, max_ctx)
+        ws = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device="cuda") if nbytes else None
+        N.pa_prefill_step_ws(self.desc, out, w.q.cuda(), self.k, self.v, w.new_k.cuda(), w.new_v.cuda(),
+                             len(w.new_seq), torch.from_numpy(w.new_seq).cuda(), torch.from_numpy(w.new_pos).cuda(),
+                             self.tables, torch.from_numpy(w.q_start()).cuda(),
+                             torch.from_numpy(w.context_lens()).cuda(), int(w.chunk.max()), max_ctx, w.scale, ws,
+                             nbytes, self.err)
+        return out
+
     def step(self):
         """pa_prefill_step: the chunk's append and the attention in one call."""
         w = self.w
@@ -348,3 +362,19 @@ def test_prefill_ws_invalid_length_and_bad_block():
     assert int(g.err.item()) & N.PA_EFLAG_BAD_BLOCK_ID
     assert np.all(out[20:30] == 0)
     assert_attention_close(out[:20], ref[:20], "sequences with valid tables")
+
+
+@pytest.mark.parametrize("kind", ["fp8", "fp8_token", "int4", "bf16"])
+def test_prefill_step_ws_equals_append_then_attention_ws(kind):
+    w = make_prefill_workload(H_q=32, H_kv=8, D=128, cached_list=[10, 150, 600], chunk_list=[40, 9, 130], seed=35)
+    a, b = QuantPrefill(w, kind, num_sink=4), QuantPrefill(w, kind, num_sink=4)
+    for g in (a, b):
+        g.append("fill")
+    a.append("new")
+    out_a, _ = a.attend_ws()
+    out_b = b.step_ws()
+    torch.cuda.synchronize()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(a.k.view(torch.uint8) if a.k.dtype != torch.uint8 else a.k,
+                       b.k.view(torch.uint8) if b.k.dtype != torch.uint8 else b.k)
+    _check(b, out_b, f"{kind} prefill step, workspace path")
