@@ -268,7 +268,7 @@ def test_one_token_chunks_agree_with_the_decode_path():
 # ---- pa_prefill_attention_ws: each attended block decoded once, then the tcgen05 kernel ----
 
 @pytest.mark.parametrize("kind", ["fp8", "fp8_token", "int4"])
-@pytest.mark.parametrize("H_q,H_kv", [(32, 8), (64, 8), (16, 4)])
+@pytest.mark.parametrize("H_q,H_kv", [(32, 8), (64, 8), (16, 4), (8, 8), (16, 8)])
 def test_prefill_ws_over_quantized_cache(kind, H_q, H_kv):
     w = make_prefill_workload(H_q=H_q, H_kv=H_kv, D=128, cached_list=[0, 17, 100, 300], chunk_list=[5, 16, 33, 70],
                               seed=31)
