@@ -203,7 +203,7 @@ class ClockSampler:
 class DecodeBench:
     """One layer's paged cache and the per-step inputs of a WINDOW-step cycle, on one GPU."""
 
-    def __init__(self, name, device, partition=0, horizon=None):
+    def __init__(self, name, device, partition=0, horizon=None, shared=False):
         import torch
         from paged_kv_cache_table_gb300 import native as N
         from paged_kv_cache_table_gb300.workloads import make_workload
@@ -258,6 +258,12 @@ class DecodeBench:
         self.ctx_dev = torch.from_numpy(np.stack(self.ctx)).to(device)
         self.max_ctx = int(max(c.max() for c in self.ctx))
         self.ws_bytes = N.pa_decode_workspace_size(self.desc, self.max_ctx, partition)
+        # shared: the prefix's whole blocks attended once for all sequences (pa_decode_attention_shared)
+        self.shared = bool(shared and w.prefix)
+        if self.shared:
+            self.shared_len = w.prefix - w.prefix % 16
+            self.shared_seqs = torch.arange(w.B, dtype=torch.int32, device=device)
+            self.ws_bytes = N.pa_decode_shared_workspace_size(self.desc, self.max_ctx, partition, self.shared_len)
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
         self.out = torch.empty((w.B, w.H_q, w.D), dtype=torch.bfloat16, device=device)
         self.step_bytes = [attention_bytes(w, c) for c in self.ctx]
@@ -372,6 +378,16 @@ class DecodeBench:
         out = P["out"]
         if buf is not None:
             q, kn, vn, out = self.ptr_e2e[buf]
+        if self.shared:
+            N.pa_kv_append(self.desc, P["k"], P["v"], kn, vn, P["tab"], pos, P["err"], stream)
+            if ev is not None:
+                ev[0].record()
+            N.pa_decode_attention_shared(self.desc, out, q, P["k"], P["v"], P["tab"], ctx, self.max_ctx, w.scale,
+                                         self.partition, self.shared_seqs.data_ptr(), w.B, self.shared_len, P["ws"],
+                                         self.ws_bytes, P["err"], stream)
+            if ev is not None:
+                ev[1].record()
+            return
         if ev is None:
             # the step as one call: the append overlaps the attention's streaming of other blocks
             N.pa_decode_step(self.desc, out, q, P["k"], P["v"], kn, vn, P["tab"], pos, ctx, self.max_ctx, w.scale,
@@ -948,6 +964,21 @@ def run_native(args):
             extra_prefix = {"unique_bytes_per_call": int(ub),
                             "attention_gbs_unique": round(ub / (a_ms / 1e3) / 1e9, 1),
                             "fork_copy_pairs": nb.fork_pairs}
+            sb = DecodeBench(name, device, args.partition, shared=True)
+            e3, _, _ = sb.run(n2, args.warmup)
+            _, a3, _ = sb.run(n2, args.warmup, per_call_events=True)
+            s_ms = float(np.mean(a3))
+            ub3 = float(np.mean([sb.unique_bytes(sb.ctx[(sb.first_step + k) % WINDOW]) for k in range(len(a3))]))
+            extra_prefix["shared_prefix"] = {
+                "path": f"pa_decode_attention_shared over the {sb.shared_len} shared positions of all {sb.w.B} "
+                        "sequences (prefix kernel + decode of the private positions + merge), after pa_kv_append",
+                "attention_ms_per_call": round(s_ms, 5),
+                "attention_gbs_unique": round(ub3 / (s_ms / 1e3) / 1e9, 1),
+                "attention_frac_unique": round(ub3 / (s_ms / 1e3) / 1e9 / peak, 4),
+                "ms_per_step": round(1e3 * e3 / len(a3), 4),
+                "tokens_per_s_per_layer": round(sb.w.B * len(a3) / e3, 1),
+                "err_flag": int(sb.err.item())}
+            del sb
         else:
             extra_prefix = {}
         r = {**extra_prefix, "value": round(by2 / e2 / 1e9, 1), "unit": "GB/s",

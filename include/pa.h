@@ -220,6 +220,43 @@ pa_status pa_decode_attention(const pa_cache_desc* desc, void* out, const void* 
                               int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * Decode attention with a shared prompt prefix attended once (AI内存系统 §3.1: requests with the
+ * same prefix point their block tables at one copy of its blocks; §3.3: only whole blocks are
+ * shared; ldpk §2.1 formula).
+ *
+ * The result is pa_decode_attention's, up to the order of the fp32 sums.  The first shared_len
+ * positions of the listed sequences are attended together: for each KV head and each 128 of
+ * those positions, one product takes the queries of all listed sequences (G heads each) against
+ * the prefix keys read once, and leaves a softmax partial (running max, sum, unnormalised output)
+ * per row; the decode kernel then visits only positions shared_len .. ctx-1 of those sequences,
+ * and its merge combines both parts by the log-sum-exp rule.
+ *   shared_seqs   device int32 [n_shared], 0 <= n_shared <= num_seqs: the sequences to share; the
+ *                 first one's table supplies the prefix blocks.  Duplicates are harmless.
+ *   shared_len    a multiple of 16 with 0 <= shared_len <= max_context_len: the prefix length.
+ * The list is checked, not trusted: a listed sequence takes the shared part only when its
+ * context covers shared_len and its table holds the first listed sequence's physical block for
+ * every prefix block; every other sequence is attended in full as by pa_decode_attention.  An
+ * entry outside [0, num_seqs) sets PA_EFLAG_BAD_SEQ and is ignored (the first one: nothing is
+ * shared); a prefix block id outside [0, num_blocks) sets PA_EFLAG_BAD_BLOCK_ID and zeroes the
+ * rows of the sequences that share it.  n_shared == 0 or shared_len == 0 is pa_decode_attention.
+ * bf16 caches without sinks or sliding window only (PA_ERR_UNSUPPORTED otherwise), head_dim 64
+ * or 128.
+ *   workspace     at least pa_decode_shared_workspace_size(desc, max_context_len, partition_size,
+ *                 shared_len) bytes, 256-byte aligned, scratch for this call only.  The size is 0
+ *                 when an argument is invalid.
+ * Other arguments, device errors and host errors as pa_decode_attention. */
+size_t pa_decode_shared_workspace_size(const pa_cache_desc* desc, int max_context_len, int partition_size,
+                                       int shared_len);
+
+pa_status pa_decode_attention_shared(const pa_cache_desc* desc, void* out, const void* q,
+                                     const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     int max_context_len, float scale, int partition_size,
+                                     const int32_t* shared_seqs, int n_shared, int shared_len,
+                                     void* workspace, size_t workspace_bytes,
+                                     int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * Chunked-prefill (extend) attention over the paged cache (ldpk §2.2: under the causal mask the
  * query of position i attends to positions up to i; ldpk §7: long prompts are prefilled in
  * chunks).  Sequence s contributes the query rows q_start[s] .. q_start[s+1]-1 of q: they are its

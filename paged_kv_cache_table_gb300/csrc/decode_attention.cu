@@ -95,6 +95,14 @@ struct DecodeParams {
   // sequence (a decode step), or null.  With them the kernel waits for that kernel only before
   // loading a block that holds such a position; without them it waits before reading anything.
   const int32_t* append_pos;
+  // A shared prefix attended apart (pa_decode_attention_shared), or null: a sequence s with
+  // shared_flags[s] == kSharedUse starts at position shared_len (a multiple of 16); its positions
+  // below it are covered by n_extra partial rows per query head computed by the prefix kernel,
+  // extra[((s * n_extra + i) * H_q + h) * (D + 4)], which the merge folds in with its own.
+  const int32_t* shared_flags;
+  const float* extra;
+  int shared_len;
+  int n_extra;
 };
 
 // Blocks of a sequence with ctx tokens; -1 for an invalid context.
@@ -109,11 +117,21 @@ __device__ __forceinline__ int window_lo(const DecodeParams& p, int ctx) {
   return (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
 }
 
-// Logical blocks a sequence's query visits (those holding positions window_lo .. ctx-1);
-// -1 for an invalid context.
-__device__ __forceinline__ int seq_span(const DecodeParams& p, int ctx) {
+// First position this kernel attends for sequence s (global index): the window's, or past the
+// shared prefix attended apart.
+__device__ __forceinline__ bool shares_prefix(const DecodeParams& p, int s) {
+  return p.shared_flags && p.shared_flags[s] == kSharedUse;
+}
+__device__ __forceinline__ int seq_lo(const DecodeParams& p, int s, int ctx) {
+  const int lo = window_lo(p, ctx);
+  return shares_prefix(p, s) ? max(lo, min(p.shared_len, max(ctx, 0))) : lo;
+}
+
+// Logical blocks a sequence's query visits (those holding positions seq_lo .. ctx-1); -1 for an
+// invalid context.
+__device__ __forceinline__ int seq_span(const DecodeParams& p, int s, int ctx) {
   const int nb = seq_blocks(p, ctx);
-  return nb <= 0 ? nb : nb - window_lo(p, ctx) / PA_BLOCK_SIZE;
+  return nb <= 0 ? nb : nb - seq_lo(p, s, ctx) / PA_BLOCK_SIZE;
 }
 
 // Largest s in [0, n) with cum[s] <= u (cum non-decreasing, cum[0] <= u).
@@ -133,6 +151,7 @@ struct Smem {
   int4* meta;
   int* cum;
   int* ctxs;
+  int* los;  // first attended position per sequence
   int* scratch;
 };
 
@@ -145,7 +164,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const DecodeParams& p) {
   s.meta = reinterpret_cast<int4*>(s.empty + p.stages);
   s.cum = reinterpret_cast<int*>(s.meta + p.stages * p.nbs);
   s.ctxs = s.cum + (p.mode == 0 ? p.B + 1 : 2);
-  s.scratch = s.ctxs + (p.mode == 0 ? p.B : 1);
+  s.los = s.ctxs + (p.mode == 0 ? p.B : 1);
+  s.scratch = s.los + (p.mode == 0 ? p.B : 1);
   return s;
 }
 
@@ -675,7 +695,7 @@ struct Producer {
 
   // logical block of list entry u of sequence s (the visited blocks start at the window)
   static __device__ __forceinline__ int logical(const DecodeParams& p, const Smem& sm, int s, int u) {
-    return window_lo(p, sm.ctxs[s]) / PA_BLOCK_SIZE + (u - sm.cum[s]);
+    return sm.los[s] / PA_BLOCK_SIZE + (u - sm.cum[s]);
   }
   static __device__ __forceinline__ int load_entry(const DecodeParams& p, const Smem& sm, const Range& r, int u) {
     if (u >= r.u1) return -1;
@@ -700,7 +720,7 @@ struct Producer {
     if (bad) set_error(p.err, PA_EFLAG_BAD_BLOCK_ID);
     // first attended token of the block: sinks and positions before the window are skipped
     const int first =
-        valid ? min(PA_BLOCK_SIZE, max(0, max(p.num_sink, window_lo(p, sm.ctxs[s])) - lb * PA_BLOCK_SIZE)) : 0;
+        valid ? min(PA_BLOCK_SIZE, max(0, max(p.num_sink, sm.los[s]) - lb * PA_BLOCK_SIZE)) : 0;
     my_meta = valid ? make_int4(s, first, min(PA_BLOCK_SIZE, sm.ctxs[s] - lb * PA_BLOCK_SIZE), bad ? 1 : 0)
                     : make_int4(-1, 0, 0, 1);
     live_mask = __ballot_sync(0xffffffffu, valid && !bad);
@@ -806,7 +826,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     int local = 0;
     for (int i = lo; i < hi; ++i) {
       const int ctx = p.context_lens[i];
-      const int nb = seq_span(p, ctx);
+      const int nb = seq_span(p, i, ctx);
       if (nb < 0 && reporter) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
       local += max(nb, 0);
     }
@@ -831,10 +851,11 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     int run = sm.scratch[warp] + incl - local;
     for (int i = lo; i < hi; ++i) {
       const int ctx = p.context_lens[i];
-      const int nb = seq_span(p, ctx);
+      const int nb = seq_span(p, i, ctx);
       run += max(nb, 0);
       sm.cum[i + 1] = run;
       sm.ctxs[i] = nb < 0 ? 0 : ctx;
+      sm.los[i] = nb < 0 ? 0 : seq_lo(p, i, ctx);
     }
     __syncthreads();
     const int T = sm.cum[p.B];
@@ -854,13 +875,14 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
     seq_base = blockIdx.y;
     nseq = 1;
     const int ctx = p.context_lens[seq_base];
-    const int nb = seq_span(p, ctx);
+    const int nb = seq_span(p, seq_base, ctx);
     if (nb < 0 && blockIdx.x == 0 && blockIdx.z == 0 && tid == 0) set_error(p.err, PA_EFLAG_CTX_OVERFLOW);
     const int nbv = max(nb, 0);
     if (tid == 0) {
       sm.cum[0] = 0;
       sm.cum[1] = nbv;
       sm.ctxs[0] = nb < 0 ? 0 : ctx;
+      sm.los[0] = nb < 0 ? 0 : seq_lo(p, seq_base, ctx);
     }
     u0 = blockIdx.x * p.ppb;
     u1 = min(nbv, u0 + p.ppb);
@@ -978,12 +1000,12 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1)
 // Merge: out = Σ_p e^{m_p - M} o_p / Σ_p e^{m_p - M} l_p (plus the bf16 sink tokens).
 // WPR = 1: one warp per (sequence, query head).  WPR = 4, for launches with few (sequence, head)
 // rows: four warps per row, each merging a quarter of the partials (the first also the sinks),
-// combined through shared memory by the same log-sum-exp rule.
+// combined through shared memory by the same log-sum-exp rule.  CH partials are loaded per
+// round: 8, or 16 when a shared prefix adds its rows (one round for both kinds).
 // ------------------------------------------------------------------------------------
-template <int D, int WPR>
+template <int D, int WPR, int CH>
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int grid_x) {
   constexpr int E = D / 32;  // dims per lane
-  constexpr int CH = 8;      // partials per round of loads
   const int s = blockIdx.x;
   const int wid = threadIdx.x >> 5;
   const int h = WPR == 1 ? blockIdx.y * 4 + wid : blockIdx.y;
@@ -1003,9 +1025,11 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
     T = p.ws_meta[p.B + 1];
   }
   const int ctx = p.context_lens[s];
-  const int nb = seq_span(p, ctx);
-  // sink positions inside the attended range [window_lo, ctx)
-  const int sink_lo = window_lo(p, ctx);
+  const int nb = seq_span(p, s, ctx);
+  // sink positions inside the attended range [seq_lo, ctx)
+  const int sink_lo = seq_lo(p, s, ctx);
+  // partial rows of a shared prefix attended apart (only when this sequence has one)
+  const int n_x = (nb < 0 || !shares_prefix(p, s)) ? 0 : p.n_extra;
   const int n_sink = (nb < 0 || part != 0) ? 0 : min(p.num_sink, ctx);
   float qv[E];
   if (n_sink > sink_lo) {
@@ -1026,10 +1050,13 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
     }
     if (p.direct_ok && c_first == c_last) return;  // the main kernel wrote this row
   }
-  const int n_parts = (c_last - c_first + 1) * p.nbs;
+  const int n_own = (c_last - c_first + 1) * p.nbs;  // this call's own partials, then the prefix's
+  const int n_parts = n_own + n_x;
   const int share = (n_parts + WPR - 1) / WPR;
   const int i_begin = min(n_parts, part * share), i_end = min(n_parts, i_begin + share);
   auto row_of = [&](int i) -> const float* {
+    if (i >= n_own)
+      return p.extra + ((static_cast<size_t>(s) * p.n_extra + (i - n_own)) * p.H_q + h) * static_cast<size_t>(D + 4);
     const int c = c_first + i / p.nbs, jj = i % p.nbs;
     const size_t slot = p.mode == 0 ? static_cast<size_t>(s + c) : static_cast<size_t>(s) * p.max_parts + c;
     return p.partials + ((slot * p.nbs + jj) * p.H_q + h) * static_cast<size_t>(D + 4);
@@ -1137,7 +1164,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, int gr
       for (int e = 0; e < E; ++e) acc[e] += sc * sh_acc[w][lane * E + e];
     }
   }
-  const float inv = (bad || nb <= 0 || !(L > 0.f)) ? 0.f : 1.f / L;
+  const float inv = (bad || nb < 0 || !(L > 0.f)) ? 0.f : 1.f / L;
 #pragma unroll
   for (int e = 0; e < E; ++e) orow[lane * E + e] = __float2bfloat16_rn(acc[e] * inv);
 }
@@ -1210,7 +1237,7 @@ pa_status make_plan(const pa_cache_desc* d, int max_ctx, int partition_size, Pla
     pl->meta_bytes = 256;
   }
   const size_t kSmemLimit = smem_limit(PA_CTAS_PER_SM);
-  const size_t cum_ints = pl->mode == 0 ? (2 * static_cast<size_t>(B) + 1) : 3;
+  const size_t cum_ints = pl->mode == 0 ? (3 * static_cast<size_t>(B) + 1) : 4;  // cum, ctxs, los
   const size_t fixed_bytes = 1024 + (cum_ints + 32) * 4;
   const size_t per_stage = pl->stage_bytes + 16 + static_cast<size_t>(pl->nbs) * 16;
   if (fixed_bytes + 2 * per_stage > kSmemLimit) return PA_ERR_UNSUPPORTED;
@@ -1241,8 +1268,10 @@ pa_status launch(const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv, c
     return PA_ERR_CUDA;
   // few (sequence, head) rows for the SMs (long contexts, small batches): four warps per row
   if (static_cast<long long>(p.B) * p.H_q < 4LL * std::max(1, sm_count_current()))
-    return launch_overlapped(merge_kernel<D, 4>, dim3(p.B, p.H_q), dim3(128), 0, stream, p, pl.grid_x);
-  return launch_overlapped(merge_kernel<D, 1>, dim3(p.B, (p.H_q + 3) / 4), dim3(128), 0, stream, p, pl.grid_x);
+    return launch_overlapped(merge_kernel<D, 4, 8>, dim3(p.B, p.H_q), dim3(128), 0, stream, p, pl.grid_x);
+  if (p.n_extra > 0)
+    return launch_overlapped(merge_kernel<D, 1, 16>, dim3(p.B, (p.H_q + 3) / 4), dim3(128), 0, stream, p, pl.grid_x);
+  return launch_overlapped(merge_kernel<D, 1, 8>, dim3(p.B, (p.H_q + 3) / 4), dim3(128), 0, stream, p, pl.grid_x);
 }
 
 }  // namespace
@@ -1257,11 +1286,21 @@ extern "C" size_t pa_decode_workspace_size(const pa_cache_desc* desc, int max_co
 
 namespace pa {
 namespace {
-// pa_decode_attention, and the attention half of pa_decode_step (append_pos non-null).
+// The prefix part of pa_decode_attention_shared, already enqueued: flags and rows as DecodeParams'.
+struct SharedPart {
+  const int32_t* flags;
+  const float* extra;
+  int shared_len;
+  int n_extra;
+};
+
+// pa_decode_attention, the attention half of pa_decode_step (append_pos non-null) and the
+// decode half of pa_decode_attention_shared (shared non-null).
 pa_status decode_attention_impl(const pa_cache_desc* desc, void* out, const void* q, const void* k_cache,
                                 const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
                                 int max_context_len, float scale, int partition_size, void* workspace,
-                                size_t workspace_bytes, int32_t* err_flag, void* stream, const int32_t* append_pos) {
+                                size_t workspace_bytes, int32_t* err_flag, void* stream, const int32_t* append_pos,
+                                const SharedPart* shared = nullptr) {
   pa::Plan pl;
   pa_status st = pa::make_plan(desc, max_context_len, partition_size, &pl);
   if (st != PA_OK) return st;
@@ -1317,7 +1356,8 @@ pa_status decode_attention_impl(const pa_cache_desc* desc, void* out, const void
   p.mode = pl.mode;
   p.ppb = pl.ppb;
   p.max_parts = pl.max_parts;
-  p.direct_ok = (pl.nbs == 1 && desc->num_sink == 0) ? 1 : 0;
+  // a row that one CTA covers is written by it, unless a shared prefix's rows are still to come
+  p.direct_ok = (pl.nbs == 1 && desc->num_sink == 0 && !shared) ? 1 : 0;
   p.stage_bytes = pl.stage_bytes;
   p.block_bytes = pl.block_bytes;
   p.block_tx = pl.block_tx;
@@ -1334,6 +1374,10 @@ pa_status decode_attention_impl(const pa_cache_desc* desc, void* out, const void
   p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.meta_bytes);
   p.err = err_flag;
   p.append_pos = append_pos;
+  p.shared_flags = shared ? shared->flags : nullptr;
+  p.extra = shared ? shared->extra : nullptr;
+  p.shared_len = shared ? shared->shared_len : 0;
+  p.n_extra = shared ? shared->n_extra : 0;
 
   cudaStream_t s = pa::as_stream(stream);
   const bool quant = pa::is_quantized(desc);
@@ -1379,6 +1423,74 @@ extern "C" pa_status pa_decode_step(const pa_cache_desc* desc, void* out, const 
   if (st != PA_OK) return st;
   return pa::decode_attention_impl(desc, out, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
                                    scale, partition_size, workspace, workspace_bytes, err_flag, stream, positions);
+}
+
+// ------------------------------------------------------------------------------------
+// Shared-prefix decode: the prefix kernel (shared_prefix.cu), then the decode kernel from each
+// member's first position past the prefix, its merge folding the prefix rows in.
+// ------------------------------------------------------------------------------------
+namespace pa {
+namespace {
+struct SharedLayout {
+  size_t flags_off, extra_off, total;
+};
+
+bool shared_layout(const pa_cache_desc* desc, int max_context_len, int partition_size, int shared_len,
+                   Plan* pl, SharedLayout* lay) {
+  if (make_plan(desc, max_context_len, partition_size, pl) != PA_OK) return false;
+  if (shared_len < 0 || shared_len % PA_BLOCK_SIZE != 0 || shared_len > max_context_len) return false;
+  auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t B = static_cast<size_t>(desc->num_seqs);
+  lay->flags_off = up(pl->ws_bytes);
+  lay->extra_off = lay->flags_off + up(B * sizeof(int32_t));
+  lay->total = lay->extra_off + B * shared_prefix_chunks(shared_len) * static_cast<size_t>(desc->num_q_heads) *
+                                    (desc->head_dim + 4) * sizeof(float);
+  return true;
+}
+}  // namespace
+}  // namespace pa
+
+extern "C" size_t pa_decode_shared_workspace_size(const pa_cache_desc* desc, int max_context_len,
+                                                  int partition_size, int shared_len) {
+  pa::Plan pl;
+  pa::SharedLayout lay;
+  return pa::shared_layout(desc, max_context_len, partition_size, shared_len, &pl, &lay) ? lay.total : 0;
+}
+
+extern "C" pa_status pa_decode_attention_shared(const pa_cache_desc* desc, void* out, const void* q,
+                                                const void* k_cache, const void* v_cache,
+                                                const int32_t* block_tables, const int32_t* context_lens,
+                                                int max_context_len, float scale, int partition_size,
+                                                const int32_t* shared_seqs, int n_shared, int shared_len,
+                                                void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                                void* stream) {
+  pa::Plan pl;
+  pa_status st = pa::make_plan(desc, max_context_len, partition_size, &pl);
+  if (st != PA_OK) return st;
+  if (pa::is_quantized(desc) || desc->num_sink > 0 || desc->sliding_window > 0) return PA_ERR_UNSUPPORTED;
+  pa::SharedLayout lay;
+  if (!pa::shared_layout(desc, max_context_len, partition_size, shared_len, &pl, &lay)) return PA_ERR_INVALID_ARG;
+  if (n_shared < 0 || n_shared > desc->num_seqs || (n_shared > 0 && !shared_seqs)) return PA_ERR_INVALID_ARG;
+  if (desc->num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+    return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+       reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u)
+    return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < lay.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+  if (n_shared == 0 || shared_len == 0)  // nothing to share: the plain decode
+    return pa::decode_attention_impl(desc, out, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                                     scale, partition_size, workspace, workspace_bytes, err_flag, stream, nullptr);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* flags = reinterpret_cast<int32_t*>(ws + lay.flags_off);
+  float* extra = reinterpret_cast<float*>(ws + lay.extra_off);
+  st = pa::launch_shared_prefix(desc, q, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+                                shared_seqs, n_shared, shared_len, flags, extra, err_flag, pa::as_stream(stream));
+  if (st != PA_OK) return st;
+  const pa::SharedPart part{flags, extra, shared_len, pa::shared_prefix_chunks(shared_len)};
+  return pa::decode_attention_impl(desc, out, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                                   scale, partition_size, workspace, lay.flags_off, err_flag, stream, nullptr, &part);
 }
 
 // ------------------------------------------------------------------------------------

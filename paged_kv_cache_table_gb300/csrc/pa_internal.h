@@ -79,6 +79,27 @@ pa_status launch_prefill_tc(const pa_cache_desc* desc, void* out, const void* q,
                             const int32_t* context_lens, int max_query_len, float scale, int32_t* err_flag,
                             cudaStream_t stream, bool step);
 
+// Shared-prefix decode (shared_prefix.cu).  Per-sequence flags, zeroed then or-ed by the prefix
+// kernel: kSharedMember = listed, in range, context covering the prefix; kSharedMismatch = some
+// prefix block of its table differs from the first listed sequence's.  Exactly kSharedUse means
+// the decode kernel starts past the prefix and the merge folds in the prefix's partial rows.
+constexpr int kSharedMember = 1;
+constexpr int kSharedMismatch = 2;
+constexpr int kSharedUse = kSharedMember;
+constexpr int kSharedChunkBlocks = 8;  // prefix blocks per partial row (128 keys)
+inline int shared_prefix_chunks(int shared_len) {
+  const int nsb = shared_len / PA_BLOCK_SIZE;
+  return (nsb + kSharedChunkBlocks - 1) / kSharedChunkBlocks;
+}
+size_t shared_prefix_smem_bytes(int head_dim);
+
+// Zeroes flags[0..num_seqs) and launches the prefix kernel: partial rows
+// extra[s][chunk][h][head_dim + 4] (o, then m and l in log2 units) for every listed sequence s.
+pa_status launch_shared_prefix(const pa_cache_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens, int max_context_len,
+                               float scale, const int32_t* shared_seqs, int n_shared, int shared_len,
+                               int32_t* flags, float* extra, int32_t* err_flag, cudaStream_t stream);
+
 inline pa_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

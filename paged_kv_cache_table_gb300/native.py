@@ -42,6 +42,7 @@ _DTYPES = {"bf16": PA_BF16, "fp8_e4m3": PA_FP8_E4M3, "e4m3": PA_FP8_E4M3, "int8"
 EXPORTED = [
     "pa_status_string", "pa_kv_append", "pa_kv_append_tokens", "pa_block_copy",
     "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_noalloc", "pa_decode_step",
+    "pa_decode_shared_workspace_size", "pa_decode_attention_shared",
     "pa_prefill_attention", "pa_prefill_step", "pa_prefill_workspace_size", "pa_prefill_attention_ws",
     "pa_prefill_step_ws",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_alloc", "pa_bm_claim", "pa_bm_incref", "pa_bm_decref",
@@ -115,6 +116,11 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_attention.restype = c_int
         L.pa_decode_attention.argtypes = [dp, vp, vp, vp, vp, vp, vp, c_int, ctypes.c_float, c_int, vp,
                                           ctypes.c_size_t, vp, vp]
+        L.pa_decode_shared_workspace_size.restype = ctypes.c_size_t
+        L.pa_decode_shared_workspace_size.argtypes = [dp, c_int, c_int, c_int]
+        L.pa_decode_attention_shared.restype = c_int
+        L.pa_decode_attention_shared.argtypes = [dp, vp, vp, vp, vp, vp, vp, c_int, ctypes.c_float, c_int, vp,
+                                                 c_int, c_int, vp, ctypes.c_size_t, vp, vp]
         L.pa_prefill_attention.restype = c_int
         L.pa_prefill_attention.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, c_int, ctypes.c_float, vp, vp]
         L.pa_prefill_workspace_size.restype = ctypes.c_size_t
@@ -244,6 +250,25 @@ def pa_decode_attention(desc, out, q, k_cache, v_cache, block_tables, context_le
                                      float(scale), int(partition_size), _ptr(workspace),
                                      int(workspace_bytes), _ptr(err_flag), _stream(stream)),
            "pa_decode_attention")
+
+
+def pa_decode_shared_workspace_size(desc, max_context_len, partition_size=0, shared_len=0) -> int:
+    return int(lib().pa_decode_shared_workspace_size(ctypes.byref(desc), int(max_context_len),
+                                                     int(partition_size), int(shared_len)))
+
+
+def pa_decode_attention_shared(desc, out, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                               scale, partition_size, shared_seqs, n_shared, shared_len, workspace,
+                               workspace_bytes=None, err_flag=None, stream=None):
+    """pa_decode_attention with a prefix shared by the listed sequences attended once (see pa.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_attention_shared(ctypes.byref(desc), _ptr(out), _ptr(q), _ptr(k_cache),
+                                            _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+                                            int(max_context_len), float(scale), int(partition_size),
+                                            _ptr(shared_seqs), int(n_shared), int(shared_len), _ptr(workspace),
+                                            int(workspace_bytes), _ptr(err_flag), _stream(stream)),
+           "pa_decode_attention_shared")
 
 
 def pa_decode_step(desc, out, q, k_cache, v_cache, k_new, v_new, block_tables, positions, context_lens,

@@ -130,6 +130,25 @@ class GpuState:
                          max_ctx, w.scale, partition, ws, nbytes, self.err)
         return out
 
+    def attend_shared(self, q, context_lens, shared_seqs, shared_len, partition=0, max_ctx=None, ws_fill=None):
+        """pa_decode_attention_shared: the listed sequences' first shared_len positions attended
+        once for all of them.  ws_fill: a byte the workspace is filled with first (else empty)."""
+        w = self.w
+        ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+        max_ctx = int(ctx.max()) if max_ctx is None else int(max_ctx)
+        out = torch.full((w.B, w.H_q, w.D), float("nan"), dtype=torch.bfloat16, device=self.dev)
+        nbytes = P.pa_decode_shared_workspace_size(self.desc, max_ctx, partition, shared_len)
+        assert nbytes > 0
+        if ws_fill is None:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+        else:
+            ws = torch.full((nbytes,), ws_fill, dtype=torch.uint8, device=self.dev)
+        seqs = torch.tensor(np.asarray(shared_seqs, dtype=np.int32), device=self.dev)
+        P.pa_decode_attention_shared(self.desc, out, q.to(self.dev), self.k, self.v, self.tables_dev,
+                                     torch.from_numpy(ctx).to(self.dev), max_ctx, w.scale, partition, seqs,
+                                     len(shared_seqs), shared_len, ws, nbytes, self.err)
+        return out
+
     def attend_noalloc(self, q, context_lens, partition=0, max_ctx=None):
         """pa_decode_attention_noalloc: the same attention with the library's static scratch."""
         w = self.w

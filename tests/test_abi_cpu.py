@@ -459,3 +459,59 @@ def test_prefill_step_ws_checks_every_argument_first():
             N.pa_prefill_step_ws(quant, FAKE, FAKE, FAKE, FAKE, a["k_new"], FAKE, a["n"], FAKE, FAKE, FAKE, FAKE,
                                  FAKE, 16, a["max_ctx"], a["scale"], a["ws"], a["nbytes"], None, 0)
         assert e.value.status == status, kw
+
+
+def test_shared_decode_workspace_size():
+    """The decode workspace, then one int32 flag per sequence, then the prefix's partial rows:
+    num_seqs x ceil(shared_len / 128) x num_q_heads rows of head_dim + 4 floats, each part
+    256-byte aligned."""
+    d = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, num_seqs=64, max_blocks_per_seq=300)
+    for part in (512, 256):
+        dec = N.pa_decode_workspace_size(d, 4096, part)
+        flags = (64 * 4 + 255) // 256 * 256
+        up = (dec + 255) // 256 * 256
+        for shared_len, chunks in ((0, 0), (16, 1), (128, 1), (1200, 10), (4096, 32)):
+            rows = 64 * chunks * 32 * (128 + 4) * 4
+            assert N.pa_decode_shared_workspace_size(d, 4096, part, shared_len) == up + flags + rows
+    # shared_len not a multiple of 16, negative, or beyond max_context_len; a bad partition
+    for bad in (24, -16, 4096 + 16):
+        assert N.pa_decode_shared_workspace_size(d, 4096, 512, bad) == 0
+    assert N.pa_decode_shared_workspace_size(d, 4096, 24, 1200) == 0
+
+
+@host_only
+def test_shared_decode_rejects_bad_arguments_on_the_host():
+    d = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, num_seqs=8, max_blocks_per_seq=100)
+    need = N.pa_decode_shared_workspace_size(d, 1000, 512, 512)
+    ws = 1 << 24
+    # pa_decode_attention_shared(desc, out, q, k, v, tables, ctx, max_ctx, scale, partition, seqs, n_shared,
+    #                            shared_len, ws, bytes)
+    good = dict(out=FAKE, max_ctx=1000, scale=0.1, seqs=FAKE, n=4, L=512, ws=ws, nbytes=need)
+    bad = [
+        (dict(scale=float("nan")), N.PA_ERR_INVALID_ARG),
+        (dict(out=0), N.PA_ERR_INVALID_ARG),
+        (dict(L=520), N.PA_ERR_INVALID_ARG),       # not a multiple of 16
+        (dict(L=1008), N.PA_ERR_INVALID_ARG),      # beyond max_context_len
+        (dict(L=-16), N.PA_ERR_INVALID_ARG),
+        (dict(n=9), N.PA_ERR_INVALID_ARG),         # more than num_seqs
+        (dict(n=-1), N.PA_ERR_INVALID_ARG),
+        (dict(seqs=0), N.PA_ERR_INVALID_ARG),      # a list is needed when n_shared > 0
+        (dict(ws=ws + 128), N.PA_ERR_INVALID_ARG),
+        (dict(nbytes=need - 1), N.PA_ERR_WORKSPACE_TOO_SMALL),
+    ]
+    for kw, status in bad:
+        a = dict(good, **kw)
+        with pytest.raises(N.PaError) as e:
+            N.pa_decode_attention_shared(d, a["out"], FAKE, FAKE, FAKE, FAKE, FAKE, a["max_ctx"], a["scale"], 512,
+                                         a["seqs"], a["n"], a["L"], a["ws"], a["nbytes"], None, 0)
+        assert e.value.status == status, kw
+    # caches the shared path does not serve
+    quant = _desc(num_q_heads=32, num_kv_heads=8, head_dim=128, num_seqs=8, max_blocks_per_seq=100,
+                  k_dtype="e4m3", v_dtype="int8", k_scales=FAKE, v_scales=FAKE)
+    sinks = _desc(num_seqs=8, max_blocks_per_seq=100, num_sink=4, k_sink=FAKE, v_sink=FAKE)
+    window = _desc(num_seqs=8, max_blocks_per_seq=100, sliding_window=256)
+    for dd in (quant, sinks, window):
+        with pytest.raises(N.PaError) as e:
+            N.pa_decode_attention_shared(dd, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1000, 0.1, 512, FAKE, 4, 512, ws,
+                                         1 << 30, None, 0)
+        assert e.value.status == N.PA_ERR_UNSUPPORTED

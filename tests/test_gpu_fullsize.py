@@ -160,4 +160,8 @@ def test_full_size_prefix_fork_and_steady_step():
         vb = np.concatenate([pv, new_v, sv, new_v])
         ref[s] = reference_seq(w, s, 0, kb, vb)
     _check_all_rows(to_f64(out), ref, "prefix_cow steady step")
+    # the 75 whole prefix blocks attended once for all sequences (pa_decode_attention_shared)
+    out_shared = g.attend_shared(w.q[0], steady + 1, list(range(w.B)), w.prefix - w.prefix % 16)
+    assert g.err_bits() == 0
+    _check_all_rows(to_f64(out_shared), ref, "prefix_cow shared prefix")
 
