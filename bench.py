@@ -42,9 +42,9 @@ WARM_SECONDS = 0.25   # warm-up runs at least this long (and at least --warmup s
 # ncu capture of each workload's attention call.  Reported only while the kernel sources hash to
 # the version the counters were taken on; null otherwise.
 NCU_TRAFFIC = {
-    "sources_sha256_16": "f470722d1057d36a",
-    "8b": 552_134_400, "70b": 543_439_104, "long_quant": 1_077_082_880, "long_quant_tok": 1_093_661_184,
-    "prefix_cow": 282_154_752, "int4_8b": 190_264_576, "swa": 1_082_067_712, "tiny": 283_136,
+    "sources_sha256_16": "9942378e63a7254b",
+    "8b": 552_082_688, "70b": 542_895_616, "long_quant": 1_077_425_664, "long_quant_tok": 1_094_054_656,
+    "prefix_cow": 282_395_392, "int4_8b": 190_622_720, "swa": 1_082_571_520, "tiny": 283_392,
 }
 KERNEL_SOURCES = ["paged_kv_cache_table_gb300/csrc/decode_attention.cu",
                   "paged_kv_cache_table_gb300/csrc/pa_device.cuh",
@@ -1134,6 +1134,9 @@ def main(argv=None):
     ap.add_argument("--attention-only", action="store_true",
                     help="with --config: one decode step, then --warmup + --steps decode-attention calls on the "
                          "same inputs, one JSON line; for profiling the decode kernel")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="with --attention-only on a workload with a shared prefix: the calls attend the prefix "
+                         "once for all sequences (pa_decode_attention_shared)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the chunked-prefill row (append + prefill attention steps) and print it; "
                          "for profiling that kernel")
@@ -1162,14 +1165,22 @@ def main(argv=None):
 
 def run_attention_only(args):
     """One decode step on --config (append + attention), then --warmup + --steps attention calls on the
-    step's inputs; prints the mean call time."""
+    step's inputs; prints the mean call time.  --shared-prefix (a workload with a shared prefix): the
+    calls go through pa_decode_attention_shared."""
     import torch
     from paged_kv_cache_table_gb300 import native as N
-    b = DecodeBench(args.config, torch.device("cuda", 0), args.partition)
+    b = DecodeBench(args.config, torch.device("cuda", 0), args.partition, shared=args.shared_prefix)
+    if args.shared_prefix and not b.shared:
+        raise SystemExit(f"--shared-prefix: workload {args.config} has no shared prefix")
     s = torch.cuda.current_stream().cuda_stream
     b.step(0, s)
 
     def call():
+        if b.shared:
+            N.pa_decode_attention_shared(b.desc, b.out, b.q[0], b.k, b.v, b.tables_dev, b.ctx_dev[0], b.max_ctx,
+                                         b.w.scale, args.partition, b.shared_seqs, b.w.B, b.shared_len, b.ws,
+                                         b.ws_bytes, b.err, s)
+            return
         N.pa_decode_attention(b.desc, b.out, b.q[0], b.k, b.v, b.tables_dev, b.ctx_dev[0], b.max_ctx, b.w.scale,
                               args.partition, b.ws, b.ws_bytes, b.err, s)
     for _ in range(max(0, args.warmup)):
@@ -1181,7 +1192,8 @@ def run_attention_only(args):
         call()
     t1.record()
     torch.cuda.synchronize()
-    print(json.dumps({"row": "decode_attention", "config": args.config, "steps": args.steps, "warmup": args.warmup,
+    print(json.dumps({"row": "decode_attention_shared" if b.shared else "decode_attention", "config": args.config,
+                      "steps": args.steps, "warmup": args.warmup,
                       "ms_per_call": round(t0.elapsed_time(t1) / max(1, args.steps), 5),
                       "err_flag": int(b.err.item())}))
     return 0 if int(b.err.item()) == 0 else 1
