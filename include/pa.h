@@ -25,6 +25,9 @@
  *   - Optional sliding window of W tokens (ldpk §5.3): each query attends only the most
  *     recent W positions, its own included, and blocks that fall wholly before the window
  *     go back to the pool (pa_bm_slide_window), so a sequence holds O(W) cache.
+ *   - Sequences that share a prompt prefix point their tables at one copy of its whole blocks
+ *     (AI内存系统 §3.1, §3.3); pa_decode_attention_shared attends those blocks once for all of
+ *     them and merges that part with each sequence's own positions.
  *
  * Memory layout (all row-major, all device memory unless stated otherwise):
  *   k_cache, v_cache  [num_blocks * 16][num_kv_heads][head_dim]  element type per k/v_dtype

@@ -159,3 +159,46 @@ def test_nothing_to_share_is_the_plain_decode():
     assert torch.equal(g.attend_shared(w.q[0], ctx, list(range(w.B)), 0), plain)
     assert torch.equal(g.attend_shared(w.q[0], ctx, [], 96), plain)
     assert g.err_bits() == 0
+
+
+def test_graph_replay_matches_eager_calls():
+    """The shared call (flag clearing, prefix kernel, decode, merge) captured once in a CUDA graph
+    and replayed with new queries in the captured buffer equals an eager call each time."""
+    w = make_workload("prefix_cow", B=8, prefix=300, suffix_range=(10, 200), steps=1)
+    g, o, ctx = _forked(w)
+    shared_len = 288
+    ctx_dev = torch.from_numpy(np.ascontiguousarray(ctx, dtype=np.int32)).to(g.dev)
+    max_ctx = int(ctx.max())
+    seqs = torch.arange(w.B, dtype=torch.int32, device=g.dev)
+    nbytes = P.pa_decode_shared_workspace_size(g.desc, max_ctx, 0, shared_len)
+    ws_graph = torch.empty(nbytes, dtype=torch.uint8, device=g.dev)
+    ws_eager = torch.empty(nbytes, dtype=torch.uint8, device=g.dev)
+    q_buf = w.q[0].to(g.dev)
+    out_buf = torch.empty((w.B, w.H_q, w.D), dtype=torch.bfloat16, device=g.dev)
+    out_eager = torch.empty_like(out_buf)
+
+    def call(q, out, ws):
+        P.pa_decode_attention_shared(g.desc, out, q, g.k, g.v, g.tables_dev, ctx_dev, max_ctx, w.scale, 0, seqs,
+                                     w.B, shared_len, ws, nbytes, g.err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(q_buf, out_buf, ws_graph)  # warm-up outside the capture
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            call(q_buf, out_buf, ws_graph)
+    torch.cuda.synchronize()
+    gen = torch.Generator().manual_seed(12)
+    for r in range(3):
+        q_new = (torch.randn((w.B, w.H_q, w.D), generator=gen) * 0.5).to(torch.bfloat16)
+        q_buf.copy_(q_new.to(g.dev))
+        graph.replay()
+        torch.cuda.synchronize()
+        call(q_buf, out_eager, ws_eager)
+        torch.cuda.synchronize()
+        assert torch.equal(out_buf, out_eager), f"replay {r}"
+        if r == 2:
+            assert_attention_close(to_f64(out_buf), o.attend(q_new, ctx), "replay vs oracle")
+    assert g.err_bits() == 0
