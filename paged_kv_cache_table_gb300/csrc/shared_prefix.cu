@@ -2,14 +2,14 @@
 //
 // Prefix sharing (AI内存系统 §3.1: requests with the same prefix point their block tables at one
 // stored copy of its blocks; §3.3: only whole blocks are shared) makes every member sequence's
-// decode read the same prefix blocks.  Attention is a sum over positions, so it splits exactly at a block boundary:
-// with the softmax kept as (running max m, sum l, unnormalised output o) per part, two parts
-// combine as
+// decode read the same prefix blocks.  Attention is a sum over positions, so it splits exactly at
+// a block boundary: with the softmax kept as (running max m, sum l, unnormalised output o) per
+// part, two parts combine as
 //   M = max(m1, m2),  l = e^{m1-M} l1 + e^{m2-M} l2,  o = e^{m1-M} o1 + e^{m2-M} o2,  out = o / l
 // (the same rule that merges the split-context partials of the decode kernel).  Here the prefix
 // part is computed once per (KV head, 128-key chunk) for all member rows together — every member's
-// G query heads stacked as the rows of one warp-level matrix product, so each prefix K/V tile is
-// read from memory once instead of once per member — and the decode kernel then visits only each
+// G query heads stacked as the rows of one warp-level matrix product, so each prefix K/V tile
+// crosses HBM once instead of once per member — and the decode kernel then visits only each
 // member's own positions past the prefix, its merge folding the prefix rows in.
 //
 // Membership is checked, not trusted: a listed sequence uses the prefix rows only if its context
