@@ -45,6 +45,10 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int ro
 bool encode_cache_map_heads(CUtensorMap* map, const void* base, int elem_bytes, int heads, int nc, int box_heads,
                             long long slots);
 
+// The same view with boxes of one 128-byte chunk x 16 slots x one head, landing as [slot][128 B]
+// swizzled (tensor_map.cpp).
+bool encode_cache_map_chunk(CUtensorMap* map, const void* base, int elem_bytes, int heads, int nc, long long slots);
+
 // TMA descriptor of the INT4 group parameters viewed as (16-byte head row, kv_head, slot) with
 // boxes of `box_heads` heads x 16 slots, no swizzle (tensor_map.cpp).
 bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots);

@@ -46,14 +46,20 @@ struct PrefixParams {
   float scale_log2;
 };
 
-// 16 bytes global -> shared; n = 0 reads nothing and fills the 16 bytes with zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int n) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+constexpr int kGroupBlocks = 2;  // blocks per copy group (one barrier each for K and for V)
+constexpr int kGroups = kSharedChunkBlocks / kGroupBlocks;
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+
+// Byte offset of (token t of a block, dim d) in a block's tile as its TMA boxes land it: one
+// [16 slots][128 bytes] box per 64 dims, under the 128-byte swizzle (the 16-byte unit index XOR
+// the slot mod 8), so that the eight rows of an ldmatrix fall in eight distinct bank groups.
+__device__ __forceinline__ uint32_t tile_off(int t, int d) {
+  return static_cast<uint32_t>((d >> 6) * (PA_BLOCK_SIZE * 128) + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4));
 }
 
 // grid (n_chunks, H_kv, ceil(n_shared * G / 64)), 128 threads.  CTA (x, y, z): KV head y, prefix
@@ -61,16 +67,19 @@ __device__ __forceinline__ void cp_async_wait() {
 // member-major order (row r: member r / G, query head y G + r % G); warp w takes the 16 rows
 // 64 z + 16 w .. +15 over all of the chunk's keys.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 3) shared_prefix_kernel(const PrefixParams p) {
-  constexpr int RS = D * 2 + 16;  // bytes per shared-memory row: 16-byte skew, conflict-free ldmatrix
-  constexpr int PPR = D * 2 / 16;  // 16-byte pieces per row
-  constexpr int KK = D / 16;       // k-steps of the score product
-  constexpr int NT = kChunkKeys / 8;  // 8-key tiles of a chunk
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ks = smem;
-  uint8_t* vs = smem + kChunkKeys * RS;
+__global__ void __launch_bounds__(kThreads, 3)
+    shared_prefix_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const PrefixParams p) {
+  constexpr int TB = PA_BLOCK_SIZE * D * 2;  // bytes of one block's tile (one KV head)
+  constexpr int KK = D / 16;                  // k-steps of the score product
+  constexpr int NT = kChunkKeys / 8;          // 8-key tiles of a chunk
+  extern __shared__ uint8_t smem_raw[];
+  // tiles 1024-byte aligned (the swizzle pattern's period): K tiles, then V tiles
+  uint8_t* ks = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* vs = ks + kSharedChunkBlocks * TB;
   __shared__ int blk[kSharedChunkBlocks];
   __shared__ int any_bad;
+  __shared__ __align__(8) uint64_t bars[2 * kGroups];  // K groups, then V groups: one phase each
 
   // the decode kernel that follows may be scheduled as this grid's CTAs finish; it waits for the
   // whole grid (and its memory) before reading anything this kernel writes
@@ -103,7 +112,17 @@ __global__ void __launch_bounds__(kThreads, 3) shared_prefix_kernel(const Prefix
   const int32_t* ltab = p.block_tables + static_cast<size_t>(leader) * p.max_blocks;
   // The leader's table is read before its context length is known: every id is range-checked
   // before use, and when the context does not cover the prefix no sequence takes these rows.
-  if (tid == 0) any_bad = 0;
+  if (tid == 0) {
+    any_bad = 0;
+#pragma unroll
+    for (int i = 0; i < 2 * kGroups; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  const int nrows = nblk * PA_BLOCK_SIZE;
+  // V tiles past the prefix's end (its last chunk) hold zeros: their weights are exactly 0, and
+  // 0 times stale bits could be NaN.  (K rows there are masked in the softmax instead.)
+  for (int i = nblk * TB / 16 + tid; i < kSharedChunkBlocks * TB / 16; i += kThreads)
+    reinterpret_cast<uint4*>(vs)[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   if (tid < nblk) {
     const int b = ltab[b0 + tid];
@@ -113,24 +132,28 @@ __global__ void __launch_bounds__(kThreads, 3) shared_prefix_kernel(const Prefix
   }
   __syncthreads();
 
-  // ---- K then V of this chunk into shared memory (two commit groups).  Rows past the chunk's
-  // last block and rows of an invalid block are zero-filled, so that every product below runs
-  // unconditionally (the tail keys are masked in the softmax) and no stale bits reach it. ----
-  const int nrows = nblk * PA_BLOCK_SIZE;
-  const uint32_t ks_a = smem_u32(ks), vs_a = smem_u32(vs);
+  // ---- K then V of this chunk into shared memory: TMA boxes of a block's 16 slots of KV head y
+  // (one per 64 dims), in groups of two blocks with a barrier each, so that the products start
+  // on the first keys while the rest are in flight.  A block with an invalid id is not
+  // loaded (its rows' results are discarded). ----
+  if (tid == 0) {
+    const uint64_t pol = l2_evict_last_policy();  // each chunk is read by every row-tile CTA
+#pragma unroll 1
+    for (int gi = 0; gi < 2 * kGroups; ++gi) {
+      const int kv = gi / kGroups;
+      int n = 0;
+      for (int bi = (gi % kGroups) * kGroupBlocks; bi < (gi % kGroups + 1) * kGroupBlocks; ++bi)
+        n += bi < nblk && blk[bi] >= 0;
+      mbar_arrive_expect_tx(&bars[gi], n * TB);
+      for (int bi = (gi % kGroups) * kGroupBlocks; bi < (gi % kGroups + 1) * kGroupBlocks; ++bi)
+        if (bi < nblk && blk[bi] >= 0)
 #pragma unroll
-  for (int pass = 0; pass < 2; ++pass) {
-    const uint8_t* pool = reinterpret_cast<const uint8_t*>(pass == 0 ? p.k : p.v);
-    const uint32_t base = pass == 0 ? ks_a : vs_a;
-#pragma unroll 4
-    for (int i = tid; i < kChunkKeys * PPR; i += kThreads) {
-      const int row = i / PPR, piece = i % PPR;
-      const int b = row < nrows ? blk[row / PA_BLOCK_SIZE] : -1;
-      const size_t slot = static_cast<size_t>(max(b, 0)) * PA_BLOCK_SIZE + (row % PA_BLOCK_SIZE);
-      cp_async16(base + row * RS + piece * 16, pool + ((slot * p.H_kv + y) * D) * 2 + piece * 16, b < 0 ? 0 : 16);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d((kv == 0 ? ks : vs) + bi * TB + c * (PA_BLOCK_SIZE * 128), kv == 0 ? &tmK : &tmV, &bars[gi],
+                        0, c, blk[bi] * PA_BLOCK_SIZE, y, pol);
     }
-    cp_async_commit();
   }
+  const uint32_t ks_a = smem_u32(ks), vs_a = smem_u32(vs);
 
   // ---- this warp's 16 rows: query fragments straight from global memory ----
 #pragma unroll
@@ -173,25 +196,30 @@ __global__ void __launch_bounds__(kThreads, 3) shared_prefix_kernel(const Prefix
     }
   }
 
-  // ---- S = Q K^T over the chunk ----
-  cp_async_wait<1>();
-  __syncthreads();
+  // ---- S = Q K^T over the chunk, one copy group at a time (every warp waits for every group,
+  // so that none leaves while a copy into this CTA may be in flight) ----
   const bool active = wr0 < rows_total;
+  bool late = false;
   float sacc[NT][4];
 #pragma unroll
   for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
   const int li = lane >> 3, lr = lane & 7;
-  if (active) {
 #pragma unroll
-    for (int kk = 0; kk < KK; ++kk) {
+  for (int gi = 0; gi < kGroups; ++gi) {
+    late |= !mbar_wait(&bars[gi], 0);
+    if (active) {
 #pragma unroll
-      for (int np = 0; np < NT / 2; ++np) {
-        // matrices: (keys 16np.., dims 16kk), (same keys, dims +8), (keys +8, dims 16kk), (keys +8, dims +8)
-        const uint32_t a = ks_a + (np * 16 + lr + 8 * (li >> 1)) * RS + (kk * 16 + 8 * (li & 1)) * 2;
-        uint32_t b00, b01, b10, b11;
-        ldsm_x4(a, b00, b01, b10, b11);
-        mma_bf16(sacc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b00, b01);
-        mma_bf16(sacc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b10, b11);
+      for (int kk = 0; kk < KK; ++kk) {
+#pragma unroll
+        for (int np = gi * kGroupBlocks; np < (gi + 1) * kGroupBlocks; ++np) {
+          // block np; matrices: (keys 0..7, dims 16kk), (keys 0..7, dims +8), (keys 8..15, dims 16kk),
+          // (keys 8..15, dims +8)
+          const uint32_t a = ks_a + np * TB + tile_off(lr + 8 * (li >> 1), kk * 16 + 8 * (li & 1));
+          uint32_t b00, b01, b10, b11;
+          ldsm_x4(a, b00, b01, b10, b11);
+          mma_bf16(sacc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b00, b01);
+          mma_bf16(sacc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b10, b11);
+        }
       }
     }
   }
@@ -235,23 +263,23 @@ __global__ void __launch_bounds__(kThreads, 3) shared_prefix_kernel(const Prefix
     ls[hf] += __shfl_xor_sync(0xffffffffu, ls[hf], 2);
   }
 
-  // ---- O = P V ----
-  cp_async_wait<0>();
-  __syncthreads();
+  // ---- O = P V, one copy group at a time ----
   float oacc[D / 8][4];
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) oacc[n][0] = oacc[n][1] = oacc[n][2] = oacc[n][3] = 0.f;
-  if (active) {
 #pragma unroll
-    for (int kt = 0; kt < NT / 2; ++kt) {
+  for (int kt = 0; kt < NT / 2; ++kt) {  // block kt
+    if (kt % kGroupBlocks == 0) late |= !mbar_wait(&bars[kGroups + kt / kGroupBlocks], 0);
+    if (active) {
       const uint32_t a0 = pack_bf16(sacc[2 * kt][0], sacc[2 * kt][1]);
       const uint32_t a1 = pack_bf16(sacc[2 * kt][2], sacc[2 * kt][3]);
       const uint32_t a2 = pack_bf16(sacc[2 * kt + 1][0], sacc[2 * kt + 1][1]);
       const uint32_t a3 = pack_bf16(sacc[2 * kt + 1][2], sacc[2 * kt + 1][3]);
 #pragma unroll
       for (int dp = 0; dp < D / 16; ++dp) {
-        // transposed matrices: (keys 16kt.., dims 16dp), (keys +8, dims 16dp), (keys 16kt.., dims +8), (keys +8, dims +8)
-        const uint32_t a = vs_a + (kt * 16 + lr + 8 * (li & 1)) * RS + (dp * 16 + 8 * (li >> 1)) * 2;
+        // transposed matrices: (keys 0..7, dims 16dp), (keys 8..15, dims 16dp), (keys 0..7, dims +8),
+        // (keys 8..15, dims +8)
+        const uint32_t a = vs_a + kt * TB + tile_off(lr + 8 * (li & 1), dp * 16 + 8 * (li >> 1));
         uint32_t b00, b01, b10, b11;
         ldsm_x4_t(a, b00, b01, b10, b11);
         mma_bf16(oacc[2 * dp], a0, a1, a2, a3, b00, b01);
@@ -260,8 +288,11 @@ __global__ void __launch_bounds__(kThreads, 3) shared_prefix_kernel(const Prefix
     }
   }
 
-  // ---- the partial rows: o (unnormalised), m, l (-1 when a prefix block id was invalid) ----
-  const bool bad = any_bad != 0;
+  // ---- the partial rows: o (unnormalised), m, l (-1 when a prefix block id was invalid or a copy
+  // did not land in time) ----
+  late = __any_sync(0xffffffffu, late);
+  if (late && lane == 0) set_error(p.err, PA_EFLAG_TIMEOUT);
+  const bool bad = any_bad != 0 || late;
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     if (srow[hf] < 0) continue;
@@ -281,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 3) shared_prefix_kernel(const Prefix
 }  // namespace
 
 size_t shared_prefix_smem_bytes(int head_dim) {
-  return static_cast<size_t>(2) * kSharedChunkBlocks * PA_BLOCK_SIZE * (head_dim * 2 + 16);
+  // K and V tiles of a chunk, plus the slack for their 1024-byte alignment
+  return static_cast<size_t>(2) * kSharedChunkBlocks * PA_BLOCK_SIZE * head_dim * 2 + 1024;
 }
 
 pa_status launch_shared_prefix(const pa_cache_desc* desc, const void* q, const void* k_cache, const void* v_cache,
@@ -312,11 +344,18 @@ pa_status launch_shared_prefix(const pa_cache_desc* desc, const void* q, const v
   const long long rows = static_cast<long long>(n_shared) * p.G;
   const dim3 grid(p.n_chunks, p.H_kv, static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta));
   const size_t smem = shared_prefix_smem_bytes(desc->head_dim);
+  // the pools as (64 dims, 64-dim chunk, slot, KV head), boxes of one chunk of one block's 16 slots
+  const long long slots = static_cast<long long>(desc->num_blocks) * PA_BLOCK_SIZE;
+  const int nc = desc->head_dim * 2 / 128;
+  CUtensorMap mk, mv;
+  if (!encode_cache_map_chunk(&mk, k_cache, 2, desc->num_kv_heads, nc, slots) ||
+      !encode_cache_map_chunk(&mv, v_cache, 2, desc->num_kv_heads, nc, slots))
+    return PA_ERR_CUDA;
   if (cudaMemsetAsync(flags, 0, static_cast<size_t>(p.B) * sizeof(int32_t), stream) != cudaSuccess)
     return PA_ERR_CUDA;
   auto kern = desc->head_dim == 128 ? shared_prefix_kernel<128> : shared_prefix_kernel<64>;
   if (!ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem)) return PA_ERR_CUDA;
-  kern<<<grid, kThreads, smem, stream>>>(p);
+  kern<<<grid, kThreads, smem, stream>>>(mk, mv, p);
   return launch_status();
 }
 

@@ -66,6 +66,24 @@ bool encode_cache_map_heads(CUtensorMap* map, const void* base, int elem_bytes, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same 4-D view with boxes of one 128-byte chunk x 16 slots x one head: a box lands as
+// [slot][128 B] with the 128-byte swizzle, so that eight consecutive slots take eight distinct
+// swizzle phases.
+bool encode_cache_map_chunk(CUtensorMap* map, const void* base, int elem_bytes, int heads, int nc, long long slots) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(128 / elem_bytes), static_cast<cuuint64_t>(nc),
+                        static_cast<cuuint64_t>(slots), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(heads) * nc * 128, static_cast<cuuint64_t>(nc) * 128};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elem_bytes), 1, PA_BLOCK_SIZE, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_param_map(CUtensorMap* map, const void* base, int heads, int box_heads, long long slots) {
   auto fn = tensor_map_encoder();
   if (!fn) return false;

@@ -155,10 +155,12 @@ def lib() -> ctypes.CDLL:
         L.pa_bm_release.restype = c_int
         L.pa_bm_release.argtypes = [vp, i32p, c_int]
         L.pa_bm_prepare_step.restype = c_int
-        L.pa_bm_prepare_step.argtypes = [vp, i32p, c_int, c_int, i32p, i32p, ctypes.POINTER(c_int),
+        # (array arguments of the per-step calls as plain addresses: ctypes pointer objects cost
+        # microseconds each to build)
+        L.pa_bm_prepare_step.argtypes = [vp, vp, c_int, c_int, vp, vp, ctypes.POINTER(c_int),
                                          ctypes.POINTER(c_int)]
         L.pa_bm_slide_window.restype = c_int
-        L.pa_bm_slide_window.argtypes = [vp, i32p, c_int, c_int, i32p, c_int, ctypes.POINTER(c_int)]
+        L.pa_bm_slide_window.argtypes = [vp, vp, c_int, c_int, vp, c_int, ctypes.POINTER(c_int)]
         u64, u8p = ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint8)
         L.pa_pc_block_hashes.restype = c_int
         L.pa_pc_block_hashes.argtypes = [i32p, c_int, u64, u64, u8p]
@@ -413,7 +415,7 @@ class BlockManager:
         pairs = np.empty((max(B, 1), 2), dtype=np.int32)
         n_pairs = ctypes.c_int(0)
         n_changed = ctypes.c_int(0)
-        st = lib().pa_bm_prepare_step(self._h, _p32(bt), B, M, _p32(pos), _p32(pairs),
+        st = lib().pa_bm_prepare_step(self._h, bt.ctypes.data, B, M, pos.ctypes.data, pairs.ctypes.data,
                                       ctypes.byref(n_pairs), ctypes.byref(n_changed))
         _check(st, "pa_bm_prepare_step")
         return pairs[:n_pairs.value].copy(), n_changed.value
@@ -425,7 +427,7 @@ class BlockManager:
         ctx = _i32(np.ascontiguousarray(context_lens, dtype=np.int32))
         B, M = bt.shape
         n_freed = ctypes.c_int(0)
-        r = lib().pa_bm_slide_window(self._h, _p32(bt), B, M, _p32(ctx), int(window), ctypes.byref(n_freed))
+        r = lib().pa_bm_slide_window(self._h, bt.ctypes.data, B, M, ctx.ctypes.data, int(window), ctypes.byref(n_freed))
         if r < 0:
             raise PaError(PA_ERR_INVALID_ARG, "pa_bm_slide_window")
         return r, n_freed.value
