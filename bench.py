@@ -42,9 +42,9 @@ WARM_SECONDS = 0.25   # warm-up runs at least this long (and at least --warmup s
 # ncu capture of each workload's attention call.  Reported only while the kernel sources hash to
 # the version the counters were taken on; null otherwise.
 NCU_TRAFFIC = {
-    "sources_sha256_16": "9942378e63a7254b",
-    "8b": 552_082_688, "70b": 542_895_616, "long_quant": 1_077_425_664, "long_quant_tok": 1_094_054_656,
-    "prefix_cow": 282_395_392, "int4_8b": 190_622_720, "swa": 1_082_571_520, "tiny": 283_392,
+    "sources_sha256_16": "44ffaa3d3391f948",
+    "8b": 552_095_488, "70b": 543_195_904, "long_quant": 1_076_637_952, "long_quant_tok": 1_093_696_768,
+    "prefix_cow": 282_179_072, "int4_8b": 190_577_920, "swa": 1_081_974_272, "tiny": 283_904,
 }
 KERNEL_SOURCES = ["paged_kv_cache_table_gb300/csrc/decode_attention.cu",
                   "paged_kv_cache_table_gb300/csrc/pa_device.cuh",
