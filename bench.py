@@ -935,14 +935,16 @@ def run_native(args):
     cow_launches = b.cow_launches
     warm_steps = b.warm_steps
     # the same steps with CUDA events around every attention call (roofline of the kernel)
-    _, att_ms, nbytes_ev = b.run(args.steps, args.warmup, per_call_events=True)
+    # (at least 200 calls: with a short --steps the mean would carry the first calls' ramp)
+    n_calls = max(args.steps, 200)
+    _, att_ms, nbytes_ev = b.run(n_calls, args.warmup, per_call_events=True)
     el_max, bytes_all = reduce_max_sum(elapsed, nbytes, device)
     value = bytes_all / el_max / 1e9
     ms_per_step = 1e3 * el_max / args.steps
     tok_s_layer = ws * w.B * args.steps / el_max
     att_mean_ms = float(np.mean(att_ms))
     att_pct = {k: round(float(np.percentile(att_ms, q)), 5) for k, q in (("p10", 10), ("median", 50), ("p90", 90))}
-    att_bytes = nbytes_ev / args.steps
+    att_bytes = nbytes_ev / n_calls
     achieved = att_bytes / (att_mean_ms / 1e3) / 1e9
     # end-to-end through the same API with host buffers
     el_e2e, nbytes_e2e = b.run_e2e(args.steps, args.warmup)
@@ -1094,7 +1096,7 @@ def run_native(args):
                                          "whole call (decode_kernel + merge_kernel)",
                          "kernel": "pa_decode_attention (decode_kernel + merge_kernel)",
                          "peak_kind": peak_kind, "ms_per_call": round(att_mean_ms, 5),
-                         "ms_per_call_percentiles": att_pct,
+                         "ms_per_call_percentiles": att_pct, "calls_timed": n_calls,
                          "algorithmic_bytes_per_call": int(att_bytes)},
             "e2e": {"value": round(bytes_e2e / el_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * el_e2e / args.steps, 5),
