@@ -28,6 +28,8 @@
 //    that saw a whole sequence writes the bf16 output directly.
 //  * In a decode step (pa_decode_step) the kernel overlaps the append launched just before it and
 //    waits for it only before the blocks that receive the appended tokens.
+//  * With a shared prefix attended apart (pa_decode_attention_shared, shared_prefix.cu) a member
+//    sequence's list starts past the prefix, and the merge folds in the prefix's partial rows.
 //  * Every wait is bounded; invalid table entries and contexts set error bits and zero rows.
 
 #include <algorithm>
